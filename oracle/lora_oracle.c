@@ -1,0 +1,247 @@
+/*
+ * lora_oracle.c -- plain, slow fp64 CPU oracle for the multi-adapter LoRA delta.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the bench's
+ * CPU-baseline leg load this file's library; the CUDA library never links,
+ * includes or calls it, and it shares no code with the CUDA kernels.
+ *
+ * What it computes (all arithmetic in IEEE double, inputs are bf16 values
+ * widened exactly to double by the caller):
+ *
+ *   Routing.  Every token t carries an adapter id i = ids[t].  Tokens of
+ *   different adapters are mixed in one batch and each token is served by its
+ *   own adapter, all adapters being resident at once
+ *   [C-LoRA report, vivodigitale.it, "Come funziona l'architettura": mixed-
+ *   adapter decode batches, one fused SGMV launch per decode step].
+ *   route(): a stable counting sort of token indices by adapter id (ties keep
+ *   the original token order), plus the start of every adapter's group.
+ *
+ *   The per-token LoRA delta for adapter i with A_i (r_i x d_in),
+ *   B_i (d_out x r_i) and scale s_i = alpha_i / r_i (standard LoRA algebra;
+ *   the pages print no formula, so this is the plain reading of the method
+ *   they describe):
+ *     shrink   h_t      = A_i x_t                      (length r_i)
+ *     expand   y_t     += s_i B_i h_t                  (length d_out)
+ *   and its backward pass, i.e. the "four cases" of the packed kernels
+ *   [PLoRA technical summary, gist.science, "2. LoRA Execution Engine",
+ *   Kernelontwerp]:
+ *     dh       dh_t     = s_i B_i^T dy_t               (reduce over d_out)
+ *     dB       dB_i     = s_i sum_{t in i} dy_t h_t^T  (reduce over tokens)
+ *     dA       dA_i     = sum_{t in i} dh_t x_t^T      (reduce over tokens)
+ *     dX       dx_t    += A_i^T dh_t                   (reduce over r_i)
+ *
+ * Layouts (row-major, the same ones the CUDA library documents):
+ *   A_cat  [sum_r, d_in]       A_i occupies rows row_off[i] .. row_off[i]+r_i-1
+ *   B_cat  ragged              B_i is the block [d_out, r_i] starting at
+ *                              element d_out*row_off[i]
+ *   H, dH  [T, r_max]          columns >= r_i of token t are zero
+ *   dA     like A_cat, dB like B_cat
+ * Tokens whose id lies outside [0, N) belong to no adapter: they contribute
+ * nothing, their H/dH rows are zero and their y/dX rows are left unchanged.
+ *
+ * Each function is the per-token (or per-adapter) definition written out as
+ * loops, with no blocking, fusion or reordering; OpenMP only splits the
+ * independent outputs across threads, every sum runs in a fixed order.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static int valid_id(int32_t i, int32_t n) { return i >= 0 && i < n; }
+
+int lora_oracle_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void lora_oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* Stable counting sort of tokens by adapter id.
+ * perm receives the valid tokens grouped by adapter, ascending id, original
+ * order inside a group; seg_start[N+1] the group starts (seg_start[N] is the
+ * number of valid tokens).  Returns the number of tokens with an id outside
+ * [0, N). */
+int64_t lora_oracle_route(int64_t T, int32_t N, const int32_t *ids,
+                          int32_t *perm, int32_t *seg_start)
+{
+    int64_t *count = (int64_t *)calloc((size_t)N, sizeof(int64_t));
+    int64_t *cursor = (int64_t *)calloc((size_t)N, sizeof(int64_t));
+    int64_t bad = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        if (valid_id(ids[t], N)) count[ids[t]] += 1;
+        else bad += 1;
+    }
+    seg_start[0] = 0;
+    for (int32_t i = 0; i < N; ++i) seg_start[i + 1] = seg_start[i] + (int32_t)count[i];
+    for (int32_t i = 0; i < N; ++i) cursor[i] = seg_start[i];
+    for (int64_t t = 0; t < T; ++t) {
+        int32_t i = ids[t];
+        if (!valid_id(i, N)) continue;
+        perm[cursor[i]] = (int32_t)t;
+        cursor[i] += 1;
+    }
+    free(count);
+    free(cursor);
+    return bad;
+}
+
+/* shrink: H[t, k] = sum_j A_i[k, j] * x[t, j] for k < r_i, zero for k >= r_i. */
+void lora_oracle_shrink(int64_t T, int32_t N, int32_t d_in, int32_t r_max,
+                        const int32_t *rank, const int64_t *row_off,
+                        const int32_t *ids, const double *A, const double *x,
+                        double *H)
+{
+    #pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t t = 0; t < T; ++t) {
+        double *h = H + t * r_max;
+        for (int32_t k = 0; k < r_max; ++k) h[k] = 0.0;
+        int32_t i = ids[t];
+        if (!valid_id(i, N)) continue;
+        const double *xt = x + t * (int64_t)d_in;
+        for (int32_t k = 0; k < rank[i]; ++k) {
+            const double *a = A + (row_off[i] + k) * (int64_t)d_in;
+            double acc = 0.0;
+            for (int32_t j = 0; j < d_in; ++j) acc += a[j] * xt[j];
+            h[k] = acc;
+        }
+    }
+}
+
+/* expand: y[t, o] += s_i * sum_k B_i[o, k] * H[t, k]. */
+void lora_oracle_expand(int64_t T, int32_t N, int32_t d_out, int32_t r_max,
+                        const int32_t *rank, const int64_t *row_off,
+                        const double *scale, const int32_t *ids,
+                        const double *B, const double *H, double *y)
+{
+    #pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t t = 0; t < T; ++t) {
+        int32_t i = ids[t];
+        if (!valid_id(i, N)) continue;
+        const int32_t r = rank[i];
+        const double *Bi = B + row_off[i] * (int64_t)d_out;
+        const double *h = H + t * r_max;
+        double *yt = y + t * (int64_t)d_out;
+        for (int32_t o = 0; o < d_out; ++o) {
+            double acc = 0.0;
+            for (int32_t k = 0; k < r; ++k) acc += Bi[(int64_t)o * r + k] * h[k];
+            yt[o] += scale[i] * acc;
+        }
+    }
+}
+
+/* dh: dH[t, k] = s_i * sum_o B_i[o, k] * dY[t, o] for k < r_i, zero beyond. */
+void lora_oracle_dh(int64_t T, int32_t N, int32_t d_out, int32_t r_max,
+                    const int32_t *rank, const int64_t *row_off,
+                    const double *scale, const int32_t *ids, const double *B,
+                    const double *dY, double *dH)
+{
+    #pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t t = 0; t < T; ++t) {
+        double *g = dH + t * r_max;
+        for (int32_t k = 0; k < r_max; ++k) g[k] = 0.0;
+        int32_t i = ids[t];
+        if (!valid_id(i, N)) continue;
+        const int32_t r = rank[i];
+        const double *Bi = B + row_off[i] * (int64_t)d_out;
+        const double *dy = dY + t * (int64_t)d_out;
+        for (int32_t k = 0; k < r; ++k) {
+            double acc = 0.0;
+            for (int32_t o = 0; o < d_out; ++o) acc += Bi[(int64_t)o * r + k] * dy[o];
+            g[k] = scale[i] * acc;
+        }
+    }
+}
+
+/* dB: dB_i[o, k] = s_i * sum_{t : ids[t] = i} dY[t, o] * H[t, k].
+ * Output uses the B_cat layout (sum_r * d_out doubles); adapters without
+ * tokens get zeros. */
+void lora_oracle_db(int64_t T, int32_t N, int32_t d_out, int32_t r_max,
+                    const int32_t *rank, const int64_t *row_off,
+                    const double *scale, const int32_t *ids, const double *dY,
+                    const double *H, double *dB)
+{
+    const int64_t sum_r = row_off[N];
+    #pragma omp parallel
+    {
+        double *acc = (double *)malloc((size_t)sum_r * sizeof(double));
+        #pragma omp for schedule(dynamic, 8)
+        for (int32_t o = 0; o < d_out; ++o) {
+            for (int64_t q = 0; q < sum_r; ++q) acc[q] = 0.0;
+            for (int64_t t = 0; t < T; ++t) {
+                int32_t i = ids[t];
+                if (!valid_id(i, N)) continue;
+                const double g = dY[t * (int64_t)d_out + o];
+                const double *h = H + t * r_max;
+                for (int32_t k = 0; k < rank[i]; ++k) acc[row_off[i] + k] += g * h[k];
+            }
+            for (int32_t i = 0; i < N; ++i) {
+                const int32_t r = rank[i];
+                double *dBi = dB + row_off[i] * (int64_t)d_out;
+                for (int32_t k = 0; k < r; ++k)
+                    dBi[(int64_t)o * r + k] = scale[i] * acc[row_off[i] + k];
+            }
+        }
+        free(acc);
+    }
+}
+
+/* dA: dA_i[k, j] = sum_{t : ids[t] = i} dH[t, k] * X[t, j]  (A_cat layout). */
+void lora_oracle_da(int64_t T, int32_t N, int32_t d_in, int32_t r_max,
+                    const int32_t *rank, const int64_t *row_off,
+                    const int32_t *ids, const double *dH, const double *X,
+                    double *dA)
+{
+    const int64_t sum_r = row_off[N];
+    #pragma omp parallel
+    {
+        double *acc = (double *)malloc((size_t)sum_r * sizeof(double));
+        #pragma omp for schedule(dynamic, 8)
+        for (int32_t j = 0; j < d_in; ++j) {
+            for (int64_t q = 0; q < sum_r; ++q) acc[q] = 0.0;
+            for (int64_t t = 0; t < T; ++t) {
+                int32_t i = ids[t];
+                if (!valid_id(i, N)) continue;
+                const double xv = X[t * (int64_t)d_in + j];
+                const double *g = dH + t * r_max;
+                for (int32_t k = 0; k < rank[i]; ++k) acc[row_off[i] + k] += g[k] * xv;
+            }
+            for (int64_t q = 0; q < sum_r; ++q) dA[q * (int64_t)d_in + j] = acc[q];
+        }
+        free(acc);
+    }
+}
+
+/* dX: dX[t, j] += sum_k A_i[k, j] * dH[t, k]. */
+void lora_oracle_dx(int64_t T, int32_t N, int32_t d_in, int32_t r_max,
+                    const int32_t *rank, const int64_t *row_off,
+                    const int32_t *ids, const double *A, const double *dH,
+                    double *dX)
+{
+    #pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t t = 0; t < T; ++t) {
+        int32_t i = ids[t];
+        if (!valid_id(i, N)) continue;
+        const double *g = dH + t * r_max;
+        double *dx = dX + t * (int64_t)d_in;
+        for (int32_t j = 0; j < d_in; ++j) {
+            double acc = 0.0;
+            for (int32_t k = 0; k < rank[i]; ++k)
+                acc += A[(row_off[i] + k) * (int64_t)d_in + j] * g[k];
+            dx[j] += acc;
+        }
+    }
+}
