@@ -1,0 +1,259 @@
+"""Python binding of ``liblora_sgmv.so``, the GB300 multi-adapter LoRA delta library.
+
+Argument marshalling only: every function here forwards torch tensors' device
+pointers and the current CUDA stream to the C ABI declared in
+``include/lora_sgmv.h`` and raises ``LoraError`` on a non-OK status.  All
+arithmetic runs in the library's CUDA kernels; there is no CPU path.  The
+functions carry the C names:
+
+    lora_build_segments, lora_sgmv_shrink, lora_sgmv_expand,
+    lora_packed_fwd, lora_packed_bwd, lora_query_status, ...
+
+PyTorch provides device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB_PATH, build as build_library  # noqa: F401
+
+__all__ = [
+    "LoraError", "AdapterTable", "Segments", "lib", "lora_abi_version", "lora_status_string",
+    "lora_segments_bytes", "lora_build_segments", "lora_workspace_bytes", "lora_sgmv_shrink",
+    "lora_sgmv_expand", "lora_packed_fwd", "lora_packed_bwd", "lora_query_status", "lora_reset_status",
+    "STATUS",
+]
+
+STATUS = {
+    0: "LORA_OK", 1: "LORA_ERR_INVALID_ARG", 2: "LORA_ERR_SHAPE", 3: "LORA_ERR_ALIGNMENT",
+    4: "LORA_ERR_BAD_ADAPTER_ID", 5: "LORA_ERR_WORKSPACE_TOO_SMALL", 6: "LORA_ERR_UNSUPPORTED",
+    7: "LORA_ERR_TIMEOUT", 8: "LORA_ERR_BAD_TABLE", 9: "LORA_ERR_BAD_SEGMENTS", 10: "LORA_ERR_CUDA",
+}
+
+
+class LoraError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {STATUS.get(self.status, self.status)}")
+
+
+class c_table(ctypes.Structure):
+    _fields_ = [("n_adapters", ctypes.c_int32), ("d_in", ctypes.c_int32), ("d_out", ctypes.c_int32),
+                ("r_max", ctypes.c_int32), ("sum_r", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("rank", ctypes.c_void_p), ("row_off", ctypes.c_void_p), ("scale", ctypes.c_void_p),
+                ("A", ctypes.c_void_p), ("B", ctypes.c_void_p)]
+
+
+class c_segments(ctypes.Structure):
+    _fields_ = [("n_tokens", ctypes.c_int32), ("n_adapters", ctypes.c_int32), ("max_tiles", ctypes.c_int32),
+                ("sorted", ctypes.c_int32), ("perm", ctypes.c_void_p), ("seg_start", ctypes.c_void_p),
+                ("tiles", ctypes.c_void_p), ("n_tiles", ctypes.c_void_p), ("status", ctypes.c_void_p),
+                ("scratch", ctypes.c_void_p), ("scratch_words", ctypes.c_int64)]
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_SZ = ctypes.c_size_t
+
+# name -> (restype, argtypes), mirrors include/lora_sgmv.h
+SIGNATURES = {
+    "lora_abi_version": (_I32, []),
+    "lora_status_string": (ctypes.c_char_p, [_I32]),
+    "lora_segments_bytes": (_SZ, [_I32, _I32]),
+    "lora_build_segments": (_I32, [_P, _P, _I32, _I32, _P, _SZ, ctypes.POINTER(c_segments), _P]),
+    "lora_workspace_bytes": (_SZ, [ctypes.POINTER(c_table), _I32]),
+    "lora_sgmv_shrink": (_I32, [_P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments), _P]),
+    "lora_sgmv_expand": (_I32, [_P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments), _P]),
+    "lora_packed_fwd": (_I32, [_P, _P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments), _P, _SZ, _P]),
+    "lora_packed_bwd": (_I32, [_P, _P, _P, _P, _P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments),
+                               _P, _SZ, _P]),
+    "lora_query_status": (_I32, [ctypes.POINTER(c_segments), _P]),
+    "lora_reset_status": (_I32, [ctypes.POINTER(c_segments), _P]),
+}
+
+
+def lib(path: str | None = None):
+    """Load the CUDA library (it must have been built: ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or os.environ.get("LORA_SGMV_LIB", LIB_PATH)
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build the CUDA library first (python -c "
+                           "'import __graft_entry__ as g; g.build()')")
+    L = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise LoraError(st, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def lora_abi_version() -> int:
+    return int(lib().lora_abi_version())
+
+
+def lora_status_string(st: int) -> str:
+    return lib().lora_status_string(int(st)).decode()
+
+
+def lora_segments_bytes(n_tokens: int, n_adapters: int) -> int:
+    return int(lib().lora_segments_bytes(int(n_tokens), int(n_adapters)))
+
+
+class AdapterTable:
+    """Device-resident stacked adapter table (keeps its tensors alive).
+
+    ``A``: bf16 [sum_r, d_in]; ``B``: bf16 flat, B_i = [d_out, r_i] blocks;
+    ``ranks`` / ``scales``: per-adapter rank and s_i = alpha_i / r_i."""
+
+    def __init__(self, A, B, ranks, scales, d_in: int, d_out: int):
+        import torch
+
+        dev = A.device
+        ranks = [int(r) for r in ranks]
+        self.rank = torch.tensor(ranks, dtype=torch.int32, device=dev)
+        off = [0]
+        for r in ranks:
+            off.append(off[-1] + r)
+        self.row_off = torch.tensor(off, dtype=torch.int32, device=dev)
+        self.scale = torch.as_tensor(scales, dtype=torch.float32).to(dev)
+        self.A = A
+        self.B = B
+        self.ranks = ranks
+        self.d_in, self.d_out = int(d_in), int(d_out)
+        self.c = c_table(len(ranks), self.d_in, self.d_out, max(ranks), off[-1], 0,
+                         self.rank.data_ptr(), self.row_off.data_ptr(), self.scale.data_ptr(),
+                         A.data_ptr(), B.data_ptr())
+
+    @property
+    def n_adapters(self):
+        return self.c.n_adapters
+
+    @property
+    def r_max(self):
+        return self.c.r_max
+
+    @property
+    def sum_r(self):
+        return self.c.sum_r
+
+
+class Segments:
+    """Routing metadata of one batch; owns its device storage."""
+
+    def __init__(self, storage, c: c_segments):
+        self.storage = storage
+        self.c = c
+
+    def _i32(self, attr, n):
+        import torch
+
+        base = self.storage.data_ptr()
+        off = (getattr(self.c, attr) - base) // 4
+        return self.storage.view(torch.int32)[off:off + n]
+
+    @property
+    def perm(self):
+        return self._i32("perm", self.c.n_tokens)
+
+    @property
+    def seg_start(self):
+        return self._i32("seg_start", self.c.n_adapters + 1)
+
+    @property
+    def n_tiles(self):
+        return self._i32("n_tiles", 1)
+
+    @property
+    def tiles(self):
+        return self._i32("tiles", 4 * self.c.max_tiles).view(-1, 4)
+
+
+def lora_build_segments(ids=None, seg_offsets=None, n_tokens=None, n_adapters=None, device=None,
+                        stream=None, storage=None) -> Segments:
+    """Build routing metadata from per-token ``ids`` (int32 [T], any order) or
+    sorted ``seg_offsets`` (int32 [N+1])."""
+    import torch
+
+    src = ids if ids is not None else seg_offsets
+    if n_tokens is None:
+        n_tokens = int(ids.numel()) if ids is not None else int(seg_offsets[-1].item())
+    if device is None:
+        device = src.device if src is not None else torch.device("cuda")
+    nbytes = lora_segments_bytes(n_tokens, n_adapters)
+    if nbytes == 0:
+        raise LoraError(2, "lora_segments_bytes")
+    if storage is None:
+        storage = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    c = c_segments()
+    st = lib().lora_build_segments(_ptr(ids), _ptr(seg_offsets), int(n_tokens), int(n_adapters),
+                                   _ptr(storage), storage.numel(), ctypes.byref(c), _stream(stream))
+    _check(st, "lora_build_segments")
+    return Segments(storage, c)
+
+
+def lora_workspace_bytes(table: AdapterTable, n_tokens: int) -> int:
+    return int(lib().lora_workspace_bytes(ctypes.byref(table.c), int(n_tokens)))
+
+
+def workspace(table: AdapterTable, n_tokens: int, device=None):
+    import torch
+
+    n = lora_workspace_bytes(table, n_tokens)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or table.A.device)
+
+
+def lora_sgmv_shrink(H, x, table: AdapterTable, segs: Segments, stream=None):
+    _check(lib().lora_sgmv_shrink(_ptr(H), _ptr(x), ctypes.byref(table.c), ctypes.byref(segs.c),
+                                  _stream(stream)), "lora_sgmv_shrink")
+    return H
+
+
+def lora_sgmv_expand(y, H, table: AdapterTable, segs: Segments, stream=None):
+    _check(lib().lora_sgmv_expand(_ptr(y), _ptr(H), ctypes.byref(table.c), ctypes.byref(segs.c),
+                                  _stream(stream)), "lora_sgmv_expand")
+    return y
+
+
+def lora_packed_fwd(y, H_save, x, table: AdapterTable, segs: Segments, ws=None, stream=None):
+    wsb = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().lora_packed_fwd(_ptr(y), _ptr(H_save), _ptr(x), ctypes.byref(table.c), ctypes.byref(segs.c),
+                                 _ptr(ws), wsb, _stream(stream)), "lora_packed_fwd")
+    return y
+
+
+def lora_packed_bwd(dX, dA, dB, dY, X, H_saved, table: AdapterTable, segs: Segments, ws, stream=None):
+    wsb = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().lora_packed_bwd(_ptr(dX), _ptr(dA), _ptr(dB), _ptr(dY), _ptr(X), _ptr(H_saved),
+                                 ctypes.byref(table.c), ctypes.byref(segs.c), _ptr(ws), wsb, _stream(stream)),
+           "lora_packed_bwd")
+
+
+def lora_query_status(segs: Segments, stream=None) -> int:
+    return int(lib().lora_query_status(ctypes.byref(segs.c), _stream(stream)))
+
+
+def lora_reset_status(segs: Segments, stream=None):
+    _check(lib().lora_reset_status(ctypes.byref(segs.c), _stream(stream)), "lora_reset_status")

@@ -1,0 +1,210 @@
+// lora_sgmv.cu -- the C ABI: argument checks, workspace layout and dispatch.
+//
+// Every entry point validates its arguments on the host before touching the
+// GPU, then enqueues its kernels on the caller's stream.  Nothing here
+// allocates, frees or synchronises (lora_query_status excepted).
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+#include "dispatch.h"
+
+using namespace lora;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+lora_status_t check_table(const lora_adapter_table *t)
+{
+    if (t == nullptr) return LORA_ERR_INVALID_ARG;
+    if (t->rank == nullptr || t->row_off == nullptr || t->scale == nullptr || t->A == nullptr ||
+        t->B == nullptr)
+        return LORA_ERR_INVALID_ARG;
+    if (t->n_adapters < 1 || t->n_adapters > kMaxAdapters) return LORA_ERR_SHAPE;
+    if (t->d_in < 8 || t->d_in > kMaxDim || (t->d_in % 8) != 0) return LORA_ERR_SHAPE;
+    if (t->d_out < 8 || t->d_out > kMaxDim || (t->d_out % 8) != 0) return LORA_ERR_SHAPE;
+    if (t->r_max < 1 || t->r_max > LORA_MAX_RANK) return LORA_ERR_SHAPE;
+    if (t->sum_r < t->r_max || (int64_t)t->sum_r > (int64_t)t->n_adapters * t->r_max) return LORA_ERR_SHAPE;
+    if (!aligned16(t->A) || !aligned16(t->B) || !aligned4(t->rank) || !aligned4(t->row_off) ||
+        !aligned4(t->scale))
+        return LORA_ERR_ALIGNMENT;
+    return LORA_OK;
+}
+
+lora_status_t check_segs(const lora_segments *s, const lora_adapter_table *t)
+{
+    if (s == nullptr) return LORA_ERR_INVALID_ARG;
+    if (s->perm == nullptr || s->seg_start == nullptr || s->tiles == nullptr || s->n_tiles == nullptr ||
+        s->status == nullptr)
+        return LORA_ERR_INVALID_ARG;
+    if (s->n_tokens < 0 || s->n_tokens > kMaxTokens || s->max_tiles < 0) return LORA_ERR_SHAPE;
+    if (t != nullptr && s->n_adapters != t->n_adapters) return LORA_ERR_SHAPE;
+    return LORA_OK;
+}
+
+lora_status_t check_device()
+{
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LORA_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return LORA_ERR_CUDA;
+    if (major != 10 || minor != 3) return LORA_ERR_UNSUPPORTED;  // built for sm_103a only
+    return LORA_OK;
+}
+
+// workspace: [H: T x r_max fp32][dH: T x r_max fp32], 256-byte aligned regions
+size_t region_bytes(int64_t T, int32_t r_max) { return (size_t)(((T * r_max * 4) + 255) & ~int64_t(255)); }
+
+size_t workspace_bytes(const lora_adapter_table *t, int32_t T) { return 2 * region_bytes(T, t->r_max); }
+
+#define LORA_TRY(expr)                          \
+    do {                                        \
+        lora_status_t _st = (expr);             \
+        if (_st != LORA_OK) return _st;         \
+    } while (0)
+
+}  // namespace
+
+extern "C" {
+
+int32_t lora_abi_version(void) { return LORA_SGMV_ABI_VERSION; }
+
+const char *lora_status_string(lora_status_t s)
+{
+    switch (s) {
+    case LORA_OK: return "LORA_OK";
+    case LORA_ERR_INVALID_ARG: return "LORA_ERR_INVALID_ARG";
+    case LORA_ERR_SHAPE: return "LORA_ERR_SHAPE";
+    case LORA_ERR_ALIGNMENT: return "LORA_ERR_ALIGNMENT";
+    case LORA_ERR_BAD_ADAPTER_ID: return "LORA_ERR_BAD_ADAPTER_ID";
+    case LORA_ERR_WORKSPACE_TOO_SMALL: return "LORA_ERR_WORKSPACE_TOO_SMALL";
+    case LORA_ERR_UNSUPPORTED: return "LORA_ERR_UNSUPPORTED";
+    case LORA_ERR_TIMEOUT: return "LORA_ERR_TIMEOUT";
+    case LORA_ERR_BAD_TABLE: return "LORA_ERR_BAD_TABLE";
+    case LORA_ERR_BAD_SEGMENTS: return "LORA_ERR_BAD_SEGMENTS";
+    case LORA_ERR_CUDA: return "LORA_ERR_CUDA";
+    }
+    return "LORA_ERR_UNKNOWN";
+}
+
+size_t lora_segments_bytes(int32_t n_tokens, int32_t n_adapters)
+{
+    const SegLayout L = seg_layout(n_tokens, n_adapters);
+    return L.ok ? (size_t)L.total_words * 4 : 0;
+}
+
+lora_status_t lora_build_segments(const int32_t *ids, const int32_t *seg_offsets, int32_t n_tokens,
+                                  int32_t n_adapters, void *storage, size_t storage_bytes,
+                                  lora_segments *out, lora_stream_t stream)
+{
+    if (out == nullptr || storage == nullptr) return LORA_ERR_INVALID_ARG;
+    if (n_tokens < 0 || n_adapters < 1) return LORA_ERR_SHAPE;
+    if ((ids == nullptr) == (seg_offsets == nullptr) && !(n_tokens == 0 && seg_offsets == nullptr))
+        return LORA_ERR_INVALID_ARG;
+    if (!aligned16(storage) || (ids && !aligned4(ids)) || (seg_offsets && !aligned4(seg_offsets)))
+        return LORA_ERR_ALIGNMENT;
+    const SegLayout L = seg_layout(n_tokens, n_adapters);
+    if (!L.ok) return LORA_ERR_SHAPE;
+    if ((size_t)L.total_words * 4 > storage_bytes) return LORA_ERR_WORKSPACE_TOO_SMALL;
+    LORA_TRY(check_device());
+    return build_segments(ids, seg_offsets, n_tokens, n_adapters, storage, storage_bytes, out,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t lora_workspace_bytes(const lora_adapter_table *table, int32_t n_tokens)
+{
+    if (check_table(table) != LORA_OK || n_tokens < 0 || n_tokens > kMaxTokens) return 0;
+    return workspace_bytes(table, n_tokens);
+}
+
+lora_status_t lora_sgmv_shrink(float *H, const void *x, const lora_adapter_table *table,
+                               const lora_segments *segs, lora_stream_t stream)
+{
+    LORA_TRY(check_table(table));
+    LORA_TRY(check_segs(segs, table));
+    if (H == nullptr || x == nullptr) return LORA_ERR_INVALID_ARG;
+    if (!aligned16(H) || !aligned16(x)) return LORA_ERR_ALIGNMENT;
+    LORA_TRY(check_device());
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return run_shrink(H, x, *table, *segs, st);
+}
+
+lora_status_t lora_sgmv_expand(void *y, const float *H, const lora_adapter_table *table,
+                               const lora_segments *segs, lora_stream_t stream)
+{
+    LORA_TRY(check_table(table));
+    LORA_TRY(check_segs(segs, table));
+    if (H == nullptr || y == nullptr) return LORA_ERR_INVALID_ARG;
+    if (!aligned16(H) || !aligned16(y)) return LORA_ERR_ALIGNMENT;
+    LORA_TRY(check_device());
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return run_expand(y, H, *table, *segs, st);
+}
+
+lora_status_t lora_packed_fwd(void *y, float *H_save, const void *x, const lora_adapter_table *table,
+                              const lora_segments *segs, void *ws, size_t ws_bytes, lora_stream_t stream)
+{
+    LORA_TRY(check_table(table));
+    LORA_TRY(check_segs(segs, table));
+    if (y == nullptr || x == nullptr) return LORA_ERR_INVALID_ARG;
+    if (!aligned16(y) || !aligned16(x) || (H_save && !aligned16(H_save)) || (ws && !aligned16(ws)))
+        return LORA_ERR_ALIGNMENT;
+    const int32_t T = segs->n_tokens;
+    float *H = H_save;
+    if (H == nullptr) {
+        if (ws == nullptr || ws_bytes < region_bytes(T, table->r_max)) return LORA_ERR_WORKSPACE_TOO_SMALL;
+        H = static_cast<float *>(ws);
+    }
+    LORA_TRY(check_device());
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return run_fwd(y, H, x, *table, *segs, st);
+}
+
+lora_status_t lora_packed_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X,
+                              const float *H_saved, const lora_adapter_table *table,
+                              const lora_segments *segs, void *ws, size_t ws_bytes, lora_stream_t stream)
+{
+    LORA_TRY(check_table(table));
+    LORA_TRY(check_segs(segs, table));
+    if (dY == nullptr || X == nullptr) return LORA_ERR_INVALID_ARG;
+    if (!aligned16(dY) || !aligned16(X) || (dX && !aligned16(dX)) || (dA && !aligned16(dA)) ||
+        (dB && !aligned16(dB)) || (H_saved && !aligned16(H_saved)) || (ws && !aligned16(ws)))
+        return LORA_ERR_ALIGNMENT;
+    const int32_t T = segs->n_tokens;
+    if (ws == nullptr || ws_bytes < workspace_bytes(table, T)) return LORA_ERR_WORKSPACE_TOO_SMALL;
+    LORA_TRY(check_device());
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float *wsH = static_cast<float *>(ws);
+    float *wsdH = reinterpret_cast<float *>(static_cast<char *>(ws) + region_bytes(T, table->r_max));
+    const float *H = H_saved;
+    if (H == nullptr) {
+        LORA_TRY(run_shrink(wsH, X, *table, *segs, st));
+        H = wsH;
+    }
+    return run_bwd(dX, dA, dB, dY, X, H, wsdH, *table, *segs, st);
+}
+
+lora_status_t lora_query_status(const lora_segments *segs, lora_stream_t stream)
+{
+    if (segs == nullptr || segs->status == nullptr) return LORA_ERR_INVALID_ARG;
+    int32_t h = 0;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&h, segs->status, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return LORA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return LORA_ERR_CUDA;
+    return static_cast<lora_status_t>(h);
+}
+
+lora_status_t lora_reset_status(const lora_segments *segs, lora_stream_t stream)
+{
+    if (segs == nullptr || segs->status == nullptr) return LORA_ERR_INVALID_ARG;
+    if (cudaMemsetAsync(segs->status, 0, sizeof(int32_t), reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return LORA_ERR_CUDA;
+    return LORA_OK;
+}
+
+}  // extern "C"

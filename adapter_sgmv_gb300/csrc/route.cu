@@ -1,0 +1,287 @@
+// route.cu -- segment-metadata builder: group a mixed-adapter batch by adapter.
+//
+// A decode or training batch mixes tokens of many adapters (C-LoRA report,
+// "Come funziona l'architettura"); the packed kernels want every adapter's
+// tokens together so that one tile reads one adapter's weights (PLoRA
+// technical summary, "2. LoRA Execution Engine").  This file builds, on the
+// device and without a host round trip:
+//   perm       the stable grouping of token indices by adapter id,
+//   seg_start  each adapter's start in perm,
+//   tiles      work tiles of at most LORA_TILE_M rows that never straddle adapters.
+//
+// Unsorted ids: a stable counting sort in warp-sized chunks.  Chunk c holds
+// tokens 32c .. 32c+31; hist[i][c] counts the tokens of adapter i in chunk c.
+// An exclusive scan of hist in adapter-major order gives, for every (i, c),
+// the first perm slot of adapter i's tokens of chunk c, and a token's rank
+// inside its chunk is the number of lower lanes with the same id
+// (__match_any_sync).  All of it is integer work and is bit-exact.
+#include "common.cuh"
+#include "internal.h"
+
+namespace lora {
+
+constexpr int kScanThreads = 1024;
+constexpr int kScanPerThread = 4;
+constexpr int kScanBlock = kScanThreads * kScanPerThread;
+
+// Block-wide exclusive scan of one value per thread (blockDim.x == 1024).
+// Returns the exclusive prefix; *block_total receives the block's sum.
+__device__ int32_t block_exclusive_scan(int32_t v, int32_t *block_total)
+{
+    __shared__ int32_t warp_sums[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t x = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        int32_t y = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int32_t w = warp_sums[lane];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            int32_t y = __shfl_up_sync(0xffffffffu, w, d);
+            if (lane >= d) w += y;
+        }
+        warp_sums[lane] = w;  // inclusive
+    }
+    __syncthreads();
+    int32_t excl = x - v + (warp > 0 ? warp_sums[warp - 1] : 0);
+    int32_t total = warp_sums[31];
+    __syncthreads();  // warp_sums may be reused by the caller's next scan
+    *block_total = total;
+    return excl;
+}
+
+// ---------------------------------------------------------------- unsorted ids
+__global__ void route_hist_kernel(const int32_t *__restrict__ ids, int32_t T, int32_t N,
+                                  int32_t n_chunks, int32_t *__restrict__ hist,
+                                  int32_t *__restrict__ status)
+{
+    const int32_t chunk = (int32_t)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (chunk >= n_chunks) return;  // whole warps exit together
+    const int64_t t = (int64_t)chunk * 32 + lane;
+    int32_t id = -1;
+    if (t < T) {
+        id = ids[t];
+        if (id < 0 || id >= N) {
+            set_status(status, LORA_ERR_BAD_ADAPTER_ID);
+            id = -1;
+        }
+    }
+    const uint32_t same = __match_any_sync(0xffffffffu, id);
+    if (id >= 0 && lane == __ffs(same) - 1) hist[(int64_t)id * n_chunks + chunk] = __popc(same);
+}
+
+__global__ void route_scatter_kernel(const int32_t *__restrict__ ids, int32_t T, int32_t N,
+                                     int32_t n_chunks, const int32_t *__restrict__ offs,
+                                     int32_t *__restrict__ perm)
+{
+    const int32_t chunk = (int32_t)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (chunk >= n_chunks) return;
+    const int64_t t = (int64_t)chunk * 32 + lane;
+    int32_t id = -1;
+    if (t < T) {
+        id = ids[t];
+        if (id < 0 || id >= N) id = -1;
+    }
+    const uint32_t same = __match_any_sync(0xffffffffu, id);
+    if (id >= 0) {
+        const int32_t rank = __popc(same & ((1u << lane) - 1u));
+        perm[offs[(int64_t)id * n_chunks + chunk] + rank] = (int32_t)t;
+    }
+}
+
+// exclusive scan of data[0..M) in place: reduce / top / apply
+__global__ void scan_reduce_kernel(const int32_t *__restrict__ data, int64_t M,
+                                   int32_t *__restrict__ block_sums)
+{
+    const int64_t base = (int64_t)blockIdx.x * kScanBlock + (int64_t)threadIdx.x * kScanPerThread;
+    int32_t s = 0;
+#pragma unroll
+    for (int q = 0; q < kScanPerThread; ++q)
+        if (base + q < M) s += data[base + q];
+    int32_t total;
+    block_exclusive_scan(s, &total);
+    if (threadIdx.x == 0) block_sums[blockIdx.x] = total;
+}
+
+__global__ void scan_top_kernel(int32_t *__restrict__ block_sums, int32_t nb,
+                                int32_t *__restrict__ total_out)
+{
+    int32_t carry = 0;
+    for (int32_t b0 = 0; b0 < nb; b0 += kScanThreads) {
+        const int32_t b = b0 + threadIdx.x;
+        const int32_t v = b < nb ? block_sums[b] : 0;
+        int32_t tot;
+        const int32_t e = block_exclusive_scan(v, &tot);
+        if (b < nb) block_sums[b] = carry + e;
+        carry += tot;
+    }
+    if (threadIdx.x == 0) *total_out = carry;
+}
+
+__global__ void scan_apply_kernel(int32_t *__restrict__ data, int64_t M,
+                                  const int32_t *__restrict__ block_sums)
+{
+    const int64_t base = (int64_t)blockIdx.x * kScanBlock + (int64_t)threadIdx.x * kScanPerThread;
+    int32_t v[kScanPerThread];
+    int32_t s = 0;
+#pragma unroll
+    for (int q = 0; q < kScanPerThread; ++q) {
+        v[q] = base + q < M ? data[base + q] : 0;
+        s += v[q];
+    }
+    int32_t total;
+    int32_t e = block_exclusive_scan(s, &total) + block_sums[blockIdx.x];
+#pragma unroll
+    for (int q = 0; q < kScanPerThread; ++q) {
+        if (base + q < M) data[base + q] = e;
+        e += v[q];
+    }
+}
+
+// ---------------------------------------------------------------- sorted input
+__global__ void route_sorted_kernel(const int32_t *__restrict__ seg_offsets, int32_t T, int32_t N,
+                                    int32_t *__restrict__ perm, int32_t *__restrict__ seg_start,
+                                    int32_t *__restrict__ status)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < T; t += stride)
+        perm[t] = (int32_t)t;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i <= N; i += stride) {
+        const int32_t v = seg_offsets[i];
+        seg_start[i] = v;
+        bool bad = (i == 0 && v != 0) || (i == N && v != T) || v < 0 || v > T;
+        if (i < N && seg_offsets[i + 1] < v) bad = true;
+        if (bad) set_status(status, LORA_ERR_BAD_SEGMENTS);
+    }
+}
+
+// ---------------------------------------------------------------- tiles
+// One block: seg_start (from the scan, when unsorted), tile counts, their
+// scan, and the tile records.  Inconsistent segments yield no tiles.
+__global__ void route_tiles_kernel(const int32_t *__restrict__ offs, int32_t n_chunks,
+                                   const int32_t *__restrict__ total, int32_t *__restrict__ seg_start,
+                                   int32_t N, const int32_t *__restrict__ perm,
+                                   int32_t *__restrict__ tiles, int32_t *__restrict__ n_tiles,
+                                   int32_t max_tiles, int32_t *__restrict__ status)
+{
+    if (offs != nullptr) {  // unsorted: seg_start[i] = offs[i][0], seg_start[N] = total
+        for (int32_t i = threadIdx.x; i <= N; i += blockDim.x)
+            seg_start[i] = i < N ? offs[(int64_t)i * n_chunks] : *total;
+        __syncthreads();
+    }
+    if (*status == LORA_ERR_BAD_SEGMENTS) {
+        for (int32_t i = threadIdx.x; i <= N; i += blockDim.x) seg_start[i] = 0;
+        if (threadIdx.x == 0) *n_tiles = 0;
+        return;
+    }
+    int32_t carry = 0;
+    for (int32_t i0 = 0; i0 < N; i0 += blockDim.x) {
+        const int32_t i = i0 + threadIdx.x;
+        int32_t begin = 0, n = 0;
+        if (i < N) {
+            begin = seg_start[i];
+            n = seg_start[i + 1] - begin;
+        }
+        const int32_t cnt = n > 0 ? (n + LORA_TILE_M - 1) / LORA_TILE_M : 0;
+        int32_t tot;
+        const int32_t base = carry + block_exclusive_scan(cnt, &tot);
+        for (int32_t q = 0; q < cnt && base + q < max_tiles; ++q) {
+            const int32_t b = begin + q * LORA_TILE_M;
+            const int32_t rows = min(LORA_TILE_M, n - q * LORA_TILE_M);
+            const int32_t contiguous = (perm[b + rows - 1] - perm[b] == rows - 1) ? 1 : 0;
+            reinterpret_cast<int4 *>(tiles)[base + q] = make_int4(i, b, rows, contiguous);
+        }
+        carry += tot;
+    }
+    if (threadIdx.x == 0) *n_tiles = min(carry, max_tiles);
+}
+
+// ---------------------------------------------------------------- host side
+SegLayout seg_layout(int32_t T, int32_t N)
+{
+    SegLayout L{};
+    if (T < 0 || N < 1 || N > kMaxAdapters || T > kMaxTokens) return L;
+    auto up = [](int64_t words) { return (words + 63) & ~int64_t(63); };  // 256-byte regions
+    L.n_chunks = (T + 31) / 32;
+    L.max_tiles = T / LORA_TILE_M + N + 1;
+    L.hist_words = (int64_t)N * L.n_chunks;
+    if (L.hist_words > kMaxHistWords) return L;
+    L.block_sums = (int32_t)((L.hist_words + kScanBlock - 1) / kScanBlock);
+    int64_t o = 0;
+    L.off_perm = o;       o += up(T > 0 ? T : 1);
+    L.off_seg = o;        o += up(N + 1);
+    L.off_tiles = o;      o += up(4 * (int64_t)L.max_tiles);
+    L.off_ntiles = o;     o += up(1);
+    L.off_status = o;     o += up(1);
+    L.off_scratch = o;
+    L.scratch_words = up(L.hist_words) + up(L.block_sums) + up(1);
+    o += L.scratch_words;
+    L.total_words = o;
+    L.ok = true;
+    return L;
+}
+
+lora_status_t build_segments(const int32_t *ids, const int32_t *seg_offsets, int32_t T, int32_t N,
+                             void *storage, size_t storage_bytes, lora_segments *out,
+                             cudaStream_t stream)
+{
+    const SegLayout L = seg_layout(T, N);
+    if (!L.ok) return LORA_ERR_SHAPE;
+    if ((size_t)L.total_words * 4 > storage_bytes) return LORA_ERR_WORKSPACE_TOO_SMALL;
+    int32_t *w = static_cast<int32_t *>(storage);
+    lora_segments s{};
+    s.n_tokens = T;
+    s.n_adapters = N;
+    s.max_tiles = L.max_tiles;
+    s.sorted = seg_offsets != nullptr ? 1 : 0;
+    s.perm = w + L.off_perm;
+    s.seg_start = w + L.off_seg;
+    s.tiles = w + L.off_tiles;
+    s.n_tiles = w + L.off_ntiles;
+    s.status = w + L.off_status;
+    s.scratch = w + L.off_scratch;
+    s.scratch_words = L.scratch_words;
+
+    if (cudaMemsetAsync(s.status, 0, 4, stream) != cudaSuccess) return LORA_ERR_CUDA;
+    if (seg_offsets != nullptr) {
+        const int threads = 256;
+        const int64_t work = (int64_t)(T > N + 1 ? T : N + 1);
+        const int blocks = (int)((work + threads - 1) / threads < 1184 ? (work + threads - 1) / threads : 1184);
+        route_sorted_kernel<<<blocks > 0 ? blocks : 1, threads, 0, stream>>>(seg_offsets, T, N, s.perm,
+                                                                              s.seg_start, s.status);
+        route_tiles_kernel<<<1, 1024, 0, stream>>>(nullptr, 0, nullptr, s.seg_start, N, s.perm, s.tiles,
+                                                   s.n_tiles, s.max_tiles, s.status);
+    } else {
+        int32_t *hist = s.scratch;
+        int32_t *bsum = hist + ((L.hist_words + 63) & ~int64_t(63));
+        int32_t *total = bsum + ((L.block_sums + 63) & ~int64_t(63));
+        if (L.hist_words > 0) {
+            if (cudaMemsetAsync(hist, 0, (size_t)L.hist_words * 4, stream) != cudaSuccess) return LORA_ERR_CUDA;
+            const int threads = 256;
+            const int blocks = (int)(((int64_t)L.n_chunks * 32 + threads - 1) / threads);
+            route_hist_kernel<<<blocks, threads, 0, stream>>>(ids, T, N, L.n_chunks, hist, s.status);
+            scan_reduce_kernel<<<L.block_sums, kScanThreads, 0, stream>>>(hist, L.hist_words, bsum);
+            scan_top_kernel<<<1, kScanThreads, 0, stream>>>(bsum, L.block_sums, total);
+            scan_apply_kernel<<<L.block_sums, kScanThreads, 0, stream>>>(hist, L.hist_words, bsum);
+            route_scatter_kernel<<<blocks, threads, 0, stream>>>(ids, T, N, L.n_chunks, hist, s.perm);
+            route_tiles_kernel<<<1, 1024, 0, stream>>>(hist, L.n_chunks, total, s.seg_start, N, s.perm,
+                                                       s.tiles, s.n_tiles, s.max_tiles, s.status);
+        } else {  // empty batch: every group empty, no tiles
+            if (cudaMemsetAsync(s.seg_start, 0, (size_t)(N + 1) * 4, stream) != cudaSuccess ||
+                cudaMemsetAsync(s.n_tiles, 0, 4, stream) != cudaSuccess)
+                return LORA_ERR_CUDA;
+        }
+    }
+    if (cudaGetLastError() != cudaSuccess) return LORA_ERR_CUDA;
+    *out = s;
+    return LORA_OK;
+}
+
+}  // namespace lora

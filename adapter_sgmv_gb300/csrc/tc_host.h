@@ -1,0 +1,23 @@
+// tc_host.h -- host helpers and launchers of the tensor-core kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lora_sgmv.h"
+
+namespace lora {
+
+// Row-major bf16 matrix [rows, cols] as a 2-D TMA tensor, box [box_rows, box_cols].
+bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                       uint32_t box_rows, bool swizzle128);
+int sm_count();
+
+// case i: out[t, k] = c * sum_j act[t, j] W(k, j)   (shrink: W = A_i, c = 1; dh: W = B_i^T, c = s_i)
+lora_status_t tc_shrink(float *H, const void *x, const lora_adapter_table &tab, const lora_segments &segs,
+                        cudaStream_t stream);
+lora_status_t tc_dh(float *dH, const void *dY, const lora_adapter_table &tab, const lora_segments &segs,
+                    cudaStream_t stream);
+
+}  // namespace lora

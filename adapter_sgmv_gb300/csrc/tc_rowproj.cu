@@ -1,0 +1,337 @@
+// tc_rowproj.cu -- case i on the 5th-generation tensor cores: a reduction over
+// the hidden dimension into a T x r result, tiled along tokens (PLoRA
+// technical summary, "2. LoRA Execution Engine": tile the concatenated LoRA
+// tensors along the sequence or hidden dimension, never along the rank).
+//
+//   shrink  H[t, k]  = sum_j x[t, j]  A_i[k, j]          (c = 1)
+//   dh      dH[t, k] = s_i sum_o dY[t, o] B_i[o, k]       (c = s_i)
+//
+// One work tile = up to 128 tokens of one adapter.  Per 64-wide slice of the
+// hidden dimension a stage holds the 128 x 64 activation block (K-major,
+// 128-byte swizzle, by TMA when the rows are consecutive tokens, else
+// gathered with cp.async) and the r_pad x 64 weight block (shrink: A_i rows by
+// TMA; dh: B_i rows by cp.async into the interleaved MN-major layout).  One
+// thread issues tcgen05.mma (M = 128, N = r_pad, K = 16) into a TMEM
+// accumulator; four epilogue warps read it back and write fp32 rows.
+//
+// Warp roles (192 threads): 0 loads, 1 issues MMAs and owns TMEM, 2..5 epilogue.
+// Pipelines: kStages smem stages (full / empty mbarriers), two TMEM
+// accumulators (tfull / tempty).  Every wait is bounded (tc::mbar_wait).
+#include "internal.h"
+#include "tc_common.cuh"
+#include "tc_host.h"
+
+namespace lora {
+namespace {
+
+using namespace tc;
+
+constexpr int kStages = 6;
+constexpr int kLag = 3;            // cp.async groups kept in flight per producer lane
+constexpr int kThreads = 192;
+constexpr uint32_t kActBytes = 128 * 64 * 2;     // one stage of activations
+constexpr uint32_t kWBytes = LORA_MAX_RANK * 64 * 2;
+constexpr uint32_t kStageBytes = kActBytes + kWBytes;
+constexpr uint32_t kTmemCols = 256;  // two accumulators of up to 128 columns
+constexpr size_t kSmemBytes = 1024 + kStages * (size_t)kStageBytes + 256;
+
+struct Smem {
+    uint8_t *act, *w;
+    uint64_t *full, *empty, *tfull, *tempty, *done;
+    uint32_t *tmem_holder;
+    volatile int32_t *abort;
+};
+
+LORA_DEV Smem carve(uint8_t *raw)
+{
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    Smem s;
+    s.act = base;
+    s.w = base + kStages * kActBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + kStages * kStageBytes);
+    s.full = bars;
+    s.empty = bars + kStages;
+    s.tfull = bars + 2 * kStages;
+    s.tempty = s.tfull + 2;
+    s.done = s.tempty + 2;
+    s.tmem_holder = reinterpret_cast<uint32_t *>(s.done + 1);
+    s.abort = reinterpret_cast<volatile int32_t *>(s.tmem_holder + 1);
+    return s;
+}
+
+LORA_DEV int32_t rpad16(int32_t r) { return (r + 15) & ~15; }
+
+template <bool kDH>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_w,
+                  float *__restrict__ out, const uint16_t *__restrict__ act, lora_adapter_table tab,
+                  lora_segments segs)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const Smem S = carve(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&S.full[i], 33);  // lane 0's expect-tx arrive + one per producer lane
+            mbar_init(&S.empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&S.tfull[i], 1);
+            mbar_init(&S.tempty[i], 4);
+        }
+        mbar_init(S.done, 1);
+        *S.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(S.tmem_holder, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *S.tmem_holder;
+    const int32_t n_tiles = *segs.n_tiles;
+    const int32_t d = kDH ? tab.d_out : tab.d_in;
+    const int32_t nk = (d + 63) / 64;
+    const uint16_t *Bw = static_cast<const uint16_t *>(tab.B);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tensormap(&map_act);
+            if (!kDH) prefetch_tensormap(&map_w);
+        }
+        uint32_t g = 0;
+        bool ok = true;
+        for (int32_t ti = blockIdx.x; ti < n_tiles && ok; ti += gridDim.x) {
+            const Tile T = load_tile(segs.tiles, ti);
+            const AdapterInfo ad = load_adapter(tab, T.adapter, segs.status);
+            if (!ad.ok) continue;
+            const int32_t r = ad.rank, rp = rpad16(r);
+            const bool contiguous = (T.flags & 1) != 0;
+            const int32_t t0 = segs.perm[T.begin];
+            int32_t tok[32];  // rows (lane >> 3) + 4 q of a gathered tile
+            if (!contiguous) {
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    const int m = (lane >> 3) + 4 * q;
+                    tok[q] = m < T.rows ? segs.perm[T.begin + m] : -1;
+                }
+            }
+            for (int32_t kb = 0; kb < nk; ++kb) {
+                const uint32_t s = g % kStages, ph = (g / kStages) & 1u;
+                if (!mbar_wait(&S.empty[s], ph ^ 1u, S.abort, segs.status)) {
+                    ok = false;
+                    break;
+                }
+                const int32_t j0 = kb * 64;
+                uint8_t *act_s = S.act + s * kActBytes;
+                uint8_t *w_s = S.w + s * kWBytes;
+                if (lane == 0) {
+                    const uint32_t bytes = (contiguous ? kActBytes : 0u) + (kDH ? 0u : (uint32_t)rp * 128u);
+                    mbar_arrive_expect_tx(&S.full[s], bytes);
+                    if (contiguous) tma_load_2d(act_s, &map_act, &S.full[s], j0, t0);
+                    if (!kDH)
+                        for (int q = 0; q < rp / 16; ++q)
+                            tma_load_2d(w_s + q * 2048, &map_w, &S.full[s], j0, ad.row_off + 16 * q);
+                }
+                if (!contiguous) {
+                    const int c = lane & 7;
+                    const bool cin = j0 + 8 * c < d;
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        const int m = (lane >> 3) + 4 * q;
+                        const bool v = tok[q] >= 0 && cin;
+                        const uint16_t *src = v ? act + (int64_t)tok[q] * d + j0 + 8 * c : act;
+                        cp_async_16(act_s + sw128_offset(m, c), src, v);
+                    }
+                }
+                if (kDH) {
+                    // B_i rows o = j0 .. j0+63 as the MN-major operand (N = k, K = o):
+                    // 16-byte chunk (o, k/8) -> (k/8) * 1024 + (o/8) * 128 + (o%8) * 16
+                    const uint16_t *Bi = Bw + (int64_t)ad.row_off * d;
+                    const int nchunks = 64 * (rp / 8);
+                    for (int e = lane; e < nchunks; e += 32) {
+                        const int o = e & 63, c = e >> 6;
+                        const bool v = (j0 + o < d) && (8 * c < r);
+                        uint8_t *dst = w_s + c * 1024 + (o >> 3) * 128 + (o & 7) * 16;
+                        if ((r & 7) == 0) {
+                            const uint16_t *src = v ? Bi + (int64_t)(j0 + o) * r + 8 * c : Bw;
+                            cp_async_16(dst, src, v);
+                        } else {  // rows not 16-byte aligned: element by element
+                            uint32_t wv[4];
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                const int k0 = 8 * c + 2 * h;
+                                const uint16_t lo = (v && k0 < r) ? Bi[(int64_t)(j0 + o) * r + k0] : 0;
+                                const uint16_t hi = (v && k0 + 1 < r) ? Bi[(int64_t)(j0 + o) * r + k0 + 1] : 0;
+                                wv[h] = (uint32_t)lo | ((uint32_t)hi << 16);
+                            }
+                            *reinterpret_cast<uint4 *>(dst) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                        }
+                    }
+                }
+                cp_async_commit();
+                if (g >= (uint32_t)kLag) {
+                    cp_async_wait<kLag>();
+                    fence_proxy_async();
+                    mbar_arrive(&S.full[(g - kLag) % kStages]);
+                }
+                ++g;
+            }
+        }
+        cp_async_wait<0>();
+        fence_proxy_async();
+        for (uint32_t u = g > (uint32_t)kLag ? g - kLag : 0u; u < g; ++u) mbar_arrive(&S.full[u % kStages]);
+        if (!ok && lane == 0) {  // aborted: let issued TMA copies land before the CTA leaves
+            for (uint32_t u = g > (uint32_t)kStages ? g - kStages : 0u; u < g; ++u) {
+                uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(&S.full[u % kStages], (u / kStages) & 1u) &&
+                       globaltimer_ns() - t0 < kWaitLimitNs / 8) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t g = 0, acc_n = 0;
+            bool ok = true;
+            for (int32_t ti = blockIdx.x; ti < n_tiles && ok; ti += gridDim.x) {
+                const Tile T = load_tile(segs.tiles, ti);
+                const AdapterInfo ad = load_adapter(tab, T.adapter, segs.status);
+                if (!ad.ok) continue;
+                const uint32_t rp = (uint32_t)rpad16(ad.rank);
+                const uint32_t acc = acc_n & 1u, aph = (acc_n >> 1) & 1u;
+                if (!mbar_wait(&S.tempty[acc], aph ^ 1u, S.abort, segs.status)) break;
+                tc_fence_after();
+                const uint32_t idesc = make_idesc_bf16(128, rp, false, kDH);
+                const uint32_t d_tmem = tmem_base + acc * 128u;
+                for (int32_t kb = 0; kb < nk; ++kb) {
+                    const uint32_t s = g % kStages, ph = (g / kStages) & 1u;
+                    if (!mbar_wait(&S.full[s], ph, S.abort, segs.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(S.act + s * kActBytes);
+                    const uint32_t w_base = smem_u32(S.w + s * kWBytes);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t adesc = make_desc(a_base + 32u * k, 16, 1024, kSwizzle128);
+                        const uint64_t bdesc = kDH ? make_desc(w_base + 256u * k, 128, 1024, kInterleave)
+                                                   : make_desc(w_base + 32u * k, 16, 1024, kSwizzle128);
+                        umma_bf16(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(&S.empty[s]);
+                    ++g;
+                }
+                if (!ok) break;
+                umma_commit(&S.tfull[acc]);
+                ++acc_n;
+            }
+            umma_commit(S.done);  // every MMA issued above has completed once this fires
+            uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(S.done, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const uint32_t lane_base = 32u * (warp & 3);
+        const int32_t r_max = tab.r_max;
+        const bool vec = (r_max & 3) == 0;
+        uint32_t acc_n = 0;
+        for (int32_t ti = blockIdx.x; ti < n_tiles; ti += gridDim.x) {
+            const Tile T = load_tile(segs.tiles, ti);
+            const AdapterInfo ad = load_adapter(tab, T.adapter, segs.status);
+            if (!ad.ok) continue;
+            const int32_t r = ad.rank, rp = rpad16(r);
+            const uint32_t acc = acc_n & 1u, aph = (acc_n >> 1) & 1u;
+            if (!mbar_wait(&S.tfull[acc], aph, S.abort, segs.status)) break;
+            tc_fence_after();
+            const int m = (int)lane_base + lane;
+            const int32_t t = m < T.rows ? segs.perm[T.begin + m] : -1;
+            const float c = kDH ? ad.scale : 1.0f;
+            float *row = out + (int64_t)(t < 0 ? 0 : t) * r_max;
+            for (int c0 = 0; c0 < rp; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(tmem_base + (lane_base << 16) + acc * 128u + (uint32_t)c0, v);
+                tmem_ld_wait();
+                if (t >= 0) {
+                    float o[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) o[e] = (c0 + e < r) ? c * __uint_as_float(v[e]) : 0.f;
+                    if (vec && c0 + 16 <= r_max) {
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4)
+                            *reinterpret_cast<float4 *>(row + c0 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            if (c0 + e < r_max) row[c0 + e] = o[e];
+                    }
+                }
+            }
+            if (t >= 0)
+                for (int k = rp; k < r_max; ++k) row[k] = 0.f;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.tempty[acc]);
+            ++acc_n;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+template <bool kDH>
+lora_status_t launch_rowproj(float *out, const void *act, const lora_adapter_table &tab, const lora_segments &segs,
+                             cudaStream_t stream)
+{
+    if (segs.n_tokens == 0 || segs.max_tiles == 0) return LORA_OK;
+    const int32_t d = kDH ? tab.d_out : tab.d_in;
+    CUtensorMap map_act, map_w;
+    if (!make_tmap_bf16_2d(&map_act, act, (uint64_t)d, (uint64_t)segs.n_tokens, 64, 128, true))
+        return LORA_ERR_CUDA;
+    if (!kDH) {
+        if (!make_tmap_bf16_2d(&map_w, tab.A, (uint64_t)tab.d_in, (uint64_t)tab.sum_r, 64, 16, true))
+            return LORA_ERR_CUDA;
+    } else {
+        map_w = map_act;  // unused
+    }
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(tc_rowproj_kernel<kDH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBytes) != cudaSuccess)
+            return LORA_ERR_CUDA;
+        attr_set = true;
+    }
+    const int sms = sm_count();
+    const int grid = segs.max_tiles < sms ? segs.max_tiles : sms;
+    tc_rowproj_kernel<kDH><<<grid, kThreads, kSmemBytes, stream>>>(map_act, map_w, out,
+                                                                    static_cast<const uint16_t *>(act), tab, segs);
+    return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+}
+
+}  // namespace
+
+lora_status_t tc_shrink(float *H, const void *x, const lora_adapter_table &tab, const lora_segments &segs,
+                        cudaStream_t stream)
+{
+    return launch_rowproj<false>(H, x, tab, segs, stream);
+}
+
+lora_status_t tc_dh(float *dH, const void *dY, const lora_adapter_table &tab, const lora_segments &segs,
+                    cudaStream_t stream)
+{
+    return launch_rowproj<true>(dH, dY, tab, segs, stream);
+}
+
+}  // namespace lora

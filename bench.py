@@ -1,0 +1,516 @@
+#!/usr/bin/env python3
+"""Throughput of the multi-adapter LoRA delta on GB300, as one JSON line.
+
+A step is one pass of the whole hot path over one batch: build the routing
+metadata, the packed forward (shrink + expand, H saved) and the packed
+backward (dH, dB, dA, dX), all through the C ABI.  The workload is the packed
+training batch 4096->4096, N=8 adapters of ranks {8,16,16,32,32,64,64,128},
+4 x 1024 tokens each (T = 32768), bf16 with fp32 accumulation; its inputs
+(x and dY 268 MB each, y 268 MB) are larger than L2, so no flush is needed
+between steps.  The decode batch (256 tokens over 8 adapters of rank 32,
+three projections) is timed beside it for the SGMV-decode GB/s figure.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs its own replica of the workload (the path
+shards by batch with no exchange); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "packed multi-LoRA fwd+bwd tokens/s"
+UNIT = "tokens/s"
+L2_BYTES = 129 * 2 ** 20
+
+
+# ---------------------------------------------------------------------------- accounting
+def step_bytes(spec: wl.Spec) -> dict:
+    """Algorithmic HBM bytes per call: each activation read once per pass, y / dX
+    read and written, adapter weights read once per pass, dA / dB written once,
+    H written by the forward and read by the backward."""
+    T, di, do = spec.n_tokens, spec.d_in, spec.d_out
+    counts = np.bincount(spec.ids, minlength=spec.n_adapters)
+    th = int((counts * spec.ranks).sum())           # sum_i T_i r_i
+    w = int(spec.sum_r) * (di + do)                 # adapter weight elements
+    fwd = 2 * T * di + 4 * T * do + 2 * w + 4 * th
+    bwd = 2 * T * do + 2 * T * di + 4 * T * di + 4 * th + 2 * w + 4 * w
+    return {"fwd": fwd, "bwd": bwd}
+
+
+def step_flops(spec: wl.Spec) -> int:
+    counts = np.bincount(spec.ids, minlength=spec.n_adapters)
+    th = int((counts * spec.ranks).sum())
+    return 6 * th * (spec.d_in + spec.d_out)
+
+
+def decode_bytes(spec: wl.Spec) -> int:
+    """x read, y read + written, weights of the adapters present read once."""
+    present = np.unique(spec.ids)
+    r = int(spec.ranks[present].sum())
+    return 2 * spec.n_tokens * spec.d_in + 4 * spec.n_tokens * spec.d_out + 2 * r * (spec.d_in + spec.d_out)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def traffic_record(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, when it still
+    matches the kernel's source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+    except Exception:
+        return None
+    if not rec:
+        return None
+    import hashlib
+
+    src = os.path.join(ROOT, rec["source"])
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return rec["bytes_per_launch"] if h == rec.get("source_sha") else None
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.12)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- our arm
+class Workload:
+    def __init__(self, spec: wl.Spec, dev):
+        import torch
+
+        import adapter_sgmv_gb300 as lora
+
+        self.spec, self.dev = spec, dev
+        self.inp = wl.device_inputs(spec, dev, y0="randn", dX0="zero")
+        self.table = lora.AdapterTable(self.inp["A"], self.inp["B"], spec.ranks.tolist(),
+                                       torch.from_numpy(spec.scales), spec.d_in, spec.d_out)
+        self.offsets = torch.from_numpy(spec.seg_offsets).to(dev) if spec.sorted else None
+        self.ids = None if spec.sorted else torch.from_numpy(spec.ids).to(dev)
+        nb = lora.lora_segments_bytes(spec.n_tokens, spec.n_adapters)
+        self.seg_storage = torch.empty(nb, dtype=torch.uint8, device=dev)
+        self.ws = lora.workspace(self.table, spec.n_tokens, dev)
+        T = spec.n_tokens
+        self.y = self.inp["y0"]
+        self.H = torch.empty((T, spec.r_max), dtype=torch.float32, device=dev)
+        self.dX = self.inp["dX0"]
+        self.dA = torch.empty((spec.sum_r, spec.d_in), dtype=torch.float32, device=dev)
+        self.dB = torch.empty((spec.sum_r * spec.d_out,), dtype=torch.float32, device=dev)
+        self.segs = None
+
+    def build(self, stream=None):
+        import adapter_sgmv_gb300 as lora
+
+        self.segs = lora.lora_build_segments(ids=self.ids, seg_offsets=self.offsets, n_tokens=self.spec.n_tokens,
+                                             n_adapters=self.spec.n_adapters, storage=self.seg_storage,
+                                             stream=stream)
+
+    def fwd(self, stream=None, x=None):
+        import adapter_sgmv_gb300 as lora
+
+        lora.lora_packed_fwd(self.y, self.H, self.inp["x"] if x is None else x, self.table, self.segs, self.ws,
+                             stream=stream)
+
+    def bwd(self, stream=None, x=None, dY=None):
+        import adapter_sgmv_gb300 as lora
+
+        lora.lora_packed_bwd(self.dX, self.dA, self.dB, self.inp["dY"] if dY is None else dY,
+                             self.inp["x"] if x is None else x, self.H, self.table, self.segs, self.ws,
+                             stream=stream)
+
+
+def kernels_per_step(spec: wl.Spec) -> int:
+    """Kernels the library launches per step (builder + forward + backward)."""
+    build = 2 if spec.sorted else 6
+    return build + 2 + 4
+
+
+def time_steps(work: Workload, steps: int, warmup: int, stream):
+    import torch
+
+    for _ in range(warmup):
+        work.build(stream)
+        work.fwd(stream)
+        work.bwd(stream)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(steps):
+        ev[k][0].record(stream)
+        work.build(stream)
+        ev[k][1].record(stream)
+        work.fwd(stream)
+        ev[k][2].record(stream)
+        work.bwd(stream)
+        ev[k][3].record(stream)
+    end.record(stream)
+    return start, end, ev
+
+
+def time_e2e(work: Workload, steps: int, warmup: int, stream):
+    """Same step with the activations coming from pinned host memory and the
+    adapter gradients going back to it, copies inside the timed region."""
+    import torch
+
+    hx = work.inp["x"].cpu().pin_memory()
+    hdy = work.inp["dY"].cpu().pin_memory()
+    hdA = torch.empty(work.dA.shape, dtype=work.dA.dtype).pin_memory()
+    hdB = torch.empty(work.dB.shape, dtype=work.dB.dtype).pin_memory()
+    dx = torch.empty_like(work.inp["x"])
+    ddy = torch.empty_like(work.inp["dY"])
+
+    def one():
+        with torch.cuda.stream(stream):
+            dx.copy_(hx, non_blocking=True)
+            ddy.copy_(hdy, non_blocking=True)
+        work.build(stream)
+        work.fwd(stream, x=dx)
+        work.bwd(stream, x=dx, dY=ddy)
+        with torch.cuda.stream(stream):
+            hdA.copy_(work.dA, non_blocking=True)
+            hdB.copy_(work.dB, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        one()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    h2d = hx.numel() * hx.element_size() + hdy.numel() * hdy.element_size()
+    d2h = hdA.numel() * hdA.element_size() + hdB.numel() * hdB.element_size()
+    return ms, h2d, d2h
+
+
+def time_decode(dev, stream, reps: int = 50):
+    """SGMV decode (packed_fwd on the decode batch) per projection, L2-cold:
+    a CUDA graph replays `reps` calls that rotate over enough independent
+    buffer sets to exceed 3x L2."""
+    import torch
+
+    import adapter_sgmv_gb300 as lora
+
+    hbm, _, _ = measured_peaks()
+    out = {}
+    for p in range(3):
+        spec = wl.decode(p)
+        nbytes = decode_bytes(spec)
+        n_sets = max(2, int(3 * L2_BYTES / nbytes) + 1)
+        ids = torch.from_numpy(spec.ids).to(dev)
+        segs = lora.lora_build_segments(ids=ids, n_adapters=spec.n_adapters)
+        sets = []
+        for q in range(n_sets):
+            s_q = wl.Spec(spec.name, spec.d_in, spec.d_out, spec.ranks, spec.alphas, spec.ids, False, seed=q,
+                          with_bwd=False)
+            inp = wl.device_inputs(s_q, dev, y0="randn", need=("A", "B", "x", "y0"))
+            tab = lora.AdapterTable(inp["A"], inp["B"], spec.ranks.tolist(), torch.from_numpy(spec.scales),
+                                    spec.d_in, spec.d_out)
+            ws = lora.workspace(tab, spec.n_tokens, dev)
+            sets.append((tab, inp["x"], inp["y0"], ws))
+        for tab, x, y, ws in sets:  # warm-up, also outside capture
+            lora.lora_packed_fwd(y, None, x, tab, segs, ws, stream=stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(reps):
+                tab, x, y, ws = sets[k % n_sets]
+                lora.lora_packed_fwd(y, None, x, tab, segs, ws, stream=stream)
+        times = []
+        with torch.cuda.stream(stream):  # replay() launches on the current stream
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            for _ in range(20):
+                s = torch.cuda.Event(enable_timing=True)
+                e = torch.cuda.Event(enable_timing=True)
+                s.record(stream)
+                g.replay()
+                e.record(stream)
+                e.synchronize()
+                times.append(s.elapsed_time(e) / reps)
+        ms = statistics.median(times)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[f"{spec.d_in}x{spec.d_out}"] = {"us_per_call": round(ms * 1e3, 3), "bytes": nbytes,
+                                            "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4)}
+        del sets, g
+        torch.cuda.empty_cache()
+    return out
+
+
+def cpu_baseline(spec: wl.Spec, target_s: float = 10.0):
+    """The fp64 oracle on a bounded sample of the same workload (first tokens of
+    every adapter), on this host's cores; tokens/s."""
+    import oracle
+
+    oracle.build()
+    cores = oracle.threads()
+    tab = oracle.Table(spec.ranks, spec.scales.astype(np.float64))
+
+    def run(per_adapter):
+        rows = []
+        for i in range(spec.n_adapters):
+            idx = np.flatnonzero(spec.ids == i)[:per_adapter]
+            rows.append(idx)
+        rows = np.concatenate(rows)
+        sub = wl.custom(spec.name, spec.d_in, spec.d_out, spec.ranks, spec.alphas, spec.ids[rows], seed=spec.seed)
+        host = wl.host_inputs(sub)
+        f = lambda k: wl.bf16_bits_to_f64(host[k])
+        A, B, x, dY, y0, dX0 = (f(k) for k in ("A", "B", "x", "dY", "y0", "dX0"))
+        t0 = time.perf_counter()
+        y, H = oracle.fwd(tab, sub.ids, A, B, x, y0)
+        oracle.bwd(tab, sub.ids, A, B, x, H, dY, dX0)
+        return len(rows), time.perf_counter() - t0
+
+    n, dt = run(2)
+    per = int(max(2, min(4096, 2 * target_s / max(dt, 1e-3))))
+    n, dt = run(per)
+    return {"value": round(n / dt, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} tokens ({per} per adapter) of the same workload, fwd+bwd in fp64, {dt:.1f} s"}
+
+
+def run_ours(args, rank, world, dev):
+    import torch
+    import torch.distributed as dist
+
+    import adapter_sgmv_gb300 as lora
+
+    lora.build_library()
+    lora.lib()
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    spec = wl.packed4096()
+    work = Workload(spec, dev)
+    with torch.cuda.stream(stream):
+        pass
+    torch.cuda.synchronize()
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        start, end, ev = time_steps(work, args.steps, args.warmup, stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    st = lora.lora_query_status(work.segs, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {lora.STATUS.get(st, st)}")
+    total_ms = start.elapsed_time(end)
+    t_build = [e[0].elapsed_time(e[1]) for e in ev]
+    t_fwd = [e[1].elapsed_time(e[2]) for e in ev]
+    t_bwd = [e[2].elapsed_time(e[3]) for e in ev]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    T = spec.n_tokens
+    value = world * T * args.steps / (total_ms * 1e-3)
+
+    hbm, tflops, peak_src = measured_peaks()
+    by = step_bytes(spec)
+    calls = {"lora_packed_fwd": (statistics.mean(t_fwd), by["fwd"]),
+             "lora_packed_bwd": (statistics.mean(t_bwd), by["bwd"])}
+    dom = max(calls, key=lambda k: calls[k][0])
+    dom_ms, dom_bytes = calls[dom]
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+
+    e2e_ms, h2d, d2h = time_e2e(work, max(3, args.steps // 2), 2, stream)
+    decode = time_decode(dev, stream) if rank == 0 and not args.no_decode else None
+    cpu = cpu_baseline(spec, args.cpu_seconds) if rank == 0 and not args.no_cpu else None
+
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, shapes of the packed training batch)",
+        "config": {"workload": "packed4096: 4096->4096, N=8 ranks {8,16,16,32,32,64,64,128}, alpha 16/32, "
+                               "8 sorted segments x 4096 tokens (T=32768), fwd+bwd",
+                   "tokens_per_step": T, "d_in": spec.d_in, "d_out": spec.d_out, "adapters": spec.n_adapters,
+                   "l2": "inputs larger than L2 (x, dY, y 268 MB each); no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "breakdown_ms": {"lora_build_segments": round(statistics.mean(t_build), 4),
+                         "lora_packed_fwd": round(statistics.mean(t_fwd), 4),
+                         "lora_packed_bwd": round(statistics.mean(t_bwd), 4)},
+        "step_bytes": by["fwd"] + by["bwd"], "step_flops": step_flops(spec),
+        "step_GB/s": round((by["fwd"] + by["bwd"]) / (ms_step * 1e-3) / 1e9, 1),
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm,
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_source": peak_src,
+                     "traffic": traffic_record(dom),
+                     "tensor_frac_at_this_time": round(step_flops(spec) / (ms_step * 1e-3) / 1e12 / tflops, 4)},
+        "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": kernels_per_step(spec) * args.steps,
+        "clocks": clk.summary(),
+        "decode_sgmv": decode,
+        "cpu_baseline": cpu,
+    }
+    return line
+
+
+# ---------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    """The fp64 oracle (the only reference this method has) on the host cores:
+    each step is a bounded sample of the same workload; tokens/s."""
+    import oracle
+
+    spec = wl.packed4096()
+    oracle.build()
+    per = args.ref_tokens_per_adapter
+    rows = np.concatenate([np.flatnonzero(spec.ids == i)[:per] for i in range(spec.n_adapters)])
+    sub = wl.custom(spec.name, spec.d_in, spec.d_out, spec.ranks, spec.alphas, spec.ids[rows], seed=spec.seed)
+    host = wl.host_inputs(sub)
+    f = lambda k: wl.bf16_bits_to_f64(host[k])
+    A, B, x, dY, y0, dX0 = (f(k) for k in ("A", "B", "x", "dY", "y0", "dX0"))
+    tab = oracle.Table(spec.ranks, spec.scales.astype(np.float64))
+
+    def step():
+        y, H = oracle.fwd(tab, sub.ids, A, B, x, y0)
+        oracle.bwd(tab, sub.ids, A, B, x, H, dY, dX0)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    n = len(rows)
+    value = n * args.steps / dt
+    cores = oracle.threads()
+    sample = f"{n} tokens per step ({per} per adapter) of the packed4096 workload, fwd+bwd in fp64"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": "packed4096 (bounded sample per step)", "tokens_per_step": n},
+        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-tokens-per-adapter", type=int, default=16)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    import torch
+
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(dev)
+        dist.init_process_group("nccl", device_id=dev)
+    line = run_ours(args, rank, world, dev)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

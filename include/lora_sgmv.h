@@ -1,0 +1,221 @@
+/*
+ * lora_sgmv.h -- C ABI of the GB300 (sm_103a) multi-adapter LoRA delta library.
+ *
+ * The operation.  A batch of T tokens mixes tokens of N LoRA adapters that are
+ * all resident in GPU memory; every token is served by its own adapter in one
+ * pass over the batch (C-LoRA report, vivodigitale.it, "Come funziona
+ * l'architettura": mixed-adapter decode batches, per-adapter work fused into one
+ * launch per decode step).  Training packs many adapters of different rank on
+ * one frozen base and runs their forward and backward together over the
+ * concatenated LoRA tensors, tiled along the token or hidden dimension rather
+ * than the small rank dimension, in four forward/backward cases (PLoRA
+ * technical summary, gist.science, "2. LoRA Execution Engine", Kernelontwerp).
+ * For token t routed to adapter i (rank r_i, scale s_i = alpha_i / r_i):
+ *     shrink   h_t   = A_i x_t                      A_i: r_i x d_in
+ *     expand   y_t  += s_i B_i h_t                  B_i: d_out x r_i
+ *     dh       dh_t  = s_i B_i^T dy_t
+ *     dB       dB_i  = s_i sum_{t in i} dy_t h_t^T
+ *     dA       dA_i  = sum_{t in i} dh_t x_t^T
+ *     dX       dx_t += A_i^T dh_t
+ * (The pages print no formula; these are the standard LoRA algebra of the
+ * method they describe.)  All products accumulate in fp32.
+ *
+ * Conventions shared by every entry point.
+ *  - Ownership: the caller allocates and frees every buffer (inputs, outputs,
+ *    segment storage, workspace).  The library never allocates or frees
+ *    device memory, keeps no global mutable state and never synchronises,
+ *    except lora_query_status.  Every call is stream-ordered on `stream`.
+ *  - Pointers marked "device" must be device (or managed) memory, 16-byte
+ *    aligned.  bf16 tensors are passed as raw 16-bit words (IEEE bfloat16).
+ *  - Errors found on the host (NULL pointer, size out of range, misalignment,
+ *    workspace too small) are returned at once and nothing is launched.
+ *    Errors found on the device (an adapter id outside [0, N), an
+ *    inconsistent adapter table, a bounded wait that gave up) are written to
+ *    the device status word of the lora_segments in use; the kernels skip the
+ *    offending work and never trap.  Read it with lora_query_status.
+ *  - Tokens whose id lies outside [0, N) belong to no adapter: their H / dH
+ *    rows are not written and their y / dX rows are left unchanged.
+ *  - y and dX accumulate (+=) and are rounded once to bf16 (nearest-even)
+ *    after the fp32 sum; H, dH, dA and dB are fp32 and are overwritten.
+ */
+#ifndef LORA_SGMV_H
+#define LORA_SGMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LORA_SGMV_ABI_VERSION 1
+
+/* Exported entry points (the library is built with hidden default visibility). */
+#if defined(__GNUC__)
+#define LORA_API __attribute__((visibility("default")))
+#else
+#define LORA_API
+#endif
+
+/* Largest supported adapter rank; sizes are checked against it. */
+#define LORA_MAX_RANK 128
+/* Token rows per work tile of the packed kernels. */
+#define LORA_TILE_M 128
+
+/* A CUDA stream (cudaStream_t / CUstream); NULL is the legacy default stream. */
+typedef struct CUstream_st *lora_stream_t;
+
+typedef enum lora_status {
+    LORA_OK = 0,
+    LORA_ERR_INVALID_ARG = 1,          /* NULL where a pointer is required, negative count */
+    LORA_ERR_SHAPE = 2,                /* a size outside the supported range */
+    LORA_ERR_ALIGNMENT = 3,            /* a pointer not 16-byte aligned */
+    LORA_ERR_BAD_ADAPTER_ID = 4,       /* device: a token id outside [0, N) */
+    LORA_ERR_WORKSPACE_TOO_SMALL = 5,  /* storage / workspace below the required bytes */
+    LORA_ERR_UNSUPPORTED = 6,          /* no kernel for this device or configuration */
+    LORA_ERR_TIMEOUT = 7,              /* device: a bounded wait gave up */
+    LORA_ERR_BAD_TABLE = 8,            /* device: rank / row offset inconsistent */
+    LORA_ERR_BAD_SEGMENTS = 9,         /* device: segment offsets not monotone or not ending at T */
+    LORA_ERR_CUDA = 10                 /* a CUDA runtime call failed */
+} lora_status_t;
+
+/*
+ * The stacked adapter table: N adapters, all resident on the device.
+ *   rank[i]      r_i, 1 <= r_i <= r_max <= LORA_MAX_RANK           (device int32 [N])
+ *   row_off[i]   sum_{j<i} r_j; row_off[N] = sum_r                   (device int32 [N+1])
+ *   scale[i]     s_i = alpha_i / r_i (fp32)                          (device float [N])
+ *   A            bf16 [sum_r, d_in] row-major: A_i is rows row_off[i] .. row_off[i]+r_i-1
+ *   B            bf16 ragged: B_i is a row-major [d_out, r_i] block starting at
+ *                element d_out * row_off[i]; total d_out * sum_r elements
+ * The host fields (n_adapters, d_in, d_out, r_max, sum_r) size the launches;
+ * the device arrays must agree with them (checked on the device: a mismatch
+ * sets LORA_ERR_BAD_TABLE and the adapter is skipped).
+ * d_in and d_out are multiples of 8 in [8, 1 << 20].
+ */
+typedef struct lora_adapter_table {
+    int32_t n_adapters;
+    int32_t d_in;
+    int32_t d_out;
+    int32_t r_max;
+    int32_t sum_r;
+    int32_t reserved;
+    const int32_t *rank;
+    const int32_t *row_off;
+    const float *scale;
+    const void *A;
+    const void *B;
+} lora_adapter_table;
+
+/*
+ * Routing metadata of one batch (built once, shared by every LoRA layer of a
+ * step).  All pointers are device memory carved out of the caller's storage
+ * by lora_build_segments; the struct itself is a plain host value.
+ *   perm[T]          token indices grouped by adapter, ascending adapter id,
+ *                    original order inside a group (stable); only the first
+ *                    seg_start[N] entries are valid (tokens with a bad id are left out)
+ *   seg_start[N+1]   start of adapter i's group in perm
+ *   tiles[4*max_tiles]  work tiles {adapter, begin (index into perm), rows (1..LORA_TILE_M),
+ *                    flags (bit 0: the rows are consecutive token indices)}, ordered by
+ *                    adapter then begin; n_tiles[0] of them are valid
+ *   status[0]        device status word (an lora_status_t, LORA_OK when clean)
+ */
+typedef struct lora_segments {
+    int32_t n_tokens;
+    int32_t n_adapters;
+    int32_t max_tiles;
+    int32_t sorted;
+    int32_t *perm;
+    int32_t *seg_start;
+    int32_t *tiles;
+    int32_t *n_tiles;
+    int32_t *status;
+    int32_t *scratch;      /* builder-internal counters (histogram / scan) */
+    int64_t scratch_words;
+} lora_segments;
+
+/* ABI version of the loaded library (LORA_SGMV_ABI_VERSION). */
+LORA_API int32_t lora_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+LORA_API const char *lora_status_string(lora_status_t status);
+
+/* Bytes of device storage lora_build_segments needs for T tokens and N adapters
+ * (0 when the sizes are out of range). */
+LORA_API size_t lora_segments_bytes(int32_t n_tokens, int32_t n_adapters);
+
+/*
+ * Segment-metadata builder: group the batch's tokens by adapter (stable) and
+ * cut every group into work tiles of at most LORA_TILE_M rows.
+ *   ids          device int32 [T]: adapter of every token, any order; or NULL
+ *   seg_offsets  device int32 [N+1]: tokens already grouped, adapter i owning
+ *                tokens seg_offsets[i] .. seg_offsets[i+1]-1; or NULL
+ *                (exactly one of ids / seg_offsets is given)
+ *   n_tokens     T >= 0;  n_adapters  N in [1, 65536]
+ *   storage      device, >= lora_segments_bytes(T, N) bytes, 16-byte aligned;
+ *                it must stay allocated while `out` is in use
+ *   out          host struct filled with pointers into storage
+ * Resets the status word.  Ids outside [0, N) set LORA_ERR_BAD_ADAPTER_ID and
+ * the tokens are left out; non-monotone offsets set LORA_ERR_BAD_SEGMENTS.
+ */
+LORA_API lora_status_t lora_build_segments(const int32_t *ids, const int32_t *seg_offsets,
+                                  int32_t n_tokens, int32_t n_adapters,
+                                  void *storage, size_t storage_bytes,
+                                  lora_segments *out, lora_stream_t stream);
+
+/* Bytes of device workspace lora_packed_fwd / lora_packed_bwd need for this
+ * table and T tokens (0 when the sizes are out of range). */
+LORA_API size_t lora_workspace_bytes(const lora_adapter_table *table, int32_t n_tokens);
+
+/*
+ * SGMV shrink (case i): H[t, 0:r_i] = A_i x_t, H[t, r_i:r_max] = 0.
+ *   H  device fp32 [T, r_max] (out);  x  device bf16 [T, d_in] (in)
+ * Rows of tokens with a bad id are not written.
+ */
+LORA_API lora_status_t lora_sgmv_shrink(float *H, const void *x, const lora_adapter_table *table,
+                               const lora_segments *segs, lora_stream_t stream);
+
+/*
+ * SGMV expand (case ii): y[t, :] += s_i B_i H[t, 0:r_i].
+ *   y  device bf16 [T, d_out] (in/out);  H  device fp32 [T, r_max] (in)
+ */
+LORA_API lora_status_t lora_sgmv_expand(void *y, const float *H, const lora_adapter_table *table,
+                               const lora_segments *segs, lora_stream_t stream);
+
+/*
+ * Packed forward = shrink then expand over all adapters of the batch.
+ *   y       device bf16 [T, d_out] (in/out, +=)
+ *   H_save  device fp32 [T, r_max] (out) to keep H for the backward, or NULL
+ *   x       device bf16 [T, d_in]
+ *   ws      device workspace of >= lora_workspace_bytes(table, T) bytes
+ *           (may be NULL when that is 0); contents need not be preserved
+ */
+LORA_API lora_status_t lora_packed_fwd(void *y, float *H_save, const void *x,
+                              const lora_adapter_table *table, const lora_segments *segs,
+                              void *ws, size_t ws_bytes, lora_stream_t stream);
+
+/*
+ * Packed backward, the four cases: dh (case i), dX (case ii), dB (case iii),
+ * dA (case iv).
+ *   dX       device bf16 [T, d_in] (in/out, +=), or NULL to skip
+ *   dA       device fp32 [sum_r, d_in] (out, overwritten; adapters with no
+ *            token get zeros), or NULL to skip
+ *   dB       device fp32, B layout, d_out * sum_r (out, overwritten), or NULL
+ *   dY       device bf16 [T, d_out];  X  device bf16 [T, d_in] (the forward input)
+ *   H_saved  device fp32 [T, r_max] from lora_packed_fwd, or NULL to recompute it
+ *   ws       device workspace of >= lora_workspace_bytes(table, T) bytes
+ */
+LORA_API lora_status_t lora_packed_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X,
+                              const float *H_saved, const lora_adapter_table *table,
+                              const lora_segments *segs, void *ws, size_t ws_bytes,
+                              lora_stream_t stream);
+
+/* Synchronise `stream` and return the device status word of `segs`. */
+LORA_API lora_status_t lora_query_status(const lora_segments *segs, lora_stream_t stream);
+
+/* Clear the device status word (stream-ordered). */
+LORA_API lora_status_t lora_reset_status(const lora_segments *segs, lora_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LORA_SGMV_H */

@@ -1,0 +1,111 @@
+"""Helpers shared by the GPU tests: move seeded inputs to the device, run the
+library through its C ABI, run the fp64 oracle on the same inputs, compare.
+
+Tolerances (fp32 accumulation of bf16 inputs): forward outputs (y, H)
+max|err| <= 5e-3 * max|ref|; gradients (dH, dA, dB, dX) <= 1e-2 * max|ref|,
+dA / dB checked per adapter block so a small-rank adapter cannot hide behind
+a large one."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import adapter_sgmv_gb300 as lora
+import oracle
+import workloads as wl
+
+FWD_TOL = 5e-3
+GRAD_TOL = 1e-2
+
+
+def bits_to_dev(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def dev_to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def rel_err(got, ref) -> float:
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if ref.size == 0:
+        return 0.0
+    scale = float(np.max(np.abs(ref)))
+    err = float(np.max(np.abs(got - ref)))
+    if scale == 0.0:
+        return 0.0 if err == 0.0 else float("inf")
+    return err / scale
+
+
+def assert_close(got, ref, tol, what):
+    e = rel_err(got, ref)
+    assert e <= tol, f"{what}: max|err|/max|ref| = {e:.3e} > {tol:.1e}"
+    return e
+
+
+class GpuCase:
+    """A spec's inputs on the device, its adapter table and its segments."""
+
+    def __init__(self, spec: wl.Spec, inputs: dict, device="cuda", route="auto"):
+        self.spec = spec
+        dev = torch.device(device)
+        self.inp = {k: (v if isinstance(v, torch.Tensor) else bits_to_dev(v, dev)) for k, v in inputs.items()}
+        self.table = lora.AdapterTable(self.inp["A"], self.inp["B"], spec.ranks.tolist(),
+                                       torch.from_numpy(spec.scales), spec.d_in, spec.d_out)
+        use_offsets = spec.sorted if route == "auto" else route == "offsets"
+        if use_offsets:
+            self.segs = lora.lora_build_segments(seg_offsets=torch.from_numpy(spec.seg_offsets).to(dev),
+                                                 n_tokens=spec.n_tokens, n_adapters=spec.n_adapters,
+                                                 device=dev)
+        else:
+            self.segs = lora.lora_build_segments(ids=torch.from_numpy(spec.ids).to(dev),
+                                                 n_adapters=spec.n_adapters, device=dev)
+        self.ws = lora.workspace(self.table, spec.n_tokens, dev)
+        self.device = dev
+
+    def fwd(self):
+        T, r_max = self.spec.n_tokens, self.spec.r_max
+        y = self.inp["y0"].clone()
+        H = torch.zeros((T, r_max), dtype=torch.float32, device=self.device)
+        lora.lora_packed_fwd(y, H, self.inp["x"], self.table, self.segs, self.ws)
+        return y, H
+
+    def bwd(self, H=None):
+        s = self.spec
+        dX = self.inp["dX0"].clone()
+        dA = torch.full((s.sum_r, s.d_in), float("nan"), dtype=torch.float32, device=self.device)
+        dB = torch.full((s.sum_r * s.d_out,), float("nan"), dtype=torch.float32, device=self.device)
+        lora.lora_packed_bwd(dX, dA, dB, self.inp["dY"], self.inp["x"], H, self.table, self.segs, self.ws)
+        return dX, dA, dB
+
+    def dH_workspace(self):
+        """dH as left in the workspace by the last backward (implementation detail, for diagnosis)."""
+        s = self.spec
+        region = ((s.n_tokens * s.r_max * 4) + 255) & ~255
+        return self.ws[region:region + s.n_tokens * s.r_max * 4].view(torch.float32).view(s.n_tokens, s.r_max)
+
+
+def oracle_all(spec: wl.Spec, host: dict, rows=None):
+    """fp64 oracle on the tokens ``rows`` (all when None) of a host-input dict."""
+    tab = oracle.Table(spec.ranks, spec.scales.astype(np.float64))
+    sel = slice(None) if rows is None else rows
+    f = lambda k: wl.bf16_bits_to_f64(host[k]) if host[k].dtype == np.uint16 else host[k]
+    ids = spec.ids[sel]
+    A, B = f("A"), f("B")
+    x, dY, y0, dX0 = f("x")[sel], f("dY")[sel], f("y0")[sel], f("dX0")[sel]
+    y, H = oracle.fwd(tab, ids, A, B, x, y0)
+    dH, dA, dB, dX = oracle.bwd(tab, ids, A, B, x, H, dY, dX0)
+    return dict(y=y, H=H, dH=dH, dA=dA, dB=dB, dX=dX)
+
+
+def check_blocks(spec, got_dA, got_dB, ref_dA, ref_dB, adapters=None):
+    errs = {}
+    d_in, d_out = spec.d_in, spec.d_out
+    off = spec.row_off
+    for i in (range(spec.n_adapters) if adapters is None else adapters):
+        a0, a1 = int(off[i]), int(off[i + 1])
+        errs[f"dA[{i}]"] = assert_close(got_dA[a0:a1], ref_dA[a0:a1], GRAD_TOL, f"dA_{i}")
+        errs[f"dB[{i}]"] = assert_close(got_dB[a0 * d_out:a1 * d_out], ref_dB[a0 * d_out:a1 * d_out],
+                                        GRAD_TOL, f"dB_{i}")
+    return errs

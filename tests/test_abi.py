@@ -1,0 +1,123 @@
+"""CPU-only checks of the C ABI: the library builds for sm_103a, loads, exports
+every entry point include/lora_sgmv.h declares, and rejects bad arguments on
+the host before any CUDA call.  Nothing here runs a kernel."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import adapter_sgmv_gb300 as lora
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lora_sgmv.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    lora.build_library()
+    return lora.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lora_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_north_star_calls():
+    names = declared_functions()
+    for n in ("lora_sgmv_shrink", "lora_sgmv_expand", "lora_packed_fwd", "lora_packed_bwd",
+              "lora_build_segments"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    names = declared_functions()
+    for n in names:
+        assert hasattr(L, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", lora.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = sorted(set(re.findall(r"\bT (lora_\w+)", out)))
+    assert exported == names, (exported, names)
+    assert set(lora.SIGNATURES) == set(names)
+
+
+def test_version_and_status_strings(L):
+    assert lora.lora_abi_version() == 1
+    for code, name in lora.STATUS.items():
+        assert lora.lora_status_string(code) == name
+    assert lora.lora_status_string(999) == "LORA_ERR_UNKNOWN"
+
+
+def test_segment_storage_sizes(L):
+    a = lora.lora_segments_bytes(256, 8)
+    b = lora.lora_segments_bytes(16384, 32)
+    assert 0 < a < b
+    assert a % 256 == 0
+    assert lora.lora_segments_bytes(0, 1) > 0
+    assert lora.lora_segments_bytes(-1, 4) == 0
+    assert lora.lora_segments_bytes(10, 0) == 0
+    assert lora.lora_segments_bytes(10, 70000) == 0
+
+
+def fake_table(**kw):
+    f = dict(n_adapters=4, d_in=256, d_out=256, r_max=16, sum_r=36, reserved=0,
+             rank=0x10000, row_off=0x20000, scale=0x30000, A=0x40000, B=0x50000)
+    f.update(kw)
+    return lora.c_table(*[f[k] for k, _ in lora.c_table._fields_])
+
+
+def test_workspace_bytes_and_table_checks(L):
+    t = fake_table()
+    n = L.lora_workspace_bytes(ctypes.byref(t), 64)
+    assert n >= 2 * 64 * 16 * 4
+    for bad in (dict(d_in=12), dict(d_out=0), dict(r_max=129), dict(r_max=0), dict(n_adapters=0),
+                dict(sum_r=8), dict(A=0), dict(B=0x50008)):
+        tb = fake_table(**bad)
+        assert L.lora_workspace_bytes(ctypes.byref(tb), 64) == 0, bad
+
+
+def test_host_side_rejections_return_before_any_cuda_call(L):
+    segs = lora.c_segments()
+    # no storage / no output struct
+    assert L.lora_build_segments(None, None, 4, 2, None, 0, ctypes.byref(segs), None) == 1
+    # both ids and offsets given
+    assert L.lora_build_segments(0x1000, 0x2000, 4, 2, 0x3000, 1 << 20, ctypes.byref(segs), None) == 1
+    # misaligned storage
+    assert L.lora_build_segments(0x1000, None, 4, 2, 0x3008, 1 << 20, ctypes.byref(segs), None) == 3
+    # storage too small
+    assert L.lora_build_segments(0x1000, None, 4, 2, 0x3000, 16, ctypes.byref(segs), None) == 5
+    t = fake_table()
+    s = lora.c_segments(64, 4, 5, 1, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0)
+    assert L.lora_sgmv_shrink(None, 0x1000, ctypes.byref(t), ctypes.byref(s), None) == 1
+    assert L.lora_sgmv_shrink(0x1004, 0x1000, ctypes.byref(t), ctypes.byref(s), None) == 3
+    assert L.lora_sgmv_expand(0x1000, 0x2000, None, ctypes.byref(s), None) == 1
+    s_bad = lora.c_segments(64, 3, 5, 1, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0)
+    assert L.lora_sgmv_expand(0x1000, 0x2000, ctypes.byref(t), ctypes.byref(s_bad), None) == 2
+    assert L.lora_packed_fwd(0x1000, None, 0x2000, ctypes.byref(t), ctypes.byref(s), None, 0, None) == 5
+    assert L.lora_packed_bwd(None, None, None, 0x1000, 0x2000, None, ctypes.byref(t), ctypes.byref(s),
+                             0x3000, 16, None) == 5
+    assert L.lora_packed_bwd(None, None, None, None, 0x2000, None, ctypes.byref(t), ctypes.byref(s),
+                             0x3000, 1 << 20, None) == 1
+    assert L.lora_query_status(None, None) == 1
+
+
+def test_binding_fails_loudly_without_the_library():
+    with pytest.raises(RuntimeError):
+        lora._lib = None
+        try:
+            lora.lib(path="/nonexistent/liblora_sgmv.so")
+        finally:
+            lora._lib = None
+
+
+def test_product_path_never_touches_the_oracle():
+    pkg = os.path.join(ROOT, "adapter_sgmv_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in src and "from oracle" not in src, f
+                assert "lora_oracle" not in src, f

@@ -1,0 +1,214 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI.
+
+Small cases run the whole oracle; the full-size workloads (the ones the bench
+times, in the same launch configuration) are checked on sampled token rows
+and on whole adapters for dA / dB."""
+import numpy as np
+import pytest
+import torch
+
+import adapter_sgmv_gb300 as lora
+import workloads as wl
+from lora_testlib import (FWD_TOL, GRAD_TOL, GpuCase, assert_close, check_blocks, dev_to_f64,
+                          oracle_all)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lora.build_library()
+    lora.lib()
+
+
+def full_check(spec, y0="zero", dX0="zero", route="auto", saved_H=True):
+    host = wl.host_inputs(spec, y0=y0, dX0=dX0)
+    case = GpuCase(spec, host, route=route)
+    y, H = case.fwd()
+    dX, dA, dB = case.bwd(H if saved_H else None)
+    torch.cuda.synchronize()
+    assert lora.lora_query_status(case.segs) == 0
+    ref = oracle_all(spec, host)
+    valid = (spec.ids >= 0) & (spec.ids < spec.n_adapters)
+    e = {}
+    e["y"] = assert_close(dev_to_f64(y)[valid], ref["y"][valid], FWD_TOL, "y")
+    e["H"] = assert_close(dev_to_f64(H)[valid], ref["H"][valid], FWD_TOL, "H")
+    e["dH"] = assert_close(dev_to_f64(case.dH_workspace())[valid], ref["dH"][valid], GRAD_TOL, "dH")
+    e["dX"] = assert_close(dev_to_f64(dX)[valid], ref["dX"][valid], GRAD_TOL, "dX")
+    e.update(check_blocks(spec, dev_to_f64(dA), dev_to_f64(dB), ref["dA"], ref["dB"]))
+    return e
+
+
+def test_tiny_config_sorted_offsets():
+    full_check(wl.tiny())
+
+
+def test_tiny_config_routed_by_ids():
+    full_check(wl.tiny(), route="ids")
+
+
+def test_tiny_config_accumulates_into_nonzero_outputs():
+    full_check(wl.tiny(), y0="randn", dX0="randn")
+
+
+def test_tiny_config_recomputes_H_when_not_saved():
+    full_check(wl.tiny(), saved_H=False)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_ragged_unsorted_mixed_ranks(seed):
+    rng = np.random.default_rng(100 + seed)
+    T, N = 333, 6
+    ranks = [4, 8, 16, 24, 64, 128]
+    ids = rng.integers(0, N, T).astype(np.int32)
+    spec = wl.custom("ragged", 136, 200, ranks, [2.0 * r for r in ranks], ids, seed=seed)
+    full_check(spec, y0="randn", dX0="randn")
+
+
+def test_long_segments_several_tiles_with_ragged_tail():
+    ranks = [16, 32, 128]
+    lengths = [300, 128, 517]
+    ids = np.concatenate([np.full(n, i, np.int32) for i, n in enumerate(lengths)])
+    spec = wl.custom("long", 512, 384, ranks, [32.0, 32.0, 32.0], ids)
+    full_check(spec)
+
+
+def test_zipf_runs_unsorted_small():
+    rng = np.random.default_rng(8)
+    runs = []
+    total = 0
+    while total < 1500:
+        n = int(min(rng.zipf(1.2), 300))
+        runs.append((min(n, 1500 - total), int(rng.integers(0, 8))))
+        total += runs[-1][0]
+    ids = np.concatenate([np.full(n, a, np.int32) for n, a in runs])
+    ranks = [8, 16, 32, 64, 128, 8, 16, 32]
+    spec = wl.custom("zipf", 256, 448, ranks, [2.0 * r for r in ranks], ids)
+    full_check(spec)
+
+
+def test_empty_adapters_get_zero_gradients():
+    ids = np.array([0] * 40 + [3] * 70, np.int32)  # adapters 1 and 2 have no token
+    spec = wl.custom("empty", 64, 96, [8, 16, 32, 16], [16.0] * 4, ids)
+    full_check(spec)
+
+
+def test_bad_ids_report_status_and_leave_rows_untouched():
+    ids = np.array([0, 1, 9, 1, -1, 0, 1, 2], np.int32)
+    spec = wl.custom("bad", 64, 64, [8, 16, 8], [16.0] * 3, ids)
+    host = wl.host_inputs(spec, y0="randn", dX0="randn")
+    case = GpuCase(spec, host, route="ids")
+    y, H = case.fwd()
+    dX, dA, dB = case.bwd(H)
+    assert lora.lora_query_status(case.segs) == 4
+    y0, dX0 = dev_to_f64(case.inp["y0"]), dev_to_f64(case.inp["dX0"])
+    for t in (2, 4):
+        assert np.array_equal(dev_to_f64(y)[t], y0[t])
+        assert np.array_equal(dev_to_f64(dX)[t], dX0[t])
+    ref = oracle_all(spec, host)
+    ok = np.array([0, 1, 3, 5, 6, 7])
+    assert_close(dev_to_f64(y)[ok], ref["y"][ok], FWD_TOL, "y")
+    check_blocks(spec, dev_to_f64(dA), dev_to_f64(dB), ref["dA"], ref["dB"])
+
+
+def test_optional_outputs_can_be_skipped():
+    spec = wl.tiny()
+    host = wl.host_inputs(spec)
+    case = GpuCase(spec, host)
+    y, H = case.fwd()
+    dA = torch.zeros((spec.sum_r, spec.d_in), device="cuda")
+    lora.lora_packed_bwd(None, dA, None, case.inp["dY"], case.inp["x"], H, case.table, case.segs, case.ws)
+    ref = oracle_all(spec, host)
+    assert_close(dev_to_f64(dA), ref["dA"], GRAD_TOL, "dA")
+
+
+@pytest.mark.parametrize("proj", [0, 1, 2])
+def test_decode_batch_shrink_expand(proj):
+    spec = wl.decode(proj)
+    host = wl.host_inputs(spec, y0="zero")
+    case = GpuCase(spec, host)
+    T = spec.n_tokens
+    H = torch.zeros((T, spec.r_max), dtype=torch.float32, device="cuda")
+    lora.lora_sgmv_shrink(H, case.inp["x"], case.table, case.segs)
+    y = case.inp["y0"].clone()
+    lora.lora_sgmv_expand(y, H, case.table, case.segs)
+    y2, H2 = case.fwd()
+    torch.cuda.synchronize()
+    ref = oracle_all(spec, host)
+    assert_close(dev_to_f64(H), ref["H"], FWD_TOL, "H")
+    assert_close(dev_to_f64(y), ref["y"], FWD_TOL, "y")
+    assert_close(dev_to_f64(y2), ref["y"], FWD_TOL, "y(packed_fwd)")
+    assert_close(dev_to_f64(H2), ref["H"], FWD_TOL, "H(packed_fwd)")
+
+
+def test_repeated_runs_are_identical():
+    spec = wl.tiny()
+    host = wl.host_inputs(spec)
+    case = GpuCase(spec, host)
+    y1, H1 = case.fwd()
+    y2, H2 = case.fwd()
+    assert torch.equal(y1, y2) and torch.equal(H1, H2)
+
+
+# ---------------------------------------------------------------------------- full size
+def sampled_rows(spec, rng, per_adapter=3):
+    rows = set()
+    seg = np.flatnonzero(np.r_[True, np.diff(spec.ids) != 0])
+    ends = np.r_[seg[1:], spec.n_tokens] - 1
+    for a, b in list(zip(seg, ends))[:: max(1, len(seg) // 24)]:
+        rows.update([int(a), int(b)])
+    for i in range(spec.n_adapters):
+        idx = np.flatnonzero(spec.ids == i)
+        if idx.size:
+            rows.update(int(v) for v in rng.choice(idx, size=min(per_adapter, idx.size), replace=False))
+    rows.update([0, spec.n_tokens - 1])
+    return np.array(sorted(rows))
+
+
+def host_rows(dev, rows):
+    return dev[torch.from_numpy(rows).to(dev.device)].float().cpu().numpy().astype(np.float64)
+
+
+FULL = {
+    "packed4096": lambda: wl.packed4096(),
+    "sweep2": lambda: wl.sweep(2),
+    "sweep32": lambda: wl.sweep(32),
+    "skewed": lambda: wl.skewed(),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FULL))
+def test_full_size_sampled(name):
+    spec = FULL[name]()
+    dev = torch.device("cuda")
+    inp = wl.device_inputs(spec, dev, y0="randn", dX0="randn")
+    case = GpuCase(spec, inp)
+    y, H = case.fwd()
+    dX, dA, dB = case.bwd(H)
+    torch.cuda.synchronize()
+    assert lora.lora_query_status(case.segs) == 0
+    rng = np.random.default_rng(0)
+    rows = sampled_rows(spec, rng)
+    host = {"A": dev_to_f64(inp["A"]), "B": dev_to_f64(inp["B"]),
+            "x": host_rows(inp["x"], rows), "dY": host_rows(inp["dY"], rows),
+            "y0": host_rows(inp["y0"], rows), "dX0": host_rows(inp["dX0"], rows)}
+    sub = wl.custom(spec.name, spec.d_in, spec.d_out, spec.ranks, spec.alphas, spec.ids[rows], sorted_=False)
+    ref = oracle_all(sub, host)
+    assert_close(host_rows(y, rows), ref["y"], FWD_TOL, "y")
+    assert_close(H[torch.from_numpy(rows).cuda()].cpu().numpy(), ref["H"], FWD_TOL, "H")
+    assert_close(host_rows(dX, rows), ref["dX"], GRAD_TOL, "dX")
+    # dA / dB of the adapters with the smallest and the largest rank: all their tokens
+    lo, hi = int(np.argmin(spec.ranks)), int(np.argmax(spec.ranks))
+    for i in sorted({lo, hi}):
+        toks = np.flatnonzero(spec.ids == i)
+        if toks.size == 0:
+            continue
+        host_i = {"A": host["A"], "B": host["B"], "x": host_rows(inp["x"], toks),
+                  "dY": host_rows(inp["dY"], toks), "y0": np.zeros((toks.size, spec.d_out)),
+                  "dX0": np.zeros((toks.size, spec.d_in))}
+        sub_i = wl.custom(spec.name, spec.d_in, spec.d_out, spec.ranks, spec.alphas, spec.ids[toks],
+                          sorted_=False)
+        ref_i = oracle_all(sub_i, host_i)
+        check_blocks(spec, dev_to_f64(dA), dev_to_f64(dB), ref_i["dA"], ref_i["dB"], adapters=[i])
