@@ -49,7 +49,8 @@ class c_segments(ctypes.Structure):
     _fields_ = [("n_tokens", ctypes.c_int32), ("n_adapters", ctypes.c_int32), ("max_tiles", ctypes.c_int32),
                 ("sorted", ctypes.c_int32), ("perm", ctypes.c_void_p), ("seg_start", ctypes.c_void_p),
                 ("tiles", ctypes.c_void_p), ("n_tiles", ctypes.c_void_p), ("status", ctypes.c_void_p),
-                ("scratch", ctypes.c_void_p), ("scratch_words", ctypes.c_int64)]
+                ("scratch", ctypes.c_void_p), ("scratch_words", ctypes.c_int64), ("max_spans", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("spans", ctypes.c_void_p), ("n_spans", ctypes.c_void_p)]
 
 
 _lib = None
@@ -189,6 +190,14 @@ class Segments:
     @property
     def tiles(self):
         return self._i32("tiles", 4 * self.c.max_tiles).view(-1, 4)
+
+    @property
+    def n_spans(self):
+        return self._i32("n_spans", 1)
+
+    @property
+    def spans(self):
+        return self._i32("spans", 4 * self.c.max_spans).view(-1, 4)
 
 
 def lora_build_segments(ids=None, seg_offsets=None, n_tokens=None, n_adapters=None, device=None,

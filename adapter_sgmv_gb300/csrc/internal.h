@@ -16,9 +16,9 @@ constexpr int32_t kMaxDim = 1 << 20;
 // word offsets of the regions of a lora_segments storage block
 struct SegLayout {
     bool ok;
-    int32_t n_chunks, max_tiles, block_sums;
+    int32_t n_chunks, max_tiles, max_spans, block_sums;
     int64_t hist_words;
-    int64_t off_perm, off_seg, off_tiles, off_ntiles, off_status, off_scratch;
+    int64_t off_perm, off_seg, off_tiles, off_ntiles, off_status, off_spans, off_nspans, off_scratch;
     int64_t scratch_words, total_words;
 };
 

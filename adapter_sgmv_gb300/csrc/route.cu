@@ -162,25 +162,12 @@ __global__ void route_sorted_kernel(const int32_t *__restrict__ seg_offsets, int
     }
 }
 
-// ---------------------------------------------------------------- tiles
-// One block: seg_start (from the scan, when unsorted), tile counts, their
-// scan, and the tile records.  Inconsistent segments yield no tiles.
-__global__ void route_tiles_kernel(const int32_t *__restrict__ offs, int32_t n_chunks,
-                                   const int32_t *__restrict__ total, int32_t *__restrict__ seg_start,
-                                   int32_t N, const int32_t *__restrict__ perm,
-                                   int32_t *__restrict__ tiles, int32_t *__restrict__ n_tiles,
-                                   int32_t max_tiles, int32_t *__restrict__ status)
+// ---------------------------------------------------------------- tiles and spans
+// Cut every adapter's group into pieces of at most `len` tokens; one record
+// {adapter, begin, rows, flags} per piece, flags bit 0 = consecutive tokens.
+__device__ void emit_pieces(const int32_t *__restrict__ seg_start, int32_t N, const int32_t *__restrict__ perm,
+                            int32_t len, int32_t *__restrict__ out, int32_t *__restrict__ n_out, int32_t max_out)
 {
-    if (offs != nullptr) {  // unsorted: seg_start[i] = offs[i][0], seg_start[N] = total
-        for (int32_t i = threadIdx.x; i <= N; i += blockDim.x)
-            seg_start[i] = i < N ? offs[(int64_t)i * n_chunks] : *total;
-        __syncthreads();
-    }
-    if (*status == LORA_ERR_BAD_SEGMENTS) {
-        for (int32_t i = threadIdx.x; i <= N; i += blockDim.x) seg_start[i] = 0;
-        if (threadIdx.x == 0) *n_tiles = 0;
-        return;
-    }
     int32_t carry = 0;
     for (int32_t i0 = 0; i0 < N; i0 += blockDim.x) {
         const int32_t i = i0 + threadIdx.x;
@@ -189,18 +176,41 @@ __global__ void route_tiles_kernel(const int32_t *__restrict__ offs, int32_t n_c
             begin = seg_start[i];
             n = seg_start[i + 1] - begin;
         }
-        const int32_t cnt = n > 0 ? (n + LORA_TILE_M - 1) / LORA_TILE_M : 0;
+        const int32_t cnt = n > 0 ? (n + len - 1) / len : 0;
         int32_t tot;
         const int32_t base = carry + block_exclusive_scan(cnt, &tot);
-        for (int32_t q = 0; q < cnt && base + q < max_tiles; ++q) {
-            const int32_t b = begin + q * LORA_TILE_M;
-            const int32_t rows = min(LORA_TILE_M, n - q * LORA_TILE_M);
+        for (int32_t q = 0; q < cnt && base + q < max_out; ++q) {
+            const int32_t b = begin + q * len;
+            const int32_t rows = min(len, n - q * len);
             const int32_t contiguous = (perm[b + rows - 1] - perm[b] == rows - 1) ? 1 : 0;
-            reinterpret_cast<int4 *>(tiles)[base + q] = make_int4(i, b, rows, contiguous);
+            reinterpret_cast<int4 *>(out)[base + q] = make_int4(i, b, rows, contiguous);
         }
         carry += tot;
     }
-    if (threadIdx.x == 0) *n_tiles = min(carry, max_tiles);
+    if (threadIdx.x == 0) *n_out = min(carry, max_out);
+}
+
+// One block: seg_start (from the scan, when unsorted), then the tile and span
+// lists.  Inconsistent segments yield no work.
+__global__ void route_tiles_kernel(const int32_t *__restrict__ offs, int32_t n_chunks,
+                                   const int32_t *__restrict__ total, int32_t *__restrict__ seg_start,
+                                   int32_t N, const int32_t *__restrict__ perm, lora_segments s)
+{
+    if (offs != nullptr) {  // unsorted: seg_start[i] = offs[i][0], seg_start[N] = total
+        for (int32_t i = threadIdx.x; i <= N; i += blockDim.x)
+            seg_start[i] = i < N ? offs[(int64_t)i * n_chunks] : *total;
+        __syncthreads();
+    }
+    if (*s.status == LORA_ERR_BAD_SEGMENTS) {
+        for (int32_t i = threadIdx.x; i <= N; i += blockDim.x) seg_start[i] = 0;
+        if (threadIdx.x == 0) {
+            *s.n_tiles = 0;
+            *s.n_spans = 0;
+        }
+        return;
+    }
+    emit_pieces(seg_start, N, perm, LORA_TILE_M, s.tiles, s.n_tiles, s.max_tiles);
+    emit_pieces(seg_start, N, perm, LORA_SPAN_TOKENS, s.spans, s.n_spans, s.max_spans);
 }
 
 // ---------------------------------------------------------------- host side
@@ -211,6 +221,7 @@ SegLayout seg_layout(int32_t T, int32_t N)
     auto up = [](int64_t words) { return (words + 63) & ~int64_t(63); };  // 256-byte regions
     L.n_chunks = (T + 31) / 32;
     L.max_tiles = T / LORA_TILE_M + N + 1;
+    L.max_spans = T / LORA_SPAN_TOKENS + N + 1;
     L.hist_words = (int64_t)N * L.n_chunks;
     if (L.hist_words > kMaxHistWords) return L;
     L.block_sums = (int32_t)((L.hist_words + kScanBlock - 1) / kScanBlock);
@@ -220,6 +231,8 @@ SegLayout seg_layout(int32_t T, int32_t N)
     L.off_tiles = o;      o += up(4 * (int64_t)L.max_tiles);
     L.off_ntiles = o;     o += up(1);
     L.off_status = o;     o += up(1);
+    L.off_spans = o;      o += up(4 * (int64_t)L.max_spans);
+    L.off_nspans = o;     o += up(1);
     L.off_scratch = o;
     L.scratch_words = up(L.hist_words) + up(L.block_sums) + up(1);
     o += L.scratch_words;
@@ -248,6 +261,9 @@ lora_status_t build_segments(const int32_t *ids, const int32_t *seg_offsets, int
     s.status = w + L.off_status;
     s.scratch = w + L.off_scratch;
     s.scratch_words = L.scratch_words;
+    s.max_spans = L.max_spans;
+    s.spans = w + L.off_spans;
+    s.n_spans = w + L.off_nspans;
 
     if (cudaMemsetAsync(s.status, 0, 4, stream) != cudaSuccess) return LORA_ERR_CUDA;
     if (seg_offsets != nullptr) {
@@ -256,8 +272,7 @@ lora_status_t build_segments(const int32_t *ids, const int32_t *seg_offsets, int
         const int blocks = (int)((work + threads - 1) / threads < 1184 ? (work + threads - 1) / threads : 1184);
         route_sorted_kernel<<<blocks > 0 ? blocks : 1, threads, 0, stream>>>(seg_offsets, T, N, s.perm,
                                                                               s.seg_start, s.status);
-        route_tiles_kernel<<<1, 1024, 0, stream>>>(nullptr, 0, nullptr, s.seg_start, N, s.perm, s.tiles,
-                                                   s.n_tiles, s.max_tiles, s.status);
+        route_tiles_kernel<<<1, 1024, 0, stream>>>(nullptr, 0, nullptr, s.seg_start, N, s.perm, s);
     } else {
         int32_t *hist = s.scratch;
         int32_t *bsum = hist + ((L.hist_words + 63) & ~int64_t(63));
@@ -271,11 +286,11 @@ lora_status_t build_segments(const int32_t *ids, const int32_t *seg_offsets, int
             scan_top_kernel<<<1, kScanThreads, 0, stream>>>(bsum, L.block_sums, total);
             scan_apply_kernel<<<L.block_sums, kScanThreads, 0, stream>>>(hist, L.hist_words, bsum);
             route_scatter_kernel<<<blocks, threads, 0, stream>>>(ids, T, N, L.n_chunks, hist, s.perm);
-            route_tiles_kernel<<<1, 1024, 0, stream>>>(hist, L.n_chunks, total, s.seg_start, N, s.perm,
-                                                       s.tiles, s.n_tiles, s.max_tiles, s.status);
+            route_tiles_kernel<<<1, 1024, 0, stream>>>(hist, L.n_chunks, total, s.seg_start, N, s.perm, s);
         } else {  // empty batch: every group empty, no tiles
             if (cudaMemsetAsync(s.seg_start, 0, (size_t)(N + 1) * 4, stream) != cudaSuccess ||
-                cudaMemsetAsync(s.n_tiles, 0, 4, stream) != cudaSuccess)
+                cudaMemsetAsync(s.n_tiles, 0, 4, stream) != cudaSuccess ||
+                cudaMemsetAsync(s.n_spans, 0, 4, stream) != cudaSuccess)
                 return LORA_ERR_CUDA;
         }
     }

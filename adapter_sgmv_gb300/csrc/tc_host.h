@@ -20,4 +20,17 @@ lora_status_t tc_shrink(float *H, const void *x, const lora_adapter_table &tab, 
 lora_status_t tc_dh(float *dH, const void *dY, const lora_adapter_table &tab, const lora_segments &segs,
                     cudaStream_t stream);
 
+// case ii: out[t, n] += c * sum_k h[t, k] W(n, k)   (expand: W = B_i, c = s_i; dX: W = A_i^T, c = 1)
+lora_status_t tc_expand(void *y, const float *H, const lora_adapter_table &tab, const lora_segments &segs,
+                        cudaStream_t stream);
+lora_status_t tc_dx(void *dX, const float *dH, const lora_adapter_table &tab, const lora_segments &segs,
+                    cudaStream_t stream);
+
+// cases iii / iv: G_i[n, k] = c * sum_{t in i} act[t, n] h[t, k]   (dB: act = dY, h = H, c = s_i;
+// dA: act = X, h = dH, c = 1); G is overwritten
+lora_status_t tc_db(float *dB, const void *dY, const float *H, const lora_adapter_table &tab,
+                    const lora_segments &segs, cudaStream_t stream);
+lora_status_t tc_da(float *dA, const float *dH, const void *X, const lora_adapter_table &tab,
+                    const lora_segments &segs, cudaStream_t stream);
+
 }  // namespace lora

@@ -61,6 +61,8 @@ extern "C" {
 #define LORA_MAX_RANK 128
 /* Token rows per work tile of the packed kernels. */
 #define LORA_TILE_M 128
+/* Tokens per span (the work unit of the reductions over tokens, dA and dB). */
+#define LORA_SPAN_TOKENS 1024
 
 /* A CUDA stream (cudaStream_t / CUstream); NULL is the legacy default stream. */
 typedef struct CUstream_st *lora_stream_t;
@@ -117,6 +119,7 @@ typedef struct lora_adapter_table {
  *   tiles[4*max_tiles]  work tiles {adapter, begin (index into perm), rows (1..LORA_TILE_M),
  *                    flags (bit 0: the rows are consecutive token indices)}, ordered by
  *                    adapter then begin; n_tiles[0] of them are valid
+ *   spans[4*max_spans]  the same cut at LORA_SPAN_TOKENS tokens; n_spans[0] valid
  *   status[0]        device status word (an lora_status_t, LORA_OK when clean)
  */
 typedef struct lora_segments {
@@ -131,6 +134,10 @@ typedef struct lora_segments {
     int32_t *status;
     int32_t *scratch;      /* builder-internal counters (histogram / scan) */
     int64_t scratch_words;
+    int32_t max_spans;
+    int32_t reserved;
+    int32_t *spans;
+    int32_t *n_spans;
 } lora_segments;
 
 /* ABI version of the loaded library (LORA_SGMV_ABI_VERSION). */

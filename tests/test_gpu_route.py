@@ -19,24 +19,24 @@ def _lib():
     lora.lib()
 
 
-def check_tiles(segs, seg_start, perm):
-    n_tiles = int(segs.n_tiles.item())
-    tiles = segs.tiles[:n_tiles].cpu().numpy()
-    N = len(seg_start) - 1
-    expect = []
-    for i in range(N):
+def expected_pieces(seg_start, perm, length):
+    out = []
+    for i in range(len(seg_start) - 1):
         n = int(seg_start[i + 1] - seg_start[i])
-        for q in range(0, n, lora_tile()):
+        for q in range(0, n, length):
             b = int(seg_start[i]) + q
-            rows = min(lora_tile(), n - q)
-            contiguous = int(perm[b + rows - 1] - perm[b] == rows - 1)
-            expect.append((i, b, rows, contiguous))
-    assert n_tiles == len(expect)
-    assert [tuple(int(v) for v in t) for t in tiles] == expect
+            rows = min(length, n - q)
+            out.append((i, b, rows, int(perm[b + rows - 1] - perm[b] == rows - 1)))
+    return out
 
 
-def lora_tile():
-    return 128
+def check_tiles(segs, seg_start, perm):
+    """Tiles (128 tokens) and spans (1024 tokens): every adapter's group cut in
+    order, nothing straddling adapters, contiguity flags right."""
+    for length, n_dev, lst in ((128, segs.n_tiles, segs.tiles), (1024, segs.n_spans, segs.spans)):
+        n = int(n_dev.item())
+        got = [tuple(int(v) for v in t) for t in lst[:n].cpu().numpy()]
+        assert got == expected_pieces(seg_start, perm, length)
 
 
 def run_ids(ids_np, N):
@@ -108,5 +108,5 @@ def test_route_inconsistent_offsets_yield_no_work(offsets, T):
     off = torch.tensor(offsets, dtype=torch.int32, device="cuda")
     segs = lora.lora_build_segments(seg_offsets=off, n_tokens=T, n_adapters=len(offsets) - 1)
     assert lora.lora_query_status(segs) == 9
-    assert int(segs.n_tiles.item()) == 0
+    assert int(segs.n_tiles.item()) == 0 and int(segs.n_spans.item()) == 0
     assert np.all(segs.seg_start.cpu().numpy() == 0)
