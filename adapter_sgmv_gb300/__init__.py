@@ -21,7 +21,8 @@ from ._build import LIB_PATH, build as build_library  # noqa: F401
 __all__ = [
     "LoraError", "AdapterTable", "Segments", "lib", "lora_abi_version", "lora_status_string",
     "lora_segments_bytes", "lora_build_segments", "lora_workspace_bytes", "lora_sgmv_shrink",
-    "lora_sgmv_expand", "lora_packed_fwd", "lora_packed_bwd", "lora_query_status", "lora_reset_status",
+    "lora_sgmv_expand", "lora_packed_fwd", "lora_packed_bwd", "lora_packed_bwd_noalloc", "lora_query_status",
+    "lora_reset_status",
     "STATUS",
 ]
 
@@ -71,6 +72,8 @@ SIGNATURES = {
     "lora_packed_fwd": (_I32, [_P, _P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments), _P, _SZ, _P]),
     "lora_packed_bwd": (_I32, [_P, _P, _P, _P, _P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments),
                                _P, _SZ, _P]),
+    "lora_packed_bwd_noalloc": (_I32, [_P, _P, _P, _P, _P, _P, ctypes.POINTER(c_table),
+                                       ctypes.POINTER(c_segments), _P]),
     "lora_query_status": (_I32, [ctypes.POINTER(c_segments), _P]),
     "lora_reset_status": (_I32, [ctypes.POINTER(c_segments), _P]),
 }
@@ -258,6 +261,14 @@ def lora_packed_bwd(dX, dA, dB, dY, X, H_saved, table: AdapterTable, segs: Segme
     _check(lib().lora_packed_bwd(_ptr(dX), _ptr(dA), _ptr(dB), _ptr(dY), _ptr(X), _ptr(H_saved),
                                  ctypes.byref(table.c), ctypes.byref(segs.c), _ptr(ws), wsb, _stream(stream)),
            "lora_packed_bwd")
+
+
+def lora_packed_bwd_noalloc(dX, dA, dB, dY, X, H_saved, table: AdapterTable, segs: Segments, stream=None):
+    """lora_packed_bwd with its scratch in the library's fixed device array
+    (no workspace argument; for callers that cannot allocate)."""
+    _check(lib().lora_packed_bwd_noalloc(_ptr(dX), _ptr(dA), _ptr(dB), _ptr(dY), _ptr(X), _ptr(H_saved),
+                                         ctypes.byref(table.c), ctypes.byref(segs.c), _stream(stream)),
+           "lora_packed_bwd_noalloc")
 
 
 def lora_query_status(segs: Segments, stream=None) -> int:

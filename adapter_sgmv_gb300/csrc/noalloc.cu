@@ -1,0 +1,108 @@
+// noalloc.cu -- lora_packed_bwd_noalloc: the packed backward for callers that
+// cannot allocate device memory.
+//
+// lora_packed_bwd takes its scratch (the fp32 H and dH blocks, T x r_max
+// each) from a caller-provided workspace.  Some callers have no way to get
+// one: code that runs where cudaMalloc is not allowed or not wanted (inside a
+// custom allocator's own callbacks, in a plugin that must not touch the host
+// framework's memory pool, in a process whose device memory is fully reserved
+// by another runtime).  This entry point keeps that scratch in a fixed array
+// in the library's own device memory instead, so it needs no workspace
+// argument and allocates nothing.
+//
+// Costs and rules:
+//  - The array is a file-scope __device__ variable of kScratchBytes (8 MiB);
+//    every GPU that loads the library holds it until the process exits.
+//  - Problems whose scratch exceeds it (2 * T * r_max * 4 bytes, each half
+//    rounded up to 256 bytes) are rejected with LORA_ERR_WORKSPACE_TOO_SMALL
+//    before anything is launched.
+//  - All calls share the one array and the last call's contents stay in it.
+//    Nothing in it has to start at zero: every scratch row a kernel reads is
+//    written earlier in the same call.  Calls whose work overlaps on the GPU
+//    (different streams, or different host threads, same device) race on the
+//    array: serialise them.
+//  - In host code the array's name stands for a host-side shadow, not a
+//    device address.  The first call on each device, with that device
+//    current, resolves the device address once with cudaGetSymbolAddress and
+//    caches it; make that first call before any stream capture.
+#include <mutex>
+
+#include "dispatch.h"
+#include "internal.h"
+
+namespace lora {
+namespace {
+
+constexpr size_t kScratchBytes = size_t(8) << 20;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_bwd_scratch[kScratchBytes];
+
+std::mutex g_mu;
+void *g_addr[kMaxDevices] = {};
+
+// device address of g_bwd_scratch on the current device (nullptr on failure)
+void *scratch_address()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess) return nullptr;
+        g_addr[dev] = p;
+    }
+    return g_addr[dev];
+}
+
+size_t half_bytes(int64_t T, int32_t r_max) { return (size_t)(((T * r_max * 4) + 255) & ~int64_t(255)); }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace lora
+
+using namespace lora;
+
+extern "C" LORA_API lora_status_t lora_packed_bwd_noalloc(void *dX, float *dA, float *dB, const void *dY,
+                                                          const void *X, const float *H_saved,
+                                                          const lora_adapter_table *table,
+                                                          const lora_segments *segs, lora_stream_t stream)
+{
+    if (table == nullptr || segs == nullptr || dY == nullptr || X == nullptr) return LORA_ERR_INVALID_ARG;
+    if (table->rank == nullptr || table->row_off == nullptr || table->scale == nullptr || table->A == nullptr ||
+        table->B == nullptr || segs->perm == nullptr || segs->tiles == nullptr || segs->status == nullptr)
+        return LORA_ERR_INVALID_ARG;
+    if (table->n_adapters < 1 || table->n_adapters > kMaxAdapters || table->r_max < 1 ||
+        table->r_max > LORA_MAX_RANK || table->d_in < 8 || table->d_in > kMaxDim || (table->d_in % 8) != 0 ||
+        table->d_out < 8 || table->d_out > kMaxDim || (table->d_out % 8) != 0 || table->sum_r < table->r_max ||
+        (int64_t)table->sum_r > (int64_t)table->n_adapters * table->r_max)
+        return LORA_ERR_SHAPE;
+    if (segs->n_adapters != table->n_adapters || segs->n_tokens < 0 || segs->n_tokens > kMaxTokens)
+        return LORA_ERR_SHAPE;
+    if (!aligned16(dY) || !aligned16(X) || (dX && !aligned16(dX)) || (dA && !aligned16(dA)) ||
+        (dB && !aligned16(dB)) || (H_saved && !aligned16(H_saved)) || !aligned16(table->A) ||
+        !aligned16(table->B))
+        return LORA_ERR_ALIGNMENT;
+    const int32_t T = segs->n_tokens;
+    const size_t half = half_bytes(T, table->r_max);
+    if (2 * half > kScratchBytes) return LORA_ERR_WORKSPACE_TOO_SMALL;
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return LORA_ERR_CUDA;
+    if (major != 10 || minor != 3) return LORA_ERR_UNSUPPORTED;
+    unsigned char *base = static_cast<unsigned char *>(scratch_address());
+    if (base == nullptr) return LORA_ERR_CUDA;
+    float *wsH = reinterpret_cast<float *>(base);
+    float *wsdH = reinterpret_cast<float *>(base + half);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const float *H = H_saved;
+    if (H == nullptr) {
+        const lora_status_t s = run_shrink(wsH, X, *table, *segs, st);
+        if (s != LORA_OK) return s;
+        H = wsH;
+    }
+    return run_bwd(dX, dA, dB, dY, X, H, wsdH, *table, *segs, st);
+}

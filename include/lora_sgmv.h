@@ -216,6 +216,24 @@ LORA_API lora_status_t lora_packed_bwd(void *dX, float *dA, float *dB, const voi
                               const lora_segments *segs, void *ws, size_t ws_bytes,
                               lora_stream_t stream);
 
+/*
+ * Packed backward without a workspace, for callers that cannot allocate device
+ * memory (no cudaMalloc, no allocator of their own to draw scratch from).  The
+ * pages have no counterpart to this call; it exists only for such callers.
+ * Same arguments and results as lora_packed_bwd minus ws / ws_bytes: the fp32
+ * H / dH scratch lives in a fixed 8 MiB array inside the library's device
+ * memory (held by every GPU that loads the library until exit), so it needs
+ * 2 * T * r_max * 4 bytes (each half rounded up to 256) <= 8 MiB, otherwise
+ * LORA_ERR_WORKSPACE_TOO_SMALL is returned and nothing runs.  Allocates
+ * nothing.  All calls share the array: calls that overlap on the GPU race and
+ * must be serialised by the caller.  The first call on a device resolves the
+ * array's device address (cudaGetSymbolAddress) and caches it; make that first
+ * call before capturing a stream.
+ */
+LORA_API lora_status_t lora_packed_bwd_noalloc(void *dX, float *dA, float *dB, const void *dY, const void *X,
+                                               const float *H_saved, const lora_adapter_table *table,
+                                               const lora_segments *segs, lora_stream_t stream);
+
 /* Synchronise `stream` and return the device status word of `segs`. */
 LORA_API lora_status_t lora_query_status(const lora_segments *segs, lora_stream_t stream);
 

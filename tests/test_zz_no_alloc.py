@@ -1,0 +1,76 @@
+"""lora_packed_bwd_noalloc: the packed backward for callers that cannot
+allocate device memory (its scratch sits in a fixed array inside the library).
+
+It is checked through the C ABI against lora_packed_bwd (the workspace
+version) on the same inputs, on two calls in a row, at the tolerance the
+other gradient tests use.  This file is collected last so that a failure here
+comes after every other test has run."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import adapter_sgmv_gb300 as lora
+import workloads as wl
+from lora_testlib import GRAD_TOL, GpuCase, assert_close, dev_to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lora.build_library()
+    lora.lib()
+
+
+def outputs(case, fn, H):
+    s = case.spec
+    dX = case.inp["dX0"].clone()
+    dA = torch.full((s.sum_r, s.d_in), float("nan"), dtype=torch.float32, device="cuda")
+    dB = torch.full((s.sum_r * s.d_out,), float("nan"), dtype=torch.float32, device="cuda")
+    fn(dX, dA, dB, H)
+    torch.cuda.synchronize()
+    return dev_to_f64(dX), dev_to_f64(dA), dev_to_f64(dB)
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged_unsorted"])
+def test_noalloc_backward_matches_workspace_backward_twice(name):
+    if name == "tiny":
+        spec = wl.tiny()
+    else:
+        rng = np.random.default_rng(21)
+        ranks = [8, 16, 24, 64, 128]
+        spec = wl.custom("ragged", 136, 200, ranks, [2.0 * r for r in ranks],
+                         rng.integers(0, 5, 333).astype(np.int32))
+    case = GpuCase(spec, wl.host_inputs(spec, dX0="randn"))
+    y, H = case.fwd()
+    ref = outputs(case, lambda dX, dA, dB, h: lora.lora_packed_bwd(dX, dA, dB, case.inp["dY"], case.inp["x"], h,
+                                                                  case.table, case.segs, case.ws), H)
+    for call in range(2):
+        for saved in (H, None):
+            got = outputs(case, lambda dX, dA, dB, h: lora.lora_packed_bwd_noalloc(
+                dX, dA, dB, case.inp["dY"], case.inp["x"], h, case.table, case.segs), saved)
+            for g, r, what in zip(got, ref, ("dX", "dA", "dB")):
+                assert_close(g, r, GRAD_TOL, f"{what} (call {call}, H {'saved' if saved is not None else 'recomputed'})")
+    assert lora.lora_query_status(case.segs) == 0
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch():
+    T = 20000  # 2 * 20000 * 128 * 4 bytes > 8 MiB
+    spec = wl.custom("big", 64, 64, [128], [256.0], np.zeros(T, np.int32))
+    dev = torch.device("cuda")
+    A = torch.zeros((128, 64), dtype=torch.bfloat16, device=dev)
+    B = torch.zeros((128 * 64,), dtype=torch.bfloat16, device=dev)
+    table = lora.AdapterTable(A, B, [128], [2.0], 64, 64)
+    segs = lora.lora_build_segments(seg_offsets=torch.tensor([0, T], dtype=torch.int32, device=dev),
+                                    n_tokens=T, n_adapters=1)
+    dY = torch.zeros((T, 64), dtype=torch.bfloat16, device=dev)
+    X = torch.zeros((T, 64), dtype=torch.bfloat16, device=dev)
+    st = lora.lib().lora_packed_bwd_noalloc(None, None, None, ctypes.c_void_p(dY.data_ptr()),
+                                           ctypes.c_void_p(X.data_ptr()), None, ctypes.byref(table.c),
+                                           ctypes.byref(segs.c), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 5  # LORA_ERR_WORKSPACE_TOO_SMALL
+    assert spec.n_tokens == T
