@@ -129,7 +129,8 @@ def lora_segments_bytes(n_tokens: int, n_adapters: int) -> int:
 class AdapterTable:
     """Device-resident stacked adapter table (keeps its tensors alive).
 
-    ``A``: bf16 [sum_r, d_in]; ``B``: bf16 flat, B_i = [d_out, r_i] blocks;
+    ``A``: bf16 [sum_r, d_in] (A_i stacked); ``B``: bf16 [sum_r, d_out]
+    (B_i transposed, stacked the same way: row row_off[i] + k = column k of B_i);
     ``ranks`` / ``scales``: per-adapter rank and s_i = alpha_i / r_i."""
 
     def __init__(self, A, B, ranks, scales, d_in: int, d_out: int):

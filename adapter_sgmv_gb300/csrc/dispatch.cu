@@ -1,36 +1,62 @@
-// dispatch.cu -- choice of kernels for each product of the LoRA delta.
+// dispatch.cu -- the sequence of kernels behind each entry point.
+//
+//   forward:  case i (shrink) writes H (optional fp32 copy for the caller) and
+//             its bf16 hi + lo split in perm order; case ii (expand) reads them.
+//   backward: case i (dh) writes bf16 dH in perm order and converts the saved
+//             H to bf16 in perm order (or case i recomputes it from X);
+//             case iii (dB), case iv (dA) and case ii (dX) read those.
 #include "dispatch.h"
 #include "tc_host.h"
 
 namespace lora {
 
+size_t handoff_region_bytes(int32_t T, int32_t r_max)
+{
+    const int64_t b = (int64_t)T * handoff_cols(r_max) * 2;
+    return (size_t)((b + 255) & ~int64_t(255));
+}
+
+size_t packed_workspace_bytes(int32_t T, int32_t r_max) { return 2 * handoff_region_bytes(T, r_max); }
+
 lora_status_t run_shrink(float *H, const void *x, const lora_adapter_table &tab, const lora_segments &segs,
                          cudaStream_t stream)
 {
-    return tc_shrink(H, x, tab, segs, stream);
+    return tc_shrink(x, tab, segs, H, nullptr, nullptr, 0, stream);
 }
 
 lora_status_t run_expand(void *y, const float *H, const lora_adapter_table &tab, const lora_segments &segs,
                          cudaStream_t stream)
 {
-    return tc_expand(y, H, tab, segs, stream);
+    return tc_expand_f32(y, H, tab, segs, stream);
 }
 
-lora_status_t run_fwd(void *y, float *H, const void *x, const lora_adapter_table &tab,
+lora_status_t run_fwd(void *y, float *H_save, const void *x, void *ws, const lora_adapter_table &tab,
                       const lora_segments &segs, cudaStream_t stream)
 {
-    lora_status_t st = run_shrink(H, x, tab, segs, stream);
+    const int32_t rw = handoff_cols(tab.r_max);
+    uint16_t *hi = static_cast<uint16_t *>(ws);
+    uint16_t *lo = reinterpret_cast<uint16_t *>(static_cast<char *>(ws) + handoff_region_bytes(segs.n_tokens, tab.r_max));
+    lora_status_t st = tc_shrink(x, tab, segs, H_save, hi, lo, rw, stream);
     if (st != LORA_OK) return st;
-    return run_expand(y, H, tab, segs, stream);
+    return tc_expand_bf16(y, hi, lo, rw, tab, segs, stream);
 }
 
-lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X, const float *H, float *dH,
+lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X, const float *H_saved, void *ws,
                       const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream)
 {
-    lora_status_t st = tc_dh(dH, dY, tab, segs, stream);
-    if (st == LORA_OK && dB != nullptr) st = tc_db(dB, dY, H, tab, segs, stream);
-    if (st == LORA_OK && dA != nullptr) st = tc_da(dA, dH, X, tab, segs, stream);
-    if (st == LORA_OK && dX != nullptr) st = tc_dx(dX, dH, tab, segs, stream);
+    const int32_t rw = handoff_cols(tab.r_max);
+    uint16_t *hb = static_cast<uint16_t *>(ws);
+    uint16_t *dhb = reinterpret_cast<uint16_t *>(static_cast<char *>(ws) + handoff_region_bytes(segs.n_tokens, tab.r_max));
+    lora_status_t st;
+    if (H_saved == nullptr) {
+        st = tc_shrink(X, tab, segs, nullptr, hb, nullptr, rw, stream);
+        if (st == LORA_OK) st = tc_dh(dY, tab, segs, dhb, nullptr, nullptr, rw, stream);
+    } else {
+        st = tc_dh(dY, tab, segs, dhb, H_saved, hb, rw, stream);
+    }
+    if (st == LORA_OK && dB != nullptr) st = tc_db(dB, dY, hb, rw, tab, segs, stream);
+    if (st == LORA_OK && dA != nullptr) st = tc_da(dA, X, dhb, rw, tab, segs, stream);
+    if (st == LORA_OK && dX != nullptr) st = tc_dx(dX, dhb, rw, tab, segs, stream);
     return st;
 }
 

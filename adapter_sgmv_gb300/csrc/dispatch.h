@@ -1,17 +1,22 @@
-// dispatch.h -- choice of kernels for each product of the LoRA delta.
+// dispatch.h -- the sequence of kernels behind each entry point.
 #pragma once
 
 #include "internal.h"
 
 namespace lora {
 
+// Workspace of the packed calls: two bf16 hand-off buffers [T, rw] (see tc_host.h).
+size_t handoff_region_bytes(int32_t T, int32_t r_max);
+size_t packed_workspace_bytes(int32_t T, int32_t r_max);
+
 lora_status_t run_shrink(float *H, const void *x, const lora_adapter_table &tab, const lora_segments &segs,
                          cudaStream_t stream);
 lora_status_t run_expand(void *y, const float *H, const lora_adapter_table &tab, const lora_segments &segs,
                          cudaStream_t stream);
-lora_status_t run_fwd(void *y, float *H, const void *x, const lora_adapter_table &tab,
+// ws: packed_workspace_bytes(T, r_max) bytes
+lora_status_t run_fwd(void *y, float *H_save, const void *x, void *ws, const lora_adapter_table &tab,
                       const lora_segments &segs, cudaStream_t stream);
-lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X, const float *H, float *dH,
+lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X, const float *H_saved, void *ws,
                       const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream);
 
 }  // namespace lora

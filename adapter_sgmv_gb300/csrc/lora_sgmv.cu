@@ -55,10 +55,7 @@ lora_status_t check_device()
     return LORA_OK;
 }
 
-// workspace: [H: T x r_max fp32][dH: T x r_max fp32], 256-byte aligned regions
-size_t region_bytes(int64_t T, int32_t r_max) { return (size_t)(((T * r_max * 4) + 255) & ~int64_t(255)); }
-
-size_t workspace_bytes(const lora_adapter_table *t, int32_t T) { return 2 * region_bytes(T, t->r_max); }
+size_t workspace_bytes(const lora_adapter_table *t, int32_t T) { return packed_workspace_bytes(T, t->r_max); }
 
 #define LORA_TRY(expr)                          \
     do {                                        \
@@ -152,15 +149,11 @@ lora_status_t lora_packed_fwd(void *y, float *H_save, const void *x, const lora_
     if (y == nullptr || x == nullptr) return LORA_ERR_INVALID_ARG;
     if (!aligned16(y) || !aligned16(x) || (H_save && !aligned16(H_save)) || (ws && !aligned16(ws)))
         return LORA_ERR_ALIGNMENT;
-    const int32_t T = segs->n_tokens;
-    float *H = H_save;
-    if (H == nullptr) {
-        if (ws == nullptr || ws_bytes < region_bytes(T, table->r_max)) return LORA_ERR_WORKSPACE_TOO_SMALL;
-        H = static_cast<float *>(ws);
-    }
+    const size_t need = workspace_bytes(table, segs->n_tokens);
+    if (need > 0 && (ws == nullptr || ws_bytes < need)) return LORA_ERR_WORKSPACE_TOO_SMALL;
     LORA_TRY(check_device());
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return run_fwd(y, H, x, *table, *segs, st);
+    return run_fwd(y, H_save, x, ws, *table, *segs, st);
 }
 
 lora_status_t lora_packed_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X,
@@ -173,18 +166,11 @@ lora_status_t lora_packed_bwd(void *dX, float *dA, float *dB, const void *dY, co
     if (!aligned16(dY) || !aligned16(X) || (dX && !aligned16(dX)) || (dA && !aligned16(dA)) ||
         (dB && !aligned16(dB)) || (H_saved && !aligned16(H_saved)) || (ws && !aligned16(ws)))
         return LORA_ERR_ALIGNMENT;
-    const int32_t T = segs->n_tokens;
-    if (ws == nullptr || ws_bytes < workspace_bytes(table, T)) return LORA_ERR_WORKSPACE_TOO_SMALL;
+    const size_t need = workspace_bytes(table, segs->n_tokens);
+    if (need > 0 && (ws == nullptr || ws_bytes < need)) return LORA_ERR_WORKSPACE_TOO_SMALL;
     LORA_TRY(check_device());
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    float *wsH = static_cast<float *>(ws);
-    float *wsdH = reinterpret_cast<float *>(static_cast<char *>(ws) + region_bytes(T, table->r_max));
-    const float *H = H_saved;
-    if (H == nullptr) {
-        LORA_TRY(run_shrink(wsH, X, *table, *segs, st));
-        H = wsH;
-    }
-    return run_bwd(dX, dA, dB, dY, X, H, wsdH, *table, *segs, st);
+    return run_bwd(dX, dA, dB, dY, X, H_saved, ws, *table, *segs, st);
 }
 
 lora_status_t lora_query_status(const lora_segments *segs, lora_stream_t stream)

@@ -1,8 +1,8 @@
 // noalloc.cu -- lora_packed_bwd_noalloc: the packed backward for callers that
 // cannot allocate device memory.
 //
-// lora_packed_bwd takes its scratch (the fp32 H and dH blocks, T x r_max
-// each) from a caller-provided workspace.  Some callers have no way to get
+// lora_packed_bwd takes its scratch (the bf16 hand-off copies of H and dH,
+// T x 64 or T x 128 each) from a caller-provided workspace.  Some callers have no way to get
 // one: code that runs where cudaMalloc is not allowed or not wanted (inside a
 // custom allocator's own callbacks, in a plugin that must not touch the host
 // framework's memory pool, in a process whose device memory is fully reserved
@@ -13,9 +13,9 @@
 // Costs and rules:
 //  - The array is a file-scope __device__ variable of kScratchBytes (8 MiB);
 //    every GPU that loads the library holds it until the process exits.
-//  - Problems whose scratch exceeds it (2 * T * r_max * 4 bytes, each half
-//    rounded up to 256 bytes) are rejected with LORA_ERR_WORKSPACE_TOO_SMALL
-//    before anything is launched.
+//  - Problems whose scratch exceeds it (2 * T * rw * 2 bytes, rw = 64 when
+//    r_max <= 64 else 128, each half rounded up to 256 bytes) are rejected
+//    with LORA_ERR_WORKSPACE_TOO_SMALL before anything is launched.
 //  - All calls share the one array and the last call's contents stay in it.
 //    Nothing in it has to start at zero: every scratch row a kernel reads is
 //    written earlier in the same call.  Calls whose work overlaps on the GPU
@@ -55,8 +55,6 @@ void *scratch_address()
     return g_addr[dev];
 }
 
-size_t half_bytes(int64_t T, int32_t r_max) { return (size_t)(((T * r_max * 4) + 255) & ~int64_t(255)); }
-
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -85,24 +83,14 @@ extern "C" LORA_API lora_status_t lora_packed_bwd_noalloc(void *dX, float *dA, f
         !aligned16(table->B))
         return LORA_ERR_ALIGNMENT;
     const int32_t T = segs->n_tokens;
-    const size_t half = half_bytes(T, table->r_max);
-    if (2 * half > kScratchBytes) return LORA_ERR_WORKSPACE_TOO_SMALL;
+    if (packed_workspace_bytes(T, table->r_max) > kScratchBytes) return LORA_ERR_WORKSPACE_TOO_SMALL;
     int dev = 0, major = 0, minor = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
         return LORA_ERR_CUDA;
     if (major != 10 || minor != 3) return LORA_ERR_UNSUPPORTED;
-    unsigned char *base = static_cast<unsigned char *>(scratch_address());
+    void *base = scratch_address();
     if (base == nullptr) return LORA_ERR_CUDA;
-    float *wsH = reinterpret_cast<float *>(base);
-    float *wsdH = reinterpret_cast<float *>(base + half);
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const float *H = H_saved;
-    if (H == nullptr) {
-        const lora_status_t s = run_shrink(wsH, X, *table, *segs, st);
-        if (s != LORA_OK) return s;
-        H = wsH;
-    }
-    return run_bwd(dX, dA, dB, dY, X, H, wsdH, *table, *segs, st);
+    return run_bwd(dX, dA, dB, dY, X, H_saved, base, *table, *segs, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -25,16 +25,6 @@ constexpr int kRows = 32;   // token rows per sub-block
 constexpr int kCols = 64;   // reduction / output columns per step
 constexpr int kPad = kCols + 1;
 
-// W(k, j) accessors ----------------------------------------------------------
-// shrink: W(k, j) = A_i[k, j]          dh: W(k, o) = B_i[o, k]
-template <bool kDH>
-LORA_DEV float rowproj_w(const uint16_t *A, const uint16_t *B, int64_t row_off, int32_t r, int32_t d,
-                         int32_t k, int32_t j)
-{
-    if (kDH) return bf16_to_f32(B[row_off * d + (int64_t)j * r + k]);
-    return bf16_to_f32(A[(row_off + k) * d + j]);
-}
-
 template <bool kDH>
 __global__ void __launch_bounds__(kThreads)
 simt_rowproj_kernel(float *__restrict__ out, const uint16_t *__restrict__ act, lora_adapter_table tab,
@@ -51,8 +41,8 @@ simt_rowproj_kernel(float *__restrict__ out, const uint16_t *__restrict__ act, l
     const int32_t d = kDH ? tab.d_out : tab.d_in;
     const int32_t r = ad.rank, r_max = tab.r_max;
     const float c = kDH ? ad.scale : 1.0f;
-    const uint16_t *A = static_cast<const uint16_t *>(tab.A);
-    const uint16_t *B = static_cast<const uint16_t *>(tab.B);
+    // W(k, j): shrink A_i[k, j]; dh B_i[j, k], i.e. row k of the stacked B_i^T
+    const uint16_t *W = static_cast<const uint16_t *>(kDH ? tab.B : tab.A) + (int64_t)ad.row_off * d;
     const int row = threadIdx.x % kRows, kg = threadIdx.x / kRows;  // k = kg + 8 q
 
     for (int m0 = 0; m0 < tile.rows; m0 += kRows) {
@@ -71,9 +61,8 @@ simt_rowproj_kernel(float *__restrict__ out, const uint16_t *__restrict__ act, l
                 act_s[m][j] = (t >= 0 && j0 + j < d) ? bf16_to_f32(act[(int64_t)t * d + j0 + j]) : 0.f;
             }
             for (int e = threadIdx.x; e < r * kCols; e += kThreads) {
-                int k, j;
-                if (kDH) { j = e / r; k = e % r; } else { k = e / kCols; j = e % kCols; }
-                w_s[k][j] = (j0 + j < d) ? rowproj_w<kDH>(A, B, ad.row_off, r, d, k, j0 + j) : 0.f;
+                const int k = e / kCols, j = e % kCols;
+                w_s[k][j] = (j0 + j < d) ? bf16_to_f32(W[(int64_t)k * d + j0 + j]) : 0.f;
             }
             __syncthreads();
 #pragma unroll 4
@@ -97,8 +86,7 @@ simt_rowproj_kernel(float *__restrict__ out, const uint16_t *__restrict__ act, l
     }
 }
 
-// W(n, k) accessors ----------------------------------------------------------
-// expand: W(o, k) = B_i[o, k]          dX: W(j, k) = A_i[k, j]
+// W(n, k): expand B_i[n, k] (row k of the stacked B_i^T); dX A_i[k, n]
 template <bool kDX>
 __global__ void __launch_bounds__(kThreads)
 simt_colproj_kernel(uint16_t *__restrict__ out, const float *__restrict__ h, lora_adapter_table tab,
@@ -117,8 +105,7 @@ simt_colproj_kernel(uint16_t *__restrict__ out, const float *__restrict__ h, lor
     if (n0 >= d) return;
     const int32_t r = ad.rank, r_max = tab.r_max;
     const float c = kDX ? 1.0f : ad.scale;
-    const uint16_t *A = static_cast<const uint16_t *>(tab.A);
-    const uint16_t *B = static_cast<const uint16_t *>(tab.B);
+    const uint16_t *W = static_cast<const uint16_t *>(kDX ? tab.A : tab.B) + (int64_t)ad.row_off * d;
     const int n = threadIdx.x % kCols, rg = threadIdx.x / kCols;  // rows rg + 4 q
 
     for (int m0 = 0; m0 < tile.rows; m0 += kRows) {
@@ -138,14 +125,8 @@ simt_colproj_kernel(uint16_t *__restrict__ out, const float *__restrict__ h, lor
                 h_s[m][k] = (t >= 0 && k < kn) ? h[(int64_t)t * r_max + k0 + k] : 0.f;
             }
             for (int e = threadIdx.x; e < kCols * kCols; e += kThreads) {
-                int nn, k;
-                if (kDX) { k = e / kCols; nn = e % kCols; } else { nn = e / kCols; k = e % kCols; }
-                float w = 0.f;
-                if (k < kn && n0 + nn < d) {
-                    if (kDX) w = bf16_to_f32(A[(ad.row_off + k0 + k) * (int64_t)d + n0 + nn]);
-                    else     w = bf16_to_f32(B[(int64_t)ad.row_off * d + (int64_t)(n0 + nn) * r + k0 + k]);
-                }
-                w_s[nn][k] = w;
+                const int k = e / kCols, nn = e % kCols;
+                w_s[nn][k] = (k < kn && n0 + nn < d) ? bf16_to_f32(W[(int64_t)(k0 + k) * d + n0 + nn]) : 0.f;
             }
             __syncthreads();
             for (int k = 0; k < kn; ++k) {
@@ -168,9 +149,10 @@ simt_colproj_kernel(uint16_t *__restrict__ out, const float *__restrict__ h, lor
     }
 }
 
-// token reductions: G_i[n, k] = c * sum_{t in i} act[t, n] h[t, k] --------------
-//   dB: act = dY (n = o), h = H,  c = s_i, G stored B-style  (i.e. [d_out, r_i] block)
-//   dA: act = X  (n = j), h = dH, c = 1,   G stored A-style  (i.e. [r_i, d_in] block)
+// token reductions: G_i[n, k] = c * sum_{t in i} act[t, n] h[t, k], stored at
+// row row_off[i] + k, column n of a [sum_r, d] array --------------------------
+//   dB: act = dY (n = o), h = H,  c = s_i  (dB_i^T stacked like B)
+//   dA: act = X  (n = j), h = dH, c = 1    (dA_i stacked like A)
 template <bool kDA>
 __global__ void __launch_bounds__(kThreads)
 simt_tokred_kernel(float *__restrict__ G, const uint16_t *__restrict__ act, const float *__restrict__ h,
@@ -221,10 +203,7 @@ simt_tokred_kernel(float *__restrict__ G, const uint16_t *__restrict__ act, cons
 #pragma unroll
         for (int q = 0; q < LORA_MAX_RANK / 4; ++q) {
             const int k = kg + 4 * q;
-            if (k < r) {
-                if (kDA) G[((int64_t)ad.row_off + k) * d + n0 + n] = c * acc[q];
-                else     G[(int64_t)ad.row_off * d + (int64_t)(n0 + n) * r + k] = c * acc[q];
-            }
+            if (k < r) G[((int64_t)ad.row_off + k) * d + n0 + n] = c * acc[q];
         }
     }
 }

@@ -7,17 +7,20 @@
 //   dX      dX[t, j] +=     sum_k dH[t, k] A_i[k, j]
 //
 // A work item is (tile of up to 128 tokens of one adapter, a 1024-column part
-// of d).  The 128 x r_pad block of H (fp32) is converted once per item into a
-// bf16 A operand; for expand it is split as h = hi + lo (both bf16) and both
-// halves are multiplied, so H enters the product at ~16-bit precision.  The
-// weight block of every 128-column chunk is the B operand: B_i rows (K-major,
-// by cp.async) for expand, A_i columns (MN-major, 128-byte swizzle, by TMA)
-// for dX.  tcgen05.mma (M = 128, N = 128, K = 16) accumulates in a ring of
-// four TMEM accumulators; the epilogue adds c * acc to the bf16 rows in place
-// (fp32 sum, one rounding).
+// of d).  The A operand is the tile's 128 x r_pad block of h in bf16: read by
+// TMA from the perm-ordered hand-off buffers the case i kernel wrote (expand
+// uses h = hi + lo, both multiplied, so H enters at ~16 significant bits), or,
+// for the standalone expand of an fp32 H, converted by four loader warps.  The
+// weights of every 128-column chunk (B_i^T or A_i rows, stacked alike) are the
+// MN-major B operand, by TMA with 128-byte swizzle.  tcgen05.mma (M = 128,
+// N = 128, K = 16) accumulates in a ring of four TMEM accumulators.  The bf16
+// rows being updated are staged through a ring of 128 x 64 shared-memory
+// blocks (TMA for consecutive tokens, cp.async gather otherwise); the epilogue
+// adds c * acc in fp32, rounds once, and writes back with a TMA store (full
+// tiles of consecutive tokens) or plain stores of the valid rows.
 //
-// Warp roles (320 threads): 0 weight loads, 1 MMA + TMEM owner, 2..5 epilogue,
-// 6..9 load and convert the H block.
+// Warp roles: 0 loads (TMA / cp.async), 1 MMA + TMEM owner, 2..5 epilogue,
+// 6..9 (loader variant only) fp32 -> bf16 conversion of the h block.
 #include "internal.h"
 #include "tc_common.cuh"
 #include "tc_host.h"
@@ -27,20 +30,21 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 320;
-constexpr int kWStages = 4;
-constexpr int kLag = 2;
+constexpr int kWStages = 2;
+constexpr int kYStages = 6;
+constexpr int kLagY = 3;
 constexpr int kNC = 128;                              // columns per MMA chunk
 constexpr int kNPart = 1024;                          // columns per work item
 constexpr uint32_t kWBytes = kNC * LORA_MAX_RANK * 2;  // one weight chunk
-constexpr uint32_t kHBytes = 128 * LORA_MAX_RANK * 2;  // one bf16 copy of the H block
-constexpr uint32_t kAcc = 4;                          // TMEM accumulators of 128 columns
+constexpr uint32_t kABytes = 128 * LORA_MAX_RANK * 2;  // one bf16 copy of the h block
+constexpr uint32_t kYBytes = 128 * 64 * 2;             // one staged 128 x 64 block of y
+constexpr uint32_t kAcc = 4;
 constexpr uint32_t kTmemCols = 512;
-constexpr size_t kSmemBytes = 1024 + kWStages * (size_t)kWBytes + 2 * (size_t)kHBytes + 256;
+constexpr size_t kSmemBytes = 1024 + kWStages * (size_t)kWBytes + 2 * (size_t)kABytes + kYStages * (size_t)kYBytes + 768;
 
 struct Smem {
-    uint8_t *w, *hhi, *hlo;
-    uint64_t *wfull, *wempty, *tfull, *tempty, *hfull, *hempty, *done;
+    uint8_t *w, *a, *y;
+    uint64_t *wfull, *wempty, *yfull, *yempty, *ysync, *tfull, *tempty, *afull, *aempty, *done;
     uint32_t *tmem_holder;
     volatile int32_t *abort;
 };
@@ -50,16 +54,19 @@ LORA_DEV Smem carve(uint8_t *raw)
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     Smem s;
     s.w = base;
-    s.hhi = base + kWStages * kWBytes;
-    s.hlo = s.hhi + kHBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(s.hlo + kHBytes);
+    s.a = s.w + kWStages * kWBytes;
+    s.y = s.a + 2 * kABytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(s.y + kYStages * kYBytes);
     s.wfull = bars;
-    s.wempty = bars + kWStages;
-    s.tfull = bars + 2 * kWStages;
+    s.wempty = s.wfull + kWStages;
+    s.yfull = s.wempty + kWStages;
+    s.yempty = s.yfull + kYStages;
+    s.ysync = s.yempty + kYStages;
+    s.tfull = s.ysync + kYStages;
     s.tempty = s.tfull + kAcc;
-    s.hfull = s.tempty + kAcc;
-    s.hempty = s.hfull + 1;
-    s.done = s.hempty + 1;
+    s.afull = s.tempty + kAcc;
+    s.aempty = s.afull + 1;
+    s.done = s.aempty + 1;
     s.tmem_holder = reinterpret_cast<uint32_t *>(s.done + 1);
     s.abort = reinterpret_cast<volatile int32_t *>(s.tmem_holder + 1);
     return s;
@@ -71,6 +78,7 @@ struct Item {
     Tile tile;
     AdapterInfo ad;
     int32_t n_lo, n_hi;
+    bool full;  // 128 consecutive tokens: TMA load and store of y
 };
 
 LORA_DEV Item load_item(const lora_adapter_table &tab, const lora_segments &segs, int32_t it, int32_t n_parts,
@@ -81,30 +89,53 @@ LORA_DEV Item load_item(const lora_adapter_table &tab, const lora_segments &segs
     I.ad = load_adapter(tab, I.tile.adapter, segs.status);
     I.n_lo = (it % n_parts) * kNPart;
     I.n_hi = min(d, I.n_lo + kNPart);
+    I.full = (I.tile.flags & 1) != 0 && I.tile.rows == 128;
     return I;
 }
 
-template <bool kDX>
-__global__ void __launch_bounds__(kThreads, 1)
-tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, uint16_t *__restrict__ out,
-                  const float *__restrict__ h, lora_adapter_table tab, lora_segments segs)
+LORA_DEV void tma_store_2d(const CUtensorMap *map, const void *smem_src, int32_t c0, int32_t c1)
 {
-    constexpr bool kSplit = !kDX;  // expand feeds H as hi + lo
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
+                 "r"(smem_u32(smem_src)), "r"(c0), "r"(c1)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+LORA_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+LORA_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+struct ColIn {
+    const float *h32;  // loader variant: fp32 h by token, stride r_max
+    float use_scale;   // 1: c = s_i, 0: c = 1
+    int32_t split;     // 1: the A operand is hi + lo
+};
+
+template <bool kLoader>
+__global__ void __launch_bounds__(kLoader ? 320 : 192, 1)
+tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_hi,
+                  const __grid_constant__ CUtensorMap map_lo, const __grid_constant__ CUtensorMap map_y,
+                  uint16_t *__restrict__ out, int32_t d, ColIn in, lora_adapter_table tab, lora_segments segs)
+{
     extern __shared__ uint8_t smem_raw[];
     const Smem S = carve(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool split = in.split != 0;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kWStages; ++i) {
-            mbar_init(&S.wfull[i], 33);
+            mbar_init(&S.wfull[i], 1);
             mbar_init(&S.wempty[i], 1);
+        }
+        for (int i = 0; i < kYStages; ++i) {
+            mbar_init(&S.yfull[i], 33);
+            mbar_init(&S.yempty[i], 1);
+            mbar_init(&S.ysync[i], 4);  // one arrive per epilogue warp once its rows are done
         }
         for (uint32_t i = 0; i < kAcc; ++i) {
             mbar_init(&S.tfull[i], 1);
             mbar_init(&S.tempty[i], 4);
         }
-        mbar_init(S.hfull, 4);
-        mbar_init(S.hempty, 1);
+        mbar_init(S.afull, kLoader ? 4 : 1);
+        mbar_init(S.aempty, 1);
         mbar_init(S.done, 1);
         *S.abort = 0;
         fence_barrier_init();
@@ -117,98 +148,139 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, uint16_t *__restric
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *S.tmem_holder;
-    const int32_t d = kDX ? tab.d_in : tab.d_out;
     const int32_t n_parts = (d + kNPart - 1) / kNPart;
     const int32_t n_items = *segs.n_tiles * n_parts;
-    const int32_t r_max = tab.r_max;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ weight producer
-        if (lane == 0 && kDX) prefetch_tensormap(&map_w);
-        const uint16_t *Bw = static_cast<const uint16_t *>(tab.B);
-        uint32_t g = 0;
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tensormap(&map_w);
+            prefetch_tensormap(&map_y);
+            if (!kLoader) {
+                prefetch_tensormap(&map_hi);
+                if (split) prefetch_tensormap(&map_lo);
+            }
+        }
+        uint32_t gw = 0, gy = 0, na = 0;
         bool ok = true;
         for (int32_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const Item I = load_item(tab, segs, it, n_parts, d);
             if (!I.ad.ok) continue;
-            const int32_t r = I.ad.rank, rp = rpad16(r);
-            for (int32_t n0 = I.n_lo; n0 < I.n_hi; n0 += kNC) {
-                const uint32_t s = g % kWStages, ph = (g / kWStages) & 1u;
-                if (!mbar_wait(&S.wempty[s], ph ^ 1u, S.abort, segs.status)) {
+            const int32_t rp = rpad16(I.ad.rank);
+            const bool contiguous = (I.tile.flags & 1) != 0;
+            const int32_t t0 = segs.perm[I.tile.begin];
+            if (!kLoader) {
+                if (!mbar_wait(S.aempty, (na & 1u) ^ 1u, S.abort, segs.status)) {
                     ok = false;
                     break;
                 }
-                uint8_t *w_s = S.w + s * kWBytes;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&S.wfull[s], kDX ? (uint32_t)rp * 256u : 0u);
-                    if (kDX) {
-                        // A_i[k, n0 + 64a ..] as MN-major 128B-swizzled atoms: column a at
-                        // a * (rp * 128), rows k in 16-row boxes
+                    const int natoms = (rp + 63) / 64;
+                    mbar_arrive_expect_tx(S.afull, (uint32_t)natoms * kYBytes * (split ? 2u : 1u));
+                    for (int a = 0; a < natoms; ++a) {
+                        tma_load_2d(S.a + a * kYBytes, &map_hi, S.afull, 64 * a, I.tile.begin);
+                        if (split) tma_load_2d(S.a + kABytes + a * kYBytes, &map_lo, S.afull, 64 * a, I.tile.begin);
+                    }
+                }
+                ++na;
+            }
+            int32_t tok[32];  // rows (lane >> 3) + 4 q of a gathered tile
+            if (!contiguous) {
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    const int m = (lane >> 3) + 4 * q;
+                    tok[q] = m < I.tile.rows ? segs.perm[I.tile.begin + m] : -1;
+                }
+            }
+            for (int32_t n0 = I.n_lo; n0 < I.n_hi && ok; n0 += kNC) {
+                // weights of the chunk: A_i / B_i^T rows k, columns n0 .. n0+127, MN-major atoms
+                {
+                    const uint32_t s = gw % kWStages, ph = (gw / kWStages) & 1u;
+                    if (!mbar_wait(&S.wempty[s], ph ^ 1u, S.abort, segs.status)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        uint8_t *w_s = S.w + s * kWBytes;
+                        mbar_arrive_expect_tx(&S.wfull[s], (uint32_t)rp * 256u);
                         for (int a = 0; a < 2; ++a)
                             for (int q = 0; q < rp / 16; ++q)
                                 tma_load_2d(w_s + a * rp * 128 + q * 2048, &map_w, &S.wfull[s], n0 + 64 * a,
                                             I.ad.row_off + 16 * q);
                     }
+                    ++gw;
                 }
-                if (!kDX) {
-                    // B_i rows o = n0 .. n0+127 as the K-major operand (N = o, K = k):
-                    // chunk (o, k/8) -> (k/8) * 2048 + (o/8) * 128 + (o%8) * 16
-                    const uint16_t *Bi = Bw + (int64_t)I.ad.row_off * d;
-                    const int nchunks = kNC * (rp / 8);
-                    for (int e = lane; e < nchunks; e += 32) {
-                        const int o = e & (kNC - 1), c = e >> 7;
-                        const bool v = (n0 + o < d) && (8 * c < r);
-                        uint8_t *dst = w_s + c * 2048 + (o >> 3) * 128 + (o & 7) * 16;
-                        if ((r & 7) == 0) {
-                            cp_async_16(dst, v ? Bi + (int64_t)(n0 + o) * r + 8 * c : Bw, v);
-                        } else {
-                            uint32_t wv[4];
+                // the two 64-column halves of the chunk's rows of y
+                for (int h = 0; h < 2; ++h) {
+                    const int32_t c0 = n0 + 64 * h;
+                    const uint32_t s = gy % kYStages, ph = (gy / kYStages) & 1u;
+                    if (!mbar_wait(&S.yempty[s], ph ^ 1u, S.abort, segs.status)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *y_s = S.y + s * kYBytes;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&S.yfull[s], contiguous ? kYBytes : 0u);
+                        if (contiguous) tma_load_2d(y_s, &map_y, &S.yfull[s], c0, t0);
+                    }
+                    if (!contiguous) {
+                        const int c = lane & 7;
+                        const bool cin = c0 + 8 * c < d;
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const int k0 = 8 * c + 2 * q;
-                                const uint16_t lo = (v && k0 < r) ? Bi[(int64_t)(n0 + o) * r + k0] : 0;
-                                const uint16_t hi = (v && k0 + 1 < r) ? Bi[(int64_t)(n0 + o) * r + k0 + 1] : 0;
-                                wv[q] = (uint32_t)lo | ((uint32_t)hi << 16);
-                            }
-                            *reinterpret_cast<uint4 *>(dst) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                        for (int q = 0; q < 32; ++q) {
+                            const int m = (lane >> 3) + 4 * q;
+                            const bool v = tok[q] >= 0 && cin;
+                            const uint16_t *src = v ? out + (int64_t)tok[q] * d + c0 + 8 * c : out;
+                            cp_async_16(y_s + sw128_offset(m, c), src, v);
                         }
                     }
+                    cp_async_commit();
+                    if (gy >= (uint32_t)kLagY) {
+                        cp_async_wait<kLagY>();
+                        fence_proxy_async();
+                        mbar_arrive(&S.yfull[(gy - kLagY) % kYStages]);
+                    }
+                    ++gy;
                 }
-                cp_async_commit();
-                if (g >= (uint32_t)kLag) {
-                    cp_async_wait<kLag>();
-                    fence_proxy_async();
-                    mbar_arrive(&S.wfull[(g - kLag) % kWStages]);
-                }
-                ++g;
             }
         }
         cp_async_wait<0>();
         fence_proxy_async();
-        for (uint32_t u = g > (uint32_t)kLag ? g - kLag : 0u; u < g; ++u) mbar_arrive(&S.wfull[u % kWStages]);
-        if (!ok && lane == 0) {
-            for (uint32_t u = g > (uint32_t)kWStages ? g - kWStages : 0u; u < g; ++u) {
+        for (uint32_t u = gy > (uint32_t)kLagY ? gy - kLagY : 0u; u < gy; ++u) mbar_arrive(&S.yfull[u % kYStages]);
+        if (!ok && lane == 0) {  // aborted: let issued copies land before the CTA leaves
+            for (uint32_t u = gy > (uint32_t)kYStages ? gy - kYStages : 0u; u < gy; ++u) {
+                uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(&S.yfull[u % kYStages], (u / kYStages) & 1u) &&
+                       globaltimer_ns() - t0 < kWaitLimitNs / 8) {
+                }
+            }
+            for (uint32_t u = gw > (uint32_t)kWStages ? gw - kWStages : 0u; u < gw; ++u) {
                 uint64_t t0 = globaltimer_ns();
                 while (!mbar_try_wait(&S.wfull[u % kWStages], (u / kWStages) & 1u) &&
                        globaltimer_ns() - t0 < kWaitLimitNs / 8) {
+                }
+            }
+            if (!kLoader && na > 0) {
+                uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(S.afull, (na - 1) & 1u) && globaltimer_ns() - t0 < kWaitLimitNs / 8) {
                 }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t g = 0, a = 0, hn = 0;
+            uint32_t gw = 0, a = 0, na = 0;
             bool ok = true;
-            const uint32_t idesc = make_idesc_bf16(128, kNC, false, kDX);
-            const uint32_t hhi = smem_u32(S.hhi), hlo = smem_u32(S.hlo);
+            const uint32_t idesc = make_idesc_bf16(128, kNC, false, true);
+            const uint32_t abase = smem_u32(S.a);
             for (int32_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
                 const Item I = load_item(tab, segs, it, n_parts, d);
                 if (!I.ad.ok) continue;
                 const int32_t rp = rpad16(I.ad.rank);
-                if (!mbar_wait(S.hfull, hn & 1u, S.abort, segs.status)) break;
+                if (!mbar_wait(S.afull, na & 1u, S.abort, segs.status)) break;
                 tc_fence_after();
                 for (int32_t n0 = I.n_lo; n0 < I.n_hi; n0 += kNC) {
-                    const uint32_t s = g % kWStages, ph = (g / kWStages) & 1u;
+                    const uint32_t s = gw % kWStages, ph = (gw / kWStages) & 1u;
                     const uint32_t acc = a % kAcc, aph = (a / kAcc) & 1u;
                     if (!mbar_wait(&S.tempty[acc], aph ^ 1u, S.abort, segs.status) ||
                         !mbar_wait(&S.wfull[s], ph, S.abort, segs.status)) {
@@ -219,22 +291,22 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, uint16_t *__restric
                     const uint32_t w_base = smem_u32(S.w + s * kWBytes);
                     const uint32_t d_tmem = tmem_base + acc * 128u;
                     for (int kk = 0; kk < rp / 16; ++kk) {
-                        const uint64_t bdesc = kDX ? make_desc(w_base + 2048u * kk, (uint32_t)rp * 128u, 1024,
-                                                               kSwizzle128)
-                                                   : make_desc(w_base + 4096u * kk, 2048, 128, kInterleave);
-                        umma_bf16(d_tmem, make_desc(hhi + 4096u * kk, 2048, 128, kInterleave), bdesc, idesc,
+                        const uint32_t aoff = (uint32_t)(kk >> 2) * kYBytes + (uint32_t)(kk & 3) * 32u;
+                        const uint64_t bdesc = make_desc(w_base + 2048u * kk, (uint32_t)rp * 128u, 1024, kSwizzle128);
+                        umma_bf16(d_tmem, make_desc(abase + aoff, 16, 1024, kSwizzle128), bdesc, idesc,
                                   kk > 0 ? 1u : 0u);
-                        if (kSplit)
-                            umma_bf16(d_tmem, make_desc(hlo + 4096u * kk, 2048, 128, kInterleave), bdesc, idesc, 1u);
+                        if (split)
+                            umma_bf16(d_tmem, make_desc(abase + kABytes + aoff, 16, 1024, kSwizzle128), bdesc, idesc,
+                                      1u);
                     }
                     umma_commit(&S.wempty[s]);
                     umma_commit(&S.tfull[acc]);
-                    ++g;
+                    ++gw;
                     ++a;
                 }
                 if (!ok) break;
-                umma_commit(S.hempty);
-                ++hn;
+                umma_commit(S.aempty);
+                ++na;
             }
             umma_commit(S.done);
             uint64_t t0 = globaltimer_ns();
@@ -242,58 +314,52 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, uint16_t *__restric
             }
         }
         __syncwarp();
-    } else if (warp >= 6) {
-        // ------------------------------------------------------------ H block loader
+    } else if (kLoader && warp >= 6) {
+        // ------------------------------------------------------------ fp32 h -> bf16 A operand
         const int m = threadIdx.x - 6 * 32;  // row 0..127 of the tile
-        const bool vec = (r_max & 3) == 0;
-        uint32_t hn = 0;
+        const int32_t r_max = tab.r_max;
+        uint32_t na = 0;
         for (int32_t it = blockIdx.x; it < n_items; it += gridDim.x) {
             const Item I = load_item(tab, segs, it, n_parts, d);
             if (!I.ad.ok) continue;
             const int32_t r = I.ad.rank, rp = rpad16(r);
-            if (!mbar_wait(S.hempty, (hn & 1u) ^ 1u, S.abort, segs.status)) break;
+            if (!mbar_wait(S.aempty, (na & 1u) ^ 1u, S.abort, segs.status)) break;
             const int32_t t = m < I.tile.rows ? segs.perm[I.tile.begin + m] : -1;
-            const float *hr = h + (int64_t)(t < 0 ? 0 : t) * r_max;
+            const float *hr = in.h32 + (int64_t)(t < 0 ? 0 : t) * r_max;
+#pragma unroll 4
             for (int kc = 0; kc < rp / 8; ++kc) {
                 float f[8];
-                if (t >= 0 && vec && 8 * kc + 8 <= r_max) {
-                    const float4 u0 = *reinterpret_cast<const float4 *>(hr + 8 * kc);
-                    const float4 u1 = *reinterpret_cast<const float4 *>(hr + 8 * kc + 4);
-                    f[0] = u0.x; f[1] = u0.y; f[2] = u0.z; f[3] = u0.w;
-                    f[4] = u1.x; f[5] = u1.y; f[6] = u1.z; f[7] = u1.w;
-                } else {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = (t >= 0 && 8 * kc + e < r_max) ? hr[8 * kc + e] : 0.f;
-                }
+                for (int e = 0; e < 8; ++e) f[e] = (t >= 0 && 8 * kc + e < r) ? hr[8 * kc + e] : 0.f;
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int e = 0; e < 8; e += 2) {
-                    const float a0 = (8 * kc + e < r) ? f[e] : 0.f;
-                    const float a1 = (8 * kc + e + 1 < r) ? f[e + 1] : 0.f;
-                    hi[e / 2] = pack_bf16(a0, a1);
-                    lo[e / 2] = pack_bf16(a0 - bf16lo(hi[e / 2]), a1 - bf16hi(hi[e / 2]));
+                    hi[e / 2] = pack_bf16(f[e], f[e + 1]);
+                    lo[e / 2] = pack_bf16(f[e] - bf16lo(hi[e / 2]), f[e + 1] - bf16hi(hi[e / 2]));
                 }
-                const uint32_t off = (uint32_t)kc * 2048u + (uint32_t)m * 16u;
-                *reinterpret_cast<uint4 *>(S.hhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                if (kSplit) *reinterpret_cast<uint4 *>(S.hlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                const uint32_t off = (uint32_t)(kc >> 3) * kYBytes + sw128_offset((uint32_t)m, (uint32_t)(kc & 7));
+                *reinterpret_cast<uint4 *>(S.a + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                if (split) *reinterpret_cast<uint4 *>(S.a + kABytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
             fence_proxy_async();
             __syncwarp();
-            if (lane == 0) mbar_arrive(S.hfull);
-            ++hn;
+            if (lane == 0) mbar_arrive(S.afull);
+            ++na;
         }
-    } else {
+    } else if (warp >= 2 && warp <= 5) {
         // ------------------------------------------------------------ epilogue
         const uint32_t lane_base = 32u * (warp & 3);
         const int m = (int)lane_base + lane;
-        uint32_t a = 0;
-        for (int32_t it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const bool leader = warp == 2 && lane == 0;
+        uint32_t a = 0, gy = 0;
+        bool ok = true;
+        for (int32_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const Item I = load_item(tab, segs, it, n_parts, d);
             if (!I.ad.ok) continue;
-            const float c = kDX ? 1.0f : I.ad.scale;
+            const float c = in.use_scale != 0.f ? I.ad.scale : 1.0f;
             const int32_t t = m < I.tile.rows ? segs.perm[I.tile.begin + m] : -1;
+            const int32_t t0 = segs.perm[I.tile.begin];
             uint16_t *row = out + (int64_t)(t < 0 ? 0 : t) * d;
-            bool ok = true;
             for (int32_t n0 = I.n_lo; n0 < I.n_hi; n0 += kNC) {
                 const uint32_t acc = a % kAcc, aph = (a / kAcc) & 1u;
                 if (!mbar_wait(&S.tfull[acc], aph, S.abort, segs.status)) {
@@ -302,43 +368,66 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, uint16_t *__restric
                 }
                 tc_fence_after();
 #pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    const int32_t c0 = n0 + 64 * half;
+                for (int h = 0; h < 2; ++h) {
+                    const int32_t c0 = n0 + 64 * h;
+                    const uint32_t s = gy % kYStages, ph = (gy / kYStages) & 1u;
+                    if (!mbar_wait(&S.yfull[s], ph, S.abort, segs.status)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *y_s = S.y + s * kYBytes;
                     uint4 yv[8];
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
-                        yv[q] = (t >= 0 && c0 + 8 * q < d) ? *reinterpret_cast<const uint4 *>(row + c0 + 8 * q)
-                                                           : make_uint4(0, 0, 0, 0);
+                        yv[q] = *reinterpret_cast<const uint4 *>(y_s + sw128_offset((uint32_t)m, (uint32_t)q));
                     uint32_t v[4][16];
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        tmem_ld16(tmem_base + (lane_base << 16) + acc * 128u + 64u * half + 16u * q, v[q]);
+                        tmem_ld16(tmem_base + (lane_base << 16) + acc * 128u + 64u * h + 16u * q, v[q]);
                     tmem_ld_wait();
-                    if (half == 1) {
+                    if (h == 1) {
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&S.tempty[acc]);
                     }
-                    if (t >= 0) {
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            if (c0 + 8 * q >= d) continue;
-                            const uint32_t *acc8 = &v[q >> 1][(q & 1) * 8];
-                            uint32_t w[4] = {yv[q].x, yv[q].y, yv[q].z, yv[q].w};
+                    for (int q = 0; q < 8; ++q) {
+                        const uint32_t *acc8 = &v[q >> 1][(q & 1) * 8];
+                        uint32_t w[4] = {yv[q].x, yv[q].y, yv[q].z, yv[q].w};
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float lo = bf16lo(w[e]) + c * __uint_as_float(acc8[2 * e]);
-                                const float hi = bf16hi(w[e]) + c * __uint_as_float(acc8[2 * e + 1]);
-                                w[e] = pack_bf16(lo, hi);
+                        for (int e = 0; e < 4; ++e) {
+                            const float lo = bf16lo(w[e]) + c * __uint_as_float(acc8[2 * e]);
+                            const float hi = bf16hi(w[e]) + c * __uint_as_float(acc8[2 * e + 1]);
+                            w[e] = pack_bf16(lo, hi);
+                        }
+                        const uint4 nv = make_uint4(w[0], w[1], w[2], w[3]);
+                        if (I.full)
+                            *reinterpret_cast<uint4 *>(y_s + sw128_offset((uint32_t)m, (uint32_t)q)) = nv;
+                        else if (t >= 0 && c0 + 8 * q < d)
+                            *reinterpret_cast<uint4 *>(row + c0 + 8 * q) = nv;
+                    }
+                    if (I.full) fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&S.ysync[s]);
+                    if (leader) {  // all four warps' rows are in place: store the block, free the stage
+                        if (!mbar_wait(&S.ysync[s], ph, S.abort, segs.status)) {
+                            ok = false;
+                        } else {
+                            if (I.full) {
+                                tma_store_2d(&map_y, y_s, c0, t0);
+                                bulk_wait_read0();
                             }
-                            *reinterpret_cast<uint4 *>(row + c0 + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+                            mbar_arrive(&S.yempty[s]);
                         }
                     }
+                    ++gy;
+                    if (!ok) break;
                 }
+                if (!ok) break;
                 ++a;
             }
-            if (!ok) break;
         }
+        if (leader) bulk_wait0();
     }
 
     tc_fence_before();
@@ -349,39 +438,64 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, uint16_t *__restric
     }
 }
 
-template <bool kDX>
-lora_status_t launch_colproj(void *out, const float *h, const lora_adapter_table &tab, const lora_segments &segs,
+template <bool kLoader>
+lora_status_t launch_colproj(uint16_t *out, int32_t d, const void *w, const uint16_t *hi, const uint16_t *lo,
+                             int32_t rw, const ColIn &in, const lora_adapter_table &tab, const lora_segments &segs,
                              cudaStream_t stream)
 {
     if (segs.n_tokens == 0 || segs.max_tiles == 0) return LORA_OK;
-    const int32_t d = kDX ? tab.d_in : tab.d_out;
-    CUtensorMap map_w;
-    if (!make_tmap_bf16_2d(&map_w, tab.A, (uint64_t)tab.d_in, (uint64_t)tab.sum_r, 64, 16, true))
+    CUtensorMap map_w, map_hi, map_lo, map_y;
+    if (!make_tmap_bf16_2d(&map_w, w, (uint64_t)d, (uint64_t)tab.sum_r, 64, 16, true) ||
+        !make_tmap_bf16_2d(&map_y, out, (uint64_t)d, (uint64_t)segs.n_tokens, 64, 128, true))
         return LORA_ERR_CUDA;
-    if (cudaFuncSetAttribute(tc_colproj_kernel<kDX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (!kLoader) {
+        if (!make_tmap_bf16_2d(&map_hi, hi, (uint64_t)rw, (uint64_t)segs.n_tokens, 64, 128, true))
+            return LORA_ERR_CUDA;
+        if (lo != nullptr) {
+            if (!make_tmap_bf16_2d(&map_lo, lo, (uint64_t)rw, (uint64_t)segs.n_tokens, 64, 128, true))
+                return LORA_ERR_CUDA;
+        } else {
+            map_lo = map_hi;
+        }
+    } else {
+        map_hi = map_y;
+        map_lo = map_y;
+    }
+    if (cudaFuncSetAttribute(tc_colproj_kernel<kLoader>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
         return LORA_ERR_CUDA;
     const int n_parts = (d + kNPart - 1) / kNPart;
     const int64_t items = (int64_t)segs.max_tiles * n_parts;
     const int sms = sm_count();
     const int grid = items < sms ? (int)items : sms;
-    tc_colproj_kernel<kDX><<<grid, kThreads, kSmemBytes, stream>>>(map_w, static_cast<uint16_t *>(out), h, tab,
-                                                                    segs);
+    tc_colproj_kernel<kLoader><<<grid, kLoader ? 320 : 192, kSmemBytes, stream>>>(map_w, map_hi, map_lo, map_y, out,
+                                                                                  d, in, tab, segs);
     return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
 }  // namespace
 
-lora_status_t tc_expand(void *y, const float *H, const lora_adapter_table &tab, const lora_segments &segs,
-                        cudaStream_t stream)
+lora_status_t tc_expand_bf16(void *y, const uint16_t *hi, const uint16_t *lo, int32_t rw,
+                             const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream)
 {
-    return launch_colproj<false>(y, H, tab, segs, stream);
+    ColIn in{nullptr, 1.f, lo != nullptr ? 1 : 0};
+    return launch_colproj<false>(static_cast<uint16_t *>(y), tab.d_out, tab.B, hi, lo, rw, in, tab, segs, stream);
 }
 
-lora_status_t tc_dx(void *dX, const float *dH, const lora_adapter_table &tab, const lora_segments &segs,
-                    cudaStream_t stream)
+lora_status_t tc_expand_f32(void *y, const float *H, const lora_adapter_table &tab, const lora_segments &segs,
+                            cudaStream_t stream)
 {
-    return launch_colproj<true>(dX, dH, tab, segs, stream);
+    ColIn in{H, 1.f, 1};
+    return launch_colproj<true>(static_cast<uint16_t *>(y), tab.d_out, tab.B, nullptr, nullptr, 0, in, tab, segs,
+                                stream);
+}
+
+lora_status_t tc_dx(void *dX, const uint16_t *dh_bf16, int32_t rw, const lora_adapter_table &tab,
+                    const lora_segments &segs, cudaStream_t stream)
+{
+    ColIn in{nullptr, 0.f, 0};
+    return launch_colproj<false>(static_cast<uint16_t *>(dX), tab.d_in, tab.A, dh_bf16, nullptr, rw, in, tab, segs,
+                                 stream);
 }
 
 }  // namespace lora

@@ -14,23 +14,33 @@ bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64
                        uint32_t box_rows, bool swizzle128);
 int sm_count();
 
-// case i: out[t, k] = c * sum_j act[t, j] W(k, j)   (shrink: W = A_i, c = 1; dh: W = B_i^T, c = s_i)
-lora_status_t tc_shrink(float *H, const void *x, const lora_adapter_table &tab, const lora_segments &segs,
-                        cudaStream_t stream);
-lora_status_t tc_dh(float *dH, const void *dY, const lora_adapter_table &tab, const lora_segments &segs,
-                    cudaStream_t stream);
+// Hand-off buffers between the kernels: bf16 [T, rw] rows in perm order (the
+// position of the token in its adapter's group), zero beyond each adapter's rank.
+inline int32_t handoff_cols(int32_t r_max) { return r_max <= 64 ? 64 : 128; }
 
-// case ii: out[t, n] += c * sum_k h[t, k] W(n, k)   (expand: W = B_i, c = s_i; dX: W = A_i^T, c = 1)
-lora_status_t tc_expand(void *y, const float *H, const lora_adapter_table &tab, const lora_segments &segs,
-                        cudaStream_t stream);
-lora_status_t tc_dx(void *dX, const float *dH, const lora_adapter_table &tab, const lora_segments &segs,
-                    cudaStream_t stream);
+// case i.  shrink: H[t, :] = A_i x_t.  Writes the fp32 H by token (H may be
+// null) and/or its bf16 hi (+ lo) split by perm position (null to skip).
+lora_status_t tc_shrink(const void *x, const lora_adapter_table &tab, const lora_segments &segs, float *H,
+                        uint16_t *hi, uint16_t *lo, int32_t rw, cudaStream_t stream);
+// case i.  dh = s_i B_i^T dy as bf16 by perm position; when h_saved is given,
+// also converts it (fp32 by token) into h_bf16 (bf16 by perm position).
+lora_status_t tc_dh(const void *dY, const lora_adapter_table &tab, const lora_segments &segs, uint16_t *dh_bf16,
+                    const float *h_saved, uint16_t *h_bf16, int32_t rw, cudaStream_t stream);
 
-// cases iii / iv: G_i[n, k] = c * sum_{t in i} act[t, n] h[t, k]   (dB: act = dY, h = H, c = s_i;
-// dA: act = X, h = dH, c = 1); G is overwritten
-lora_status_t tc_db(float *dB, const void *dY, const float *H, const lora_adapter_table &tab,
+// case ii.  y += s_i B_i h from the bf16 hand-off buffers (lo may be null).
+lora_status_t tc_expand_bf16(void *y, const uint16_t *hi, const uint16_t *lo, int32_t rw,
+                             const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream);
+// case ii.  y += s_i B_i h from an fp32 H by token (converted in the kernel).
+lora_status_t tc_expand_f32(void *y, const float *H, const lora_adapter_table &tab, const lora_segments &segs,
+                            cudaStream_t stream);
+// case ii.  dX += A_i^T dh from the bf16 hand-off buffer.
+lora_status_t tc_dx(void *dX, const uint16_t *dh_bf16, int32_t rw, const lora_adapter_table &tab,
                     const lora_segments &segs, cudaStream_t stream);
-lora_status_t tc_da(float *dA, const float *dH, const void *X, const lora_adapter_table &tab,
+
+// cases iii / iv, output [sum_r, d] overwritten: dB[row_off + k, o] and dA[row_off + k, j].
+lora_status_t tc_db(float *dB, const void *dY, const uint16_t *h_bf16, int32_t rw, const lora_adapter_table &tab,
+                    const lora_segments &segs, cudaStream_t stream);
+lora_status_t tc_da(float *dA, const void *X, const uint16_t *dh_bf16, int32_t rw, const lora_adapter_table &tab,
                     const lora_segments &segs, cudaStream_t stream);
 
 }  // namespace lora

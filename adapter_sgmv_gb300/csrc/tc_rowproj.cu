@@ -6,17 +6,23 @@
 //   shrink  H[t, k]  = sum_j x[t, j]  A_i[k, j]          (c = 1)
 //   dh      dH[t, k] = s_i sum_o dY[t, o] B_i[o, k]       (c = s_i)
 //
-// One work tile = up to 128 tokens of one adapter.  Per 64-wide slice of the
-// hidden dimension a stage holds the 128 x 64 activation block (K-major,
-// 128-byte swizzle, by TMA when the rows are consecutive tokens, else
-// gathered with cp.async) and the r_pad x 64 weight block (shrink: A_i rows by
-// TMA; dh: B_i rows by cp.async into the interleaved MN-major layout).  One
-// thread issues tcgen05.mma (M = 128, N = r_pad, K = 16) into a TMEM
-// accumulator; four epilogue warps read it back and write fp32 rows.
+// A and B are stored alike (A_i and B_i^T stacked, [sum_r, d]), so both
+// products read their weights the same way: r_pad x 64 blocks by TMA as the
+// K-major B operand.  One work tile = up to 128 tokens of one adapter.  Per
+// 64-wide slice of d a stage holds the 128 x 64 activation block (K-major,
+// 128-byte swizzle: TMA when the rows are consecutive tokens, else cp.async
+// gather) and the weight block; one thread issues tcgen05.mma (M = 128,
+// N = r_pad, K = 16) into a TMEM accumulator; four epilogue warps write
+//   - out_f32[t, :]  = c * acc   (fp32, stride r_max; optional)
+//   - out_hi[p, :]   = bf16(c * acc), out_lo[p, :] = bf16(c * acc - hi)
+//     (row p = the token's position in perm, stride rw; both optional)
+//   - hin_bf16[p, :] = bf16(hin[t, :])  (optional: converts a saved fp32 H
+//     into the same hand-off format, for the backward)
+// with zeros in columns r_i .. end.  The perm-ordered bf16 rows are what the
+// case ii / iii / iv kernels read by TMA.
 //
 // Warp roles (192 threads): 0 loads, 1 issues MMAs and owns TMEM, 2..5 epilogue.
-// Pipelines: kStages smem stages (full / empty mbarriers), two TMEM
-// accumulators (tfull / tempty).  Every wait is bounded (tc::mbar_wait).
+// Every wait is bounded (tc::mbar_wait).
 #include "internal.h"
 #include "tc_common.cuh"
 #include "tc_host.h"
@@ -29,7 +35,7 @@ using namespace tc;
 constexpr int kStages = 6;
 constexpr int kLag = 3;            // cp.async groups kept in flight per producer lane
 constexpr int kThreads = 192;
-constexpr uint32_t kActBytes = 128 * 64 * 2;     // one stage of activations
+constexpr uint32_t kActBytes = 128 * 64 * 2;
 constexpr uint32_t kWBytes = LORA_MAX_RANK * 64 * 2;
 constexpr uint32_t kStageBytes = kActBytes + kWBytes;
 constexpr uint32_t kTmemCols = 256;  // two accumulators of up to 128 columns
@@ -61,10 +67,18 @@ LORA_DEV Smem carve(uint8_t *raw)
 
 LORA_DEV int32_t rpad16(int32_t r) { return (r + 15) & ~15; }
 
-template <bool kDH>
+struct RowOut {
+    float *f32;           // [T, r_max] by token, or null
+    uint16_t *hi, *lo;    // [T, rw] by perm position, or null
+    const float *hin;     // [T, r_max] fp32 by token to convert, or null
+    uint16_t *hin_bf16;   // [T, rw] by perm position
+    int32_t rw;
+    float scale_is_adapter;  // 1: c = s_i, 0: c = 1
+};
+
 __global__ void __launch_bounds__(kThreads, 1)
 tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_w,
-                  float *__restrict__ out, const uint16_t *__restrict__ act, lora_adapter_table tab,
+                  const uint16_t *__restrict__ act, int32_t d, RowOut o, lora_adapter_table tab,
                   lora_segments segs)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -93,15 +107,13 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
     tc_fence_after();
     const uint32_t tmem_base = *S.tmem_holder;
     const int32_t n_tiles = *segs.n_tiles;
-    const int32_t d = kDH ? tab.d_out : tab.d_in;
     const int32_t nk = (d + 63) / 64;
-    const uint16_t *Bw = static_cast<const uint16_t *>(tab.B);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             prefetch_tensormap(&map_act);
-            if (!kDH) prefetch_tensormap(&map_w);
+            prefetch_tensormap(&map_w);
         }
         uint32_t g = 0;
         bool ok = true;
@@ -109,7 +121,7 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
             const Tile T = load_tile(segs.tiles, ti);
             const AdapterInfo ad = load_adapter(tab, T.adapter, segs.status);
             if (!ad.ok) continue;
-            const int32_t r = ad.rank, rp = rpad16(r);
+            const int32_t rp = rpad16(ad.rank);
             const bool contiguous = (T.flags & 1) != 0;
             const int32_t t0 = segs.perm[T.begin];
             int32_t tok[32];  // rows (lane >> 3) + 4 q of a gathered tile
@@ -130,12 +142,10 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
                 uint8_t *act_s = S.act + s * kActBytes;
                 uint8_t *w_s = S.w + s * kWBytes;
                 if (lane == 0) {
-                    const uint32_t bytes = (contiguous ? kActBytes : 0u) + (kDH ? 0u : (uint32_t)rp * 128u);
-                    mbar_arrive_expect_tx(&S.full[s], bytes);
+                    mbar_arrive_expect_tx(&S.full[s], (contiguous ? kActBytes : 0u) + (uint32_t)rp * 128u);
                     if (contiguous) tma_load_2d(act_s, &map_act, &S.full[s], j0, t0);
-                    if (!kDH)
-                        for (int q = 0; q < rp / 16; ++q)
-                            tma_load_2d(w_s + q * 2048, &map_w, &S.full[s], j0, ad.row_off + 16 * q);
+                    for (int q = 0; q < rp / 16; ++q)
+                        tma_load_2d(w_s + q * 2048, &map_w, &S.full[s], j0, ad.row_off + 16 * q);
                 }
                 if (!contiguous) {
                     const int c = lane & 7;
@@ -146,31 +156,6 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
                         const bool v = tok[q] >= 0 && cin;
                         const uint16_t *src = v ? act + (int64_t)tok[q] * d + j0 + 8 * c : act;
                         cp_async_16(act_s + sw128_offset(m, c), src, v);
-                    }
-                }
-                if (kDH) {
-                    // B_i rows o = j0 .. j0+63 as the MN-major operand (N = k, K = o):
-                    // 16-byte chunk (o, k/8) -> (k/8) * 1024 + (o/8) * 128 + (o%8) * 16
-                    const uint16_t *Bi = Bw + (int64_t)ad.row_off * d;
-                    const int nchunks = 64 * (rp / 8);
-                    for (int e = lane; e < nchunks; e += 32) {
-                        const int o = e & 63, c = e >> 6;
-                        const bool v = (j0 + o < d) && (8 * c < r);
-                        uint8_t *dst = w_s + c * 1024 + (o >> 3) * 128 + (o & 7) * 16;
-                        if ((r & 7) == 0) {
-                            const uint16_t *src = v ? Bi + (int64_t)(j0 + o) * r + 8 * c : Bw;
-                            cp_async_16(dst, src, v);
-                        } else {  // rows not 16-byte aligned: element by element
-                            uint32_t wv[4];
-#pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                const int k0 = 8 * c + 2 * h;
-                                const uint16_t lo = (v && k0 < r) ? Bi[(int64_t)(j0 + o) * r + k0] : 0;
-                                const uint16_t hi = (v && k0 + 1 < r) ? Bi[(int64_t)(j0 + o) * r + k0 + 1] : 0;
-                                wv[h] = (uint32_t)lo | ((uint32_t)hi << 16);
-                            }
-                            *reinterpret_cast<uint4 *>(dst) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                        }
                     }
                 }
                 cp_async_commit();
@@ -206,7 +191,7 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
                 const uint32_t acc = acc_n & 1u, aph = (acc_n >> 1) & 1u;
                 if (!mbar_wait(&S.tempty[acc], aph ^ 1u, S.abort, segs.status)) break;
                 tc_fence_after();
-                const uint32_t idesc = make_idesc_bf16(128, rp, false, kDH);
+                const uint32_t idesc = make_idesc_bf16(128, rp, false, false);
                 const uint32_t d_tmem = tmem_base + acc * 128u;
                 for (int32_t kb = 0; kb < nk; ++kb) {
                     const uint32_t s = g % kStages, ph = (g / kStages) & 1u;
@@ -218,12 +203,9 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
                     const uint32_t a_base = smem_u32(S.act + s * kActBytes);
                     const uint32_t w_base = smem_u32(S.w + s * kWBytes);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint64_t adesc = make_desc(a_base + 32u * k, 16, 1024, kSwizzle128);
-                        const uint64_t bdesc = kDH ? make_desc(w_base + 256u * k, 128, 1024, kInterleave)
-                                                   : make_desc(w_base + 32u * k, 16, 1024, kSwizzle128);
-                        umma_bf16(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
-                    }
+                    for (int k = 0; k < 4; ++k)
+                        umma_bf16(d_tmem, make_desc(a_base + 32u * k, 16, 1024, kSwizzle128),
+                                  make_desc(w_base + 32u * k, 16, 1024, kSwizzle128), idesc, (kb | k) != 0 ? 1u : 0u);
                     umma_commit(&S.empty[s]);
                     ++g;
                 }
@@ -252,34 +234,71 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
             if (!mbar_wait(&S.tfull[acc], aph, S.abort, segs.status)) break;
             tc_fence_after();
             const int m = (int)lane_base + lane;
-            const int32_t t = m < T.rows ? segs.perm[T.begin + m] : -1;
-            const float c = kDH ? ad.scale : 1.0f;
-            float *row = out + (int64_t)(t < 0 ? 0 : t) * r_max;
+            const bool valid = m < T.rows;
+            const int64_t p = (int64_t)T.begin + m;
+            const int32_t t = valid ? segs.perm[p] : -1;
+            const float c = o.scale_is_adapter != 0.f ? ad.scale : 1.0f;
+            float *row = o.f32 != nullptr ? o.f32 + (int64_t)(t < 0 ? 0 : t) * r_max : nullptr;
+            uint16_t *rhi = o.hi != nullptr ? o.hi + p * o.rw : nullptr;
+            uint16_t *rlo = o.lo != nullptr ? o.lo + p * o.rw : nullptr;
             for (int c0 = 0; c0 < rp; c0 += 16) {
                 uint32_t v[16];
                 tmem_ld16(tmem_base + (lane_base << 16) + acc * 128u + (uint32_t)c0, v);
                 tmem_ld_wait();
-                if (t >= 0) {
-                    float o[16];
+                if (!valid) continue;
+                float f[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) o[e] = (c0 + e < r) ? c * __uint_as_float(v[e]) : 0.f;
+                for (int e = 0; e < 16; ++e) f[e] = (c0 + e < r) ? c * __uint_as_float(v[e]) : 0.f;
+                if (row != nullptr) {
                     if (vec && c0 + 16 <= r_max) {
 #pragma unroll
                         for (int e = 0; e < 16; e += 4)
-                            *reinterpret_cast<float4 *>(row + c0 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                            *reinterpret_cast<float4 *>(row + c0 + e) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
                     } else {
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
-                            if (c0 + e < r_max) row[c0 + e] = o[e];
+                            if (c0 + e < r_max) row[c0 + e] = f[e];
+                    }
+                }
+                if (rhi != nullptr) {
+                    uint32_t hw[8], lw[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        hw[e] = pack_bf16(f[2 * e], f[2 * e + 1]);
+                        lw[e] = pack_bf16(f[2 * e] - bf16lo(hw[e]), f[2 * e + 1] - bf16hi(hw[e]));
+                    }
+                    *reinterpret_cast<uint4 *>(rhi + c0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4 *>(rhi + c0 + 8) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+                    if (rlo != nullptr) {
+                        *reinterpret_cast<uint4 *>(rlo + c0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                        *reinterpret_cast<uint4 *>(rlo + c0 + 8) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
                     }
                 }
             }
-            if (t >= 0)
-                for (int k = rp; k < r_max; ++k) row[k] = 0.f;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.tempty[acc]);
             ++acc_n;
+            if (!valid) continue;
+            // zero tails and the optional conversion of a saved fp32 H
+            if (row != nullptr)
+                for (int k = rp; k < r_max; ++k) row[k] = 0.f;
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            for (int k = rp; k < o.rw; k += 8) {
+                if (rhi != nullptr) *reinterpret_cast<uint4 *>(rhi + k) = z;
+                if (rlo != nullptr) *reinterpret_cast<uint4 *>(rlo + k) = z;
+            }
+            if (o.hin != nullptr) {
+                const float *src = o.hin + (int64_t)t * r_max;
+                uint16_t *dst = o.hin_bf16 + p * o.rw;
+                for (int k = 0; k < o.rw; k += 8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2)
+                        w[e / 2] = pack_bf16(k + e < r ? src[k + e] : 0.f, k + e + 1 < r ? src[k + e + 1] : 0.f);
+                    *reinterpret_cast<uint4 *>(dst + k) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
         }
     }
 
@@ -291,47 +310,38 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
     }
 }
 
-template <bool kDH>
-lora_status_t launch_rowproj(float *out, const void *act, const lora_adapter_table &tab, const lora_segments &segs,
-                             cudaStream_t stream)
+lora_status_t launch_rowproj(const void *act, const void *w, int32_t d, const RowOut &o,
+                             const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream)
 {
     if (segs.n_tokens == 0 || segs.max_tiles == 0) return LORA_OK;
-    const int32_t d = kDH ? tab.d_out : tab.d_in;
     CUtensorMap map_act, map_w;
-    if (!make_tmap_bf16_2d(&map_act, act, (uint64_t)d, (uint64_t)segs.n_tokens, 64, 128, true))
+    if (!make_tmap_bf16_2d(&map_act, act, (uint64_t)d, (uint64_t)segs.n_tokens, 64, 128, true) ||
+        !make_tmap_bf16_2d(&map_w, w, (uint64_t)d, (uint64_t)tab.sum_r, 64, 16, true))
         return LORA_ERR_CUDA;
-    if (!kDH) {
-        if (!make_tmap_bf16_2d(&map_w, tab.A, (uint64_t)tab.d_in, (uint64_t)tab.sum_r, 64, 16, true))
-            return LORA_ERR_CUDA;
-    } else {
-        map_w = map_act;  // unused
-    }
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(tc_rowproj_kernel<kDH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemBytes) != cudaSuccess)
-            return LORA_ERR_CUDA;
-        attr_set = true;
-    }
+    if (cudaFuncSetAttribute(tc_rowproj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+        cudaSuccess)
+        return LORA_ERR_CUDA;
     const int sms = sm_count();
     const int grid = segs.max_tiles < sms ? segs.max_tiles : sms;
-    tc_rowproj_kernel<kDH><<<grid, kThreads, kSmemBytes, stream>>>(map_act, map_w, out,
-                                                                    static_cast<const uint16_t *>(act), tab, segs);
+    tc_rowproj_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_act, map_w, static_cast<const uint16_t *>(act), d,
+                                                              o, tab, segs);
     return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
 }  // namespace
 
-lora_status_t tc_shrink(float *H, const void *x, const lora_adapter_table &tab, const lora_segments &segs,
-                        cudaStream_t stream)
+lora_status_t tc_shrink(const void *x, const lora_adapter_table &tab, const lora_segments &segs, float *H,
+                        uint16_t *hi, uint16_t *lo, int32_t rw, cudaStream_t stream)
 {
-    return launch_rowproj<false>(H, x, tab, segs, stream);
+    RowOut o{H, hi, lo, nullptr, nullptr, rw, 0.f};
+    return launch_rowproj(x, tab.A, tab.d_in, o, tab, segs, stream);
 }
 
-lora_status_t tc_dh(float *dH, const void *dY, const lora_adapter_table &tab, const lora_segments &segs,
-                    cudaStream_t stream)
+lora_status_t tc_dh(const void *dY, const lora_adapter_table &tab, const lora_segments &segs, uint16_t *dh_bf16,
+                    const float *h_saved, uint16_t *h_bf16, int32_t rw, cudaStream_t stream)
 {
-    return launch_rowproj<true>(dH, dY, tab, segs, stream);
+    RowOut o{nullptr, dh_bf16, nullptr, h_saved, h_bf16, rw, 1.f};
+    return launch_rowproj(dY, tab.B, tab.d_out, o, tab, segs, stream);
 }
 
 }  // namespace lora

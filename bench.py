@@ -169,7 +169,7 @@ class Workload:
         self.H = torch.empty((T, spec.r_max), dtype=torch.float32, device=dev)
         self.dX = self.inp["dX0"]
         self.dA = torch.empty((spec.sum_r, spec.d_in), dtype=torch.float32, device=dev)
-        self.dB = torch.empty((spec.sum_r * spec.d_out,), dtype=torch.float32, device=dev)
+        self.dB = torch.empty((spec.sum_r, spec.d_out), dtype=torch.float32, device=dev)
         self.segs = None
 
     def build(self, stream=None):

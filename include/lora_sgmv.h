@@ -87,8 +87,10 @@ typedef enum lora_status {
  *   row_off[i]   sum_{j<i} r_j; row_off[N] = sum_r                   (device int32 [N+1])
  *   scale[i]     s_i = alpha_i / r_i (fp32)                          (device float [N])
  *   A            bf16 [sum_r, d_in] row-major: A_i is rows row_off[i] .. row_off[i]+r_i-1
- *   B            bf16 ragged: B_i is a row-major [d_out, r_i] block starting at
- *                element d_out * row_off[i]; total d_out * sum_r elements
+ *   B            bf16 [sum_r, d_out] row-major: B_i transposed and stacked like A,
+ *                i.e. row row_off[i]+k holds column k of B_i (B_i[o, k] = B[row_off[i]+k, o]).
+ *                Stored this way every weight operand of every kernel is a plain 2-D
+ *                tile of A or B that one TMA tensor map can address.
  * The host fields (n_adapters, d_in, d_out, r_max, sum_r) size the launches;
  * the device arrays must agree with them (checked on the device: a mismatch
  * sets LORA_ERR_BAD_TABLE and the adapter is skipped).
@@ -193,8 +195,10 @@ LORA_API lora_status_t lora_sgmv_expand(void *y, const float *H, const lora_adap
  *   y       device bf16 [T, d_out] (in/out, +=)
  *   H_save  device fp32 [T, r_max] (out) to keep H for the backward, or NULL
  *   x       device bf16 [T, d_in]
- *   ws      device workspace of >= lora_workspace_bytes(table, T) bytes
- *           (may be NULL when that is 0); contents need not be preserved
+ *   ws      device workspace of >= lora_workspace_bytes(table, T) bytes (may be
+ *           NULL when that is 0); it carries H from the shrink to the expand as
+ *           bf16 (a hi + lo pair, ~16 significant bits); contents need not be
+ *           preserved after the call
  */
 LORA_API lora_status_t lora_packed_fwd(void *y, float *H_save, const void *x,
                               const lora_adapter_table *table, const lora_segments *segs,
@@ -206,10 +210,13 @@ LORA_API lora_status_t lora_packed_fwd(void *y, float *H_save, const void *x,
  *   dX       device bf16 [T, d_in] (in/out, +=), or NULL to skip
  *   dA       device fp32 [sum_r, d_in] (out, overwritten; adapters with no
  *            token get zeros), or NULL to skip
- *   dB       device fp32, B layout, d_out * sum_r (out, overwritten), or NULL
+ *   dB       device fp32 [sum_r, d_out], B's layout (row row_off[i]+k = column k of
+ *            dB_i; out, overwritten), or NULL
  *   dY       device bf16 [T, d_out];  X  device bf16 [T, d_in] (the forward input)
  *   H_saved  device fp32 [T, r_max] from lora_packed_fwd, or NULL to recompute it
- *   ws       device workspace of >= lora_workspace_bytes(table, T) bytes
+ *   ws       device workspace of >= lora_workspace_bytes(table, T) bytes; it carries
+ *            bf16 copies of H and dH between the four cases (the dB, dA and dX
+ *            products consume bf16 H / dH with fp32 accumulation)
  */
 LORA_API lora_status_t lora_packed_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X,
                               const float *H_saved, const lora_adapter_table *table,
@@ -220,10 +227,11 @@ LORA_API lora_status_t lora_packed_bwd(void *dX, float *dA, float *dB, const voi
  * Packed backward without a workspace, for callers that cannot allocate device
  * memory (no cudaMalloc, no allocator of their own to draw scratch from).  The
  * pages have no counterpart to this call; it exists only for such callers.
- * Same arguments and results as lora_packed_bwd minus ws / ws_bytes: the fp32
- * H / dH scratch lives in a fixed 8 MiB array inside the library's device
+ * Same arguments and results as lora_packed_bwd minus ws / ws_bytes: the bf16
+ * H / dH hand-off scratch lives in a fixed 8 MiB array inside the library's device
  * memory (held by every GPU that loads the library until exit), so it needs
- * 2 * T * r_max * 4 bytes (each half rounded up to 256) <= 8 MiB, otherwise
+ * lora_workspace_bytes(table, T) <= 8 MiB (2 * T * 64 bf16 when r_max <= 64,
+ * 2 * T * 128 otherwise, each half rounded up to 256 bytes), otherwise
  * LORA_ERR_WORKSPACE_TOO_SMALL is returned and nothing runs.  Allocates
  * nothing.  All calls share the array: calls that overlap on the GPU race and
  * must be serialised by the caller.  The first call on a device resolves the

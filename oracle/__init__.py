@@ -143,10 +143,11 @@ def shrink(tab: Table, ids, A, x, r_max: int | None = None):
 
 
 def expand(tab: Table, ids, B, H, y0):
-    """y = y0 + s_i B_i h_t per token (y0 is copied, not modified)."""
+    """y = y0 + s_i B_i h_t per token (y0 is copied, not modified).
+    ``B`` is Bt_cat [sum_r, d_out] (B_i transposed, stacked like A)."""
     lib = _load()
     ids = _c(ids, np.int32)
-    B = _c(B, np.float64).reshape(-1)
+    B = _c(B, np.float64)
     H = _c(H, np.float64)
     y = np.array(y0, dtype=np.float64, copy=True, order="C")
     T, d_out = y.shape
@@ -159,7 +160,7 @@ def dh(tab: Table, ids, B, dY, r_max: int | None = None):
     lib = _load()
     r_max = tab.r_max if r_max is None else r_max
     ids = _c(ids, np.int32)
-    B = _c(B, np.float64).reshape(-1)
+    B = _c(B, np.float64)
     dY = _c(dY, np.float64)
     T, d_out = dY.shape
     out = np.zeros((T, r_max), dtype=np.float64)
@@ -174,7 +175,7 @@ def db(tab: Table, ids, dY, H):
     dY = _c(dY, np.float64)
     H = _c(H, np.float64)
     T, d_out = dY.shape
-    out = np.zeros(tab.sum_r * d_out, dtype=np.float64)
+    out = np.zeros((tab.sum_r, d_out), dtype=np.float64)
     lib.lora_oracle_db(*_hdr(tab, T, d_out, H.shape[1]), _p(tab.scale, _f64p), _p(ids, _i32p),
                        _p(dY, _f64p), _p(H, _f64p), _p(out, _f64p))
     return out

@@ -32,10 +32,11 @@
  *
  * Layouts (row-major, the same ones the CUDA library documents):
  *   A_cat  [sum_r, d_in]       A_i occupies rows row_off[i] .. row_off[i]+r_i-1
- *   B_cat  ragged              B_i is the block [d_out, r_i] starting at
- *                              element d_out*row_off[i]
+ *   Bt_cat [sum_r, d_out]      B_i transposed, stacked like A_cat: row
+ *                              row_off[i]+k holds column k of B_i, so
+ *                              B_i[o, k] = Bt_cat[row_off[i]+k, o]
  *   H, dH  [T, r_max]          columns >= r_i of token t are zero
- *   dA     like A_cat, dB like B_cat
+ *   dA     like A_cat, dBt like Bt_cat
  * Tokens whose id lies outside [0, N) belong to no adapter: they contribute
  * nothing, their H/dH rows are zero and their y/dX rows are left unchanged.
  *
@@ -125,19 +126,18 @@ void lora_oracle_shrink(int64_t T, int32_t N, int32_t d_in, int32_t r_max,
 void lora_oracle_expand(int64_t T, int32_t N, int32_t d_out, int32_t r_max,
                         const int32_t *rank, const int64_t *row_off,
                         const double *scale, const int32_t *ids,
-                        const double *B, const double *H, double *y)
+                        const double *Bt, const double *H, double *y)
 {
     #pragma omp parallel for schedule(dynamic, 4)
     for (int64_t t = 0; t < T; ++t) {
         int32_t i = ids[t];
         if (!valid_id(i, N)) continue;
         const int32_t r = rank[i];
-        const double *Bi = B + row_off[i] * (int64_t)d_out;
         const double *h = H + t * r_max;
         double *yt = y + t * (int64_t)d_out;
         for (int32_t o = 0; o < d_out; ++o) {
             double acc = 0.0;
-            for (int32_t k = 0; k < r; ++k) acc += Bi[(int64_t)o * r + k] * h[k];
+            for (int32_t k = 0; k < r; ++k) acc += Bt[(row_off[i] + k) * (int64_t)d_out + o] * h[k];
             yt[o] += scale[i] * acc;
         }
     }
@@ -146,7 +146,7 @@ void lora_oracle_expand(int64_t T, int32_t N, int32_t d_out, int32_t r_max,
 /* dh: dH[t, k] = s_i * sum_o B_i[o, k] * dY[t, o] for k < r_i, zero beyond. */
 void lora_oracle_dh(int64_t T, int32_t N, int32_t d_out, int32_t r_max,
                     const int32_t *rank, const int64_t *row_off,
-                    const double *scale, const int32_t *ids, const double *B,
+                    const double *scale, const int32_t *ids, const double *Bt,
                     const double *dY, double *dH)
 {
     #pragma omp parallel for schedule(dynamic, 4)
@@ -156,23 +156,23 @@ void lora_oracle_dh(int64_t T, int32_t N, int32_t d_out, int32_t r_max,
         int32_t i = ids[t];
         if (!valid_id(i, N)) continue;
         const int32_t r = rank[i];
-        const double *Bi = B + row_off[i] * (int64_t)d_out;
         const double *dy = dY + t * (int64_t)d_out;
         for (int32_t k = 0; k < r; ++k) {
+            const double *b = Bt + (row_off[i] + k) * (int64_t)d_out;
             double acc = 0.0;
-            for (int32_t o = 0; o < d_out; ++o) acc += Bi[(int64_t)o * r + k] * dy[o];
+            for (int32_t o = 0; o < d_out; ++o) acc += b[o] * dy[o];
             g[k] = scale[i] * acc;
         }
     }
 }
 
 /* dB: dB_i[o, k] = s_i * sum_{t : ids[t] = i} dY[t, o] * H[t, k].
- * Output uses the B_cat layout (sum_r * d_out doubles); adapters without
- * tokens get zeros. */
+ * Output uses the Bt_cat layout: dBt[row_off[i]+k, o] = dB_i[o, k]; adapters
+ * without tokens get zeros. */
 void lora_oracle_db(int64_t T, int32_t N, int32_t d_out, int32_t r_max,
                     const int32_t *rank, const int64_t *row_off,
                     const double *scale, const int32_t *ids, const double *dY,
-                    const double *H, double *dB)
+                    const double *H, double *dBt)
 {
     const int64_t sum_r = row_off[N];
     #pragma omp parallel
@@ -188,12 +188,9 @@ void lora_oracle_db(int64_t T, int32_t N, int32_t d_out, int32_t r_max,
                 const double *h = H + t * r_max;
                 for (int32_t k = 0; k < rank[i]; ++k) acc[row_off[i] + k] += g * h[k];
             }
-            for (int32_t i = 0; i < N; ++i) {
-                const int32_t r = rank[i];
-                double *dBi = dB + row_off[i] * (int64_t)d_out;
-                for (int32_t k = 0; k < r; ++k)
-                    dBi[(int64_t)o * r + k] = scale[i] * acc[row_off[i] + k];
-            }
+            for (int32_t i = 0; i < N; ++i)
+                for (int32_t k = 0; k < rank[i]; ++k)
+                    dBt[(row_off[i] + k) * (int64_t)d_out + o] = scale[i] * acc[row_off[i] + k];
         }
         free(acc);
     }

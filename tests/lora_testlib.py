@@ -75,15 +75,23 @@ class GpuCase:
         s = self.spec
         dX = self.inp["dX0"].clone()
         dA = torch.full((s.sum_r, s.d_in), float("nan"), dtype=torch.float32, device=self.device)
-        dB = torch.full((s.sum_r * s.d_out,), float("nan"), dtype=torch.float32, device=self.device)
+        dB = torch.full((s.sum_r, s.d_out), float("nan"), dtype=torch.float32, device=self.device)
         lora.lora_packed_bwd(dX, dA, dB, self.inp["dY"], self.inp["x"], H, self.table, self.segs, self.ws)
         return dX, dA, dB
 
     def dH_workspace(self):
-        """dH as left in the workspace by the last backward (implementation detail, for diagnosis)."""
+        """dH as left in the workspace by the last backward, in token order
+        (implementation detail, for diagnosis): the second hand-off buffer,
+        bf16 [T, rw] rows in perm order."""
         s = self.spec
-        region = ((s.n_tokens * s.r_max * 4) + 255) & ~255
-        return self.ws[region:region + s.n_tokens * s.r_max * 4].view(torch.float32).view(s.n_tokens, s.r_max)
+        rw = 64 if s.r_max <= 64 else 128
+        region = ((s.n_tokens * rw * 2) + 255) & ~255
+        dhb = self.ws[region:region + s.n_tokens * rw * 2].view(torch.bfloat16).view(s.n_tokens, rw)
+        n_valid = int(self.segs.seg_start[-1].item())
+        perm = self.segs.perm[:n_valid].long()
+        out = torch.zeros((s.n_tokens, s.r_max), dtype=torch.float32, device=self.device)
+        out[perm] = dhb[:n_valid, :s.r_max].float()
+        return out
 
 
 def oracle_all(spec: wl.Spec, host: dict, rows=None):
@@ -106,6 +114,5 @@ def check_blocks(spec, got_dA, got_dB, ref_dA, ref_dB, adapters=None):
     for i in (range(spec.n_adapters) if adapters is None else adapters):
         a0, a1 = int(off[i]), int(off[i + 1])
         errs[f"dA[{i}]"] = assert_close(got_dA[a0:a1], ref_dA[a0:a1], GRAD_TOL, f"dA_{i}")
-        errs[f"dB[{i}]"] = assert_close(got_dB[a0 * d_out:a1 * d_out], ref_dB[a0 * d_out:a1 * d_out],
-                                        GRAD_TOL, f"dB_{i}")
+        errs[f"dB[{i}]"] = assert_close(got_dB[a0:a1], ref_dB[a0:a1], GRAD_TOL, f"dB_{i}")
     return errs

@@ -48,10 +48,11 @@ def close(a, b, rel=1e-12):
 
 
 def B_block(P, i, d_out):
+    """B_i as the d_out x r_i matrix (stored transposed: rows of B are columns of B_i)."""
     tab = P["tab"]
     r = int(tab.rank[i])
-    o = int(tab.row_off[i]) * d_out
-    return P["B"][o:o + d_out * r].reshape(d_out, r)
+    a0 = int(tab.row_off[i])
+    return P["B"][a0:a0 + r].T
 
 
 # ---------------------------------------------------------------- routing
@@ -93,13 +94,13 @@ def test_single_adapter_is_plain_lora_matmul(r, d_in, d_out, T):
     out = run_all(P)
     s = float(spec.scales[0])
     A, x, dY = P["A"], P["x"], P["dY"]
-    B = P["B"].reshape(d_out, r)
+    B = P["B"].T  # B_i, d_out x r (stored as its transpose)
     H = x @ A.T
     close(out["H"], H)
     close(out["y"], P["y0"] + s * (H @ B.T))
     dH = s * (dY @ B)
     close(out["dH"], dH)
-    close(out["dB"].reshape(d_out, r), s * (dY.T @ H))
+    close(out["dB"].T, s * (dY.T @ H))
     close(out["dA"], dH.T @ x)
     close(out["dX"], P["dX0"] + dH @ A)
 
@@ -121,7 +122,7 @@ def brute_force(P, spec):
     for i in range(N):
         toks = [t for t in range(T) if spec.ids[t] == i]
         r = int(ranks[i])
-        b0 = int(off[i]) * d_out
+        a0 = int(off[i])
         for t in toks:
             for k in range(r):
                 acc = 0.0
@@ -131,12 +132,12 @@ def brute_force(P, spec):
             for o in range(d_out):
                 acc = 0.0
                 for k in range(r):
-                    acc += Bf[b0 + o * r + k] * H[t, k]
+                    acc += Bf[a0 + k, o] * H[t, k]
                 y[t, o] += s[i] * acc
             for k in range(r):
                 acc = 0.0
                 for o in range(d_out):
-                    acc += dY[t, o] * Bf[b0 + o * r + k]
+                    acc += dY[t, o] * Bf[a0 + k, o]
                 dH[t, k] = s[i] * acc
             for j in range(d_in):
                 acc = 0.0
@@ -145,7 +146,7 @@ def brute_force(P, spec):
                 dX[t, j] += acc
         for o in range(d_out):
             for k in range(r):
-                dB[b0 + o * r + k] = s[i] * sum(dY[t, o] * H[t, k] for t in toks)
+                dB[a0 + k, o] = s[i] * sum(dY[t, o] * H[t, k] for t in toks)
         for k in range(r):
             for j in range(d_in):
                 dA[off[i] + k, j] = sum(dH[t, k] * x[t, j] for t in toks)
@@ -207,17 +208,15 @@ def test_zero_B_adapter_contributes_nothing():
     spec = wl.tiny()
     P = make(spec, y0="randn", dX0="randn")
     i = 2
-    d_out = spec.d_out
-    o = int(spec.row_off[i]) * d_out
-    P["B"][o:o + d_out * int(spec.ranks[i])] = 0.0
+    a0, a1 = int(spec.row_off[i]), int(spec.row_off[i + 1])
+    P["B"][a0:a1] = 0.0
     out = run_all(P)
     rows = spec.ids == i
     close(out["y"][rows], P["y0"][rows], 0.0)
     assert np.all(out["dH"][rows] == 0.0)
-    a0, a1 = int(spec.row_off[i]), int(spec.row_off[i + 1])
     assert np.all(out["dA"][a0:a1] == 0.0)
     close(out["dX"][rows], P["dX0"][rows], 0.0)
-    assert np.any(out["dB"][o:o + d_out * int(spec.ranks[i])] != 0.0)  # dB_i = s dY^T H is not zero
+    assert np.any(out["dB"][a0:a1] != 0.0)  # dB_i = s dY^T H is not zero
     assert np.any(out["y"][~rows] != P["y0"][~rows])
 
 
@@ -257,14 +256,14 @@ def test_packing_equals_sequential_single_adapter_runs():
         tab1 = oracle.Table([r], [float(spec.scales[i])])
         ids1 = np.zeros(rows.size, np.int32)
         A1 = P["A"][a0:a0 + r]
-        B1 = B_block(P, i, d_out).reshape(-1)
+        B1 = P["B"][a0:a0 + r]
         y, H = oracle.fwd(tab1, ids1, A1, B1, P["x"][rows], P["y0"][rows])
         dH, dA, dB, dX = oracle.bwd(tab1, ids1, A1, B1, P["x"][rows], H, P["dY"][rows], P["dX0"][rows])
         close(out["y"][rows], y, 0.0)
         close(out["H"][rows, :r], H, 0.0)
         close(out["dX"][rows], dX, 0.0)
         close(out["dA"][a0:a0 + r], dA, 1e-13)
-        close(out["dB"][a0 * d_out:(a0 + r) * d_out], dB, 1e-13)
+        close(out["dB"][a0:a0 + r], dB, 1e-13)
         assert d_in == P["x"].shape[1]
 
 
@@ -282,10 +281,10 @@ def test_zero_rank_padding_changes_nothing():
         r = int(spec.ranks[i])
         a0 = int(spec.row_off[i])
         A2.append(np.vstack([P["A"][a0:a0 + r], np.zeros((pad, d_in))]))
-        B2.append(np.hstack([B_block(P, i, d_out), np.zeros((d_out, pad))]).reshape(-1))
+        B2.append(np.vstack([P["B"][a0:a0 + r], np.zeros((pad, d_out))]))
     Q = dict(P)
     Q["A"] = np.vstack(A2)
-    Q["B"] = np.concatenate(B2)
+    Q["B"] = np.vstack(B2)
     Q["tab"] = oracle.Table(ranks2, spec.scales.astype(np.float64))  # s_i held fixed
     outp = run_all(Q, r_max=int(ranks2.max()))
     close(outp["y"], out["y"], 0.0)
@@ -313,7 +312,7 @@ def test_splitting_an_adapter_into_two_identical_ones():
     scales2 = np.concatenate([spec.scales, [spec.scales[i]]]).astype(np.float64)
     Q = dict(P)
     Q["A"] = np.vstack([P["A"], P["A"][a0:a0 + r]])
-    Q["B"] = np.concatenate([P["B"], B_block(P, i, d_out).reshape(-1)])
+    Q["B"] = np.vstack([P["B"], P["B"][a0:a0 + r]])
     Q["tab"] = oracle.Table(ranks2, scales2)
     ids2 = P["ids"].copy()
     rows = np.flatnonzero(ids2 == i)
@@ -324,8 +323,7 @@ def test_splitting_an_adapter_into_two_identical_ones():
         close(outp[k], out[k], 0.0)
     s0 = int(spec.sum_r)
     close(outp["dA"][a0:a0 + r] + outp["dA"][s0:s0 + r], out["dA"][a0:a0 + r], 1e-13)
-    close(outp["dB"][a0 * d_out:(a0 + r) * d_out] + outp["dB"][s0 * d_out:(s0 + r) * d_out],
-          out["dB"][a0 * d_out:(a0 + r) * d_out], 1e-13)
+    close(outp["dB"][a0:a0 + r] + outp["dB"][s0:s0 + r], out["dB"][a0:a0 + r], 1e-13)
 
 
 # ---------------------------------------------------------------- I9: linearity in s_i
@@ -342,8 +340,7 @@ def test_doubling_alpha_doubles_the_adapters_contribution():
     rows = spec.ids == i
     close(outp["y"][rows] - P["y0"][rows], 2.0 * (out["y"][rows] - P["y0"][rows]), 1e-14)
     close(outp["y"][~rows], out["y"][~rows], 0.0)
-    d_out = spec.d_out
-    b0, b1 = int(spec.row_off[i]) * d_out, int(spec.row_off[i + 1]) * d_out
+    b0, b1 = int(spec.row_off[i]), int(spec.row_off[i + 1])
     close(outp["dB"][b0:b1], 2.0 * out["dB"][b0:b1], 0.0)
     close(outp["dH"][rows], 2.0 * out["dH"][rows], 0.0)
     # dA_i = dH^T X and dX pick up s_i through dH
@@ -362,4 +359,4 @@ def test_tokens_without_adapter_and_empty_adapters():
         close(out["dX"][t], P["dX0"][t], 0.0)
         assert np.all(out["H"][t] == 0.0) and np.all(out["dH"][t] == 0.0)
     assert np.all(out["dA"][4:12] == 0.0)
-    assert np.all(out["dB"][4 * 8:] == 0.0)
+    assert np.all(out["dB"][4:12] == 0.0)

@@ -30,7 +30,7 @@ def outputs(case, fn, H):
     s = case.spec
     dX = case.inp["dX0"].clone()
     dA = torch.full((s.sum_r, s.d_in), float("nan"), dtype=torch.float32, device="cuda")
-    dB = torch.full((s.sum_r * s.d_out,), float("nan"), dtype=torch.float32, device="cuda")
+    dB = torch.full((s.sum_r, s.d_out), float("nan"), dtype=torch.float32, device="cuda")
     fn(dX, dA, dB, H)
     torch.cuda.synchronize()
     return dev_to_f64(dX), dev_to_f64(dA), dev_to_f64(dB)
@@ -63,7 +63,7 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     spec = wl.custom("big", 64, 64, [128], [256.0], np.zeros(T, np.int32))
     dev = torch.device("cuda")
     A = torch.zeros((128, 64), dtype=torch.bfloat16, device=dev)
-    B = torch.zeros((128 * 64,), dtype=torch.bfloat16, device=dev)
+    B = torch.zeros((128, 64), dtype=torch.bfloat16, device=dev)
     table = lora.AdapterTable(A, B, [128], [2.0], 64, 64)
     segs = lora.lora_build_segments(seg_offsets=torch.tensor([0, T], dtype=torch.int32, device=dev),
                                     n_tokens=T, n_adapters=1)

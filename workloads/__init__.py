@@ -13,6 +13,8 @@ weights: the delta is a linear map, so only shapes and value ranges matter.
 
 Value recipe (every tensor bf16, rounded to nearest-even from fp32):
   x, dY, y0, dX0 ~ N(0, 1); A_i ~ U(-1/sqrt(d_in), +1/sqrt(d_in)); B_i ~ N(0, 0.02^2).
+Layouts: A [sum_r, d_in] (A_i stacked); B [sum_r, d_out] (B_i transposed,
+stacked the same way: row row_off[i] + k is column k of B_i).
 Each tensor draws from its own stream, numpy ``default_rng([seed, k])`` on
 the host or a ``torch.Generator`` seeded ``seed * 1000 + k`` on a device.
 """
@@ -218,7 +220,7 @@ def random_spec(rng, T, N, d_in, d_out, rank_choices=(8, 16, 32), sorted_=False,
 def host_inputs(spec: Spec, y0: str = "zero", dX0: str = "zero") -> dict:
     """bf16 bit arrays (uint16) drawn on the host with numpy.
 
-    Keys: A [sum_r, d_in], B [d_out * sum_r] (ragged blocks B_i [d_out, r_i]),
+    Keys: A [sum_r, d_in], B [sum_r, d_out] (B_i transposed, stacked like A),
     x [T, d_in], dY [T, d_out], y0 [T, d_out], dX0 [T, d_in].
     ``y0`` / ``dX0`` are "zero" or "randn"."""
     T, d_in, d_out, sr, s = spec.n_tokens, spec.d_in, spec.d_out, spec.sum_r, spec.seed
@@ -229,7 +231,7 @@ def host_inputs(spec: Spec, y0: str = "zero", dX0: str = "zero") -> dict:
     lim = 1.0 / math.sqrt(d_in)
     out = {
         "A": f32_to_bf16_bits(rng(_S_A).uniform(-lim, lim, size=(sr, d_in)).astype(np.float32)),
-        "B": f32_to_bf16_bits(rng(_S_B).normal(0.0, 0.02, size=(d_out * sr,)).astype(np.float32)),
+        "B": f32_to_bf16_bits(rng(_S_B).normal(0.0, 0.02, size=(sr, d_out)).astype(np.float32)),
         "x": f32_to_bf16_bits(rng(_S_X).standard_normal(size=(T, d_in), dtype=np.float32)),
     }
     out["dY"] = f32_to_bf16_bits(rng(_S_DY).standard_normal(size=(T, d_out), dtype=np.float32))
@@ -263,7 +265,7 @@ def device_inputs(spec: Spec, device, y0: str = "zero", dX0: str = "zero", need=
         a = torch.rand((sr, d_in), generator=gen(_S_A), device=device, dtype=torch.float32)
         out["A"] = (a * (2 * lim) - lim).to(torch.bfloat16)
     if "B" in keys:
-        out["B"] = (torch.randn((d_out * sr,), generator=gen(_S_B), device=device) * 0.02).to(torch.bfloat16)
+        out["B"] = (torch.randn((sr, d_out), generator=gen(_S_B), device=device) * 0.02).to(torch.bfloat16)
     if "x" in keys:
         out["x"] = torch.randn((T, d_in), generator=gen(_S_X), device=device).to(torch.bfloat16)
     if "dY" in keys:
