@@ -30,9 +30,13 @@ lora_status_t run_expand(void *y, const float *H, const lora_adapter_table &tab,
     return tc_expand_f32(y, H, tab, segs, stream);
 }
 
+// batches up to this many tokens take the one-launch decode kernel
+constexpr int32_t kDecodeMaxTokens = 512;
+
 lora_status_t run_fwd(void *y, float *H_save, const void *x, void *ws, const lora_adapter_table &tab,
                       const lora_segments &segs, cudaStream_t stream)
 {
+    if (segs.n_tokens <= kDecodeMaxTokens) return tc_decode_fwd(y, H_save, x, tab, segs, stream);
     const int32_t rw = handoff_cols(tab.r_max);
     uint16_t *hi = static_cast<uint16_t *>(ws);
     uint16_t *lo = reinterpret_cast<uint16_t *>(static_cast<char *>(ws) + handoff_region_bytes(segs.n_tokens, tab.r_max));

@@ -165,29 +165,42 @@ __global__ void route_sorted_kernel(const int32_t *__restrict__ seg_offsets, int
 // ---------------------------------------------------------------- tiles and spans
 // Cut every adapter's group into pieces of at most `len` tokens; one record
 // {adapter, begin, rows, flags} per piece, flags bit 0 = consecutive tokens.
+// Phase 1 scans the per-adapter piece counts into base[0..N] (scratch);
+// phase 2 lets every thread emit pieces, finding the owning adapter of piece
+// q by binary search (base[i] <= q < base[i+1]; empty adapters never match).
 __device__ void emit_pieces(const int32_t *__restrict__ seg_start, int32_t N, const int32_t *__restrict__ perm,
-                            int32_t len, int32_t *__restrict__ out, int32_t *__restrict__ n_out, int32_t max_out)
+                            int32_t len, int32_t *__restrict__ out, int32_t *__restrict__ n_out, int32_t max_out,
+                            int32_t *__restrict__ base)
 {
     int32_t carry = 0;
     for (int32_t i0 = 0; i0 < N; i0 += blockDim.x) {
         const int32_t i = i0 + threadIdx.x;
-        int32_t begin = 0, n = 0;
-        if (i < N) {
-            begin = seg_start[i];
-            n = seg_start[i + 1] - begin;
-        }
+        const int32_t n = i < N ? seg_start[i + 1] - seg_start[i] : 0;
         const int32_t cnt = n > 0 ? (n + len - 1) / len : 0;
         int32_t tot;
-        const int32_t base = carry + block_exclusive_scan(cnt, &tot);
-        for (int32_t q = 0; q < cnt && base + q < max_out; ++q) {
-            const int32_t b = begin + q * len;
-            const int32_t rows = min(len, n - q * len);
-            const int32_t contiguous = (perm[b + rows - 1] - perm[b] == rows - 1) ? 1 : 0;
-            reinterpret_cast<int4 *>(out)[base + q] = make_int4(i, b, rows, contiguous);
-        }
+        const int32_t e = block_exclusive_scan(cnt, &tot);
+        if (i < N) base[i] = carry + e;
         carry += tot;
     }
-    if (threadIdx.x == 0) *n_out = min(carry, max_out);
+    if (threadIdx.x == 0) base[N] = carry;
+    __syncthreads();
+    const int32_t total = min(carry, max_out);
+    for (int32_t q = threadIdx.x; q < total; q += blockDim.x) {
+        int32_t lo = 0, hi = N;
+        while (hi - lo > 1) {
+            const int32_t mid = (lo + hi) >> 1;
+            if (base[mid] <= q) lo = mid;
+            else hi = mid;
+        }
+        const int32_t j = q - base[lo];
+        const int32_t n = seg_start[lo + 1] - seg_start[lo];
+        const int32_t b = seg_start[lo] + j * len;
+        const int32_t rows = min(len, n - j * len);
+        const int32_t contiguous = (perm[b + rows - 1] - perm[b] == rows - 1) ? 1 : 0;
+        reinterpret_cast<int4 *>(out)[q] = make_int4(lo, b, rows, contiguous);
+    }
+    if (threadIdx.x == 0) *n_out = total;
+    __syncthreads();  // base is reused by the next call
 }
 
 // One block: seg_start (from the scan, when unsorted), then the tile and span
@@ -209,8 +222,9 @@ __global__ void route_tiles_kernel(const int32_t *__restrict__ offs, int32_t n_c
         }
         return;
     }
-    emit_pieces(seg_start, N, perm, LORA_TILE_M, s.tiles, s.n_tiles, s.max_tiles);
-    emit_pieces(seg_start, N, perm, LORA_SPAN_TOKENS, s.spans, s.n_spans, s.max_spans);
+    int32_t *base = s.scratch + (s.scratch_words - (((int64_t)N + 1 + 63) & ~int64_t(63)));
+    emit_pieces(seg_start, N, perm, LORA_TILE_M, s.tiles, s.n_tiles, s.max_tiles, base);
+    emit_pieces(seg_start, N, perm, LORA_SPAN_TOKENS, s.spans, s.n_spans, s.max_spans, base);
 }
 
 // ---------------------------------------------------------------- host side
@@ -234,7 +248,7 @@ SegLayout seg_layout(int32_t T, int32_t N)
     L.off_spans = o;      o += up(4 * (int64_t)L.max_spans);
     L.off_nspans = o;     o += up(1);
     L.off_scratch = o;
-    L.scratch_words = up(L.hist_words) + up(L.block_sums) + up(1);
+    L.scratch_words = up(L.hist_words) + up(L.block_sums) + up(1) + up((int64_t)N + 1);  // + piece bases
     o += L.scratch_words;
     L.total_words = o;
     L.ok = true;

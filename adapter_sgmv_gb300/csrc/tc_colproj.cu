@@ -32,7 +32,7 @@ using namespace tc;
 
 constexpr int kWStages = 2;
 constexpr int kYStages = 6;
-constexpr int kLagY = 3;
+constexpr int kLagY = 2;
 constexpr int kNC = 128;                              // columns per MMA chunk
 constexpr int kNPart = 1024;                          // columns per work item
 constexpr uint32_t kWBytes = kNC * LORA_MAX_RANK * 2;  // one weight chunk
@@ -100,7 +100,13 @@ LORA_DEV void tma_store_2d(const CUtensorMap *map, const void *smem_src, int32_t
                  : "memory");
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-LORA_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+template <int N>
+LORA_DEV void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
+constexpr int kStoreLag = 2;  // TMA stores whose smem reads may still be pending
+// Freeing stage g - kYStages needs the store of stage g - kYStages + kStoreLag,
+// which needs that stage's deferred arrive, issued with stage g - kYStages +
+// kStoreLag + kLagY; that must come before the producer's wait on stage g.
+static_assert(kLagY + kStoreLag < kYStages, "y-stage ring too shallow for the arrive and store lags");
 LORA_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 struct ColIn {
@@ -323,7 +329,7 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
             const Item I = load_item(tab, segs, it, n_parts, d);
             if (!I.ad.ok) continue;
             const int32_t r = I.ad.rank, rp = rpad16(r);
-            if (!mbar_wait(S.aempty, (na & 1u) ^ 1u, S.abort, segs.status)) break;
+            if (!mbar_wait_warp(S.aempty, (na & 1u) ^ 1u, S.abort, segs.status)) break;
             const int32_t t = m < I.tile.rows ? segs.perm[I.tile.begin + m] : -1;
             const float *hr = in.h32 + (int64_t)(t < 0 ? 0 : t) * r_max;
 #pragma unroll 4
@@ -353,6 +359,10 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
         const bool leader = warp == 2 && lane == 0;
         uint32_t a = 0, gy = 0;
         bool ok = true;
+        // leader only: stages whose TMA store may still be reading shared memory,
+        // oldest first; a stage goes back to the producer once its store has read it
+        int32_t pend[kStoreLag + 1];
+        int npend = 0;
         for (int32_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const Item I = load_item(tab, segs, it, n_parts, d);
             if (!I.ad.ok) continue;
@@ -362,7 +372,7 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
             uint16_t *row = out + (int64_t)(t < 0 ? 0 : t) * d;
             for (int32_t n0 = I.n_lo; n0 < I.n_hi; n0 += kNC) {
                 const uint32_t acc = a % kAcc, aph = (a / kAcc) & 1u;
-                if (!mbar_wait(&S.tfull[acc], aph, S.abort, segs.status)) {
+                if (!mbar_wait_warp(&S.tfull[acc], aph, S.abort, segs.status)) {
                     ok = false;
                     break;
                 }
@@ -371,7 +381,7 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                 for (int h = 0; h < 2; ++h) {
                     const int32_t c0 = n0 + 64 * h;
                     const uint32_t s = gy % kYStages, ph = (gy / kYStages) & 1u;
-                    if (!mbar_wait(&S.yfull[s], ph, S.abort, segs.status)) {
+                    if (!mbar_wait_warp(&S.yfull[s], ph, S.abort, segs.status)) {
                         ok = false;
                         break;
                     }
@@ -409,16 +419,24 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                     if (I.full) fence_proxy_async();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&S.ysync[s]);
-                    if (leader) {  // all four warps' rows are in place: store the block, free the stage
-                        if (!mbar_wait(&S.ysync[s], ph, S.abort, segs.status)) {
+                    if (warp == 2) {  // all four warps' rows are in place: store the block, free stages
+                        if (!mbar_wait_warp(&S.ysync[s], ph, S.abort, segs.status)) {
                             ok = false;
-                        } else {
+                        } else if (leader) {
                             if (I.full) {
                                 tma_store_2d(&map_y, y_s, c0, t0);
-                                bulk_wait_read0();
+                                pend[npend++] = (int32_t)s;
+                                if (npend > kStoreLag) {  // the oldest store has read its stage
+                                    bulk_wait_read<kStoreLag>();
+                                    mbar_arrive(&S.yempty[pend[0]]);
+                                    for (int q = 1; q < npend; ++q) pend[q - 1] = pend[q];
+                                    --npend;
+                                }
+                            } else {
+                                mbar_arrive(&S.yempty[s]);
                             }
-                            mbar_arrive(&S.yempty[s]);
                         }
+                        __syncwarp();
                     }
                     ++gy;
                     if (!ok) break;
@@ -426,8 +444,20 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                 if (!ok) break;
                 ++a;
             }
+            // end of the item: every pending store finishes reading and its stage is
+            // handed back, so the producer never waits on a stage held across items
+            if (leader) {
+                bulk_wait_read<0>();
+                for (int q = 0; q < npend; ++q) mbar_arrive(&S.yempty[pend[q]]);
+                npend = 0;
+            }
+            __syncwarp();
         }
-        if (leader) bulk_wait0();
+        if (leader) {
+            bulk_wait0();
+            for (int q = 0; q < npend; ++q) mbar_arrive(&S.yempty[pend[q]]);
+        }
+        __syncwarp();
     }
 
     tc_fence_before();

@@ -79,6 +79,16 @@ LORA_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int32_t *abort_
     }
 }
 
+// Warp-uniform bounded wait: every lane of the warp calls it and every lane
+// gets the same answer, so a time-out can never split a warp in front of a
+// .sync.aligned instruction (tcgen05.ld / alloc / dealloc), which would wait
+// for the missing lanes forever.
+LORA_DEV bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile int32_t *abort_flag, int32_t *status)
+{
+    const bool ok = mbar_wait(bar, parity, abort_flag, status);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------- TMA
 LORA_DEV void tma_load_2d(void *smem_dst, const CUtensorMap *map, uint64_t *bar, int32_t c0, int32_t c1)
 {

@@ -231,7 +231,7 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
             if (!ad.ok) continue;
             const int32_t r = ad.rank, rp = rpad16(r);
             const uint32_t acc = acc_n & 1u, aph = (acc_n >> 1) & 1u;
-            if (!mbar_wait(&S.tfull[acc], aph, S.abort, segs.status)) break;
+            if (!mbar_wait_warp(&S.tfull[acc], aph, S.abort, segs.status)) break;
             tc_fence_after();
             const int m = (int)lane_base + lane;
             const bool valid = m < T.rows;

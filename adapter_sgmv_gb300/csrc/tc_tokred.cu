@@ -243,7 +243,7 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
             const Item I = load_item(tab, segs, it, n_ranges, d);
             if (!I.ad.ok) continue;
             const int32_t r = I.ad.rank, rp = rpad16(r);
-            if (!mbar_wait(S.tfull, nitem & 1u, S.abort, segs.status)) break;
+            if (!mbar_wait_warp(S.tfull, nitem & 1u, S.abort, segs.status)) break;
             tc_fence_after();
             const float c = use_scale != 0.f ? I.ad.scale : 1.0f;
             for (int q = 0; q < 4; ++q) {
