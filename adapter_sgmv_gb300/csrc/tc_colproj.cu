@@ -169,6 +169,7 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
         }
         uint32_t gw = 0, gy = 0, na = 0;
         bool ok = true;
+        ArriveQueue<kLagY, kYStages> aq;
         for (int32_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const Item I = load_item(tab, segs, it, n_parts, d);
             if (!I.ad.ok) continue;
@@ -240,19 +241,12 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                             cp_async_16(y_s + sw128_offset(m, c), src, v);
                         }
                     }
-                    cp_async_commit();
-                    if (gy >= (uint32_t)kLagY) {
-                        cp_async_wait<kLagY>();
-                        fence_proxy_async();
-                        mbar_arrive(&S.yfull[(gy - kLagY) % kYStages]);
-                    }
+                    aq.issued(S.yfull, gy, !contiguous);
                     ++gy;
                 }
             }
         }
-        cp_async_wait<0>();
-        fence_proxy_async();
-        for (uint32_t u = gy > (uint32_t)kLagY ? gy - kLagY : 0u; u < gy; ++u) mbar_arrive(&S.yfull[u % kYStages]);
+        aq.drain(S.yfull);
         if (!ok && lane == 0) {  // aborted: let issued copies land before the CTA leaves
             for (uint32_t u = gy > (uint32_t)kYStages ? gy - kYStages : 0u; u < gy; ++u) {
                 uint64_t t0 = globaltimer_ns();

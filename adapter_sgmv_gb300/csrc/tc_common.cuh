@@ -57,20 +57,27 @@ LORA_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete, for at most
-// kWaitLimitNs.  On time-out the CTA-wide abort flag and the status word are
-// set and false is returned; callers then stop issuing work and leave.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// Wait for the phase with the given parity to complete, for a bounded time.
+// The bound is counted in SM clock cycles (kWaitLimitCycles, about 2-3 s at
+// GB300 clocks), read only every 1024 polls so that a wait that completes
+// soon costs nothing but the polls.  On time-out the CTA-wide abort flag and
+// the status word are set and false is returned; callers then stop issuing
+// work and leave.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;      // bound of the rare clean-up waits (globaltimer)
+constexpr long long kWaitLimitCycles = 4000000000ll;  // bound of pipeline waits (SM clock)
 
 LORA_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int32_t *abort_flag, int32_t *status)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    long long t0 = 0;
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0u) {
+        if ((it & 1023u) == 0u) {
             if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            const long long now = clock64();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > kWaitLimitCycles) {
                 *abort_flag = 1;
                 set_status(status, LORA_ERR_TIMEOUT);
                 return false;
@@ -117,6 +124,47 @@ LORA_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) 
 
 // generic-proxy shared-memory writes -> visible to the async proxy (tcgen05.mma, TMA)
 LORA_DEV void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// ---------------------------------------------------------------- producer arrivals
+// A producer lane owes one arrive per pipeline stage on that stage's "full"
+// barrier (whose count includes one arrive per producer lane).  Stages filled
+// only by TMA are covered by the expect-tx bytes, so the lane arrives at once.
+// Stages with cp.async copies can only be released after the copies land:
+// their arrives are deferred by kLag stages (cp.async.wait_group keeps kLag
+// groups in flight) and flushed before any immediate arrive, so stages always
+// complete in order and no consumer waits on a stage behind a later one.
+template <int kLag, int kStages>
+struct ArriveQueue {
+    uint32_t q[kLag + 1];
+    int n = 0;
+
+    LORA_DEV void drain(uint64_t *full)
+    {
+        if (n == 0) return;
+        cp_async_wait<0>();
+        fence_proxy_async();
+        for (int i = 0; i < n; ++i) mbar_arrive(&full[q[i] % kStages]);
+        n = 0;
+    }
+    // call once per stage g after issuing its copies; `gathered`: cp.async used
+    LORA_DEV void issued(uint64_t *full, uint32_t g, bool gathered)
+    {
+        if (!gathered) {
+            drain(full);
+            mbar_arrive(&full[g % kStages]);
+            return;
+        }
+        cp_async_commit();
+        q[n++] = g;
+        if (n > kLag) {
+            cp_async_wait<kLag>();
+            fence_proxy_async();
+            mbar_arrive(&full[q[0] % kStages]);
+            for (int i = 1; i < n; ++i) q[i - 1] = q[i];
+            --n;
+        }
+    }
+};
 
 // ---------------------------------------------------------------- tcgen05
 // Shared-memory matrix descriptor (tcgen05 "matrix descriptor"):

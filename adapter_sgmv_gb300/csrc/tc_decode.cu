@@ -4,25 +4,24 @@
 // into a single GPU launch per decode step).
 //
 // A decode batch has few tokens per adapter, so the tokens sit on the N side
-// of every tensor-core product (N = 32) and the long dimensions on M and K:
-//   phase 1  D1[k, t] = sum_j A_i[k, j] x[t, j]    (M = 128 rank rows, N = 32
+// of every tensor-core product (N = 48) and the long dimensions on M and K:
+//   phase 1  D1[k, t] = sum_j A_i[k, j] x[t, j]    (M = 128 rank rows, N = 48
 //            tokens, K = this CTA's share of d_in: split-K over the cluster)
 //   phase 2  the cluster's eight partial D1 are summed through distributed
 //            shared memory (each CTA sums r_pad / 8 rank rows and scatters the
 //            bf16 hi + lo result into all eight CTAs)
 //   phase 3  D3[o, t] = sum_k B_i[o, k] h[t, k]    (M = 128 output columns,
-//            N = 32 tokens, K = r_pad) for this CTA's 128-column chunks, and
+//            N = 48 tokens, K = r_pad) for this CTA's 128-column chunks, and
 //            y[t, o] += s_i * D3[o, t] straight from TMEM (a warp's 32 lanes
 //            are 32 consecutive columns of one token row).
-// Work item = (tile, 32-token sub-tile, column part); clusters of eight CTAs
-// walk the items; every CTA of a cluster sees the same items.
+// Work item = (tile, 48-token sub-tile, column part); clusters of eight CTAs
+// walk the items; every CTA of a cluster sees the same items.  The weights of
+// a CTA's first two output chunks and its first chunk's y values are fetched
+// while phase 1 runs, so phase 3 starts from data already on chip.
 //
-// All waits are bounded: the cluster-wide syncs inside the item loop are
-// mbarrier handshakes (every CTA arrives on every CTA's barrier, each waits on
-// its own with a time limit) and no CTA leaves the item loop early, so a
-// time-out can only make the kernel skip work.  The hardware cluster barrier
-// is used only at the start (barrier initialisation) and at the end, which
-// every CTA reaches unconditionally.
+// All mbarrier waits are bounded and no CTA leaves the item loop early: a
+// time-out only makes the kernel skip work, and every CTA of a cluster still
+// reaches every cluster barrier (the hardware one) after a bounded time.
 #include "internal.h"
 #include "tc_common.cuh"
 #include "tc_host.h"
@@ -36,14 +35,14 @@ constexpr int kCS = 8;          // CTAs per cluster
 constexpr int kThreads = 128;
 constexpr int kStages = 4;
 constexpr int kLag = 2;
-constexpr int kTok = 32;        // tokens per work item (MMA N)
+constexpr int kTok = 48;        // tokens per work item (MMA N)
 constexpr uint32_t kABytes = 128 * 64 * 2;   // phase-1 A block: up to 128 rank rows x 64
-constexpr uint32_t kXBytes = kTok * 64 * 2;  // phase-1 B block: 32 token rows x 64
+constexpr uint32_t kXBytes = kTok * 64 * 2;  // phase-1 B block: 48 token rows x 64 (one h atom too)
 constexpr uint32_t kWBytes = LORA_MAX_RANK * 128 * 2;  // phase-3 A block: r_pad x 128 columns
 constexpr uint32_t kHBytes = kTok * LORA_MAX_RANK * 2; // bf16 h, one copy
 constexpr int kPStride = kTok + 1;                      // fp32 partial row stride
 constexpr uint32_t kPBytes = LORA_MAX_RANK * kPStride * 4;
-constexpr uint32_t kTmemCols = 128;
+constexpr uint32_t kTmemCols = 256;  // D1: 48 columns at 0; D3: two slots of 48 at 64 and 128
 constexpr size_t kSmemBytes =
     1024 + kStages * (size_t)(kABytes + kXBytes) + 2 * (size_t)kWBytes + 2 * (size_t)kHBytes + kPBytes + 512;
 
@@ -122,11 +121,25 @@ LORA_DEV bool cbar_try_wait(uint64_t *bar, uint32_t parity)
         : "memory");
     return ok != 0;
 }
-LORA_DEV float ld_cluster_f32(uint32_t cluster_addr)
+// the same shared fp32 word in all eight CTAs of the cluster, summed; the
+// eight remote loads are issued back to back in one statement
+LORA_DEV float sum_cluster_f32(uint32_t saddr)
 {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
-    return v;
+    float v0, v1, v2, v3, v4, v5, v6, v7;
+    asm volatile(
+        "{\n\t.reg .b32 a<8>;\n\t"
+        "mapa.shared::cluster.u32 a0, %8, 0;\n\tmapa.shared::cluster.u32 a1, %8, 1;\n\t"
+        "mapa.shared::cluster.u32 a2, %8, 2;\n\tmapa.shared::cluster.u32 a3, %8, 3;\n\t"
+        "mapa.shared::cluster.u32 a4, %8, 4;\n\tmapa.shared::cluster.u32 a5, %8, 5;\n\t"
+        "mapa.shared::cluster.u32 a6, %8, 6;\n\tmapa.shared::cluster.u32 a7, %8, 7;\n\t"
+        "ld.shared::cluster.f32 %0, [a0];\n\tld.shared::cluster.f32 %1, [a1];\n\t"
+        "ld.shared::cluster.f32 %2, [a2];\n\tld.shared::cluster.f32 %3, [a3];\n\t"
+        "ld.shared::cluster.f32 %4, [a4];\n\tld.shared::cluster.f32 %5, [a5];\n\t"
+        "ld.shared::cluster.f32 %6, [a6];\n\tld.shared::cluster.f32 %7, [a7];\n\t}"
+        : "=f"(v0), "=f"(v1), "=f"(v2), "=f"(v3), "=f"(v4), "=f"(v5), "=f"(v6), "=f"(v7)
+        : "r"(saddr)
+        : "memory");
+    return ((v0 + v1) + (v2 + v3)) + ((v4 + v5) + (v6 + v7));
 }
 LORA_DEV void st_cluster_u16(uint32_t cluster_addr, uint16_t v)
 {
@@ -141,28 +154,18 @@ LORA_DEV void hw_cluster_sync()
 // generic-proxy writes, local or to other CTAs of the cluster -> async proxy
 LORA_DEV void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
 
-// Cluster-wide barrier with a time limit: each thread's prior shared-memory
-// writes (local or remote) are released to the cluster before its CTA's
-// arrive; the wait acquires them.  Returns false on time-out.
-LORA_DEV bool cluster_sync(const Smem &S, uint32_t &phase, int32_t *status)
+// Cluster-wide barrier inside the work loop.  Every CTA of a cluster walks the
+// same items and every wait between two of these barriers is bounded, so all
+// CTAs reach each barrier after a bounded time; the hardware cluster barrier
+// (release / acquire) is then safe and much cheaper than an mbarrier handshake.
+LORA_DEV bool cluster_sync(const Smem &, uint32_t &phase, int32_t *)
 {
-    __syncthreads();
-    if (threadIdx.x < kCS) remote_arrive(map_rank(smem_u32(S.cbar), threadIdx.x));
-    bool ok = cbar_try_wait(S.cbar, phase);
-    if (!ok) {
-        const uint64_t t0 = globaltimer_ns();
-        while (!(ok = cbar_try_wait(S.cbar, phase))) {
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                *S.abort = 1;
-                set_status(status, LORA_ERR_TIMEOUT);
-                break;
-            }
-        }
-    }
+    hw_cluster_sync();
     phase ^= 1u;
-    __syncthreads();
-    return ok;
+    return true;
 }
+
+constexpr int kSubs = (LORA_TILE_M + kTok - 1) / kTok;  // token sub-tiles per tile
 
 struct Item {
     Tile tile;
@@ -176,7 +179,7 @@ LORA_DEV Item load_item(const lora_adapter_table &tab, const lora_segments &segs
                         int32_t part_cols)
 {
     Item I;
-    const int32_t per_tile = 4 * n_parts;
+    const int32_t per_tile = kSubs * n_parts;
     I.tile = load_tile(segs.tiles, it / per_tile);
     const int32_t sub = (it % per_tile) / n_parts, part = it % n_parts;
     I.sub_begin = sub * kTok;
@@ -186,6 +189,17 @@ LORA_DEV Item load_item(const lora_adapter_table &tab, const lora_segments &segs
     I.ad = load_adapter(tab, I.tile.adapter, segs.status);
     I.live = I.rows > 0 && I.n_lo < I.n_hi && I.ad.ok;
     return I;
+}
+
+// phase-3 weights of output chunk c (columns o0 .. o0+127): B_i^T rows k as the
+// MN-major A operand, two 64-column atoms of r_pad rows
+LORA_DEV void load_w(const Smem &S, const CUtensorMap *map_b, uint32_t slot, int32_t o0, int32_t row_off, int32_t rp)
+{
+    uint8_t *w_s = S.w + slot * kWBytes;
+    mbar_arrive_expect_tx(&S.wfull[slot], (uint32_t)rp * 256u);
+    for (int a = 0; a < 2; ++a)
+        for (int q = 0; q < rp / 16; ++q)
+            tma_load_2d(w_s + a * rp * 128 + q * 2048, map_b, &S.wfull[slot], o0 + 64 * a, row_off + 16 * q);
 }
 
 __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kThreads, 1)
@@ -221,26 +235,32 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *S.tmem_holder;
+    const uint32_t tmem_lane = (32u * warp) << 16;
     uint32_t cphase = 0;
     // every CTA of the cluster has initialised its barriers before anyone arrives remotely
     hw_cluster_sync();
 
-    const int32_t n_items = *segs.n_tiles * 4 * n_parts;
+    const int32_t n_items = *segs.n_tiles * kSubs * n_parts;
     const int32_t nkb = (d_in + 63) / 64;
     const int32_t kb_per = (nkb + kCS - 1) / kCS;
     const int32_t kb0 = min(nkb, (int32_t)rho * kb_per), kb1 = min(nkb, kb0 + kb_per);
     const int32_t nmy = kb1 - kb0;
-    uint32_t g = 0, np1 = 0, gw = 0;  // stage counter, items done, phase-3 chunks done
+    uint32_t g = 0, np1 = 0, gw = 0;  // phase-1 stages issued, phase-1 commits, phase-3 chunks
 
     for (int32_t it = cluster_id(); it < n_items; it += n_clusters()) {
         const Item I = load_item(tab, segs, it, n_parts, part_cols);
         if (!I.live) continue;  // uniform across the cluster: same item, same decision
         const int32_t r = I.ad.rank, rp = rpad16(r);
+        const int32_t nch = (I.n_hi - I.n_lo + 127) / 128;  // 128-column chunks of the part
         if (threadIdx.x < kTok)
             S.tok[threadIdx.x] = threadIdx.x < I.rows ? segs.perm[I.tile.begin + I.sub_begin + threadIdx.x] : -1;
         __syncthreads();
         const bool run = *S.abort == 0;
         __syncthreads();
+        // this CTA's chunks are c = rho, rho + 8, ...: fetch the first two chunks' weights now
+        if (threadIdx.x == 0 && run)
+            for (int32_t j = 0; j < 2 && (int32_t)rho + kCS * j < nch; ++j)
+                load_w(S, &map_b, (gw + j) & 1u, I.n_lo + 128 * ((int32_t)rho + kCS * j), I.ad.row_off, rp);
 
         // ---------------------------------------------------------------- phase 1 (split-K shrink)
         if (run) {
@@ -255,7 +275,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                         for (int q = 0; q < rp / 16; ++q)
                             tma_load_2d(S.a + s * kABytes + q * 2048, &map_a, &S.full[s], j0, I.ad.row_off + 16 * q);
                     }
-                    // 32 token rows x 8 chunks of 16 bytes: two per thread
+                    // kTok token rows x 8 chunks of 16 bytes
                     for (int e = threadIdx.x; e < kTok * 8; e += kThreads) {
                         const int m = e >> 3, c = e & 7;
                         const int32_t t = S.tok[m];
@@ -286,14 +306,22 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
             if (threadIdx.x == 0) umma_commit(S.p1done);
             g += (uint32_t)nmy;
         }
+        // y values of this CTA's first chunk (this thread's column, every token), fetched early
+        uint16_t yv[kTok];
+        {
+            const int32_t o = I.n_lo + 128 * (int32_t)rho + 32 * warp + lane;
+            const bool col = (int32_t)rho < nch && o < I.n_hi;
+#pragma unroll
+            for (int t = 0; t < kTok; ++t) yv[t] = (col && S.tok[t] >= 0) ? y[(int64_t)S.tok[t] * d_out + o] : 0;
+        }
         // partial D1 (lanes = rank rows, columns = tokens) -> shared memory
         {
             const bool have =
                 __syncthreads_and(run && nmy > 0 && mbar_wait(S.p1done, np1 & 1u, S.abort, segs.status)) != 0;
             tc_fence_after();
-            uint32_t v[2][16];
-            tmem_ld16(tmem_base + ((32u * warp) << 16), v[0]);
-            tmem_ld16(tmem_base + ((32u * warp) << 16) + 16u, v[1]);
+            uint32_t v[3][16];
+#pragma unroll
+            for (int q = 0; q < 3; ++q) tmem_ld16(tmem_base + tmem_lane + 16u * q, v[q]);
             tmem_ld_wait();
             tc_fence_before();
             const int k = 32 * warp + lane;
@@ -308,14 +336,11 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
             const int kr = rp / kCS;  // rank rows owned by this CTA (r_pad is a multiple of 16)
             for (int e = threadIdx.x; e < kr * kTok; e += kThreads) {
                 const int k = (int)rho * kr + e / kTok, t = e % kTok;
-                float acc = 0.f;
-#pragma unroll
-                for (int c = 0; c < kCS; ++c)
-                    acc += ld_cluster_f32(map_rank(smem_u32(S.part + k * kPStride + t), (uint32_t)c));
+                float acc = sum_cluster_f32(smem_u32(S.part + k * kPStride + t));
                 if (k >= r) acc = 0.f;
                 const uint16_t hi = f32_to_bf16(acc);
                 const uint16_t lo = f32_to_bf16(acc - bf16_to_f32(hi));
-                // element (t, k) of the K-major 128-byte-swizzled h block [32 x 64] atoms
+                // element (t, k) of the K-major 128-byte-swizzled h block [kTok x 64] atoms
                 const uint32_t off = (uint32_t)(k >> 6) * kXBytes + sw128_offset((uint32_t)t, (uint32_t)((k & 63) >> 3)) +
                                      (uint32_t)(k & 7) * 2u;
 #pragma unroll
@@ -337,46 +362,39 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
         fence_proxy_async();
 
         // ---------------------------------------------------------------- phase 3 (expand, this CTA's chunks)
-        const int32_t nch = (I.n_hi - I.n_lo + 127) / 128;
         const uint32_t idesc3 = make_idesc_bf16(128, kTok, true, false);
         for (int32_t c = (int32_t)rho, j = 0; c < nch; c += kCS, ++j) {
             const int32_t o0 = I.n_lo + 128 * c;
             const uint32_t slot = gw & 1u, ph = (gw >> 1) & 1u;
-            bool have = false;
+            const uint32_t d3 = tmem_base + 64u + 64u * slot;
             if (threadIdx.x == 0 && run) {
-                uint8_t *w_s = S.w + slot * kWBytes;
-                mbar_arrive_expect_tx(&S.wfull[slot], (uint32_t)rp * 256u);
-                for (int a = 0; a < 2; ++a)
-                    for (int q = 0; q < rp / 16; ++q)
-                        tma_load_2d(w_s + a * rp * 128 + q * 2048, &map_b, &S.wfull[slot], o0 + 64 * a,
-                                    I.ad.row_off + 16 * q);
                 if (mbar_wait(&S.wfull[slot], ph, S.abort, segs.status)) {
                     tc_fence_after();
-                    const uint32_t wb = smem_u32(w_s), hh = smem_u32(S.hhi), hl = smem_u32(S.hlo);
+                    const uint32_t wb = smem_u32(S.w + slot * kWBytes), hh = smem_u32(S.hhi), hl = smem_u32(S.hlo);
                     for (int kk = 0; kk < rp / 16; ++kk) {
                         const uint64_t adesc = make_desc(wb + 2048u * kk, (uint32_t)rp * 128u, 1024, kSwizzle128);
                         const uint32_t hoff = (uint32_t)(kk >> 2) * kXBytes + (uint32_t)(kk & 3) * 32u;
-                        umma_bf16(tmem_base + 32u + 32u * slot, adesc, make_desc(hh + hoff, 16, 1024, kSwizzle128),
-                                  idesc3, kk > 0 ? 1u : 0u);
-                        umma_bf16(tmem_base + 32u + 32u * slot, adesc, make_desc(hl + hoff, 16, 1024, kSwizzle128),
-                                  idesc3, 1u);
+                        umma_bf16(d3, adesc, make_desc(hh + hoff, 16, 1024, kSwizzle128), idesc3, kk > 0 ? 1u : 0u);
+                        umma_bf16(d3, adesc, make_desc(hl + hoff, 16, 1024, kSwizzle128), idesc3, 1u);
                     }
                 }
                 umma_commit(&S.d3full[slot]);
             }
-            have = __syncthreads_and(run && mbar_wait(&S.d3full[slot], ph, S.abort, segs.status) &&
-                                     *S.abort == 0) != 0;
+            const int32_t o = o0 + 32 * warp + lane;
+            if (j > 0) {  // later chunks: fetch y while the MMA runs
+#pragma unroll
+                for (int t = 0; t < kTok; ++t)
+                    yv[t] = (o < I.n_hi && S.tok[t] >= 0) ? y[(int64_t)S.tok[t] * d_out + o] : 0;
+            }
+            const bool have = __syncthreads_and(run && mbar_wait(&S.d3full[slot], ph, S.abort, segs.status) &&
+                                                *S.abort == 0) != 0;
             tc_fence_after();
-            uint32_t v[2][16];
-            tmem_ld16(tmem_base + ((32u * warp) << 16) + 32u + 32u * slot, v[0]);
-            tmem_ld16(tmem_base + ((32u * warp) << 16) + 32u + 32u * slot + 16u, v[1]);
+            uint32_t v[3][16];
+#pragma unroll
+            for (int q = 0; q < 3; ++q) tmem_ld16(d3 + tmem_lane + 16u * q, v[q]);
             tmem_ld_wait();
             tc_fence_before();
-            const int32_t o = o0 + 32 * warp + lane;
             if (have && o < I.n_hi) {
-                uint16_t yv[kTok];
-#pragma unroll
-                for (int t = 0; t < kTok; ++t) yv[t] = S.tok[t] >= 0 ? y[(int64_t)S.tok[t] * d_out + o] : 0;
 #pragma unroll
                 for (int t = 0; t < kTok; ++t)
                     if (S.tok[t] >= 0)
@@ -384,7 +402,9 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                             f32_to_bf16(bf16_to_f32(yv[t]) + I.ad.scale * __uint_as_float(v[t >> 4][t & 15]));
             }
             ++gw;
-            __syncthreads();  // TMEM slot and w slot reuse
+            __syncthreads();  // TMEM slot and weight slot free again
+            if (threadIdx.x == 0 && run && c + 2 * kCS < nch)  // weights of this slot's next chunk
+                load_w(S, &map_b, slot, I.n_lo + 128 * (c + 2 * kCS), I.ad.row_off, rp);
         }
         __syncthreads();
     }
@@ -411,9 +431,29 @@ lora_status_t tc_decode_fwd(void *y, float *H_save, const void *x, const lora_ad
     if (cudaFuncSetAttribute(tc_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
         cudaSuccess)
         return LORA_ERR_CUDA;
+    // as many clusters as can be resident at once (eight-SM clusters must fit in
+    // one GPC, so this is below SMs / 8), so that no cluster waits for a second wave
     const int sms = sm_count();
-    const int clusters = sms / kCS > 0 ? sms / kCS : 1;
-    // column parts: enough items to give every cluster one (32-token sub-tiles ~ T / 32 + N)
+    int clusters = sms / kCS > 0 ? sms / kCS : 1;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(clusters * kCS);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = kCS;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int active = 0;
+        if (cudaOccupancyMaxActiveClusters(&active, tc_decode_kernel, &cfg) == cudaSuccess && active > 0 &&
+            active < clusters)
+            clusters = active;
+        cudaGetLastError();
+    }
+    // column parts: enough items to give every cluster one (sub-tiles ~ T / kTok + 1)
     const int est = (segs.n_tokens + kTok - 1) / kTok + 1;
     int n_parts = clusters / est;
     n_parts = n_parts < 1 ? 1 : n_parts;

@@ -43,6 +43,21 @@ bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64
     return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_f32_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                      uint32_t box_rows)
+{
+    auto fn = encode_fn();
+    if (fn == nullptr || rows == 0 || cols == 0) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 4};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box, estride,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int sm_count()
 {
     int dev = 0, n = 0;

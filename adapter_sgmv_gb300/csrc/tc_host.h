@@ -12,6 +12,9 @@ namespace lora {
 // Row-major bf16 matrix [rows, cols] as a 2-D TMA tensor, box [box_rows, box_cols].
 bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
                        uint32_t box_rows, bool swizzle128);
+// Row-major fp32 matrix [rows, cols] as a 2-D TMA tensor (no swizzle), box [box_rows, box_cols].
+bool make_tmap_f32_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                      uint32_t box_rows);
 int sm_count();
 
 // Hand-off buffers between the kernels: bf16 [T, rw] rows in perm order (the

@@ -117,6 +117,7 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
         }
         uint32_t g = 0;
         bool ok = true;
+        ArriveQueue<kLag, kStages> aq;
         for (int32_t ti = blockIdx.x; ti < n_tiles && ok; ti += gridDim.x) {
             const Tile T = load_tile(segs.tiles, ti);
             const AdapterInfo ad = load_adapter(tab, T.adapter, segs.status);
@@ -158,18 +159,11 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
                         cp_async_16(act_s + sw128_offset(m, c), src, v);
                     }
                 }
-                cp_async_commit();
-                if (g >= (uint32_t)kLag) {
-                    cp_async_wait<kLag>();
-                    fence_proxy_async();
-                    mbar_arrive(&S.full[(g - kLag) % kStages]);
-                }
+                aq.issued(S.full, g, !contiguous);
                 ++g;
             }
         }
-        cp_async_wait<0>();
-        fence_proxy_async();
-        for (uint32_t u = g > (uint32_t)kLag ? g - kLag : 0u; u < g; ++u) mbar_arrive(&S.full[u % kStages]);
+        aq.drain(S.full);
         if (!ok && lane == 0) {  // aborted: let issued TMA copies land before the CTA leaves
             for (uint32_t u = g > (uint32_t)kStages ? g - kStages : 0u; u < g; ++u) {
                 uint64_t t0 = globaltimer_ns();

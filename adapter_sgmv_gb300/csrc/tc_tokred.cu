@@ -14,8 +14,9 @@
 // copied with cp.async and zero-filled so that rows past the span add
 // nothing).  A work item is (span of <= LORA_SPAN_TOKENS tokens of one
 // adapter, 512 columns of d): four TMEM accumulators of up to 128 columns
-// accumulate over the span in 32-token stages, then are added into the
-// zero-initialised output with fp32 red.global.add (spans of an adapter sum).
+// accumulate over the span in 32-token stages; the epilogue stages each
+// warp's 32 x r_pad block in shared memory and adds it into the
+// zero-initialised output with TMA bulk reductions (spans of an adapter sum).
 //
 // Warp roles (192 threads): 0 loads, 1 MMA + TMEM owner, 2..5 epilogue.
 #include "internal.h"
@@ -28,7 +29,7 @@ namespace {
 using namespace tc;
 
 constexpr int kThreads = 192;
-constexpr int kStages = 5;
+constexpr int kStages = 4;
 constexpr int kLag = 2;
 constexpr int kTok = 32;                                  // tokens per stage
 constexpr int kRange = 512;                               // columns of d per work item
@@ -36,11 +37,12 @@ constexpr uint32_t kActBytes = kTok * kRange * 2;         // 8 boxes of [64 cols
 constexpr uint32_t kBox = kTok * 64 * 2;                  // one [64 x 32] box
 constexpr uint32_t kHBytes = 2 * kBox;                    // h: up to 128 columns
 constexpr uint32_t kStageBytes = kActBytes + kHBytes;
+constexpr uint32_t kRedBytes = LORA_MAX_RANK * 32 * 4;  // per epilogue warp: [r_pad rows x 32 columns] fp32
 constexpr uint32_t kTmemCols = 512;
-constexpr size_t kSmemBytes = 1024 + kStages * (size_t)kStageBytes + 256;
+constexpr size_t kSmemBytes = 1024 + kStages * (size_t)kStageBytes + 4 * (size_t)kRedBytes + 256;
 
 struct Smem {
-    uint8_t *act, *h;
+    uint8_t *act, *h, *red;
     uint64_t *full, *empty, *tfull, *tempty, *done;
     uint32_t *tmem_holder;
     volatile int32_t *abort;
@@ -52,7 +54,8 @@ LORA_DEV Smem carve(uint8_t *raw)
     Smem s;
     s.act = base;
     s.h = base + kStages * kActBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(s.h + kStages * kHBytes);
+    s.red = s.h + kStages * kHBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(s.red + 4 * kRedBytes);
     s.full = bars;
     s.empty = bars + kStages;
     s.tfull = bars + 2 * kStages;
@@ -83,10 +86,21 @@ LORA_DEV Item load_item(const lora_adapter_table &tab, const lora_segments &segs
     return I;
 }
 
+LORA_DEV void tma_reduce_add_2d(const CUtensorMap *map, const void *smem_src, int32_t c0, int32_t c1)
+{
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
+                 "r"(smem_u32(smem_src)), "r"(c0), "r"(c1)
+                 : "memory");
+}
+LORA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+LORA_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+LORA_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __global__ void __launch_bounds__(kThreads, 1)
 tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_h,
-                 float *__restrict__ G, const uint16_t *__restrict__ act, int32_t d, const uint16_t *__restrict__ hbuf,
-                 int32_t rw, float use_scale, lora_adapter_table tab, lora_segments segs)
+                 const __grid_constant__ CUtensorMap map_g, const uint16_t *__restrict__ act, int32_t d,
+                 const uint16_t *__restrict__ hbuf, int32_t rw, float use_scale, lora_adapter_table tab,
+                 lora_segments segs)
 {
     extern __shared__ uint8_t smem_raw[];
     const Smem S = carve(smem_raw);
@@ -122,6 +136,7 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
         }
         uint32_t g = 0;
         bool ok = true;
+        ArriveQueue<kLag, kStages> aq;
         for (int32_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const Item I = load_item(tab, segs, it, n_ranges, d);
             if (!I.ad.ok) continue;
@@ -173,18 +188,11 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
                         cp_async_16(h_s + (c >> 3) * kBox + sw128_offset((uint32_t)m, (uint32_t)(c & 7)), src, v);
                     }
                 }
-                cp_async_commit();
-                if (g >= (uint32_t)kLag) {
-                    cp_async_wait<kLag>();
-                    fence_proxy_async();
-                    mbar_arrive(&S.full[(g - kLag) % kStages]);
-                }
+                aq.issued(S.full, g, !contiguous || !h_tma);
                 ++g;
             }
         }
-        cp_async_wait<0>();
-        fence_proxy_async();
-        for (uint32_t u = g > (uint32_t)kLag ? g - kLag : 0u; u < g; ++u) mbar_arrive(&S.full[u % kStages]);
+        aq.drain(S.full);
         if (!ok && lane == 0) {
             for (uint32_t u = g > (uint32_t)kStages ? g - kStages : 0u; u < g; ++u) {
                 uint64_t t0 = globaltimer_ns();
@@ -237,34 +245,49 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
+        // Each warp owns 32 columns n (its TMEM lanes) of every chunk: it writes
+        // c * acc as [r_pad rows k x 32 columns] fp32 into its staging block and
+        // adds the block into G (rows row_off + k, columns n) with TMA bulk
+        // reductions of [16 x 32].  Rows k in [r_i, r_pad) add exact zeros (h is
+        // zero there); rows and columns past G's edge are clipped by the TMA.
         const uint32_t lane_base = 32u * (warp & 3);
+        float *red = reinterpret_cast<float *>(S.red + (warp - 2) * kRedBytes);
         uint32_t nitem = 0;
         for (int32_t it = blockIdx.x; it < n_items; it += gridDim.x) {
             const Item I = load_item(tab, segs, it, n_ranges, d);
             if (!I.ad.ok) continue;
-            const int32_t r = I.ad.rank, rp = rpad16(r);
+            const int32_t rp = rpad16(I.ad.rank);
             if (!mbar_wait_warp(S.tfull, nitem & 1u, S.abort, segs.status)) break;
             tc_fence_after();
             const float c = use_scale != 0.f ? I.ad.scale : 1.0f;
             for (int q = 0; q < 4; ++q) {
                 if (q >= I.n_chunks) break;
-                const int32_t n = I.n_base + 128 * q + (int32_t)lane_base + lane;
-                float *col = G + (int64_t)I.ad.row_off * d + n;
+                if (lane == 0) bulk_wait_read0();  // the previous chunk's reductions have read the block
+                __syncwarp();
                 for (int c0 = 0; c0 < rp; c0 += 16) {
                     uint32_t v[16];
                     tmem_ld16(tmem_base + (lane_base << 16) + 128u * q + (uint32_t)c0, v);
                     tmem_ld_wait();
-                    if (n >= d) continue;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        if (c0 + e < r) red_add_f32(col + (int64_t)(c0 + e) * d, c * __uint_as_float(v[e]));
+                    for (int e = 0; e < 16; ++e) red[(c0 + e) * 32 + lane] = c * __uint_as_float(v[e]);
                 }
+                fence_proxy_async();
+                __syncwarp();
+                const int32_t n0 = I.n_base + 128 * q + (int32_t)lane_base;
+                if (lane == 0 && n0 < d) {  // a box wholly past column d - 1 is not issued
+                    for (int q16 = 0; q16 < rp / 16; ++q16)
+                        tma_reduce_add_2d(&map_g, red + q16 * 16 * 32, n0, I.ad.row_off + 16 * q16);
+                    bulk_commit();
+                }
+                __syncwarp();
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(S.tempty);
             ++nitem;
         }
+        if (lane == 0) bulk_wait0();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -281,9 +304,10 @@ lora_status_t launch_tokred(float *G, const void *act, int32_t d, const uint16_t
     const size_t gbytes = (size_t)tab.sum_r * (size_t)d * sizeof(float);
     if (cudaMemsetAsync(G, 0, gbytes, stream) != cudaSuccess) return LORA_ERR_CUDA;
     if (segs.n_tokens == 0 || segs.max_spans == 0) return LORA_OK;
-    CUtensorMap map_act, map_h;
+    CUtensorMap map_act, map_h, map_g;
     if (!make_tmap_bf16_2d(&map_act, act, (uint64_t)d, (uint64_t)segs.n_tokens, 64, kTok, true) ||
-        !make_tmap_bf16_2d(&map_h, hbuf, (uint64_t)rw, (uint64_t)segs.n_tokens, 64, kTok, true))
+        !make_tmap_bf16_2d(&map_h, hbuf, (uint64_t)rw, (uint64_t)segs.n_tokens, 64, kTok, true) ||
+        !make_tmap_f32_2d(&map_g, G, (uint64_t)d, (uint64_t)tab.sum_r, 32, 16))
         return LORA_ERR_CUDA;
     if (cudaFuncSetAttribute(tc_tokred_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
         cudaSuccess)
@@ -292,8 +316,8 @@ lora_status_t launch_tokred(float *G, const void *act, int32_t d, const uint16_t
     const int64_t items = (int64_t)segs.max_spans * n_ranges;
     const int sms = sm_count();
     const int grid = items < sms ? (int)items : sms;
-    tc_tokred_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_act, map_h, G, static_cast<const uint16_t *>(act), d,
-                                                             hbuf, rw, use_scale, tab, segs);
+    tc_tokred_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_act, map_h, map_g, static_cast<const uint16_t *>(act),
+                                                             d, hbuf, rw, use_scale, tab, segs);
     return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 

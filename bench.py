@@ -223,6 +223,24 @@ def time_steps(work: Workload, steps: int, warmup: int, stream):
     return start, end, ev
 
 
+def time_config(spec: wl.Spec, dev, stream, steps: int = 10, warmup: int = 3) -> dict:
+    """One full step (build + fwd + bwd) of another workload: ms and tokens/s."""
+    import torch
+
+    work = Workload(spec, dev)
+    start, end, _ = time_steps(work, steps, warmup, stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    by = step_bytes(spec)
+    hbm, _, _ = measured_peaks()
+    out = {"tokens": spec.n_tokens, "ms_per_step": round(ms, 4), "tokens/s": round(spec.n_tokens / (ms * 1e-3), 1),
+           "GB/s": round((by["fwd"] + by["bwd"]) / (ms * 1e-3) / 1e9, 1),
+           "frac_of_hbm": round((by["fwd"] + by["bwd"]) / (ms * 1e-3) / 1e9 / hbm, 4)}
+    del work
+    torch.cuda.empty_cache()
+    return out
+
+
 def time_e2e(work: Workload, steps: int, warmup: int, stream):
     """Same step with the activations coming from pinned host memory and the
     adapter gradients going back to it, copies inside the timed region."""
@@ -358,6 +376,8 @@ def run_ours(args, rank, world, dev):
     lora.lib()
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)
+    if args.decode_only:  # the decode measurement alone (profiling runs)
+        return {"decode_sgmv": time_decode(dev, stream)} if rank == 0 else None
     spec = wl.packed4096(tokens_per_adapter=args.tokens_per_adapter)
     work = Workload(spec, dev)
     torch.cuda.synchronize()
@@ -396,6 +416,12 @@ def run_ours(args, rank, world, dev):
 
     e2e_ms, h2d, d2h = time_e2e(work, max(3, args.steps // 2), 2, stream) if not args.no_e2e else (None, 0, 0)
     decode = time_decode(dev, stream) if rank == 0 and not args.no_decode else None
+    others = None
+    if rank == 0 and not args.no_sweep:
+        del work
+        torch.cuda.empty_cache()
+        others = {f"sweep3584x18944_N{n}": time_config(wl.sweep(n), dev, stream) for n in (2, 4, 8, 16, 32)}
+        others["skewed4096x14336_N32"] = time_config(wl.skewed(), dev, stream)
     cpu = cpu_baseline(spec, args.cpu_seconds) if rank == 0 and not args.no_cpu else None
 
     if rank != 0:
@@ -423,6 +449,7 @@ def run_ours(args, rank, world, dev):
         "gpu_launches": kernels_per_step(spec) * args.steps,
         "clocks": clk.summary(),
         "decode_sgmv": decode,
+        "other_workloads": others,
         "cpu_baseline": cpu,
     }
     return line
@@ -480,6 +507,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-tokens-per-adapter", type=int, default=16)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the adapter-count sweep and the skewed batch")
+    ap.add_argument("--decode-only", action="store_true", help="time only the decode batch (profiling runs)")
     ap.add_argument("--tokens-per-adapter", type=int, default=4096,
                     help="tokens per adapter of the packed batch (4096 is the benchmarked workload; "
                          "smaller values give the small profiling case)")
