@@ -19,8 +19,10 @@
 // adds c * acc in fp32, rounds once, and writes back with a TMA store (full
 // tiles of consecutive tokens) or plain stores of the valid rows.
 //
-// Warp roles: 0 loads (TMA / cp.async), 1 MMA + TMEM owner, 2..5 epilogue,
-// 6..9 (loader variant only) fp32 -> bf16 conversion of the h block.
+// Warp roles: 0 loads (TMA / cp.async), 1 MMA + TMEM owner, then the
+// epilogue: warps 2..9 for sorted batches (both column halves of a chunk at
+// once), else 2..5; in the loader variant 2..5 epilogue and 6..9 fp32 -> bf16
+// conversion of the h block.
 #include "internal.h"
 #include "tc_common.cuh"
 #include "tc_host.h"
@@ -102,11 +104,14 @@ LORA_DEV void tma_store_2d(const CUtensorMap *map, const void *smem_src, int32_t
 }
 template <int N>
 LORA_DEV void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
-constexpr int kStoreLag = 2;  // TMA stores whose smem reads may still be pending
-// Freeing stage g - kYStages needs the store of stage g - kYStages + kStoreLag,
-// which needs that stage's deferred arrive, issued with stage g - kYStages +
-// kStoreLag + kLagY; that must come before the producer's wait on stage g.
-static_assert(kLagY + kStoreLag < kYStages, "y-stage ring too shallow for the arrive and store lags");
+// Per store leader, the TMA stores whose shared-memory reads may still be
+// pending: none with eight epilogue warps (one leader per column half), one
+// with four (one leader for both halves).
+template <int kEpi>
+__host__ __device__ constexpr int store_lag() { return kEpi == 8 ? 0 : 1; }
+// Threads: producer and MMA warps, the epilogue, and the loader warps.
+template <bool kLoader, int kEpi>
+__host__ __device__ constexpr int threads_of() { return 64 + 32 * kEpi + (kLoader ? 128 : 0); }
 LORA_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 struct ColIn {
@@ -115,12 +120,26 @@ struct ColIn {
     int32_t split;     // 1: the A operand is hi + lo
 };
 
-template <bool kLoader>
-__global__ void __launch_bounds__(kLoader ? 320 : 192, 1)
+template <bool kLoader, int kEpi>
+__global__ void __launch_bounds__(threads_of<kLoader, kEpi>(), 1)
 tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_hi,
                   const __grid_constant__ CUtensorMap map_lo, const __grid_constant__ CUtensorMap map_y,
                   uint16_t *__restrict__ out, int32_t d, ColIn in, lora_adapter_table tab, lora_segments segs)
 {
+    // epilogue warps: eight (sorted batches: every tile is a run of consecutive
+    // tokens), else four; four when warps 6..9 convert the fp32 h block
+    static_assert((kEpi == 4 || kEpi == 8) && !(kLoader && kEpi == 8), "epilogue of four or eight warps");
+    constexpr int kHStep = kEpi / 4;
+    constexpr int kStoreLag = store_lag<kEpi>();
+    // A stage of a full tile is freed once its leader has issued kStoreLag more
+    // stores, i.e. after stage g + kStoreLag (four warps: one leader for both
+    // halves) or g + 2 kStoreLag (eight: one leader per half) is worked on; TMA
+    // stages arrive when issued, so the producer can fill that stage once an
+    // earlier one is freed.  A gathered stage is released kLagY stages after it
+    // was issued and is freed without a store.  Tiles of the two kinds never
+    // share an item, and every item ends with its stores drained.
+    static_assert(kLagY < kYStages && (kEpi / 4) * kStoreLag < kYStages,
+                  "y-stage ring too shallow for the arrive and store lags");
     extern __shared__ uint8_t smem_raw[];
     const Smem S = carve(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -134,11 +153,11 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
         for (int i = 0; i < kYStages; ++i) {
             mbar_init(&S.yfull[i], 33);
             mbar_init(&S.yempty[i], 1);
-            mbar_init(&S.ysync[i], 4);  // one arrive per epilogue warp once its rows are done
+            mbar_init(&S.ysync[i], 4);  // one arrive per warp of the group once its rows are done
         }
         for (uint32_t i = 0; i < kAcc; ++i) {
             mbar_init(&S.tfull[i], 1);
-            mbar_init(&S.tempty[i], 4);
+            mbar_init(&S.tempty[i], kEpi);
         }
         mbar_init(S.afull, kLoader ? 4 : 1);
         mbar_init(S.aempty, 1);
@@ -191,12 +210,18 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                 }
                 ++na;
             }
-            int32_t tok[32];  // rows (lane >> 3) + 4 q of a gathered tile
+            // tokens of a gathered tile's rows, -1 past its end: in the 192-thread
+            // kernel the 32 rows (lane >> 3) + 4 q this lane copies sit in
+            // registers; in the 320-thread ones (a smaller register budget per
+            // thread) row lane + 32 i sits in tok[i] and is passed by shuffles
+            constexpr bool kTokShfl = threads_of<kLoader, kEpi>() > 192;
+            constexpr int kTokRegs = kTokShfl ? 4 : 32;
+            int32_t tok[kTokRegs];
             if (!contiguous) {
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const int m = (lane >> 3) + 4 * q;
-                    tok[q] = m < I.tile.rows ? segs.perm[I.tile.begin + m] : -1;
+                for (int i = 0; i < kTokRegs; ++i) {
+                    const int m = kTokShfl ? lane + 32 * i : (lane >> 3) + 4 * i;
+                    tok[i] = m < I.tile.rows ? segs.perm[I.tile.begin + m] : -1;
                 }
             }
             for (int32_t n0 = I.n_lo; n0 < I.n_hi && ok; n0 += kNC) {
@@ -233,12 +258,25 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                     if (!contiguous) {
                         const int c = lane & 7;
                         const bool cin = c0 + 8 * c < d;
+                        // rows (lane >> 3) + 4 q, eight rows at a time
 #pragma unroll
-                        for (int q = 0; q < 32; ++q) {
-                            const int m = (lane >> 3) + 4 * q;
-                            const bool v = tok[q] >= 0 && cin;
-                            const uint16_t *src = v ? out + (int64_t)tok[q] * d + c0 + 8 * c : out;
-                            cp_async_16(y_s + sw128_offset(m, c), src, v);
+                        for (int qb = 0; qb < 32; qb += 8) {
+                            int32_t tk[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const int m = (lane >> 3) + 4 * (qb + j);
+                                if constexpr (kTokShfl)
+                                    tk[j] = __shfl_sync(0xffffffffu, tok[(qb >> 3) & (kTokRegs - 1)], m & 31);
+                                else
+                                    tk[j] = tok[(qb + j) & (kTokRegs - 1)];
+                            }
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const int m = (lane >> 3) + 4 * (qb + j);
+                                const bool v = tk[j] >= 0 && cin;
+                                const uint16_t *src = v ? out + (int64_t)tk[j] * d + c0 + 8 * c : out;
+                                cp_async_16(y_s + sw128_offset(m, c), src, v);
+                            }
                         }
                     }
                     aq.issued(S.yfull, gy, !contiguous);
@@ -346,12 +384,18 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
             if (lane == 0) mbar_arrive(S.afull);
             ++na;
         }
-    } else if (warp >= 2 && warp <= 5) {
+    } else if (warp >= 2 && warp < 2 + kEpi) {
         // ------------------------------------------------------------ epilogue
+        // Group hg of four warps (one per TMEM sub-partition) takes the column
+        // halves h = hg, hg + kHStep of every chunk: with eight epilogue warps
+        // both halves of a chunk are worked on at once, each with its own
+        // store leader (lane 0 of the group's first warp).
+        const int hg = (warp - 2) >> 2;
         const uint32_t lane_base = 32u * (warp & 3);
         const int m = (int)lane_base + lane;
-        const bool leader = warp == 2 && lane == 0;
-        uint32_t a = 0, gy = 0;
+        const bool leader = (warp & 3) == 2 && lane == 0;
+        const bool lead_warp = (warp & 3) == 2;
+        uint32_t a = 0;
         bool ok = true;
         // leader only: stages whose TMA store may still be reading shared memory,
         // oldest first; a stage goes back to the producer once its store has read it
@@ -372,8 +416,9 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                 }
                 tc_fence_after();
 #pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
+                for (int h = hg; h < 2; h += kHStep) {
                     const int32_t c0 = n0 + 64 * h;
+                    const uint32_t gy = 2u * a + (uint32_t)h;  // the producer fills two stages per chunk
                     const uint32_t s = gy % kYStages, ph = (gy / kYStages) & 1u;
                     if (!mbar_wait_warp(&S.yfull[s], ph, S.abort, segs.status)) {
                         ok = false;
@@ -389,7 +434,7 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                     for (int q = 0; q < 4; ++q)
                         tmem_ld16(tmem_base + (lane_base << 16) + acc * 128u + 64u * h + 16u * q, v[q]);
                     tmem_ld_wait();
-                    if (h == 1) {
+                    if (h + kHStep >= 2) {  // this warp's last read of the accumulator
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&S.tempty[acc]);
@@ -413,7 +458,7 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                     if (I.full) fence_proxy_async();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&S.ysync[s]);
-                    if (warp == 2) {  // all four warps' rows are in place: store the block, free stages
+                    if (lead_warp) {  // the group's four warps have their rows in place: store, free stages
                         if (!mbar_wait_warp(&S.ysync[s], ph, S.abort, segs.status)) {
                             ok = false;
                         } else if (leader) {
@@ -432,7 +477,6 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                         }
                         __syncwarp();
                     }
-                    ++gy;
                     if (!ok) break;
                 }
                 if (!ok) break;
@@ -462,7 +506,7 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     }
 }
 
-template <bool kLoader>
+template <bool kLoader, int kEpi>
 lora_status_t launch_colproj(uint16_t *out, int32_t d, const void *w, const uint16_t *hi, const uint16_t *lo,
                              int32_t rw, const ColIn &in, const lora_adapter_table &tab, const lora_segments &segs,
                              cudaStream_t stream)
@@ -485,14 +529,14 @@ lora_status_t launch_colproj(uint16_t *out, int32_t d, const void *w, const uint
         map_hi = map_y;
         map_lo = map_y;
     }
-    if (cudaFuncSetAttribute(tc_colproj_kernel<kLoader>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(tc_colproj_kernel<kLoader, kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
         return LORA_ERR_CUDA;
     const int n_parts = (d + kNPart - 1) / kNPart;
     const int64_t items = (int64_t)segs.max_tiles * n_parts;
     const int sms = sm_count();
     const int grid = items < sms ? (int)items : sms;
-    tc_colproj_kernel<kLoader><<<grid, kLoader ? 320 : 192, kSmemBytes, stream>>>(map_w, map_hi, map_lo, map_y, out,
+    tc_colproj_kernel<kLoader, kEpi><<<grid, threads_of<kLoader, kEpi>(), kSmemBytes, stream>>>(map_w, map_hi, map_lo, map_y, out,
                                                                                   d, in, tab, segs);
     return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
@@ -503,14 +547,16 @@ lora_status_t tc_expand_bf16(void *y, const uint16_t *hi, const uint16_t *lo, in
                              const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream)
 {
     ColIn in{nullptr, 1.f, lo != nullptr ? 1 : 0};
-    return launch_colproj<false>(static_cast<uint16_t *>(y), tab.d_out, tab.B, hi, lo, rw, in, tab, segs, stream);
+    if (segs.sorted != 0)
+        return launch_colproj<false, 8>(static_cast<uint16_t *>(y), tab.d_out, tab.B, hi, lo, rw, in, tab, segs, stream);
+    return launch_colproj<false, 4>(static_cast<uint16_t *>(y), tab.d_out, tab.B, hi, lo, rw, in, tab, segs, stream);
 }
 
 lora_status_t tc_expand_f32(void *y, const float *H, const lora_adapter_table &tab, const lora_segments &segs,
                             cudaStream_t stream)
 {
     ColIn in{H, 1.f, 1};
-    return launch_colproj<true>(static_cast<uint16_t *>(y), tab.d_out, tab.B, nullptr, nullptr, 0, in, tab, segs,
+    return launch_colproj<true, 4>(static_cast<uint16_t *>(y), tab.d_out, tab.B, nullptr, nullptr, 0, in, tab, segs,
                                 stream);
 }
 
@@ -518,8 +564,11 @@ lora_status_t tc_dx(void *dX, const uint16_t *dh_bf16, int32_t rw, const lora_ad
                     const lora_segments &segs, cudaStream_t stream)
 {
     ColIn in{nullptr, 0.f, 0};
-    return launch_colproj<false>(static_cast<uint16_t *>(dX), tab.d_in, tab.A, dh_bf16, nullptr, rw, in, tab, segs,
-                                 stream);
+    if (segs.sorted != 0)
+        return launch_colproj<false, 8>(static_cast<uint16_t *>(dX), tab.d_in, tab.A, dh_bf16, nullptr, rw, in, tab,
+                                        segs, stream);
+    return launch_colproj<false, 4>(static_cast<uint16_t *>(dX), tab.d_in, tab.A, dh_bf16, nullptr, rw, in, tab, segs,
+                                    stream);
 }
 
 }  // namespace lora

@@ -168,14 +168,23 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
                 }
                 if (!contiguous) {
                     // token row m, 16-byte chunk c of the 512 columns: box b = c / 8 holds
-                    // columns 64 b .. 64 b + 63 as a [32 x 128 B] 128-byte-swizzled block
+                    // columns 64 b .. 64 b + 63 as a [32 x 128 B] 128-byte-swizzled block.
+                    // Lane m reads row m's token once; lanes take chunks lane, lane + 32.
                     const int nch = I.n_chunks * 16;
-                    for (int e = lane; e < kTok * nch; e += 32) {
-                        const int m = e / nch, c = e % nch;
-                        const bool v = (m < valid) && (I.n_base + 8 * c < d);
-                        const int32_t t = v ? segs.perm[p0 + kTok * st + m] : 0;
-                        const uint16_t *src = v ? act + (int64_t)t * d + I.n_base + 8 * c : act;
-                        cp_async_16(act_s + (c >> 3) * kBox + sw128_offset((uint32_t)m, (uint32_t)(c & 7)), src, v);
+                    const int32_t tl = lane < valid ? segs.perm[p0 + kTok * st + lane] : -1;
+#pragma unroll 4
+                    for (int m = 0; m < kTok; ++m) {
+                        const int32_t t = __shfl_sync(0xffffffffu, tl, m);
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const int c = lane + 32 * j;
+                            if (c < nch) {
+                                const bool v = t >= 0 && I.n_base + 8 * c < d;
+                                const uint16_t *src = v ? act + (int64_t)t * d + I.n_base + 8 * c : act;
+                                cp_async_16(act_s + (c >> 3) * kBox + sw128_offset((uint32_t)m, (uint32_t)(c & 7)), src,
+                                            v);
+                            }
+                        }
                     }
                 }
                 if (!h_tma) {
