@@ -16,7 +16,15 @@ size_t handoff_region_bytes(int32_t T, int32_t r_max)
     return (size_t)((b + 255) & ~int64_t(255));
 }
 
-size_t packed_workspace_bytes(int32_t T, int32_t r_max) { return 2 * handoff_region_bytes(T, r_max); }
+// batches up to this many tokens take the decode kernels
+constexpr int32_t kDecodeMaxTokens = 512;
+
+size_t packed_workspace_bytes(int32_t T, int32_t r_max)
+{
+    const size_t packed = 2 * handoff_region_bytes(T, r_max);
+    const size_t decode = T <= kDecodeMaxTokens ? decode_workspace_bytes(T, r_max) : 0;
+    return packed > decode ? packed : decode;
+}
 
 lora_status_t run_shrink(float *H, const void *x, const lora_adapter_table &tab, const lora_segments &segs,
                          cudaStream_t stream)
@@ -30,13 +38,10 @@ lora_status_t run_expand(void *y, const float *H, const lora_adapter_table &tab,
     return tc_expand_f32(y, H, tab, segs, stream);
 }
 
-// batches up to this many tokens take the one-launch decode kernel
-constexpr int32_t kDecodeMaxTokens = 512;
-
 lora_status_t run_fwd(void *y, float *H_save, const void *x, void *ws, const lora_adapter_table &tab,
                       const lora_segments &segs, cudaStream_t stream)
 {
-    if (segs.n_tokens <= kDecodeMaxTokens) return tc_decode_fwd(y, H_save, x, tab, segs, stream);
+    if (segs.n_tokens <= kDecodeMaxTokens) return tc_decode_fwd(y, H_save, x, ws, tab, segs, stream);
     const int32_t rw = handoff_cols(tab.r_max);
     uint16_t *hi = static_cast<uint16_t *>(ws);
     uint16_t *lo = reinterpret_cast<uint16_t *>(static_cast<char *>(ws) + handoff_region_bytes(segs.n_tokens, tab.r_max));

@@ -46,9 +46,12 @@ lora_status_t tc_db(float *dB, const void *dY, const uint16_t *h_bf16, int32_t r
 lora_status_t tc_da(float *dA, const void *X, const uint16_t *dh_bf16, int32_t rw, const lora_adapter_table &tab,
                     const lora_segments &segs, cudaStream_t stream);
 
-// decode-sized batches: shrink and expand of all adapters in one launch
-// (split-K over clusters of eight CTAs); H_save may be null.
-lora_status_t tc_decode_fwd(void *y, float *H_save, const void *x, const lora_adapter_table &tab,
+// decode-sized batches: split-K shrink of all adapters into fp32 partials in
+// ws, then the expand as a programmatic dependent launch; H_save may be null.
+// ws: decode_workspace_bytes(T, r_max) bytes.
+constexpr int32_t kDecodeSlices = 16;  // most slices of d_in (partial buffers)
+size_t decode_workspace_bytes(int32_t T, int32_t r_max);
+lora_status_t tc_decode_fwd(void *y, float *H_save, const void *x, void *ws, const lora_adapter_table &tab,
                             const lora_segments &segs, cudaStream_t stream);
 
 }  // namespace lora
