@@ -7,16 +7,19 @@
 // the step is bound by latency (the working set is a few MB).  Two launches,
 // each over all adapters, chained by programmatic dependent launch:
 //
-//   shrink  work item = (tile of <= 128 tokens of one adapter, slice of d_in)
-//           P_s[t, k] = sum_{j in slice s} x[t, j] A_i[k, j]   (fp32 partials)
+//   shrink  a cluster per tile of <= 128 tokens of one adapter; CTA s of the
+//           cluster takes slice s of d_in:
+//           P_s[t, k] = sum_{j in slice s} x[t, j] A_i[k, j]   (fp32, shared memory)
+//           then the cluster adds the slices through distributed shared
+//           memory, h[t, k] = sum_s P_s[t, k], each CTA a share of the rows,
+//           and writes h (fp32) for the expand
 //   expand  work item = (tile, 256-column slice of d_out)
-//           h[t, k]   = sum_s P_s[t, k]
 //           y[t, o]  += s_i sum_k h[t, k] B_i[o, k]
 //
 // The expand kernel is launched as a programmatic dependent of the shrink: its
 // CTAs start while the shrink runs and fetch their B_i^T block and the y rows
 // they update (inputs the shrink does not write) before waiting for the shrink
-// grid to complete; the partials are then summed from L2.
+// grid to complete; h is then read from L2.
 //
 // The products are warp-level bf16 tensor-core MMAs (m16n8k16, fp32
 // accumulate): with 16..128 tokens per tile and rank 16..128 the operand
@@ -49,8 +52,8 @@ struct Geom {
     int32_t rows_cap;  // tile rows the shared buffers hold (multiple of 16, <= 128)
     int32_t rp_cap;    // rank rows they hold: r_max rounded up to 16
     int32_t kw;        // shrink: columns per slice of d_in (multiple of kKC)
-    int32_t ks;        // shrink: slices; partial buffers
-    int32_t stages;    // shrink: pipeline depth (<= kMaxStages)
+    int32_t ks;        // shrink: slices of d_in = CTAs per cluster (<= kDecodeSlices)
+    int32_t stages;    // shrink: stages of rows_cap + rp_cap rows the ring holds (>= 2)
     int32_t ns;        // expand: slices of d_out
 };
 
@@ -89,8 +92,57 @@ LORA_DEV void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint3
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// hardware cluster barrier; every CTA of a cluster reaches each one (a cluster
+// shares its tile, so early exits are cluster-wide)
+LORA_DEV void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// 16 bytes of CTA `rank`'s shared memory at this CTA's shared address `saddr`
+LORA_DEV float4 ld_cluster_f4(uint32_t saddr, uint32_t rank)
+{
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(saddr), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(ra)
+                 : "memory");
+    return v;
+}
+
 LORA_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 LORA_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// A work item's tile, its adapter's table entry and the token of row
+// threadIdx.x, read in two rounds of memory latency instead of four: the tile
+// alongside the tile count, the table entry alongside the token.  For a tile
+// index past the count the dependent reads use clamped indexes (so they stay
+// in bounds) and their values are discarded.
+struct DecTile {
+    Tile T;
+    AdapterInfo ad;
+    int32_t my_tok;
+    bool run;
+};
+
+LORA_DEV DecTile dec_tile(const lora_adapter_table &tab, const lora_segments &segs, int32_t ti)
+{
+    DecTile d;
+    const int32_t n_tiles = *segs.n_tiles;
+    d.T = load_tile(segs.tiles, ti);
+    const int32_t a = min(max(d.T.adapter, 0), tab.n_adapters - 1);
+    const int32_t b = min(max(d.T.begin, 0), segs.n_tokens - 1);
+    d.ad.rank = __ldg(tab.rank + a);
+    d.ad.row_off = __ldg(tab.row_off + a);
+    d.ad.scale = __ldg(tab.scale + a);
+    d.my_tok = segs.perm[min(b + (int32_t)threadIdx.x, segs.n_tokens - 1)];
+    d.run = ti < n_tiles;
+    d.ad.ok = d.ad.rank >= 1 && d.ad.rank <= tab.r_max && d.ad.row_off >= 0 &&
+              (int64_t)d.ad.row_off + d.ad.rank <= (int64_t)tab.sum_r;
+    if (d.run && !d.ad.ok) set_status(segs.status, LORA_ERR_BAD_TABLE);
+    return d;
+}
 
 size_t shrink_smem(const Geom &g)
 {
@@ -109,51 +161,65 @@ size_t expand_smem(const Geom &g)
 // m-tile, each taking every (8 / mg)-th k16 step, all rank columns.  Each
 // k-group leaves its sums in shared memory; they are added in a fixed order
 // and the tile's partial goes to P_s in perm order.
-__global__ void __launch_bounds__(kThreads) dec_shrink_kernel(const uint16_t *__restrict__ x, float *__restrict__ part,
-                                                              Geom g, lora_adapter_table tab, lora_segments segs)
+__global__ void __launch_bounds__(kThreads, 2) dec_shrink_kernel(const uint16_t *__restrict__ x, float *__restrict__ hfin,
+                                                              float *__restrict__ H_save, Geom g,
+                                                              lora_adapter_table tab, lora_segments segs)
 {
     pdl_launch_dependents();  // the expand may start its own loads now
     const int32_t ti = blockIdx.x / g.ks, sl = blockIdx.x % g.ks;
-    if (ti >= *segs.n_tiles) return;
-    const Tile T = load_tile(segs.tiles, ti);
-    const AdapterInfo ad = load_adapter(tab, T.adapter, segs.status);
-    if (!ad.ok) return;
+    const DecTile D = dec_tile(tab, segs, ti);
+    if (!D.run || !D.ad.ok) return;
+    const Tile &T = D.T;
+    const AdapterInfo &ad = D.ad;
     const int32_t d_in = tab.d_in;
     const int rows = T.rows, r = ad.rank, rp = rpad16(r), rows16 = (rows + 15) & ~15;
 
     extern __shared__ __align__(16) uint8_t smem[];
-    uint16_t *xs = reinterpret_cast<uint16_t *>(smem);          // [stages][rows_cap][kXStride]
-    uint16_t *as = xs + (size_t)g.stages * g.rows_cap * kXStride;  // [stages][rp_cap][kXStride]
-    float *P = reinterpret_cast<float *>(as + (size_t)g.stages * g.rp_cap * kXStride);  // [kg][rows16][rp]
+    // ring of stages sized for this tile: [rows16 x rows of x | rp rows of A_i] x kXStride
+    uint16_t *ring = reinterpret_cast<uint16_t *>(smem);
+    float *P = reinterpret_cast<float *>(ring + (size_t)g.stages * (g.rows_cap + g.rp_cap) * kXStride);  // [kg][rows16][rp]
     int32_t *tok = reinterpret_cast<int32_t *>(P + (size_t)kPRows * g.rp_cap);          // [rows16]
-
-    for (int i = threadIdx.x; i < rows16; i += kThreads) tok[i] = i < rows ? segs.perm[T.begin + i] : -1;
-    __syncthreads();
 
     const int32_t j_lo = sl * g.kw, j_hi = min(d_in, j_lo + g.kw);
     const int nchunks = (j_hi - j_lo + kKC - 1) / kKC;
+    // as many stages as fit the ring for this tile's rows and rank (the host
+    // sized it for at least two of the largest), all chunks at once if possible
+    const int stage_elems = (rows16 + rp) * kXStride;
+    const int stages =
+        max(2, min(min(kMaxStages, nchunks + 1), (int)((size_t)g.stages * (g.rows_cap + g.rp_cap) / (rows16 + rp))));
+    uint16_t *xs = ring;             // stage s: xs + s * stage_elems, rows16 rows
+    uint16_t *as = ring + rows16 * kXStride;  // stage s: as + s * stage_elems, rp rows
     // chunk c -> stage s: x rows (gathered) and A_i rows, 16-byte pieces; past the
     // slice, the tile or the rank the pieces are zero-filled
-    auto load = [&](int c, int s) {
+    auto load_x = [&](int c, int s) {
         const int32_t j0 = j_lo + c * kKC;
-        uint16_t *xd = xs + (size_t)s * g.rows_cap * kXStride;
+        uint16_t *xd = xs + (size_t)s * stage_elems;
         for (int i = threadIdx.x; i < rows16 * (kKC / 8); i += kThreads) {
             const int m = i / (kKC / 8), p = i % (kKC / 8);
             const int32_t t = tok[m], j = j0 + 8 * p;
             const bool v = t >= 0 && j < j_hi;
             cp_async_16(xd + m * kXStride + 8 * p, v ? x + (int64_t)t * d_in + j : x, v);
         }
-        uint16_t *wd = as + (size_t)s * g.rp_cap * kXStride;
+    };
+    auto load_a = [&](int c, int s) {
+        const int32_t j0 = j_lo + c * kKC;
+        const uint16_t *A = static_cast<const uint16_t *>(tab.A);
+        uint16_t *wd = as + (size_t)s * stage_elems;
         for (int i = threadIdx.x; i < rp * (kKC / 8); i += kThreads) {
             const int k = i / (kKC / 8), p = i % (kKC / 8);
             const int32_t j = j0 + 8 * p;
             const bool v = k < r && j < j_hi;
-            const uint16_t *A = static_cast<const uint16_t *>(tab.A);
             cp_async_16(wd + k * kXStride + 8 * p, v ? A + (int64_t)(ad.row_off + k) * d_in + j : A, v);
         }
     };
-    for (int c = 0; c < g.stages - 1; ++c) {
-        if (c < nchunks) load(c, c);
+    // the first stages' weights need no tokens: they go out before the tokens
+    // land; each chunk's weights sit in its own or an earlier copy group
+    for (int c = 0; c < stages - 1; ++c)
+        if (c < nchunks) load_a(c, c);
+    if (threadIdx.x < rows16) tok[threadIdx.x] = (int)threadIdx.x < rows ? D.my_tok : -1;
+    __syncthreads();
+    for (int c = 0; c < stages - 1; ++c) {
+        if (c < nchunks) load_x(c, c);
         cp_async_commit();
     }
 
@@ -170,17 +236,20 @@ __global__ void __launch_bounds__(kThreads) dec_shrink_kernel(const uint16_t *__
     for (int n = 0; n < 16; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 
     for (int c = 0; c < nchunks; ++c) {
-        cp_async_wait_n(g.stages - 2);
+        cp_async_wait_n(stages - 2);
         __syncthreads();  // chunk c landed for every thread; stage (c - 1) % stages is free
         {
-            const int cn = c + g.stages - 1;
-            if (cn < nchunks) load(cn, cn % g.stages);
+            const int cn = c + stages - 1;
+            if (cn < nchunks) {
+                load_a(cn, cn % stages);
+                load_x(cn, cn % stages);
+            }
             cp_async_commit();
         }
         if (!active) continue;
-        const int s = c % g.stages;
-        const uint16_t *xt = xs + (size_t)s * g.rows_cap * kXStride;
-        const uint16_t *at = as + (size_t)s * g.rp_cap * kXStride;
+        const int s = c % stages;
+        const uint16_t *xt = xs + (size_t)s * stage_elems;
+        const uint16_t *at = as + (size_t)s * stage_elems;
         for (int kk = my_k; kk < kKC / 16; kk += kg) {
             uint32_t a[4];
             ldsm_x4(smem_u32(xt + (16 * my_m + lr + 8 * (lj & 1)) * kXStride + 16 * kk + 8 * (lj >> 1)), a);
@@ -208,9 +277,9 @@ __global__ void __launch_bounds__(kThreads) dec_shrink_kernel(const uint16_t *__
         }
     }
     __syncthreads();
-    // the k-groups are added in a fixed order, so the result does not depend on timing
-    float *dst = part + ((int64_t)sl * segs.n_tokens + T.begin) * g.rp_cap;
-    for (int i = threadIdx.x; i < rows * (rp / 4); i += kThreads) {
+    // this CTA's slice partial: the k-groups added in a fixed order into the
+    // first [rows16 x rp] block of P (the result does not depend on timing)
+    for (int i = threadIdx.x; i < rows16 * (rp / 4); i += kThreads) {
         const int m = i / (rp / 4), k4 = i % (rp / 4);
         float4 v = *reinterpret_cast<const float4 *>(P + m * rp + 4 * k4);
         for (int q = 1; q < kg; ++q) {
@@ -220,25 +289,62 @@ __global__ void __launch_bounds__(kThreads) dec_shrink_kernel(const uint16_t *__
             v.z += u.z;
             v.w += u.w;
         }
-        *reinterpret_cast<float4 *>(dst + (int64_t)m * g.rp_cap + 4 * k4) = v;
+        *reinterpret_cast<float4 *>(P + m * rp + 4 * k4) = v;
     }
+    cluster_sync();  // every slice partial of the tile is complete
+    // CTA sl adds rows sl, sl + ks, ... over the cluster in rank order
+    const int32_t r_max = tab.r_max;
+    const int my_rows = rows > sl ? (rows - sl + g.ks - 1) / g.ks : 0;
+    for (int i = threadIdx.x; i < my_rows * (rp / 4); i += kThreads) {
+        const int m = sl + g.ks * (i / (rp / 4)), k4 = i % (rp / 4);
+        const uint32_t sa = smem_u32(P + m * rp + 4 * k4);
+        float4 v[kDecodeSlices];
+#pragma unroll
+        for (int q = 0; q < kDecodeSlices; ++q)
+            if (q < g.ks) v[q] = ld_cluster_f4(sa, (uint32_t)q);
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < kDecodeSlices; ++q) {
+            if (q < g.ks) {
+                e[0] += v[q].x;
+                e[1] += v[q].y;
+                e[2] += v[q].z;
+                e[3] += v[q].w;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (4 * k4 + u >= r) e[u] = 0.f;
+        *reinterpret_cast<float4 *>(hfin + ((int64_t)T.begin + m) * g.rp_cap + 4 * k4) = make_float4(e[0], e[1], e[2], e[3]);
+        if (H_save != nullptr) {
+            const int32_t t = tok[m];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (4 * k4 + u < r_max) H_save[(int64_t)t * r_max + 4 * k4 + u] = e[u];
+        }
+    }
+    if (H_save != nullptr)  // columns r_pad .. r_max - 1 of this CTA's rows
+        for (int i = threadIdx.x; i < my_rows * r_max; i += kThreads) {
+            const int m = sl + g.ks * (i / r_max), k = i % r_max;
+            if (k >= rp) H_save[(int64_t)tok[m] * r_max + k] = 0.f;
+        }
+    cluster_sync();  // no CTA leaves while another may still read its partial
 }
 
 // ------------------------------------------------------------------ expand
 // Warp w owns columns 32 w .. 32 w + 31 of the slice (four n-tiles) and walks
 // the tile's m-tiles; y is updated in shared memory and written back in
 // 16-byte pieces.
-__global__ void __launch_bounds__(kThreads) dec_expand_kernel(uint16_t *__restrict__ y, float *__restrict__ H_save,
-                                                              const float *__restrict__ part, Geom g,
-                                                              lora_adapter_table tab, lora_segments segs)
+__global__ void __launch_bounds__(kThreads, 2) dec_expand_kernel(uint16_t *__restrict__ y, const float *__restrict__ hfin,
+                                                              Geom g, lora_adapter_table tab, lora_segments segs)
 {
     const int32_t ti = blockIdx.x / g.ns, nsl = blockIdx.x % g.ns;
     // the routing was complete before the shrink started, so it can be read
     // before the wait; so can B and y, which the shrink does not write
-    if (ti >= *segs.n_tiles) return;
-    const Tile T = load_tile(segs.tiles, ti);
-    const AdapterInfo ad = load_adapter(tab, T.adapter, segs.status);
-    if (!ad.ok) return;
+    const DecTile D = dec_tile(tab, segs, ti);
+    if (!D.run || !D.ad.ok) return;
+    const Tile &T = D.T;
+    const AdapterInfo &ad = D.ad;
     const int32_t d_out = tab.d_out;
     const int rows = T.rows, r = ad.rank, rp = rpad16(r), rows16 = (rows + 15) & ~15;
     const int hs = g.rp_cap + 8;  // bf16 per row of the h operand
@@ -250,8 +356,6 @@ __global__ void __launch_bounds__(kThreads) dec_expand_kernel(uint16_t *__restri
     uint16_t *hl = hh + (size_t)g.rows_cap * hs;                  // [rows_cap][hs] bf16 lo of h
     int32_t *tok = reinterpret_cast<int32_t *>(hl + (size_t)g.rows_cap * hs);
 
-    for (int i = threadIdx.x; i < rows16; i += kThreads) tok[i] = i < rows ? segs.perm[T.begin + i] : -1;
-    __syncthreads();
     const int32_t o_lo = nsl * kNW;
     for (int i = threadIdx.x; i < rp * (kNW / 8); i += kThreads) {
         const int k = i / (kNW / 8), p = i % (kNW / 8);
@@ -260,6 +364,8 @@ __global__ void __launch_bounds__(kThreads) dec_expand_kernel(uint16_t *__restri
         const uint16_t *B = static_cast<const uint16_t *>(tab.B);
         cp_async_16(bs + k * kYStride + 8 * p, v ? B + (int64_t)(ad.row_off + k) * d_out + o : B, v);
     }
+    if (threadIdx.x < rows16) tok[threadIdx.x] = (int)threadIdx.x < rows ? D.my_tok : -1;
+    __syncthreads();
     for (int i = threadIdx.x; i < rows * (kNW / 8); i += kThreads) {
         const int m = i / (kNW / 8), p = i % (kNW / 8);
         const int32_t o = o_lo + 8 * p;
@@ -268,55 +374,18 @@ __global__ void __launch_bounds__(kThreads) dec_expand_kernel(uint16_t *__restri
     }
     cp_async_commit();
 
-    pdl_wait();  // the shrink grid has completed and its partials are visible
+    pdl_wait();  // the shrink grid has completed and h is visible
 
-    const int32_t r_max = tab.r_max;
     for (int i = threadIdx.x; i < rows16 * (rp / 4); i += kThreads) {
         const int m = i / (rp / 4), k4 = i % (rp / 4);
-        float e[4] = {0.f, 0.f, 0.f, 0.f};
-        if (m < rows) {
-            const float *src = part + ((int64_t)T.begin + m) * g.rp_cap + 4 * k4;
-            const int64_t stride = (int64_t)segs.n_tokens * g.rp_cap;
-            int s = 0;
-            for (; s + 4 <= g.ks; s += 4) {
-                float4 v[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) v[u] = __ldcg(reinterpret_cast<const float4 *>(src + (s + u) * stride));
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    e[0] += v[u].x;
-                    e[1] += v[u].y;
-                    e[2] += v[u].z;
-                    e[3] += v[u].w;
-                }
-            }
-            for (; s < g.ks; ++s) {
-                const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + s * stride));
-                e[0] += v.x;
-                e[1] += v.y;
-                e[2] += v.z;
-                e[3] += v.w;
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (4 * k4 + u >= r) e[u] = 0.f;
-        const uint32_t h01 = pack_bf16(e[0], e[1]), h23 = pack_bf16(e[2], e[3]);
-        const uint32_t l01 = pack_bf16(e[0] - bf16lo(h01), e[1] - bf16hi(h01));
-        const uint32_t l23 = pack_bf16(e[2] - bf16lo(h23), e[3] - bf16hi(h23));
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (m < rows) v = __ldcg(reinterpret_cast<const float4 *>(hfin + ((int64_t)T.begin + m) * g.rp_cap + 4 * k4));
+        const uint32_t h01 = pack_bf16(v.x, v.y), h23 = pack_bf16(v.z, v.w);
+        const uint32_t l01 = pack_bf16(v.x - bf16lo(h01), v.y - bf16hi(h01));
+        const uint32_t l23 = pack_bf16(v.z - bf16lo(h23), v.w - bf16hi(h23));
         *reinterpret_cast<uint2 *>(hh + m * hs + 4 * k4) = make_uint2(h01, h23);
         *reinterpret_cast<uint2 *>(hl + m * hs + 4 * k4) = make_uint2(l01, l23);
-        if (H_save != nullptr && nsl == 0 && m < rows) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (4 * k4 + u < r_max) H_save[(int64_t)tok[m] * r_max + 4 * k4 + u] = e[u];
-        }
     }
-    if (H_save != nullptr && nsl == 0)  // columns r_pad .. r_max - 1
-        for (int i = threadIdx.x; i < rows * r_max; i += kThreads) {
-            const int m = i / r_max, k = i % r_max;
-            if (k >= rp) H_save[(int64_t)tok[m] * r_max + k] = 0.f;
-        }
     tc::cp_async_wait<0>();
     __syncthreads();
 
@@ -371,7 +440,8 @@ Geom make_geom(const lora_adapter_table &tab, const lora_segments &segs)
     const int32_t T = segs.n_tokens;
     g.rows_cap = std::min<int32_t>(LORA_TILE_M, (T + 15) & ~15);
     g.rp_cap = (tab.r_max + 15) & ~15;
-    // slices of at least 256 columns, at most kDecodeSlices of them
+    // slices of at least 256 columns, at most kDecodeSlices of them (one CTA
+    // of the tile's cluster each)
     const int32_t per = (tab.d_in + kDecodeSlices - 1) / kDecodeSlices;
     g.kw = std::max<int32_t>(2 * kKC, ((per + kKC - 1) / kKC) * kKC);
     g.ks = (tab.d_in + g.kw - 1) / g.kw;
@@ -391,7 +461,7 @@ Geom make_geom(const lora_adapter_table &tab, const lora_segments &segs)
 
 size_t decode_workspace_bytes(int32_t T, int32_t r_max)
 {
-    return (size_t)kDecodeSlices * (size_t)T * (size_t)((r_max + 15) & ~15) * sizeof(float);
+    return (size_t)T * (size_t)((r_max + 15) & ~15) * sizeof(float);
 }
 
 lora_status_t tc_decode_fwd(void *y, float *H_save, const void *x, void *ws, const lora_adapter_table &tab,
@@ -399,29 +469,44 @@ lora_status_t tc_decode_fwd(void *y, float *H_save, const void *x, void *ws, con
 {
     if (segs.n_tokens == 0 || segs.max_tiles == 0) return LORA_OK;
     const Geom g = make_geom(tab, segs);
-    float *part = static_cast<float *>(ws);
+    float *hfin = static_cast<float *>(ws);
     const size_t s1 = shrink_smem(g), s2 = expand_smem(g);
     if (cudaFuncSetAttribute(dec_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1) != cudaSuccess ||
+        cudaFuncSetAttribute(dec_shrink_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
         cudaFuncSetAttribute(dec_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2) != cudaSuccess)
         return LORA_ERR_CUDA;
-    dec_shrink_kernel<<<segs.max_tiles * g.ks, kThreads, s1, stream>>>(static_cast<const uint16_t *>(x), part, g, tab,
-                                                                        segs);
-    if (cudaGetLastError() != cudaSuccess) return LORA_ERR_CUDA;
-
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(segs.max_tiles * g.ns));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = s2;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const float *cpart = part;
-    if (cudaLaunchKernelEx(&cfg, dec_expand_kernel, static_cast<uint16_t *>(y), H_save, cpart, g, tab, segs) !=
-        cudaSuccess)
-        return LORA_ERR_CUDA;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(segs.max_tiles * g.ks));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = s1;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)g.ks;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, dec_shrink_kernel, static_cast<const uint16_t *>(x), hfin, H_save, g, tab,
+                               segs) != cudaSuccess)
+            return LORA_ERR_CUDA;
+    }
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(segs.max_tiles * g.ns));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = s2;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const float *ch = hfin;
+        if (cudaLaunchKernelEx(&cfg, dec_expand_kernel, static_cast<uint16_t *>(y), ch, g, tab, segs) != cudaSuccess)
+            return LORA_ERR_CUDA;
+    }
     return LORA_OK;
 }
 

@@ -46,10 +46,10 @@ lora_status_t tc_db(float *dB, const void *dY, const uint16_t *h_bf16, int32_t r
 lora_status_t tc_da(float *dA, const void *X, const uint16_t *dh_bf16, int32_t rw, const lora_adapter_table &tab,
                     const lora_segments &segs, cudaStream_t stream);
 
-// decode-sized batches: split-K shrink of all adapters into fp32 partials in
-// ws, then the expand as a programmatic dependent launch; H_save may be null.
-// ws: decode_workspace_bytes(T, r_max) bytes.
-constexpr int32_t kDecodeSlices = 16;  // most slices of d_in (partial buffers)
+// decode-sized batches: the shrink split over d_in across a cluster per tile
+// (fp32 h in ws), then the expand as a programmatic dependent launch; H_save
+// may be null.  ws: decode_workspace_bytes(T, r_max) bytes.
+constexpr int32_t kDecodeSlices = 16;  // most slices of d_in (CTAs per cluster)
 size_t decode_workspace_bytes(int32_t T, int32_t r_max);
 lora_status_t tc_decode_fwd(void *y, float *H_save, const void *x, void *ws, const lora_adapter_table &tab,
                             const lora_segments &segs, cudaStream_t stream);
