@@ -124,6 +124,17 @@ def test_optional_outputs_can_be_skipped():
     assert_close(dev_to_f64(dA), ref["dA"], GRAD_TOL, "dA")
 
 
+def test_decode_path_full_tiles_rank_128_ragged_edges():
+    # T = 512 still takes the decode kernels: 128-row tiles at rank 128, a d_in
+    # whose last slice ends 8 columns into a k16 step, a d_out with an 8-column tail
+    ranks = [128, 64, 8]
+    lengths = [300, 150, 62]
+    rng = np.random.default_rng(5)
+    ids = rng.permutation(np.concatenate([np.full(n, i, np.int32) for i, n in enumerate(lengths)]))
+    spec = wl.custom("decode_edges", 4104, 776, ranks, [2.0 * r for r in ranks], ids)
+    full_check(spec, y0="randn")
+
+
 @pytest.mark.parametrize("proj", [0, 1, 2])
 def test_decode_batch_shrink_expand(proj):
     spec = wl.decode(proj)
