@@ -21,8 +21,8 @@ from ._build import LIB_PATH, build as build_library  # noqa: F401
 __all__ = [
     "LoraError", "AdapterTable", "Segments", "lib", "lora_abi_version", "lora_status_string",
     "lora_segments_bytes", "lora_build_segments", "lora_workspace_bytes", "lora_sgmv_shrink",
-    "lora_sgmv_expand", "lora_packed_fwd", "lora_packed_bwd", "lora_packed_bwd_noalloc", "lora_query_status",
-    "lora_reset_status",
+    "lora_sgmv_expand", "lora_packed_fwd", "lora_packed_bwd", "lora_packed_fwd_marked", "lora_packed_bwd_marked",
+    "lora_packed_bwd_noalloc", "lora_query_status", "lora_reset_status",
     "STATUS",
 ]
 
@@ -72,6 +72,10 @@ SIGNATURES = {
     "lora_packed_fwd": (_I32, [_P, _P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments), _P, _SZ, _P]),
     "lora_packed_bwd": (_I32, [_P, _P, _P, _P, _P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments),
                                _P, _SZ, _P]),
+    "lora_packed_fwd_marked": (_I32, [_P, _P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments), _P, _SZ,
+                                      _P, ctypes.POINTER(_P), _I32, ctypes.POINTER(_I32)]),
+    "lora_packed_bwd_marked": (_I32, [_P, _P, _P, _P, _P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments),
+                                      _P, _SZ, _P, ctypes.POINTER(_P), _I32, ctypes.POINTER(_I32)]),
     "lora_packed_bwd_noalloc": (_I32, [_P, _P, _P, _P, _P, _P, ctypes.POINTER(c_table),
                                        ctypes.POINTER(c_segments), _P]),
     "lora_query_status": (_I32, [ctypes.POINTER(c_segments), _P]),
@@ -262,6 +266,44 @@ def lora_packed_bwd(dX, dA, dB, dY, X, H_saved, table: AdapterTable, segs: Segme
     _check(lib().lora_packed_bwd(_ptr(dX), _ptr(dA), _ptr(dB), _ptr(dY), _ptr(X), _ptr(H_saved),
                                  ctypes.byref(table.c), ctypes.byref(segs.c), _ptr(ws), wsb, _stream(stream)),
            "lora_packed_bwd")
+
+
+def _events(events, stream):
+    """ctypes array of the cudaEvent_t handles of torch.cuda.Event objects
+    (an event that was never recorded is recorded once so that it exists)."""
+    import torch
+
+    for e in events:
+        if e.cuda_event == 0:
+            e.record(stream if stream is not None else torch.cuda.current_stream())
+    return (_P * max(1, len(events)))(*[e.cuda_event for e in events])
+
+
+def lora_packed_fwd_marked(y, H_save, x, table: AdapterTable, segs: Segments, ws, events, stream=None) -> int:
+    """lora_packed_fwd recording ``events`` (torch.cuda.Event) around its
+    kernels: events[2k] before and events[2k + 1] after kernel k.  Returns the
+    number of events recorded."""
+    wsb = 0 if ws is None else ws.numel() * ws.element_size()
+    arr = _events(events, stream)
+    n = ctypes.c_int32(0)
+    _check(lib().lora_packed_fwd_marked(_ptr(y), _ptr(H_save), _ptr(x), ctypes.byref(table.c), ctypes.byref(segs.c),
+                                        _ptr(ws), wsb, _stream(stream), arr, len(events), ctypes.byref(n)),
+           "lora_packed_fwd_marked")
+    return int(n.value)
+
+
+def lora_packed_bwd_marked(dX, dA, dB, dY, X, H_saved, table: AdapterTable, segs: Segments, ws, events,
+                           stream=None) -> int:
+    """lora_packed_bwd recording ``events`` around its kernels (see
+    lora_packed_fwd_marked).  Returns the number of events recorded."""
+    wsb = 0 if ws is None else ws.numel() * ws.element_size()
+    arr = _events(events, stream)
+    n = ctypes.c_int32(0)
+    _check(lib().lora_packed_bwd_marked(_ptr(dX), _ptr(dA), _ptr(dB), _ptr(dY), _ptr(X), _ptr(H_saved),
+                                        ctypes.byref(table.c), ctypes.byref(segs.c), _ptr(ws), wsb, _stream(stream),
+                                        arr, len(events), ctypes.byref(n)),
+           "lora_packed_bwd_marked")
+    return int(n.value)
 
 
 def lora_packed_bwd_noalloc(dX, dA, dB, dY, X, H_saved, table: AdapterTable, segs: Segments, stream=None):

@@ -38,34 +38,63 @@ lora_status_t run_expand(void *y, const float *H, const lora_adapter_table &tab,
     return tc_expand_f32(y, H, tab, segs, stream);
 }
 
-lora_status_t run_fwd(void *y, float *H_save, const void *x, void *ws, const lora_adapter_table &tab,
-                      const lora_segments &segs, cudaStream_t stream)
+namespace {
+
+void mark(Marks *m, cudaStream_t stream)
 {
-    if (segs.n_tokens <= kDecodeMaxTokens) return tc_decode_fwd(y, H_save, x, ws, tab, segs, stream);
+    if (m != nullptr && m->k < m->n) cudaEventRecord(static_cast<cudaEvent_t>(m->ev[m->k++]), stream);
+}
+
+// launch `f` between a pair of marks
+template <class F>
+lora_status_t marked(Marks *m, cudaStream_t stream, F f)
+{
+    mark(m, stream);
+    const lora_status_t st = f();
+    mark(m, stream);
+    return st;
+}
+
+}  // namespace
+
+lora_status_t run_fwd(void *y, float *H_save, const void *x, void *ws, const lora_adapter_table &tab,
+                      const lora_segments &segs, cudaStream_t stream, Marks *marks)
+{
+    if (segs.n_tokens <= kDecodeMaxTokens)  // one pair of marks around both decode launches
+        return marked(marks, stream, [&] { return tc_decode_fwd(y, H_save, x, ws, tab, segs, stream); });
     const int32_t rw = handoff_cols(tab.r_max);
     uint16_t *hi = static_cast<uint16_t *>(ws);
     uint16_t *lo = reinterpret_cast<uint16_t *>(static_cast<char *>(ws) + handoff_region_bytes(segs.n_tokens, tab.r_max));
-    lora_status_t st = tc_shrink(x, tab, segs, H_save, hi, lo, rw, stream);
+    lora_status_t st = marked(marks, stream, [&] { return tc_shrink(x, tab, segs, H_save, hi, lo, rw, stream); });
     if (st != LORA_OK) return st;
-    return tc_expand_bf16(y, hi, lo, rw, tab, segs, stream);
+    return marked(marks, stream, [&] { return tc_expand_bf16(y, hi, lo, rw, tab, segs, stream); });
 }
 
 lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X, const float *H_saved, void *ws,
-                      const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream)
+                      const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream, Marks *marks)
 {
     const int32_t rw = handoff_cols(tab.r_max);
     uint16_t *hb = static_cast<uint16_t *>(ws);
     uint16_t *dhb = reinterpret_cast<uint16_t *>(static_cast<char *>(ws) + handoff_region_bytes(segs.n_tokens, tab.r_max));
+    // dA and dB are sums over token spans added into zeroed outputs
+    if (dB != nullptr && cudaMemsetAsync(dB, 0, (size_t)tab.sum_r * tab.d_out * sizeof(float), stream) != cudaSuccess)
+        return LORA_ERR_CUDA;
+    if (dA != nullptr && cudaMemsetAsync(dA, 0, (size_t)tab.sum_r * tab.d_in * sizeof(float), stream) != cudaSuccess)
+        return LORA_ERR_CUDA;
     lora_status_t st;
     if (H_saved == nullptr) {
-        st = tc_shrink(X, tab, segs, nullptr, hb, nullptr, rw, stream);
-        if (st == LORA_OK) st = tc_dh(dY, tab, segs, dhb, nullptr, nullptr, rw, stream);
+        st = marked(marks, stream, [&] { return tc_shrink(X, tab, segs, nullptr, hb, nullptr, rw, stream); });
+        if (st == LORA_OK)
+            st = marked(marks, stream, [&] { return tc_dh(dY, tab, segs, dhb, nullptr, nullptr, rw, stream); });
     } else {
-        st = tc_dh(dY, tab, segs, dhb, H_saved, hb, rw, stream);
+        st = marked(marks, stream, [&] { return tc_dh(dY, tab, segs, dhb, H_saved, hb, rw, stream); });
     }
-    if (st == LORA_OK && dB != nullptr) st = tc_db(dB, dY, hb, rw, tab, segs, stream);
-    if (st == LORA_OK && dA != nullptr) st = tc_da(dA, X, dhb, rw, tab, segs, stream);
-    if (st == LORA_OK && dX != nullptr) st = tc_dx(dX, dhb, rw, tab, segs, stream);
+    if (st == LORA_OK && dB != nullptr)
+        st = marked(marks, stream, [&] { return tc_db(dB, dY, hb, rw, tab, segs, stream); });
+    if (st == LORA_OK && dA != nullptr)
+        st = marked(marks, stream, [&] { return tc_da(dA, X, dhb, rw, tab, segs, stream); });
+    if (st == LORA_OK && dX != nullptr)
+        st = marked(marks, stream, [&] { return tc_dx(dX, dhb, rw, tab, segs, stream); });
     return st;
 }
 

@@ -9,14 +9,23 @@ namespace lora {
 size_t handoff_region_bytes(int32_t T, int32_t r_max);
 size_t packed_workspace_bytes(int32_t T, int32_t r_max);
 
+// Optional CUDA events recorded around each kernel of a call (measurement):
+// ev[2k] before and ev[2k + 1] after the k-th kernel, while room is left.
+struct Marks {
+    void *const *ev;
+    int32_t n;
+    int32_t k;
+};
+
 lora_status_t run_shrink(float *H, const void *x, const lora_adapter_table &tab, const lora_segments &segs,
                          cudaStream_t stream);
 lora_status_t run_expand(void *y, const float *H, const lora_adapter_table &tab, const lora_segments &segs,
                          cudaStream_t stream);
 // ws: packed_workspace_bytes(T, r_max) bytes
 lora_status_t run_fwd(void *y, float *H_save, const void *x, void *ws, const lora_adapter_table &tab,
-                      const lora_segments &segs, cudaStream_t stream);
+                      const lora_segments &segs, cudaStream_t stream, Marks *marks = nullptr);
 lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X, const float *H_saved, void *ws,
-                      const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream);
+                      const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream,
+                      Marks *marks = nullptr);
 
 }  // namespace lora

@@ -57,11 +57,44 @@ lora_status_t check_device()
 
 size_t workspace_bytes(const lora_adapter_table *t, int32_t T) { return packed_workspace_bytes(T, t->r_max); }
 
+
 #define LORA_TRY(expr)                          \
     do {                                        \
         lora_status_t _st = (expr);             \
         if (_st != LORA_OK) return _st;         \
     } while (0)
+
+lora_status_t packed_fwd(void *y, float *H_save, const void *x, const lora_adapter_table *table,
+                         const lora_segments *segs, void *ws, size_t ws_bytes, lora_stream_t stream, Marks *marks)
+{
+    LORA_TRY(check_table(table));
+    LORA_TRY(check_segs(segs, table));
+    if (y == nullptr || x == nullptr) return LORA_ERR_INVALID_ARG;
+    if (!aligned16(y) || !aligned16(x) || (H_save && !aligned16(H_save)) || (ws && !aligned16(ws)))
+        return LORA_ERR_ALIGNMENT;
+    const size_t need = workspace_bytes(table, segs->n_tokens);
+    if (need > 0 && (ws == nullptr || ws_bytes < need)) return LORA_ERR_WORKSPACE_TOO_SMALL;
+    LORA_TRY(check_device());
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return run_fwd(y, H_save, x, ws, *table, *segs, st, marks);
+}
+
+lora_status_t packed_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X, const float *H_saved,
+                         const lora_adapter_table *table, const lora_segments *segs, void *ws, size_t ws_bytes,
+                         lora_stream_t stream, Marks *marks)
+{
+    LORA_TRY(check_table(table));
+    LORA_TRY(check_segs(segs, table));
+    if (dY == nullptr || X == nullptr) return LORA_ERR_INVALID_ARG;
+    if (!aligned16(dY) || !aligned16(X) || (dX && !aligned16(dX)) || (dA && !aligned16(dA)) ||
+        (dB && !aligned16(dB)) || (H_saved && !aligned16(H_saved)) || (ws && !aligned16(ws)))
+        return LORA_ERR_ALIGNMENT;
+    const size_t need = workspace_bytes(table, segs->n_tokens);
+    if (need > 0 && (ws == nullptr || ws_bytes < need)) return LORA_ERR_WORKSPACE_TOO_SMALL;
+    LORA_TRY(check_device());
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return run_bwd(dX, dA, dB, dY, X, H_saved, ws, *table, *segs, st, marks);
+}
 
 }  // namespace
 
@@ -144,33 +177,37 @@ lora_status_t lora_sgmv_expand(void *y, const float *H, const lora_adapter_table
 lora_status_t lora_packed_fwd(void *y, float *H_save, const void *x, const lora_adapter_table *table,
                               const lora_segments *segs, void *ws, size_t ws_bytes, lora_stream_t stream)
 {
-    LORA_TRY(check_table(table));
-    LORA_TRY(check_segs(segs, table));
-    if (y == nullptr || x == nullptr) return LORA_ERR_INVALID_ARG;
-    if (!aligned16(y) || !aligned16(x) || (H_save && !aligned16(H_save)) || (ws && !aligned16(ws)))
-        return LORA_ERR_ALIGNMENT;
-    const size_t need = workspace_bytes(table, segs->n_tokens);
-    if (need > 0 && (ws == nullptr || ws_bytes < need)) return LORA_ERR_WORKSPACE_TOO_SMALL;
-    LORA_TRY(check_device());
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return run_fwd(y, H_save, x, ws, *table, *segs, st);
+    return packed_fwd(y, H_save, x, table, segs, ws, ws_bytes, stream, nullptr);
 }
 
 lora_status_t lora_packed_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X,
                               const float *H_saved, const lora_adapter_table *table,
                               const lora_segments *segs, void *ws, size_t ws_bytes, lora_stream_t stream)
 {
-    LORA_TRY(check_table(table));
-    LORA_TRY(check_segs(segs, table));
-    if (dY == nullptr || X == nullptr) return LORA_ERR_INVALID_ARG;
-    if (!aligned16(dY) || !aligned16(X) || (dX && !aligned16(dX)) || (dA && !aligned16(dA)) ||
-        (dB && !aligned16(dB)) || (H_saved && !aligned16(H_saved)) || (ws && !aligned16(ws)))
-        return LORA_ERR_ALIGNMENT;
-    const size_t need = workspace_bytes(table, segs->n_tokens);
-    if (need > 0 && (ws == nullptr || ws_bytes < need)) return LORA_ERR_WORKSPACE_TOO_SMALL;
-    LORA_TRY(check_device());
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return run_bwd(dX, dA, dB, dY, X, H_saved, ws, *table, *segs, st);
+    return packed_bwd(dX, dA, dB, dY, X, H_saved, table, segs, ws, ws_bytes, stream, nullptr);
+}
+
+lora_status_t lora_packed_fwd_marked(void *y, float *H_save, const void *x, const lora_adapter_table *table,
+                                     const lora_segments *segs, void *ws, size_t ws_bytes, lora_stream_t stream,
+                                     void *const *events, int32_t n_events, int32_t *n_recorded)
+{
+    if (n_events < 0 || (n_events > 0 && events == nullptr)) return LORA_ERR_INVALID_ARG;
+    Marks m{events, n_events, 0};
+    const lora_status_t st = packed_fwd(y, H_save, x, table, segs, ws, ws_bytes, stream, &m);
+    if (n_recorded != nullptr) *n_recorded = m.k;
+    return st;
+}
+
+lora_status_t lora_packed_bwd_marked(void *dX, float *dA, float *dB, const void *dY, const void *X,
+                                     const float *H_saved, const lora_adapter_table *table,
+                                     const lora_segments *segs, void *ws, size_t ws_bytes, lora_stream_t stream,
+                                     void *const *events, int32_t n_events, int32_t *n_recorded)
+{
+    if (n_events < 0 || (n_events > 0 && events == nullptr)) return LORA_ERR_INVALID_ARG;
+    Marks m{events, n_events, 0};
+    const lora_status_t st = packed_bwd(dX, dA, dB, dY, X, H_saved, table, segs, ws, ws_bytes, stream, &m);
+    if (n_recorded != nullptr) *n_recorded = m.k;
+    return st;
 }
 
 lora_status_t lora_query_status(const lora_segments *segs, lora_stream_t stream)

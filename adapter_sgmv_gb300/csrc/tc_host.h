@@ -40,7 +40,8 @@ lora_status_t tc_expand_f32(void *y, const float *H, const lora_adapter_table &t
 lora_status_t tc_dx(void *dX, const uint16_t *dh_bf16, int32_t rw, const lora_adapter_table &tab,
                     const lora_segments &segs, cudaStream_t stream);
 
-// cases iii / iv, output [sum_r, d] overwritten: dB[row_off + k, o] and dA[row_off + k, j].
+// cases iii / iv, output [sum_r, d] accumulated into (the caller zeroes it):
+// dB[row_off + k, o] and dA[row_off + k, j].
 lora_status_t tc_db(float *dB, const void *dY, const uint16_t *h_bf16, int32_t rw, const lora_adapter_table &tab,
                     const lora_segments &segs, cudaStream_t stream);
 lora_status_t tc_da(float *dA, const void *X, const uint16_t *dh_bf16, int32_t rw, const lora_adapter_table &tab,

@@ -310,8 +310,6 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
 lora_status_t launch_tokred(float *G, const void *act, int32_t d, const uint16_t *hbuf, int32_t rw, float use_scale,
                             const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream)
 {
-    const size_t gbytes = (size_t)tab.sum_r * (size_t)d * sizeof(float);
-    if (cudaMemsetAsync(G, 0, gbytes, stream) != cudaSuccess) return LORA_ERR_CUDA;
     if (segs.n_tokens == 0 || segs.max_spans == 0) return LORA_OK;
     CUtensorMap map_act, map_h, map_g;
     if (!make_tmap_bf16_2d(&map_act, act, (uint64_t)d, (uint64_t)segs.n_tokens, 64, kTok, true) ||

@@ -51,6 +51,25 @@ def step_bytes(spec: wl.Spec) -> dict:
     return {"fwd": fwd, "bwd": bwd}
 
 
+# kernels of a step in launch order (forward, then backward with H saved), and
+# the kernel template each one runs
+STEP_KERNELS = (("shrink", "tc_rowproj"), ("expand", "tc_colproj"), ("dh", "tc_rowproj"), ("dB", "tc_tokred"),
+                ("dA", "tc_tokred"), ("dX", "tc_colproj"))
+
+
+def kernel_bytes(spec: wl.Spec) -> dict:
+    """Algorithmic HBM bytes of each kernel launch of a step: its activations
+    read once, y / dX read and written, its adapter weights read once, H / dH
+    (r_i columns) written or read once, dA / dB written once."""
+    T, di, do = spec.n_tokens, spec.d_in, spec.d_out
+    counts = np.bincount(spec.ids, minlength=spec.n_adapters)
+    th = int((counts * spec.ranks).sum())           # sum_i T_i r_i
+    r = int(spec.sum_r)
+    return {"shrink": 2 * T * di + 2 * r * di + 4 * th, "expand": 4 * T * do + 2 * r * do + 4 * th,
+            "dh": 2 * T * do + 2 * r * do + 4 * th, "dB": 2 * T * do + 4 * th + 4 * r * do,
+            "dA": 2 * T * di + 4 * th + 4 * r * di, "dX": 4 * T * di + 2 * r * di + 4 * th}
+
+
 def step_flops(spec: wl.Spec) -> int:
     counts = np.bincount(spec.ids, minlength=spec.n_adapters)
     th = int((counts * spec.ranks).sum())
@@ -74,16 +93,17 @@ def measured_peaks():
         return 6800.0, 1900.0, "fallback"
 
 
-def traffic_record(kernel: str):
-    """DRAM bytes per launch from a committed ncu summary, when it still
-    matches the kernel's source (else None)."""
+def traffic_record(kernel: str, n_tokens: int):
+    """DRAM bytes per launch from a committed ncu summary of the same kernel on
+    the same workload size, when it still matches the kernel's source (else
+    None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f).get(kernel)
     except Exception:
         return None
-    if not rec:
+    if not rec or rec.get("tokens") != n_tokens:
         return None
     import hashlib
 
@@ -179,18 +199,28 @@ class Workload:
                                              n_adapters=self.spec.n_adapters, storage=self.seg_storage,
                                              stream=stream)
 
-    def fwd(self, stream=None, x=None):
+    def fwd(self, stream=None, x=None, events=None):
+        """Packed forward; with ``events`` the marked call records them around
+        its kernels (events[2k], events[2k + 1] bracket kernel k)."""
         import adapter_sgmv_gb300 as lora
 
-        lora.lora_packed_fwd(self.y, self.H, self.inp["x"] if x is None else x, self.table, self.segs, self.ws,
-                             stream=stream)
+        x = self.inp["x"] if x is None else x
+        if events is None:
+            lora.lora_packed_fwd(self.y, self.H, x, self.table, self.segs, self.ws, stream=stream)
+        else:
+            lora.lora_packed_fwd_marked(self.y, self.H, x, self.table, self.segs, self.ws, events, stream=stream)
 
-    def bwd(self, stream=None, x=None, dY=None):
+    def bwd(self, stream=None, x=None, dY=None, events=None):
         import adapter_sgmv_gb300 as lora
 
-        lora.lora_packed_bwd(self.dX, self.dA, self.dB, self.inp["dY"] if dY is None else dY,
-                             self.inp["x"] if x is None else x, self.H, self.table, self.segs, self.ws,
-                             stream=stream)
+        x = self.inp["x"] if x is None else x
+        dY = self.inp["dY"] if dY is None else dY
+        if events is None:
+            lora.lora_packed_bwd(self.dX, self.dA, self.dB, dY, x, self.H, self.table, self.segs, self.ws,
+                                 stream=stream)
+        else:
+            lora.lora_packed_bwd_marked(self.dX, self.dA, self.dB, dY, x, self.H, self.table, self.segs, self.ws,
+                                        events, stream=stream)
 
 
 def kernels_per_step(spec: wl.Spec) -> int:
@@ -199,7 +229,11 @@ def kernels_per_step(spec: wl.Spec) -> int:
     return build + 2 + 4
 
 
-def time_steps(work: Workload, steps: int, warmup: int, stream):
+def time_steps(work: Workload, steps: int, warmup: int, stream, per_kernel: bool = False):
+    """Warm-up, then `steps` timed steps between two events on `stream`.
+    Returns (start, end, call events per step, kernel event pairs per step);
+    with per_kernel the library records an event pair around every kernel
+    of the packed calls (same kernels, same stream)."""
     import torch
 
     for _ in range(warmup):
@@ -208,6 +242,12 @@ def time_steps(work: Workload, steps: int, warmup: int, stream):
         work.bwd(stream)
     torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(STEP_KERNELS))] for _ in range(steps)]
+    if per_kernel:  # create the events outside the timed region
+        for row in kev:
+            for e in row:
+                e.record(stream)
+        torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
@@ -215,12 +255,12 @@ def time_steps(work: Workload, steps: int, warmup: int, stream):
         ev[k][0].record(stream)
         work.build(stream)
         ev[k][1].record(stream)
-        work.fwd(stream)
+        work.fwd(stream, events=kev[k][:4] if per_kernel else None)
         ev[k][2].record(stream)
-        work.bwd(stream)
+        work.bwd(stream, events=kev[k][4:] if per_kernel else None)
         ev[k][3].record(stream)
     end.record(stream)
-    return start, end, ev
+    return start, end, ev, (kev if per_kernel else None)
 
 
 def time_config(spec: wl.Spec, dev, stream, steps: int = 10, warmup: int = 3) -> dict:
@@ -228,7 +268,7 @@ def time_config(spec: wl.Spec, dev, stream, steps: int = 10, warmup: int = 3) ->
     import torch
 
     work = Workload(spec, dev)
-    start, end, _ = time_steps(work, steps, warmup, stream)
+    start, end, _, _ = time_steps(work, steps, warmup, stream)
     torch.cuda.synchronize()
     ms = start.elapsed_time(end) / steps
     by = step_bytes(spec)
@@ -386,7 +426,7 @@ def run_ours(args, rank, world, dev):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
-        start, end, ev = time_steps(work, args.steps, args.warmup, stream)
+        start, end, ev, kev = time_steps(work, args.steps, args.warmup, stream, per_kernel=True)
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -408,10 +448,23 @@ def run_ours(args, rank, world, dev):
 
     hbm, tflops, peak_src = measured_peaks()
     by = step_bytes(spec)
-    calls = {"lora_packed_fwd": (statistics.mean(t_fwd), by["fwd"]),
-             "lora_packed_bwd": (statistics.mean(t_bwd), by["bwd"])}
-    dom = max(calls, key=lambda k: calls[k][0])
-    dom_ms, dom_bytes = calls[dom]
+    # each kernel's mean duration over the timed steps, from the event pairs the
+    # library recorded around it on the launching stream
+    kb = kernel_bytes(spec)
+    per_kernel = {}
+    for j, (use, tmpl) in enumerate(STEP_KERNELS):
+        ms = statistics.mean(row[2 * j].elapsed_time(row[2 * j + 1]) for row in kev)
+        per_kernel[use] = {"kernel": tmpl, "ms": round(ms, 4), "bytes": kb[use],
+                           "GB/s": round(kb[use] / (ms * 1e-3) / 1e9, 1)}
+    templates = {}
+    for use, tmpl in STEP_KERNELS:
+        t = templates.setdefault(tmpl, {"ms": 0.0, "bytes": 0, "launches": 0})
+        t["ms"] += per_kernel[use]["ms"]
+        t["bytes"] += kb[use]
+        t["launches"] += 1
+    dom = max(templates, key=lambda k: templates[k]["ms"])  # the most time per step
+    dom_ms = templates[dom]["ms"] / templates[dom]["launches"]
+    dom_bytes = templates[dom]["bytes"] / templates[dom]["launches"]
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
 
     e2e_ms, h2d, d2h = time_e2e(work, max(3, args.steps // 2), 2, stream) if not args.no_e2e else (None, 0, 0)
@@ -442,8 +495,11 @@ def run_ours(args, rank, world, dev):
         "step_GB/s": round((by["fwd"] + by["bwd"]) / (ms_step * 1e-3) / 1e9, 1),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm,
                      "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_source": peak_src,
-                     "traffic": traffic_record(dom),
+                     "traffic": traffic_record(dom, spec.n_tokens),
+                     "bytes_per_launch": int(dom_bytes), "ms_per_launch": round(dom_ms, 4),
+                     "launches_per_step": templates[dom]["launches"],
                      "tensor_frac_at_this_time": round(step_flops(spec) / (ms_step * 1e-3) / 1e12 / tflops, 4)},
+        "kernels_ms": per_kernel,
         "e2e": ({"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                  "d2h_bytes_per_step": d2h} if e2e_ms is not None else None),
         "gpu_launches": kernels_per_step(spec) * args.steps,

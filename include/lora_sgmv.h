@@ -196,9 +196,9 @@ LORA_API lora_status_t lora_sgmv_expand(void *y, const float *H, const lora_adap
  *   H_save  device fp32 [T, r_max] (out) to keep H for the backward, or NULL
  *   x       device bf16 [T, d_in]
  *   ws      device workspace of >= lora_workspace_bytes(table, T) bytes (may be
- *           NULL when that is 0); it carries H from the shrink to the expand as
- *           bf16 (a hi + lo pair, ~16 significant bits); contents need not be
- *           preserved after the call
+ *           NULL when that is 0); it carries H from the shrink to the expand:
+ *           as bf16 hi + lo (~16 significant bits), or in fp32 for batches of at
+ *           most 512 tokens; contents need not be preserved after the call
  */
 LORA_API lora_status_t lora_packed_fwd(void *y, float *H_save, const void *x,
                               const lora_adapter_table *table, const lora_segments *segs,
@@ -222,6 +222,33 @@ LORA_API lora_status_t lora_packed_bwd(void *dX, float *dA, float *dB, const voi
                               const float *H_saved, const lora_adapter_table *table,
                               const lora_segments *segs, void *ws, size_t ws_bytes,
                               lora_stream_t stream);
+
+/*
+ * Measurement variants of lora_packed_fwd / lora_packed_bwd: the same checks,
+ * kernels and results, and in addition CUDA events are recorded on `stream`
+ * around each kernel launch: events[2k] before and events[2k + 1] after the
+ * k-th kernel, while 2k + 1 < n_events.  The pages have no counterpart; these
+ * exist so a caller can time each kernel of the path on its own stream.
+ *   events      n_events cudaEvent_t handles (as void *) created by the
+ *               caller, or NULL when n_events is 0; they are only recorded
+ *   n_recorded  out, may be NULL: events recorded (2 x kernels launched)
+ * Kernel order.  Forward: case i (shrink), case ii (expand); a batch of at
+ * most 512 tokens gets one pair around its two decode launches.  Backward:
+ * [case i shrink, when H_saved is NULL], case i (dh), case iii (dB, if
+ * requested), case iv (dA, if requested), case ii (dX, if requested).  The
+ * zeroing of dA / dB precedes the first pair.
+ * Errors: those of the unmarked call; LORA_ERR_INVALID_ARG when n_events < 0
+ * or events is NULL with n_events > 0.
+ */
+LORA_API lora_status_t lora_packed_fwd_marked(void *y, float *H_save, const void *x,
+                                              const lora_adapter_table *table, const lora_segments *segs,
+                                              void *ws, size_t ws_bytes, lora_stream_t stream,
+                                              void *const *events, int32_t n_events, int32_t *n_recorded);
+LORA_API lora_status_t lora_packed_bwd_marked(void *dX, float *dA, float *dB, const void *dY, const void *X,
+                                              const float *H_saved, const lora_adapter_table *table,
+                                              const lora_segments *segs, void *ws, size_t ws_bytes,
+                                              lora_stream_t stream, void *const *events, int32_t n_events,
+                                              int32_t *n_recorded);
 
 /*
  * Packed backward without a workspace, for callers that cannot allocate device
