@@ -122,7 +122,7 @@ struct ColIn {
 
 template <bool kLoader, int kEpi>
 __global__ void __launch_bounds__(threads_of<kLoader, kEpi>(), 1)
-tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_hi,
+tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ CUtensorMap map_hi,
                   const __grid_constant__ CUtensorMap map_lo, const __grid_constant__ CUtensorMap map_y,
                   uint16_t *__restrict__ out, int32_t d, ColIn in, lora_adapter_table tab, lora_segments segs)
 {
@@ -179,7 +179,9 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            prefetch_tensormap(&map_w);
+            prefetch_tensormap(&map_w.m16);
+            prefetch_tensormap(&map_w.m32);
+            prefetch_tensormap(&map_w.m64);
             prefetch_tensormap(&map_y);
             if (!kLoader) {
                 prefetch_tensormap(&map_hi);
@@ -236,9 +238,7 @@ tc_colproj_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                         uint8_t *w_s = S.w + s * kWBytes;
                         mbar_arrive_expect_tx(&S.wfull[s], (uint32_t)rp * 256u);
                         for (int a = 0; a < 2; ++a)
-                            for (int q = 0; q < rp / 16; ++q)
-                                tma_load_2d(w_s + a * rp * 128 + q * 2048, &map_w, &S.wfull[s], n0 + 64 * a,
-                                            I.ad.row_off + 16 * q);
+                            tma_load_rows(w_s + a * rp * 128, map_w, &S.wfull[s], n0 + 64 * a, I.ad.row_off, rp);
                     }
                     ++gw;
                 }
@@ -512,8 +512,9 @@ lora_status_t launch_colproj(uint16_t *out, int32_t d, const void *w, const uint
                              cudaStream_t stream)
 {
     if (segs.n_tokens == 0 || segs.max_tiles == 0) return LORA_OK;
-    CUtensorMap map_w, map_hi, map_lo, map_y;
-    if (!make_tmap_bf16_2d(&map_w, w, (uint64_t)d, (uint64_t)tab.sum_r, 64, 16, true) ||
+    WMaps map_w;
+    CUtensorMap map_hi, map_lo, map_y;
+    if (!make_wmaps(&map_w, w, (uint64_t)d, (uint64_t)tab.sum_r) ||
         !make_tmap_bf16_2d(&map_y, out, (uint64_t)d, (uint64_t)segs.n_tokens, 64, 128, true))
         return LORA_ERR_CUDA;
     if (!kLoader) {

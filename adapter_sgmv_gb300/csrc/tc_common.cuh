@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "tc_host.h"
 
 namespace lora {
 namespace tc {
@@ -109,6 +110,18 @@ LORA_DEV void tma_load_2d(void *smem_dst, const CUtensorMap *map, uint64_t *bar,
 LORA_DEV void prefetch_tensormap(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// rows row0 .. row0 + rp - 1 (rp a multiple of 16), columns col .. col + 63,
+// to dst as consecutive 1 KB atoms of eight 128-byte rows
+LORA_DEV void tma_load_rows(uint8_t *dst, const WMaps &wm, uint64_t *bar, int32_t col, int32_t row0, int32_t rp)
+{
+    for (int32_t k0 = 0; k0 < rp;) {
+        const int32_t rem = rp - k0;
+        const CUtensorMap *m = rem >= 64 ? &wm.m64 : rem >= 32 ? &wm.m32 : &wm.m16;
+        tma_load_2d(dst + k0 * 128, m, bar, col, row0 + k0);
+        k0 += rem >= 64 ? 64 : rem >= 32 ? 32 : 16;
+    }
 }
 
 // ---------------------------------------------------------------- cp.async (16 B, zero-fill when !pred)

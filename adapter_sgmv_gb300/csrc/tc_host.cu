@@ -58,6 +58,13 @@ bool make_tmap_f32_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_
     return r == CUDA_SUCCESS;
 }
 
+bool make_wmaps(WMaps *maps, const void *base, uint64_t cols, uint64_t rows)
+{
+    return make_tmap_bf16_2d(&maps->m16, base, cols, rows, 64, 16, true) &&
+           make_tmap_bf16_2d(&maps->m32, base, cols, rows, 64, 32, true) &&
+           make_tmap_bf16_2d(&maps->m64, base, cols, rows, 64, 64, true);
+}
+
 int sm_count()
 {
     int dev = 0, n = 0;

@@ -13,6 +13,15 @@ namespace lora {
 bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
                        uint32_t box_rows, bool swizzle128);
 // Row-major fp32 matrix [rows, cols] as a 2-D TMA tensor (no swizzle), box [box_rows, box_cols].
+// Three tensor maps over one weight matrix ([sum_r, d] bf16, 128-byte swizzle,
+// 64 columns wide) with boxes of 16, 32 and 64 rows: rp rows are fetched with
+// as few boxes as possible (64-row boxes first), so that one stage of a rank
+// 128 adapter takes two TMA copies instead of eight.
+struct WMaps {
+    CUtensorMap m16, m32, m64;
+};
+bool make_wmaps(WMaps *maps, const void *base, uint64_t cols, uint64_t rows);
+
 bool make_tmap_f32_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
                       uint32_t box_rows);
 int sm_count();

@@ -77,7 +77,7 @@ struct RowOut {
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
-tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_w,
+tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_constant__ WMaps map_w,
                   const uint16_t *__restrict__ act, int32_t d, RowOut o, lora_adapter_table tab,
                   lora_segments segs)
 {
@@ -113,7 +113,9 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             prefetch_tensormap(&map_act);
-            prefetch_tensormap(&map_w);
+            prefetch_tensormap(&map_w.m16);
+            prefetch_tensormap(&map_w.m32);
+            prefetch_tensormap(&map_w.m64);
         }
         uint32_t g = 0;
         bool ok = true;
@@ -145,8 +147,7 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&S.full[s], (contiguous ? kActBytes : 0u) + (uint32_t)rp * 128u);
                     if (contiguous) tma_load_2d(act_s, &map_act, &S.full[s], j0, t0);
-                    for (int q = 0; q < rp / 16; ++q)
-                        tma_load_2d(w_s + q * 2048, &map_w, &S.full[s], j0, ad.row_off + 16 * q);
+                    tma_load_rows(w_s, map_w, &S.full[s], j0, ad.row_off, rp);
                 }
                 if (!contiguous) {
                     const int c = lane & 7;
@@ -308,9 +309,10 @@ lora_status_t launch_rowproj(const void *act, const void *w, int32_t d, const Ro
                              const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream)
 {
     if (segs.n_tokens == 0 || segs.max_tiles == 0) return LORA_OK;
-    CUtensorMap map_act, map_w;
+    CUtensorMap map_act;
+    WMaps map_w;
     if (!make_tmap_bf16_2d(&map_act, act, (uint64_t)d, (uint64_t)segs.n_tokens, 64, 128, true) ||
-        !make_tmap_bf16_2d(&map_w, w, (uint64_t)d, (uint64_t)tab.sum_r, 64, 16, true))
+        !make_wmaps(&map_w, w, (uint64_t)d, (uint64_t)tab.sum_r))
         return LORA_ERR_CUDA;
     if (cudaFuncSetAttribute(tc_rowproj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
         cudaSuccess)
