@@ -58,6 +58,21 @@ bool make_tmap_f32_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_
     return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_bf16_blocks(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint32_t box_rows,
+                           uint32_t box_blocks)
+{
+    auto fn = encode_fn();
+    if (fn == nullptr || rows == 0 || cols == 0 || cols % 64 != 0) return false;
+    cuuint64_t dims[3] = {64, rows, cols / 64};
+    cuuint64_t strides[2] = {cols * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, box_blocks};
+    cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estride,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool make_wmaps(WMaps *maps, const void *base, uint64_t cols, uint64_t rows)
 {
     return make_tmap_bf16_2d(&maps->m16, base, cols, rows, 64, 16, true) &&

@@ -22,6 +22,13 @@ struct WMaps {
 };
 bool make_wmaps(WMaps *maps, const void *base, uint64_t cols, uint64_t rows);
 
+// A bf16 [rows, cols] row-major matrix (cols a multiple of 64) seen as 3-D
+// (64 columns, rows, cols / 64 column blocks), 128-byte swizzle: one box of
+// {64, box_rows, box_blocks} lands as box_blocks consecutive [box_rows x 128 B]
+// swizzled blocks, i.e. as box_blocks separate 2-D boxes would.
+bool make_tmap_bf16_blocks(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint32_t box_rows,
+                           uint32_t box_blocks);
+
 bool make_tmap_f32_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
                       uint32_t box_rows);
 int sm_count();

@@ -97,10 +97,11 @@ LORA_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;
 LORA_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kThreads, 1)
-tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_h,
+tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_act3,
+                 const __grid_constant__ CUtensorMap map_h,
                  const __grid_constant__ CUtensorMap map_g, const uint16_t *__restrict__ act, int32_t d,
-                 const uint16_t *__restrict__ hbuf, int32_t rw, float use_scale, lora_adapter_table tab,
-                 lora_segments segs)
+                 const uint16_t *__restrict__ hbuf, int32_t rw, float use_scale, int32_t blocks3,
+                 lora_adapter_table tab, lora_segments segs)
 {
     extern __shared__ uint8_t smem_raw[];
     const Smem S = carve(smem_raw);
@@ -131,7 +132,7 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            prefetch_tensormap(&map_act);
+            prefetch_tensormap(blocks3 ? &map_act3 : &map_act);
             prefetch_tensormap(&map_h);
         }
         uint32_t g = 0;
@@ -156,12 +157,19 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
                 const int valid = min(kTok, I.span.rows - kTok * st);  // rows of this stage in the span
                 const bool h_tma = valid == kTok;
                 if (lane == 0) {
-                    const uint32_t bytes = (contiguous ? (uint32_t)I.n_chunks * 2u * kBox : 0u) +
+                    // a 3-D box always moves all eight blocks (past d: zero-filled)
+                    const uint32_t act_bytes = blocks3 ? kActBytes : (uint32_t)I.n_chunks * 2u * kBox;
+                    const uint32_t bytes = (contiguous ? act_bytes : 0u) +
                                            (h_tma ? (uint32_t)natoms * kBox : 0u);
                     mbar_arrive_expect_tx(&S.full[s], bytes);
-                    if (contiguous)
-                        for (int b = 0; b < 2 * I.n_chunks; ++b)
-                            tma_load_2d(act_s + b * kBox, &map_act, &S.full[s], I.n_base + 64 * b, t0 + kTok * st);
+                    if (contiguous) {
+                        if (blocks3)  // all 2 n_chunks 64-column blocks of the stage in one copy
+                            tma_load_3d(act_s, &map_act3, &S.full[s], 0, t0 + kTok * st, I.n_base / 64);
+                        else
+                            for (int b = 0; b < 2 * I.n_chunks; ++b)
+                                tma_load_2d(act_s + b * kBox, &map_act, &S.full[s], I.n_base + 64 * b,
+                                            t0 + kTok * st);
+                    }
                     if (h_tma)
                         for (int a = 0; a < natoms; ++a)
                             tma_load_2d(h_s + a * kBox, &map_h, &S.full[s], 64 * a, p0 + kTok * st);
@@ -311,7 +319,12 @@ lora_status_t launch_tokred(float *G, const void *act, int32_t d, const uint16_t
                             const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream)
 {
     if (segs.n_tokens == 0 || segs.max_spans == 0) return LORA_OK;
-    CUtensorMap map_act, map_h, map_g;
+    CUtensorMap map_act, map_act3, map_h, map_g;
+    // d a multiple of 64: a stage's eight column blocks come in one 3-D copy
+    const int32_t blocks3 = (d % 64 == 0 && make_tmap_bf16_blocks(&map_act3, act, (uint64_t)d,
+                                                                   (uint64_t)segs.n_tokens, kTok, 8))
+                                ? 1
+                                : 0;
     if (!make_tmap_bf16_2d(&map_act, act, (uint64_t)d, (uint64_t)segs.n_tokens, 64, kTok, true) ||
         !make_tmap_bf16_2d(&map_h, hbuf, (uint64_t)rw, (uint64_t)segs.n_tokens, 64, kTok, true) ||
         !make_tmap_f32_2d(&map_g, G, (uint64_t)d, (uint64_t)tab.sum_r, 32, 16))
@@ -323,8 +336,10 @@ lora_status_t launch_tokred(float *G, const void *act, int32_t d, const uint16_t
     const int64_t items = (int64_t)segs.max_spans * n_ranges;
     const int sms = sm_count();
     const int grid = items < sms ? (int)items : sms;
-    tc_tokred_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_act, map_h, map_g, static_cast<const uint16_t *>(act),
-                                                             d, hbuf, rw, use_scale, tab, segs);
+    if (!blocks3) map_act3 = map_act;
+    tc_tokred_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_act, map_act3, map_h, map_g,
+                                                             static_cast<const uint16_t *>(act), d, hbuf, rw,
+                                                             use_scale, blocks3, tab, segs);
     return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
