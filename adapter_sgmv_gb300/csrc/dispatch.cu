@@ -5,6 +5,8 @@
 //   backward: case i (dh) writes bf16 dH in perm order and converts the saved
 //             H to bf16 in perm order (or case i recomputes it from X);
 //             case iii (dB), case iv (dA) and case ii (dX) read those.
+#include <mutex>
+
 #include "dispatch.h"
 #include "tc_host.h"
 
@@ -43,6 +45,41 @@ namespace {
 void mark(Marks *m, cudaStream_t stream)
 {
     if (m != nullptr && m->k < m->n) cudaEventRecord(static_cast<cudaEvent_t>(m->ev[m->k++]), stream);
+}
+
+// Two streams and three events per device on which the backward runs its
+// three independent products (dB, dA, dX) side by side, so that the tail of
+// one kernel's last wave overlaps the others.  Created on first use and kept;
+// the mutex also serialises the enqueue of each fork / join, so that calls
+// from several host threads never wait on each other's events.
+constexpr int kMaxDevices = 64;
+struct Side {
+    cudaStream_t s[2];
+    cudaEvent_t ev[3];
+    bool ready;
+};
+Side g_side[kMaxDevices];
+std::mutex g_side_mu;
+
+Side *side_for_device()  // called with g_side_mu held; nullptr: run serially
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    Side &S = g_side[dev];
+    if (!S.ready) {
+        for (auto &st : S.s)
+            if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) {
+                cudaGetLastError();
+                return nullptr;
+            }
+        for (auto &e : S.ev)
+            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+                cudaGetLastError();
+                return nullptr;
+            }
+        S.ready = true;
+    }
+    return &S;
 }
 
 // launch `f` between a pair of marks
@@ -89,12 +126,28 @@ lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void
     } else {
         st = marked(marks, stream, [&] { return tc_dh(dY, tab, segs, dhb, H_saved, hb, rw, stream); });
     }
-    if (st == LORA_OK && dB != nullptr)
-        st = marked(marks, stream, [&] { return tc_db(dB, dY, hb, rw, tab, segs, stream); });
-    if (st == LORA_OK && dA != nullptr)
-        st = marked(marks, stream, [&] { return tc_da(dA, X, dhb, rw, tab, segs, stream); });
+    if (st != LORA_OK) return st;
+    // dB, dA and dX read only what the steps above wrote: fork them
+    std::lock_guard<std::mutex> lock(g_side_mu);
+    Side *sd = (dB != nullptr || dA != nullptr) ? side_for_device() : nullptr;
+    cudaStream_t sB = sd != nullptr ? sd->s[0] : stream, sA = sd != nullptr ? sd->s[1] : stream;
+    if (sd != nullptr) {
+        if (cudaEventRecord(sd->ev[0], stream) != cudaSuccess) return LORA_ERR_CUDA;
+        if ((dB != nullptr && cudaStreamWaitEvent(sB, sd->ev[0], 0) != cudaSuccess) ||
+            (dA != nullptr && cudaStreamWaitEvent(sA, sd->ev[0], 0) != cudaSuccess))
+            return LORA_ERR_CUDA;
+    }
+    if (dB != nullptr) st = marked(marks, sB, [&] { return tc_db(dB, dY, hb, rw, tab, segs, sB); });
+    if (st == LORA_OK && dA != nullptr) st = marked(marks, sA, [&] { return tc_da(dA, X, dhb, rw, tab, segs, sA); });
     if (st == LORA_OK && dX != nullptr)
         st = marked(marks, stream, [&] { return tc_dx(dX, dhb, rw, tab, segs, stream); });
+    if (sd != nullptr) {  // join: the caller's stream waits for both side streams
+        if ((dB != nullptr && (cudaEventRecord(sd->ev[1], sB) != cudaSuccess ||
+                               cudaStreamWaitEvent(stream, sd->ev[1], 0) != cudaSuccess)) ||
+            (dA != nullptr && (cudaEventRecord(sd->ev[2], sA) != cudaSuccess ||
+                               cudaStreamWaitEvent(stream, sd->ev[2], 0) != cudaSuccess)))
+            return LORA_ERR_CUDA;
+    }
     return st;
 }
 
