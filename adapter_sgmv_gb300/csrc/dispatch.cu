@@ -129,7 +129,9 @@ lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void
     if (st != LORA_OK) return st;
     // dB, dA and dX read only what the steps above wrote: fork them
     std::lock_guard<std::mutex> lock(g_side_mu);
-    Side *sd = (dB != nullptr || dA != nullptr) ? side_for_device() : nullptr;
+    // (a marked call runs them one after another on the caller's stream, so that
+    // each event pair brackets one kernel alone)
+    Side *sd = (marks == nullptr && (dB != nullptr || dA != nullptr)) ? side_for_device() : nullptr;
     cudaStream_t sB = sd != nullptr ? sd->s[0] : stream, sA = sd != nullptr ? sd->s[1] : stream;
     if (sd != nullptr) {
         if (cudaEventRecord(sd->ev[0], stream) != cudaSuccess) return LORA_ERR_CUDA;

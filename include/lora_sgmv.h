@@ -236,7 +236,10 @@ LORA_API lora_status_t lora_packed_bwd(void *dX, float *dA, float *dB, const voi
  * most 512 tokens gets one pair around its two decode launches.  Backward:
  * [case i shrink, when H_saved is NULL], case i (dh), case iii (dB, if
  * requested), case iv (dA, if requested), case ii (dX, if requested).  The
- * zeroing of dA / dB precedes the first pair.
+ * zeroing of dA / dB precedes the first pair.  The plain backward runs dB and
+ * dA on two internal streams next to dX; the marked one runs all of its
+ * kernels one after another on `stream`, so that each pair brackets one
+ * kernel alone.
  * Errors: those of the unmarked call; LORA_ERR_INVALID_ARG when n_events < 0
  * or events is NULL with n_events > 0.
  */
