@@ -83,6 +83,9 @@ def decode_bytes(spec: wl.Spec) -> int:
     return 2 * spec.n_tokens * spec.d_in + 4 * spec.n_tokens * spec.d_out + 2 * r * (spec.d_in + spec.d_out)
 
 
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e datasheet figure, for context beside the measured copy bandwidth
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -119,7 +122,7 @@ def traffic_record(kernel: str, n_tokens: int):
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,clocks.mem")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -148,7 +151,7 @@ class ClockSampler:
             self.lines = [ln for ln in out.splitlines() if ln.strip()]
 
     def summary(self):
-        sm, smax, reasons = [], [], set()
+        sm, smax, mem, reasons = [], [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for ln in self.lines:
             f = [v.strip() for v in ln.split(",")]
@@ -157,6 +160,8 @@ class ClockSampler:
             try:
                 sm.append(float(f[1]))
                 smax.append(float(f[2]))
+                if len(f) > 9:
+                    mem.append(float(f[9]))
             except ValueError:
                 continue
             for n, v in zip(names, f[5:9]):
@@ -165,7 +170,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "mem_mhz": statistics.median(mem) if mem else None, "samples": len(sm)}
 
 
 # ---------------------------------------------------------------------------- our arm
@@ -263,8 +268,10 @@ def time_steps(work: Workload, steps: int, warmup: int, stream, per_kernel: bool
     return start, end, ev, (kev if per_kernel else None)
 
 
-def time_config(spec: wl.Spec, dev, stream, steps: int = 10, warmup: int = 3) -> dict:
-    """One full step (build + fwd + bwd) of another workload: ms and tokens/s."""
+def time_config(spec: wl.Spec, dev, stream, steps: int = 10, warmup: int = 3, sequential: bool = False) -> dict:
+    """One full step (build + fwd + bwd) of another workload: ms and tokens/s.
+    With `sequential`, the same step is also timed as one single-adapter step
+    per adapter (N builds, N forwards, N backwards) for the packing speed-up."""
     import torch
 
     work = Workload(spec, dev)
@@ -278,6 +285,30 @@ def time_config(spec: wl.Spec, dev, stream, steps: int = 10, warmup: int = 3) ->
            "frac_of_hbm": round((by["fwd"] + by["bwd"]) / (ms * 1e-3) / 1e9 / hbm, 4)}
     del work
     torch.cuda.empty_cache()
+    if sequential:
+        subs = []
+        for i in range(spec.n_adapters):
+            n = int((spec.ids == i).sum())
+            if n:
+                subs.append(Workload(wl.custom(f"{spec.name}_a{i}", spec.d_in, spec.d_out, [spec.ranks[i]],
+                                               [spec.alphas[i]], np.zeros(n, np.int32), seed=i), dev))
+        for _ in range(warmup):
+            for w in subs:
+                w.build(stream), w.fwd(stream), w.bwd(stream)
+        torch.cuda.synchronize()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(steps):
+            for w in subs:
+                w.build(stream), w.fwd(stream), w.bwd(stream)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        seq = s0.elapsed_time(s1) / steps
+        out["sequential_ms_per_step"] = round(seq, 4)
+        out["packing_speedup"] = round(seq / ms, 3)
+        del subs
+        torch.cuda.empty_cache()
     return out
 
 
@@ -399,9 +430,22 @@ def time_decode(dev, stream, reps: int = 50):
                 e.synchronize()
                 times.append(s.elapsed_time(e) / reps)
         ms = statistics.median(times)
+        # single call, not graphed: launch latency included, one call at a time
+        eager = []
+        with torch.cuda.stream(stream):
+            for k in range(20):
+                tab, x, y, ws = sets[k % n_sets]
+                s = torch.cuda.Event(enable_timing=True)
+                e = torch.cuda.Event(enable_timing=True)
+                s.record(stream)
+                lora.lora_packed_fwd(y, None, x, tab, segs, ws, stream=stream)
+                e.record(stream)
+                e.synchronize()
+                eager.append(s.elapsed_time(e))
         gbs = nbytes / (ms * 1e-3) / 1e9
         out[f"{spec.d_in}x{spec.d_out}"] = {"us_per_call": round(ms * 1e3, 3), "bytes": nbytes,
-                                            "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4)}
+                                            "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4),
+                                            "us_per_call_eager": round(statistics.median(eager) * 1e3, 3)}
         del sets, g
         torch.cuda.empty_cache()
     return out
@@ -438,8 +482,16 @@ def cpu_baseline(spec: wl.Spec, target_s: float = 10.0):
             break
         per = int(max(per + 1, min(4096, per * target_s / max(dt, 1e-3))))
         n, dt = run(per)
+    # one host thread on a smaller sample, beside the all-core figure
+    oracle.set_threads(1)
+    try:
+        per1 = max(2, per // max(1, cores))
+        n1, dt1 = run(per1)
+    finally:
+        oracle.set_threads(cores)
     return {"value": round(n / dt, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{n} tokens ({per} per adapter) of the same workload, fwd+bwd in fp64, {dt:.1f} s"}
+            "sample": f"{n} tokens ({per} per adapter) of the same workload, fwd+bwd in fp64, {dt:.1f} s",
+            "one_thread": {"value": round(n1 / dt1, 2), "sample": f"{n1} tokens, {dt1:.1f} s"}}
 
 
 def run_ours(args, rank, world, dev):
@@ -514,7 +566,12 @@ def run_ours(args, rank, world, dev):
     if rank == 0 and not args.no_sweep:
         del work
         torch.cuda.empty_cache()
-        others = {f"sweep3584x18944_N{n}": time_config(wl.sweep(n), dev, stream) for n in (2, 4, 8, 16, 32)}
+        others = {f"sweep3584x18944_N{n}": time_config(wl.sweep(n), dev, stream, sequential=True)
+                  for n in (2, 4, 8, 16, 32)}
+        base = others["sweep3584x18944_N2"]["tokens/s"]
+        for n in (2, 4, 8, 16, 32):  # tokens/s(N) / tokens/s(2): flat means linear in N
+            others[f"sweep3584x18944_N{n}"]["efficiency_vs_N2"] = round(
+                others[f"sweep3584x18944_N{n}"]["tokens/s"] / base, 3)
         others["skewed4096x14336_N32"] = time_config(wl.skewed(), dev, stream)
     cpu = cpu_baseline(spec, args.cpu_seconds) if rank == 0 and not args.no_cpu else None
 
@@ -536,6 +593,7 @@ def run_ours(args, rank, world, dev):
         "step_GB/s": round((by["fwd"] + by["bwd"]) / (ms_step * 1e-3) / 1e9, 1),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm,
                      "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_source": peak_src,
+                     "nominal_gbs": NOMINAL_HBM_GBS, "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                      "traffic": traffic_record(dom, spec.n_tokens),
                      "bytes_per_launch": int(dom_bytes), "ms_per_launch": round(dom_ms, 4),
                      "launches_per_step": templates[dom]["launches"],
