@@ -64,7 +64,10 @@ def _load():
         lib.lora_oracle_db.argtypes = common + [_f64p, _i32p, _f64p, _f64p, _f64p]
         lib.lora_oracle_da.argtypes = common + [_i32p, _f64p, _f64p, _f64p]
         lib.lora_oracle_dx.argtypes = common + [_i32p, _f64p, _f64p, _f64p]
-        for name in ("shrink", "expand", "dh", "db", "da", "dx"):
+        lib.lora_oracle_adamw.argtypes = [ctypes.c_int32, ctypes.c_int32, _i32p, _i64p, _f64p, _i32p,
+                                          ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                                          _f64p, _f64p, _f64p, _f64p]
+        for name in ("shrink", "expand", "dh", "db", "da", "dx", "adamw"):
             getattr(lib, f"lora_oracle_{name}").restype = None
         _lib = lib
         return lib
@@ -215,3 +218,21 @@ def bwd(tab: Table, ids, A, B, X, H, dY, dX0, r_max: int | None = None):
     """Packed backward: (dH, dA, dB, dX) from saved H and incoming dY."""
     g = dh(tab, ids, B, dY, r_max if r_max is not None else H.shape[1])
     return g, da(tab, ids, g, X), db(tab, ids, dY, H), dx(tab, ids, A, g, dX0)
+
+
+def adamw(tab: Table, w, g, m, v, lr, step, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8,
+          weight_decay: float = 0.0):
+    """One AdamW step per adapter over a [sum_r, d] weight matrix (rows of
+    adapter i at tab.row_off[i]); returns the new (w, m, v) in fp64."""
+    lib = _load()
+    w = np.array(w, dtype=np.float64, copy=True, order="C")
+    m = np.array(m, dtype=np.float64, copy=True, order="C")
+    v = np.array(v, dtype=np.float64, copy=True, order="C")
+    g = _c(g, np.float64)
+    lr = _c(np.broadcast_to(np.asarray(lr, dtype=np.float64), (tab.n,)), np.float64)
+    step = _c(np.broadcast_to(np.asarray(step, dtype=np.int32), (tab.n,)), np.int32)
+    d = w.shape[1]
+    lib.lora_oracle_adamw(tab.n, d, _p(tab.rank, _i32p), _p(tab.row_off, _i64p),
+                          _p(lr, _f64p), _p(step, _i32p), beta1, beta2, eps, weight_decay, _p(w, _f64p), _p(g, _f64p),
+                          _p(m, _f64p), _p(v, _f64p))
+    return w, m, v

@@ -40,10 +40,20 @@
  * Tokens whose id lies outside [0, N) belong to no adapter: they contribute
  * nothing, their H/dH rows are zero and their y/dX rows are left unchanged.
  *
+ *   Optimizer step.  Every tenant keeps FP32 master weights, optimizer
+ *   moments and gradient buffers beside its LoRA parameters [C-LoRA report,
+ *   vivodigitale.it, "Come funziona l'architettura": the AdapterStore].  The
+ *   pages name no optimizer; the reading taken is AdamW (Adam moments with
+ *   bias correction, weight decay decoupled from the gradient), per adapter
+ *   with its own learning rate and step number:
+ *     w <- w - lr wd w;  m <- b1 m + (1 - b1) g;  v <- b2 v + (1 - b2) g^2
+ *     w <- w - lr (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps)
+ *
  * Each function is the per-token (or per-adapter) definition written out as
  * loops, with no blocking, fusion or reordering; OpenMP only splits the
  * independent outputs across threads, every sum runs in a fixed order.
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -239,6 +249,29 @@ void lora_oracle_dx(int64_t T, int32_t N, int32_t d_in, int32_t r_max,
             for (int32_t k = 0; k < rank[i]; ++k)
                 acc += A[(row_off[i] + k) * (int64_t)d_in + j] * g[k];
             dx[j] += acc;
+        }
+    }
+}
+
+/* AdamW: one step over a weight matrix laid out like A_cat / Bt_cat
+ * ([sum_r, d] rows, adapter i = rows row_off[i] .. row_off[i]+rank[i]-1),
+ * adapter i with learning rate lr[i] and step number t = step[i] >= 1.
+ * w, m, v are updated in place; g is the gradient. */
+void lora_oracle_adamw(int32_t N, int32_t d, const int32_t *rank, const int64_t *row_off,
+                       const double *lr, const int32_t *step, double beta1, double beta2,
+                       double eps, double weight_decay, double *w, const double *g,
+                       double *m, double *v)
+{
+    for (int32_t i = 0; i < N; ++i) {
+        const double bc1 = 1.0 - pow(beta1, (double)step[i]);
+        const double bc2 = 1.0 - pow(beta2, (double)step[i]);
+        const int64_t e0 = row_off[i] * (int64_t)d, e1 = (row_off[i] + rank[i]) * (int64_t)d;
+        #pragma omp parallel for schedule(static)
+        for (int64_t e = e0; e < e1; ++e) {
+            w[e] -= lr[i] * weight_decay * w[e];
+            m[e] = beta1 * m[e] + (1.0 - beta1) * g[e];
+            v[e] = beta2 * v[e] + (1.0 - beta2) * g[e] * g[e];
+            w[e] -= lr[i] * (m[e] / bc1) / (sqrt(v[e] / bc2) + eps);
         }
     }
 }

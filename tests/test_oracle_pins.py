@@ -360,3 +360,54 @@ def test_tokens_without_adapter_and_empty_adapters():
         assert np.all(out["H"][t] == 0.0) and np.all(out["dH"][t] == 0.0)
     assert np.all(out["dA"][4:12] == 0.0)
     assert np.all(out["dB"][4:12] == 0.0)
+
+
+# ---------------------------------------------------------------- optimizer step
+def test_adamw_first_step_closed_form():
+    # t = 1 from zero moments: m_hat = g and v_hat = g^2, so the step is
+    # w (1 - lr wd) - lr g / (|g| + eps)
+    tab = oracle.Table([3, 5], [1.0, 1.0])
+    rng = np.random.default_rng(11)
+    w = rng.standard_normal((8, 16))
+    g = rng.standard_normal((8, 16))
+    lr = np.array([1e-3, 5e-3])
+    w1, m1, v1 = oracle.adamw(tab, w, g, np.zeros_like(w), np.zeros_like(w), lr, 1, beta1=0.9, beta2=0.99,
+                              eps=1e-6, weight_decay=0.1)
+    lr_rows = np.repeat(lr, [3, 5])[:, None]
+    ref = w * (1 - lr_rows * 0.1) - lr_rows * g / (np.abs(g) + 1e-6)
+    assert np.allclose(w1, ref, rtol=1e-13, atol=1e-15)
+    assert np.allclose(m1, 0.1 * g, rtol=1e-14) and np.allclose(v1, 0.01 * g * g, rtol=1e-13)
+
+
+def test_adamw_matches_torch_optimizer_over_several_steps():
+    torch = pytest.importorskip("torch")
+    ranks = [2, 4, 3]
+    tab = oracle.Table(ranks, [1.0] * 3)
+    rng = np.random.default_rng(12)
+    d = 24
+    w = rng.standard_normal((sum(ranks), d))
+    lrs = [1e-2, 3e-3, 7e-4]
+    params = [torch.tensor(w[o:o + r].copy(), dtype=torch.float64, requires_grad=True)
+              for o, r in zip(tab.row_off[:-1], ranks)]
+    opt = torch.optim.AdamW([{"params": [p], "lr": lr} for p, lr in zip(params, lrs)], betas=(0.9, 0.95), eps=1e-7,
+                            weight_decay=0.05)
+    m = np.zeros_like(w)
+    v = np.zeros_like(w)
+    for t in range(1, 5):
+        g = rng.standard_normal(w.shape)
+        for p, o, r in zip(params, tab.row_off[:-1], ranks):
+            p.grad = torch.tensor(g[o:o + r].copy(), dtype=torch.float64)
+        opt.step()
+        w, m, v = oracle.adamw(tab, w, g, m, v, lrs, t, beta1=0.9, beta2=0.95, eps=1e-7, weight_decay=0.05)
+    ref = np.concatenate([p.detach().numpy() for p in params])
+    assert np.allclose(w, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_adamw_zero_learning_rate_keeps_weights_and_moves_moments():
+    tab = oracle.Table([4, 4], [1.0, 1.0])
+    rng = np.random.default_rng(13)
+    w = rng.standard_normal((8, 8))
+    g = rng.standard_normal((8, 8))
+    w1, m1, _ = oracle.adamw(tab, w, g, np.zeros_like(w), np.zeros_like(w), [0.0, 1e-3], [3, 7], weight_decay=0.1)
+    assert np.array_equal(w1[:4], w[:4]) and not np.array_equal(w1[4:], w[4:])
+    assert np.allclose(m1, 0.1 * g, rtol=1e-14)
