@@ -22,7 +22,7 @@ __all__ = [
     "LoraError", "AdapterTable", "Segments", "lib", "lora_abi_version", "lora_status_string",
     "lora_segments_bytes", "lora_build_segments", "lora_workspace_bytes", "lora_sgmv_shrink",
     "lora_sgmv_expand", "lora_packed_fwd", "lora_packed_bwd", "lora_packed_fwd_marked", "lora_packed_bwd_marked",
-    "lora_packed_bwd_noalloc", "lora_query_status", "lora_reset_status",
+    "lora_packed_bwd_noalloc", "lora_adamw_step", "lora_query_status", "lora_reset_status",
     "STATUS",
 ]
 
@@ -78,6 +78,8 @@ SIGNATURES = {
                                       _P, _SZ, _P, ctypes.POINTER(_P), _I32, ctypes.POINTER(_I32)]),
     "lora_packed_bwd_noalloc": (_I32, [_P, _P, _P, _P, _P, _P, ctypes.POINTER(c_table),
                                        ctypes.POINTER(c_segments), _P]),
+    "lora_adamw_step": (_I32, [ctypes.POINTER(c_table), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float,
+                                ctypes.c_float, ctypes.c_float, ctypes.c_float, _P]),
     "lora_query_status": (_I32, [ctypes.POINTER(c_segments), _P]),
     "lora_reset_status": (_I32, [ctypes.POINTER(c_segments), _P]),
 }
@@ -312,6 +314,15 @@ def lora_packed_bwd_noalloc(dX, dA, dB, dY, X, H_saved, table: AdapterTable, seg
     _check(lib().lora_packed_bwd_noalloc(_ptr(dX), _ptr(dA), _ptr(dB), _ptr(dY), _ptr(X), _ptr(H_saved),
                                          ctypes.byref(table.c), ctypes.byref(segs.c), _stream(stream)),
            "lora_packed_bwd_noalloc")
+
+
+def lora_adamw_step(table: AdapterTable, wA, wB, gA, gB, mA, vA, mB, vB, lr, step, beta1=0.9, beta2=0.999,
+                    eps=1e-8, weight_decay=0.0, stream=None):
+    """One AdamW step per adapter (lr: fp32 [N], step: int32 [N] device
+    tensors); also rewrites the table's bf16 A / B from the new masters."""
+    _check(lib().lora_adamw_step(ctypes.byref(table.c), _ptr(wA), _ptr(wB), _ptr(gA), _ptr(gB), _ptr(mA), _ptr(vA),
+                                 _ptr(mB), _ptr(vB), _ptr(lr), _ptr(step), beta1, beta2, eps, weight_decay,
+                                 _stream(stream)), "lora_adamw_step")
 
 
 def lora_query_status(segs: Segments, stream=None) -> int:

@@ -28,4 +28,10 @@ lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void
                       const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream,
                       Marks *marks = nullptr);
 
+// one AdamW step over A and B^T (fp32 masters, moments) and their bf16 copies
+// in the table (adamw.cu)
+lora_status_t run_adamw(const lora_adapter_table &tab, float *wA, float *wB, const float *gA, const float *gB,
+                        float *mA, float *vA, float *mB, float *vB, const float *lr, const int32_t *step, float beta1,
+                        float beta2, float eps, float weight_decay, cudaStream_t stream);
+
 }  // namespace lora

@@ -210,6 +210,26 @@ lora_status_t lora_packed_bwd_marked(void *dX, float *dA, float *dB, const void 
     return st;
 }
 
+lora_status_t lora_adamw_step(const lora_adapter_table *table, float *wA, float *wB, const float *gA, const float *gB,
+                              float *mA, float *vA, float *mB, float *vB, const float *lr, const int32_t *step,
+                              float beta1, float beta2, float eps, float weight_decay, lora_stream_t stream)
+{
+    LORA_TRY(check_table(table));
+    const void *f32[] = {wA, wB, gA, gB, mA, vA, mB, vB};
+    for (const void *p : f32) {
+        if (p == nullptr) return LORA_ERR_INVALID_ARG;
+        if (!aligned16(p)) return LORA_ERR_ALIGNMENT;
+    }
+    if (lr == nullptr || step == nullptr) return LORA_ERR_INVALID_ARG;
+    if (!aligned4(lr) || !aligned4(step)) return LORA_ERR_ALIGNMENT;
+    if (!(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f) || !(eps >= 0.f) ||
+        !(weight_decay >= 0.f))
+        return LORA_ERR_INVALID_ARG;
+    LORA_TRY(check_device());
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return run_adamw(*table, wA, wB, gA, gB, mA, vA, mB, vB, lr, step, beta1, beta2, eps, weight_decay, st);
+}
+
 lora_status_t lora_query_status(const lora_segments *segs, lora_stream_t stream)
 {
     if (segs == nullptr || segs->status == nullptr) return LORA_ERR_INVALID_ARG;

@@ -451,6 +451,50 @@ def time_decode(dev, stream, reps: int = 50):
     return out
 
 
+def time_adamw(spec: wl.Spec, dev, stream, reps: int = 20) -> dict:
+    """The fused per-adapter AdamW step (masters, moments, bf16 refresh) on
+    the workload's adapter table, rotating over enough buffer sets to exceed
+    L2; algorithmic bytes 30 per weight (w, g, m, v read, w, m, v written in
+    fp32, the bf16 copy written)."""
+    import torch
+
+    import adapter_sgmv_gb300 as lora
+
+    hbm, _, _ = measured_peaks()
+    sr = int(spec.sum_r)
+    elems = sr * (spec.d_in + spec.d_out)
+    nbytes = 30 * elems
+    n_sets = max(2, int(3 * L2_BYTES / nbytes) + 1)
+    sets = []
+    for q in range(n_sets):
+        z = lambda d: torch.zeros((sr, d), dtype=torch.float32, device=dev)
+        r = lambda d: torch.randn((sr, d), dtype=torch.float32, device=dev) * 0.01
+        A_bf = torch.zeros((sr, spec.d_in), dtype=torch.bfloat16, device=dev)
+        B_bf = torch.zeros((sr, spec.d_out), dtype=torch.bfloat16, device=dev)
+        tab = lora.AdapterTable(A_bf, B_bf, spec.ranks.tolist(), torch.from_numpy(spec.scales), spec.d_in, spec.d_out)
+        sets.append((tab, r(spec.d_in), r(spec.d_out), r(spec.d_in), r(spec.d_out), z(spec.d_in), z(spec.d_in),
+                     z(spec.d_out), z(spec.d_out)))
+    lr = torch.full((spec.n_adapters,), 1e-4, device=dev)
+    step = torch.ones(spec.n_adapters, dtype=torch.int32, device=dev)
+    with torch.cuda.stream(stream):
+        for k in range(n_sets + 3):
+            lora.lora_adamw_step(*sets[k % n_sets][:1], *sets[k % n_sets][1:], lr, step, stream=stream)
+        torch.cuda.synchronize()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for k in range(reps):
+            lora.lora_adamw_step(*sets[k % n_sets][:1], *sets[k % n_sets][1:], lr, step, stream=stream)
+        s1.record(stream)
+        torch.cuda.synchronize()
+    us = s0.elapsed_time(s1) / reps * 1e3
+    gbs = nbytes / (us * 1e-6) / 1e9
+    del sets
+    torch.cuda.empty_cache()
+    return {"us_per_step": round(us, 2), "weights": elems, "bytes": nbytes, "GB/s": round(gbs, 1),
+            "frac_of_hbm": round(gbs / hbm, 4)}
+
+
 def cpu_baseline(spec: wl.Spec, target_s: float = 10.0):
     """The fp64 oracle on a bounded sample of the same workload (first tokens of
     every adapter), on this host's cores; tokens/s."""
@@ -573,6 +617,7 @@ def run_ours(args, rank, world, dev):
             others[f"sweep3584x18944_N{n}"]["efficiency_vs_N2"] = round(
                 others[f"sweep3584x18944_N{n}"]["tokens/s"] / base, 3)
         others["skewed4096x14336_N32"] = time_config(wl.skewed(), dev, stream)
+    adamw = time_adamw(spec, dev, stream) if rank == 0 else None
     cpu = cpu_baseline(spec, args.cpu_seconds) if rank == 0 and not args.no_cpu else None
 
     if rank != 0:
@@ -607,6 +652,7 @@ def run_ours(args, rank, world, dev):
         "gpu_launches": kernels_per_step(spec) * args.steps,
         "clocks": clk.summary(),
         "decode_sgmv": decode,
+        "adamw_step": adamw,
         "other_workloads": others,
         "cpu_baseline": cpu,
     }

@@ -254,6 +254,35 @@ LORA_API lora_status_t lora_packed_bwd_marked(void *dX, float *dA, float *dB, co
                                               int32_t *n_recorded);
 
 /*
+ * One optimizer step for every adapter of the table, fused with the refresh
+ * of the bf16 weights the forward reads.  Each tenant keeps FP32 master
+ * weights, optimizer moments and gradient buffers beside its LoRA parameters
+ * (C-LoRA report, "Come funziona l'architettura": the AdapterStore); the
+ * pages name no optimizer, and the step is AdamW, adapter i with its own
+ * learning rate lr[i] and step number t = step[i] (>= 1, the caller advances
+ * it):
+ *   w <- w - lr wd w;  m <- b1 m + (1 - b1) g;  v <- b2 v + (1 - b2) g^2
+ *   w <- w - lr (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps)
+ * and the table's bf16 A / B rows are overwritten with round-to-nearest-even(w).
+ *   wA, mA, vA  device fp32 [sum_r, d_in]   master A and its moments (in/out;
+ *               the moments start at zero)
+ *   wB, mB, vB  device fp32 [sum_r, d_out]  master B^T (stored like the table's
+ *               B) and its moments (in/out)
+ *   gA, gB      device fp32 gradients in the same layouts (dA, dB of
+ *               lora_packed_bwd)
+ *   lr          device fp32 [n_adapters]; step  device int32 [n_adapters]
+ *   beta1, beta2 in [0, 1), eps >= 0, weight_decay >= 0
+ * Writes the table's A and B (its bf16 weights).  Errors: LORA_ERR_INVALID_ARG
+ * (null pointer, hyper-parameter out of range), LORA_ERR_ALIGNMENT (fp32
+ * arrays need 16-byte, lr / step 4-byte alignment), the table checks of the
+ * other calls.  The pages have no optimizer kernel of their own.
+ */
+LORA_API lora_status_t lora_adamw_step(const lora_adapter_table *table, float *wA, float *wB, const float *gA,
+                                       const float *gB, float *mA, float *vA, float *mB, float *vB, const float *lr,
+                                       const int32_t *step, float beta1, float beta2, float eps, float weight_decay,
+                                       lora_stream_t stream);
+
+/*
  * Packed backward without a workspace, for callers that cannot allocate device
  * memory (no cudaMalloc, no allocator of their own to draw scratch from).  The
  * pages have no counterpart to this call; it exists only for such callers.
