@@ -67,7 +67,8 @@ def _load():
         lib.lora_oracle_adamw.argtypes = [ctypes.c_int32, ctypes.c_int32, _i32p, _i64p, _f64p, _i32p,
                                           ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_double,
                                           _f64p, _f64p, _f64p, _f64p]
-        for name in ("shrink", "expand", "dh", "db", "da", "dx", "adamw"):
+        lib.lora_oracle_base.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _f64p, _f64p, _f64p]
+        for name in ("shrink", "expand", "dh", "db", "da", "dx", "adamw", "base"):
             getattr(lib, f"lora_oracle_{name}").restype = None
         _lib = lib
         return lib
@@ -236,3 +237,22 @@ def adamw(tab: Table, w, g, m, v, lr, step, beta1: float = 0.9, beta2: float = 0
                           _p(lr, _f64p), _p(step, _i32p), beta1, beta2, eps, weight_decay, _p(w, _f64p), _p(g, _f64p),
                           _p(m, _f64p), _p(v, _f64p))
     return w, m, v
+
+
+def base(W, x):
+    """Base projection y = x W^T (W is [d_out, d_in], x is [T, d_in])."""
+    lib = _load()
+    W = _c(W, np.float64)
+    x = _c(x, np.float64)
+    T, d_in = x.shape
+    d_out = W.shape[0]
+    assert W.shape[1] == d_in
+    y = np.zeros((T, d_out), dtype=np.float64)
+    lib.lora_oracle_base(T, d_in, d_out, _p(W, _f64p), _p(x, _f64p), _p(y, _f64p))
+    return y
+
+
+def base_lora_fwd(tab: Table, ids, W, A, B, x, r_max: int | None = None):
+    """A LoRA layer's forward: (y, H) with H = shrink(x) and
+    y = x W^T + expand(H), i.e. the base projection plus the delta."""
+    return fwd(tab, ids, A, B, x, base(W, x), r_max)

@@ -49,6 +49,13 @@
  *     w <- w - lr wd w;  m <- b1 m + (1 - b1) g;  v <- b2 v + (1 - b2) g^2
  *     w <- w - lr (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps)
  *
+ *   Base projection with the delta.  The frozen base weight W (d_out x d_in)
+ *   is shared by every adapter of a packed batch, which is what packing
+ *   amortises [PLoRA technical summary, gist.science, "2. LoRA Execution
+ *   Engine"]; a LoRA layer's output is the base projection plus the delta:
+ *     base     y_t      = W x_t                        (every token)
+ *   and the layer output is base followed by expand(shrink) above.
+ *
  * Each function is the per-token (or per-adapter) definition written out as
  * loops, with no blocking, fusion or reordering; OpenMP only splits the
  * independent outputs across threads, every sum runs in a fixed order.
@@ -272,6 +279,24 @@ void lora_oracle_adamw(int32_t N, int32_t d, const int32_t *rank, const int64_t 
             m[e] = beta1 * m[e] + (1.0 - beta1) * g[e];
             v[e] = beta2 * v[e] + (1.0 - beta2) * g[e] * g[e];
             w[e] -= lr[i] * (m[e] / bc1) / (sqrt(v[e] / bc2) + eps);
+        }
+    }
+}
+
+/* base: y[t, o] = sum_j W[o, j] * x[t, j] for every token (W row-major
+ * [d_out, d_in]), overwriting y. */
+void lora_oracle_base(int64_t T, int32_t d_in, int32_t d_out, const double *W,
+                      const double *x, double *y)
+{
+    #pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t t = 0; t < T; ++t) {
+        const double *xt = x + t * (int64_t)d_in;
+        double *yt = y + t * (int64_t)d_out;
+        for (int32_t o = 0; o < d_out; ++o) {
+            const double *w = W + (int64_t)o * d_in;
+            double acc = 0.0;
+            for (int32_t j = 0; j < d_in; ++j) acc += w[j] * xt[j];
+            yt[o] = acc;
         }
     }
 }

@@ -411,3 +411,53 @@ def test_adamw_zero_learning_rate_keeps_weights_and_moves_moments():
     w1, m1, _ = oracle.adamw(tab, w, g, np.zeros_like(w), np.zeros_like(w), [0.0, 1e-3], [3, 7], weight_decay=0.1)
     assert np.array_equal(w1[:4], w[:4]) and not np.array_equal(w1[4:], w[4:])
     assert np.allclose(m1, 0.1 * g, rtol=1e-14)
+
+
+# ---------------------------------------------------------------- base projection + delta
+def test_base_matches_numpy_matmul():
+    rng = np.random.default_rng(21)
+    W = rng.standard_normal((13, 9))
+    x = rng.standard_normal((6, 9))
+    assert np.allclose(oracle.base(W, x), x @ W.T, rtol=1e-13, atol=1e-13)
+
+
+def test_base_identity_and_permutation_weights_are_exact():
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal((7, 10))
+    assert np.array_equal(oracle.base(np.eye(10), x), x)
+    p = rng.permutation(10)
+    P = np.eye(10)[p]  # row o of W picks input p[o]
+    assert np.array_equal(oracle.base(P, x), x[:, p])
+
+
+def test_base_rank_one_weight_closed_form():
+    # W = u v^T: y_t = u (v . x_t); a transposed W or swapped loop bound fails
+    rng = np.random.default_rng(23)
+    u = rng.standard_normal(11)
+    v = rng.standard_normal(5)
+    x = rng.standard_normal((4, 5))
+    assert np.allclose(oracle.base(np.outer(u, v), x), np.outer(x @ v, u), rtol=1e-13, atol=1e-13)
+
+
+def test_layer_forward_is_base_plus_single_adapter_lora():
+    # one adapter: y = x W^T + s x A^T B^T with numpy @ (the plain LoRA layer)
+    spec = wl.custom("layer1", 24, 40, [6], [18.0], np.zeros(9, np.int32), seed=5)
+    P = make(spec)
+    W = f64(wl.base_weight(spec))
+    y, H = oracle.base_lora_fwd(P["tab"], P["ids"], W, P["A"], P["B"], P["x"])
+    s = float(spec.scales[0])
+    close(H, P["x"] @ P["A"].T)
+    close(y, P["x"] @ W.T + s * (P["x"] @ P["A"].T) @ P["B"])
+
+
+def test_layer_forward_reduces_to_its_parts():
+    # W = 0: the packed delta alone; A = 0: the base alone
+    ids = np.array([1, 1, 0, 2, 0, 1, 2, 2, 2, 0], np.int32)
+    spec = wl.custom("layer3", 16, 24, [2, 5, 3], [4.0, 10.0, 3.0], ids, seed=6)
+    P = make(spec)
+    W = f64(wl.base_weight(spec))
+    y, H = oracle.base_lora_fwd(P["tab"], P["ids"], np.zeros_like(W), P["A"], P["B"], P["x"])
+    y_d, H_d = oracle.fwd(P["tab"], P["ids"], P["A"], P["B"], P["x"], np.zeros((10, 24)))
+    assert np.array_equal(y, y_d) and np.array_equal(H, H_d)
+    y0, _ = oracle.base_lora_fwd(P["tab"], P["ids"], W, np.zeros_like(P["A"]), P["B"], P["x"])
+    close(y0, P["x"] @ W.T)

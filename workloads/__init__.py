@@ -12,7 +12,8 @@ varying as in PLoRA's search space.  None of them needs a dataset or trained
 weights: the delta is a linear map, so only shapes and value ranges matter.
 
 Value recipe (every tensor bf16, rounded to nearest-even from fp32):
-  x, dY, y0, dX0 ~ N(0, 1); A_i ~ U(-1/sqrt(d_in), +1/sqrt(d_in)); B_i ~ N(0, 0.02^2).
+  x, dY, y0, dX0 ~ N(0, 1); A_i ~ U(-1/sqrt(d_in), +1/sqrt(d_in)); B_i ~ N(0, 0.02^2);
+  the frozen base weight W [d_out, d_in] ~ U(-1/sqrt(d_in), +1/sqrt(d_in)).
 Layouts: A [sum_r, d_in] (A_i stacked); B [sum_r, d_out] (B_i transposed,
 stacked the same way: row row_off[i] + k is column k of B_i).
 Each tensor draws from its own stream, numpy ``default_rng([seed, k])`` on
@@ -31,7 +32,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 SKEWED_FIXTURE = os.path.join(_HERE, "skewed_seed0.json")
 
 # stream indices, one per tensor
-_S_A, _S_B, _S_X, _S_DY, _S_Y0, _S_DX0 = 1, 2, 3, 4, 5, 6
+_S_A, _S_B, _S_X, _S_DY, _S_Y0, _S_DX0, _S_W = 1, 2, 3, 4, 5, 6, 7
 
 
 # ----------------------------------------------------------------------------
@@ -246,9 +247,18 @@ def host_inputs(spec: Spec, y0: str = "zero", dX0: str = "zero") -> dict:
     return out
 
 
+def base_weight(spec: Spec) -> np.ndarray:
+    """bf16 bits of the frozen base weight W [d_out, d_in] (row-major, the
+    layout of a linear layer's weight), drawn on the host."""
+    lim = 1.0 / math.sqrt(spec.d_in)
+    g = np.random.default_rng([spec.seed, _S_W])
+    return f32_to_bf16_bits(g.uniform(-lim, lim, size=(spec.d_out, spec.d_in)).astype(np.float32))
+
+
 def device_inputs(spec: Spec, device, y0: str = "zero", dX0: str = "zero", need=None) -> dict:
     """The same recipe drawn on a torch device (bf16 tensors), for sizes too
-    large to draw on the host.  ``need`` restricts the keys produced."""
+    large to draw on the host.  ``need`` restricts the keys produced; the
+    base weight "W" is produced only when asked for."""
     import torch
 
     T, d_in, d_out, sr, s = spec.n_tokens, spec.d_in, spec.d_out, spec.sum_r, spec.seed
@@ -275,6 +285,9 @@ def device_inputs(spec: Spec, device, y0: str = "zero", dX0: str = "zero", need=
             out["y0"] = torch.randn((T, d_out), generator=gen(_S_Y0), device=device).to(torch.bfloat16)
         else:
             out["y0"] = torch.zeros((T, d_out), device=device, dtype=torch.bfloat16)
+    if "W" in keys:
+        w = torch.rand((d_out, d_in), generator=gen(_S_W), device=device, dtype=torch.float32)
+        out["W"] = (w * (2 * lim) - lim).to(torch.bfloat16)
     if "dX0" in keys:
         if dX0 == "randn":
             out["dX0"] = torch.randn((T, d_in), generator=gen(_S_DX0), device=device).to(torch.bfloat16)
