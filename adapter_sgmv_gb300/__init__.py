@@ -22,7 +22,8 @@ __all__ = [
     "LoraError", "AdapterTable", "Segments", "lib", "lora_abi_version", "lora_status_string",
     "lora_segments_bytes", "lora_build_segments", "lora_workspace_bytes", "lora_sgmv_shrink",
     "lora_sgmv_expand", "lora_packed_fwd", "lora_packed_bwd", "lora_packed_fwd_marked", "lora_packed_bwd_marked",
-    "lora_packed_bwd_noalloc", "lora_adamw_step", "lora_query_status", "lora_reset_status",
+    "lora_packed_bwd_noalloc", "lora_adamw_step", "lora_fused_base_workspace_bytes", "lora_fused_base_fwd",
+    "lora_query_status", "lora_reset_status",
     "STATUS",
 ]
 
@@ -80,6 +81,9 @@ SIGNATURES = {
                                        ctypes.POINTER(c_segments), _P]),
     "lora_adamw_step": (_I32, [ctypes.POINTER(c_table), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float,
                                 ctypes.c_float, ctypes.c_float, ctypes.c_float, _P]),
+    "lora_fused_base_workspace_bytes": (_SZ, [ctypes.POINTER(c_table), _I32]),
+    "lora_fused_base_fwd": (_I32, [_P, _P, _P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments), _P, _SZ,
+                                   _P]),
     "lora_query_status": (_I32, [ctypes.POINTER(c_segments), _P]),
     "lora_reset_status": (_I32, [ctypes.POINTER(c_segments), _P]),
 }
@@ -323,6 +327,19 @@ def lora_adamw_step(table: AdapterTable, wA, wB, gA, gB, mA, vA, mB, vB, lr, ste
     _check(lib().lora_adamw_step(ctypes.byref(table.c), _ptr(wA), _ptr(wB), _ptr(gA), _ptr(gB), _ptr(mA), _ptr(vA),
                                  _ptr(mB), _ptr(vB), _ptr(lr), _ptr(step), beta1, beta2, eps, weight_decay,
                                  _stream(stream)), "lora_adamw_step")
+
+
+def lora_fused_base_workspace_bytes(table: AdapterTable, n_tokens: int) -> int:
+    return int(lib().lora_fused_base_workspace_bytes(ctypes.byref(table.c), int(n_tokens)))
+
+
+def lora_fused_base_fwd(y, H_save, x, W, table: AdapterTable, segs: Segments, ws, stream=None):
+    """y = x W^T + the packed LoRA delta, in one launch (segment-sorted batch;
+    H_save may be None).  ws: at least lora_fused_base_workspace_bytes bytes."""
+    wsb = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().lora_fused_base_fwd(_ptr(y), _ptr(H_save), _ptr(x), _ptr(W), ctypes.byref(table.c),
+                                     ctypes.byref(segs.c), _ptr(ws), wsb, _stream(stream)), "lora_fused_base_fwd")
+    return y
 
 
 def lora_query_status(segs: Segments, stream=None) -> int:

@@ -8,6 +8,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "dispatch.h"
+#include "tc_host.h"
 
 using namespace lora;
 
@@ -228,6 +229,30 @@ lora_status_t lora_adamw_step(const lora_adapter_table *table, float *wA, float 
     LORA_TRY(check_device());
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     return run_adamw(*table, wA, wB, gA, gB, mA, vA, mB, vB, lr, step, beta1, beta2, eps, weight_decay, st);
+}
+
+size_t lora_fused_base_workspace_bytes(const lora_adapter_table *table, int32_t n_tokens)
+{
+    if (check_table(table) != LORA_OK || n_tokens < 0) return 0;
+    const SegLayout L = seg_layout(n_tokens, table->n_adapters);
+    return L.ok ? base_workspace_bytes(n_tokens, table->r_max, L.max_tiles) : 0;
+}
+
+lora_status_t lora_fused_base_fwd(void *y, float *H_save, const void *x, const void *W,
+                                  const lora_adapter_table *table, const lora_segments *segs, void *ws,
+                                  size_t ws_bytes, lora_stream_t stream)
+{
+    LORA_TRY(check_table(table));
+    LORA_TRY(check_segs(segs, table));
+    if (y == nullptr || x == nullptr || W == nullptr) return LORA_ERR_INVALID_ARG;
+    if (!aligned16(y) || !aligned16(x) || !aligned16(W) || (H_save && !aligned16(H_save)) ||
+        (ws && !aligned16(ws)))
+        return LORA_ERR_ALIGNMENT;
+    if (segs->n_tokens > 0 && segs->sorted == 0) return LORA_ERR_UNSUPPORTED;
+    const size_t need = base_workspace_bytes(segs->n_tokens, table->r_max, segs->max_tiles);
+    if (segs->n_tokens > 0 && (ws == nullptr || ws_bytes < need)) return LORA_ERR_WORKSPACE_TOO_SMALL;
+    LORA_TRY(check_device());
+    return tc_base_fwd(y, H_save, x, W, ws, *table, *segs, reinterpret_cast<cudaStream_t>(stream));
 }
 
 lora_status_t lora_query_status(const lora_segments *segs, lora_stream_t stream)

@@ -71,4 +71,11 @@ size_t decode_workspace_bytes(int32_t T, int32_t r_max);
 lora_status_t tc_decode_fwd(void *y, float *H_save, const void *x, void *ws, const lora_adapter_table &tab,
                             const lora_segments &segs, cudaStream_t stream);
 
+// Base projection plus packed delta in one persistent launch (segment-sorted
+// batches): y = x W^T + s_i (x A_i^T) B_i^T, H (fp32, may be null) = x A_i^T.
+// ws: base_workspace_bytes(T, r_max, segs.max_tiles) bytes.
+size_t base_workspace_bytes(int32_t T, int32_t r_max, int32_t max_tiles);
+lora_status_t tc_base_fwd(void *y, float *H, const void *x, const void *W, void *ws, const lora_adapter_table &tab,
+                          const lora_segments &segs, cudaStream_t stream);
+
 }  // namespace lora

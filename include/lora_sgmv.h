@@ -283,6 +283,32 @@ LORA_API lora_status_t lora_adamw_step(const lora_adapter_table *table, float *w
                                        lora_stream_t stream);
 
 /*
+ * A LoRA layer's forward in one persistent launch: the base projection with
+ * the packed delta on the same fp32 accumulators,
+ *   y_t = W x_t + s_i B_i (A_i x_t)          (token t of adapter i)
+ * The frozen base weight W is shared by every adapter of the batch, which is
+ * what packing amortises (PLoRA technical summary, "2. LoRA Execution
+ * Engine": base-model computation shared across the packed adapters).
+ *   y       device bf16 [T, d_out] (out, overwritten; rounded once from fp32)
+ *   H_save  device fp32 [T, r_max] (out): h = A_i x_t, zero beyond r_i, for
+ *           lora_packed_bwd; or NULL
+ *   x       device bf16 [T, d_in];  W  device bf16 [d_out, d_in] row-major
+ *           (a linear layer's weight)
+ *   segs    built from seg_offsets (tokens grouped by adapter, the packed
+ *           layout); a batch routed from unsorted ids gives LORA_ERR_UNSUPPORTED
+ *   ws      device workspace of >= lora_fused_base_workspace_bytes(table, T)
+ *           bytes: the bf16 s_i h hand-off rows and one ready counter per tile
+ * The delta's h enters the expand as bf16 (s_i h rounded once); products
+ * accumulate in fp32.  The kernel is a cooperative launch (one CTA per SM,
+ * all resident).  Errors: those of lora_packed_fwd; LORA_ERR_TIMEOUT on the
+ * device if a wait between CTAs gives up (it is bounded).
+ */
+LORA_API size_t lora_fused_base_workspace_bytes(const lora_adapter_table *table, int32_t n_tokens);
+LORA_API lora_status_t lora_fused_base_fwd(void *y, float *H_save, const void *x, const void *W,
+                                           const lora_adapter_table *table, const lora_segments *segs,
+                                           void *ws, size_t ws_bytes, lora_stream_t stream);
+
+/*
  * Packed backward without a workspace, for callers that cannot allocate device
  * memory (no cudaMalloc, no allocator of their own to draw scratch from).  The
  * pages have no counterpart to this call; it exists only for such callers.
