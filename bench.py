@@ -495,6 +495,75 @@ def time_adamw(spec: wl.Spec, dev, stream, reps: int = 20) -> dict:
             "frac_of_hbm": round(gbs / hbm, 4)}
 
 
+def time_fused_base(spec: wl.Spec, dev, stream, reps: int = 10) -> dict:
+    """A LoRA layer's forward, y = x W^T + the packed delta, in the library's
+    single persistent launch (lora_fused_base_fwd), against the same layer
+    done unfused: the base GEMM by cuBLAS (torch.matmul) then lora_packed_fwd
+    accumulating the delta into its output.  Inputs (x 268 MB) exceed L2.
+    Algorithmic flops: 2 T d_in d_out (base) + 2 sum_t r_i (d_in + d_out)."""
+    import torch
+
+    import adapter_sgmv_gb300 as lora
+
+    _, bf16_peak, src = measured_peaks()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            sustained = float(json.load(f)["bf16_tflops_sustained"])
+    except Exception:
+        sustained = None
+    inp = wl.device_inputs(spec, dev, need={"A", "B", "x", "W"})
+    T, d_in, d_out = spec.n_tokens, spec.d_in, spec.d_out
+    tab = lora.AdapterTable(inp["A"], inp["B"], spec.ranks.tolist(), torch.from_numpy(spec.scales), d_in, d_out)
+    segs = lora.lora_build_segments(seg_offsets=torch.from_numpy(spec.seg_offsets).to(dev), n_tokens=T,
+                                    n_adapters=spec.n_adapters, device=dev)
+    ws_f = torch.empty(lora.lora_fused_base_workspace_bytes(tab, T), dtype=torch.uint8, device=dev)
+    ws_p = lora.workspace(tab, T, dev)
+    y = torch.empty((T, d_out), dtype=torch.bfloat16, device=dev)
+    H = torch.empty((T, spec.r_max), dtype=torch.float32, device=dev)
+    x, W = inp["x"], inp["W"]
+    rank_tok = np.repeat(spec.ranks.astype(np.int64), np.diff(spec.seg_offsets))
+    flops = 2 * T * d_in * d_out + 2 * int(rank_tok.sum()) * (d_in + d_out)
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            for _ in range(reps):
+                fn()
+            s1.record(stream)
+            torch.cuda.synchronize()
+        return s0.elapsed_time(s1) / reps
+
+    fused = lambda: lora.lora_fused_base_fwd(y, H, x, W, tab, segs, ws_f, stream=stream)
+    ms = timed(fused)
+    assert lora.lora_query_status(segs) == 0
+    ms_cublas = timed(lambda: torch.matmul(x, W.t(), out=y))
+
+    def unfused():
+        torch.matmul(x, W.t(), out=y)
+        lora.lora_packed_fwd(y, H, x, tab, segs, ws_p, stream=stream)
+
+    ms_unfused = timed(unfused)
+    tf = flops / (ms * 1e-3) / 1e12
+    out = {"workload": f"packed4096 layer forward: T={T}, {d_in}->{d_out}, ranks "
+                       f"{{{','.join(str(int(r)) for r in spec.ranks)}}}, y = x W^T + s_i (x A_i^T) B_i^T",
+           "ms": round(ms, 4), "flops": flops,
+           "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": bf16_peak, "unit": "TFLOP/s",
+                        "frac": round(tf / bf16_peak, 4), "peak_source": f"{src} (burst, cuBLAS bf16)",
+                        "frac_of_sustained": round(tf / sustained, 4) if sustained else None},
+           "cublas_base_ms": round(ms_cublas, 4),
+           "cublas_base_TFLOP/s": round(2 * T * d_in * d_out / (ms_cublas * 1e-3) / 1e12, 1),
+           "unfused_ms": round(ms_unfused, 4),
+           "speedup_vs_unfused": round(ms_unfused / ms, 3)}
+    del inp, y, H, ws_f, ws_p, segs, tab
+    torch.cuda.empty_cache()
+    return out
+
+
 def cpu_baseline(spec: wl.Spec, target_s: float = 10.0):
     """The fp64 oracle on a bounded sample of the same workload (first tokens of
     every adapter), on this host's cores; tokens/s."""
@@ -618,6 +687,7 @@ def run_ours(args, rank, world, dev):
                 others[f"sweep3584x18944_N{n}"]["tokens/s"] / base, 3)
         others["skewed4096x14336_N32"] = time_config(wl.skewed(), dev, stream)
     adamw = time_adamw(spec, dev, stream) if rank == 0 else None
+    fused = time_fused_base(spec, dev, stream) if rank == 0 and not args.no_fused else None
     cpu = cpu_baseline(spec, args.cpu_seconds) if rank == 0 and not args.no_cpu else None
 
     if rank != 0:
@@ -653,6 +723,7 @@ def run_ours(args, rank, world, dev):
         "clocks": clk.summary(),
         "decode_sgmv": decode,
         "adamw_step": adamw,
+        "fused_base_lora": fused,
         "other_workloads": others,
         "cpu_baseline": cpu,
     }
@@ -712,6 +783,7 @@ def main():
     ap.add_argument("--ref-tokens-per-adapter", type=int, default=16)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="skip the adapter-count sweep and the skewed batch")
+    ap.add_argument("--no-fused", action="store_true", help="skip the fused base + delta layer forward")
     ap.add_argument("--decode-only", action="store_true", help="time only the decode batch (profiling runs)")
     ap.add_argument("--tokens-per-adapter", type=int, default=4096,
                     help="tokens per adapter of the packed batch (4096 is the benchmarked workload; "
