@@ -23,6 +23,7 @@ __all__ = [
     "lora_segments_bytes", "lora_build_segments", "lora_workspace_bytes", "lora_sgmv_shrink",
     "lora_sgmv_expand", "lora_packed_fwd", "lora_packed_bwd", "lora_packed_fwd_marked", "lora_packed_bwd_marked",
     "lora_packed_bwd_noalloc", "lora_adamw_step", "lora_fused_base_workspace_bytes", "lora_fused_base_fwd",
+    "lora_multi_workspace_bytes", "lora_multi_fwd",
     "lora_query_status", "lora_reset_status",
     "STATUS",
 ]
@@ -81,6 +82,9 @@ SIGNATURES = {
                                        ctypes.POINTER(c_segments), _P]),
     "lora_adamw_step": (_I32, [ctypes.POINTER(c_table), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float,
                                 ctypes.c_float, ctypes.c_float, ctypes.c_float, _P]),
+    "lora_multi_workspace_bytes": (_SZ, [_I32, ctypes.POINTER(c_table), _I32]),
+    "lora_multi_fwd": (_I32, [_I32, ctypes.POINTER(_P), ctypes.POINTER(_P), _P, ctypes.POINTER(c_table),
+                              ctypes.POINTER(c_segments), _P, _SZ, _P]),
     "lora_fused_base_workspace_bytes": (_SZ, [ctypes.POINTER(c_table), _I32]),
     "lora_fused_base_fwd": (_I32, [_P, _P, _P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments), _P, _SZ,
                                    _P]),
@@ -327,6 +331,29 @@ def lora_adamw_step(table: AdapterTable, wA, wB, gA, gB, mA, vA, mB, vB, lr, ste
     _check(lib().lora_adamw_step(ctypes.byref(table.c), _ptr(wA), _ptr(wB), _ptr(gA), _ptr(gB), _ptr(mA), _ptr(vA),
                                  _ptr(mB), _ptr(vB), _ptr(lr), _ptr(step), beta1, beta2, eps, weight_decay,
                                  _stream(stream)), "lora_adamw_step")
+
+
+def _tables(tables):
+    return (c_table * len(tables))(*[t.c for t in tables])
+
+
+def lora_multi_workspace_bytes(tables, n_tokens: int) -> int:
+    """Workspace of lora_multi_fwd for these AdapterTables and T tokens."""
+    return int(lib().lora_multi_workspace_bytes(len(tables), _tables(tables), int(n_tokens)))
+
+
+def lora_multi_fwd(ys, H_saves, x, tables, segs: Segments, ws, stream=None):
+    """Packed forward of len(tables) projections sharing x (one y / table per
+    projection; H_saves: None or a list with None entries allowed)."""
+    n = len(tables)
+    if len(ys) != n or (H_saves is not None and len(H_saves) != n):
+        raise ValueError("one y (and H_save) per table")
+    y_arr = (_P * n)(*[_ptr(y) for y in ys])
+    h_arr = None if H_saves is None else (_P * n)(*[_ptr(h) for h in H_saves])
+    wsb = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().lora_multi_fwd(n, y_arr, h_arr, _ptr(x), _tables(tables), ctypes.byref(segs.c), _ptr(ws), wsb,
+                                _stream(stream)), "lora_multi_fwd")
+    return ys
 
 
 def lora_fused_base_workspace_bytes(table: AdapterTable, n_tokens: int) -> int:

@@ -21,6 +21,11 @@
 // they update (inputs the shrink does not write) before waiting for the shrink
 // grid to complete; h is then read from L2.
 //
+// Several projections that read the same x (q / k / v, gate / up) go through
+// the same two launches: blockIdx.y selects the projection, each with its own
+// adapter table, output and h buffer, so a layer's decode LoRA work costs two
+// launches however many projections share the input.
+//
 // The products are warp-level bf16 tensor-core MMAs (m16n8k16, fp32
 // accumulate): with 16..128 tokens per tile and rank 16..128 the operand
 // tiles are far below the 128-row tcgen05 shapes, and TMEM allocation and
@@ -48,13 +53,23 @@ constexpr int kYStride = kNW + 8;
 constexpr int kMaxStages = 6;
 constexpr int kPRows = 128;        // shrink: k-groups x tile rows of per-warp sums (8 / mg x 16 mg at most)
 
+// The projections of one call (blockIdx.y): tables share d_in and the adapter
+// count; ranks, scales, B and d_out are per projection.
+struct ProjSet {
+    lora_adapter_table tab[kMaxProjections];
+    uint16_t *y[kMaxProjections];
+    float *H[kMaxProjections];     // fp32 H by token, or null
+    float *hfin[kMaxProjections];  // [T, rp_cap] fp32 h hand-off
+    int32_t n;
+};
+
 struct Geom {
     int32_t rows_cap;  // tile rows the shared buffers hold (multiple of 16, <= 128)
-    int32_t rp_cap;    // rank rows they hold: r_max rounded up to 16
+    int32_t rp_cap;    // rank rows they hold: the largest r_max rounded up to 16
     int32_t kw;        // shrink: columns per slice of d_in (multiple of kKC)
     int32_t ks;        // shrink: slices of d_in = CTAs per cluster (<= kDecodeSlices)
     int32_t stages;    // shrink: stages of rows_cap + rp_cap rows the ring holds (>= 2)
-    int32_t ns;        // expand: slices of d_out
+    int32_t ns;        // expand: slices of the widest d_out
 };
 
 LORA_DEV int32_t rpad16(int32_t r) { return (r + 15) & ~15; }
@@ -161,12 +176,15 @@ size_t expand_smem(const Geom &g)
 // m-tile, each taking every (8 / mg)-th k16 step, all rank columns.  Each
 // k-group leaves its sums in shared memory; they are added in a fixed order
 // and the tile's partial goes to P_s in perm order.
-__global__ void __launch_bounds__(kThreads, 2) dec_shrink_kernel(const uint16_t *__restrict__ x, float *__restrict__ hfin,
-                                                              float *__restrict__ H_save, Geom g,
-                                                              lora_adapter_table tab, lora_segments segs)
+__global__ void __launch_bounds__(kThreads, 2) dec_shrink_kernel(const uint16_t *__restrict__ x,
+                                                              const __grid_constant__ ProjSet ps, Geom g,
+                                                              lora_segments segs)
 {
     pdl_launch_dependents();  // the expand may start its own loads now
     const int32_t ti = blockIdx.x / g.ks, sl = blockIdx.x % g.ks;
+    const lora_adapter_table &tab = ps.tab[blockIdx.y];
+    float *__restrict__ hfin = ps.hfin[blockIdx.y];
+    float *__restrict__ H_save = ps.H[blockIdx.y];
     const DecTile D = dec_tile(tab, segs, ti);
     if (!D.run || !D.ad.ok) return;
     const Tile &T = D.T;
@@ -335,10 +353,14 @@ __global__ void __launch_bounds__(kThreads, 2) dec_shrink_kernel(const uint16_t 
 // Warp w owns columns 32 w .. 32 w + 31 of the slice (four n-tiles) and walks
 // the tile's m-tiles; y is updated in shared memory and written back in
 // 16-byte pieces.
-__global__ void __launch_bounds__(kThreads, 2) dec_expand_kernel(uint16_t *__restrict__ y, const float *__restrict__ hfin,
-                                                              Geom g, lora_adapter_table tab, lora_segments segs)
+__global__ void __launch_bounds__(kThreads, 2) dec_expand_kernel(const __grid_constant__ ProjSet ps, Geom g,
+                                                              lora_segments segs)
 {
     const int32_t ti = blockIdx.x / g.ns, nsl = blockIdx.x % g.ns;
+    const lora_adapter_table &tab = ps.tab[blockIdx.y];
+    uint16_t *__restrict__ y = ps.y[blockIdx.y];
+    const float *__restrict__ hfin = ps.hfin[blockIdx.y];
+    if (nsl * kNW >= tab.d_out) return;  // a narrower projection has fewer slices
     // the routing was complete before the shrink started, so it can be read
     // before the wait; so can B and y, which the shrink does not write
     const DecTile D = dec_tile(tab, segs, ti);
@@ -434,12 +456,18 @@ __global__ void __launch_bounds__(kThreads, 2) dec_expand_kernel(uint16_t *__res
     }
 }
 
-Geom make_geom(const lora_adapter_table &tab, const lora_segments &segs)
+Geom make_geom(const ProjSet &ps, const lora_segments &segs)
 {
     Geom g;
+    const lora_adapter_table &tab = ps.tab[0];  // d_in is common to the set
     const int32_t T = segs.n_tokens;
+    int32_t r_max = 0, d_out = 0;
+    for (int p = 0; p < ps.n; ++p) {
+        r_max = std::max(r_max, ps.tab[p].r_max);
+        d_out = std::max(d_out, ps.tab[p].d_out);
+    }
     g.rows_cap = std::min<int32_t>(LORA_TILE_M, (T + 15) & ~15);
-    g.rp_cap = (tab.r_max + 15) & ~15;
+    g.rp_cap = (r_max + 15) & ~15;
     // slices of at least 256 columns, at most kDecodeSlices of them (one CTA
     // of the tile's cluster each)
     const int32_t per = (tab.d_in + kDecodeSlices - 1) / kDecodeSlices;
@@ -453,7 +481,7 @@ Geom make_geom(const lora_adapter_table &tab, const lora_segments &segs)
     int32_t st = (int32_t)((100u * 1024u > fixed ? 100u * 1024u - fixed : 0) / stage);
     st = std::min<int32_t>(std::min<int32_t>(st, chunks), kMaxStages);
     g.stages = std::max<int32_t>(st, 2);
-    g.ns = (tab.d_out + kNW - 1) / kNW;
+    g.ns = (d_out + kNW - 1) / kNW;
     return g;
 }
 
@@ -464,12 +492,23 @@ size_t decode_workspace_bytes(int32_t T, int32_t r_max)
     return (size_t)T * (size_t)((r_max + 15) & ~15) * sizeof(float);
 }
 
-lora_status_t tc_decode_fwd(void *y, float *H_save, const void *x, void *ws, const lora_adapter_table &tab,
-                            const lora_segments &segs, cudaStream_t stream)
+lora_status_t tc_decode_multi(int32_t n_proj, void *const *y, float *const *H_save, const void *x, void *ws,
+                              const lora_adapter_table *tabs, const lora_segments &segs, cudaStream_t stream)
 {
-    if (segs.n_tokens == 0 || segs.max_tiles == 0) return LORA_OK;
-    const Geom g = make_geom(tab, segs);
-    float *hfin = static_cast<float *>(ws);
+    if (segs.n_tokens == 0 || segs.max_tiles == 0 || n_proj == 0) return LORA_OK;
+    if (n_proj < 0 || n_proj > kMaxProjections) return LORA_ERR_SHAPE;
+    ProjSet ps = {};
+    ps.n = n_proj;
+    int32_t r_max = 0;
+    for (int p = 0; p < n_proj; ++p) r_max = std::max(r_max, tabs[p].r_max);
+    const size_t per = decode_workspace_bytes(segs.n_tokens, r_max);
+    for (int p = 0; p < n_proj; ++p) {
+        ps.tab[p] = tabs[p];
+        ps.y[p] = static_cast<uint16_t *>(y[p]);
+        ps.H[p] = H_save != nullptr ? H_save[p] : nullptr;
+        ps.hfin[p] = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + (size_t)p * per);
+    }
+    const Geom g = make_geom(ps, segs);
     const size_t s1 = shrink_smem(g), s2 = expand_smem(g);
     if (cudaFuncSetAttribute(dec_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1) != cudaSuccess ||
         cudaFuncSetAttribute(dec_shrink_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
@@ -477,7 +516,7 @@ lora_status_t tc_decode_fwd(void *y, float *H_save, const void *x, void *ws, con
         return LORA_ERR_CUDA;
     {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(segs.max_tiles * g.ks));
+        cfg.gridDim = dim3((unsigned)(segs.max_tiles * g.ks), (unsigned)n_proj);
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = s1;
         cfg.stream = stream;
@@ -488,13 +527,12 @@ lora_status_t tc_decode_fwd(void *y, float *H_save, const void *x, void *ws, con
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, dec_shrink_kernel, static_cast<const uint16_t *>(x), hfin, H_save, g, tab,
-                               segs) != cudaSuccess)
+        if (cudaLaunchKernelEx(&cfg, dec_shrink_kernel, static_cast<const uint16_t *>(x), ps, g, segs) != cudaSuccess)
             return LORA_ERR_CUDA;
     }
     {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(segs.max_tiles * g.ns));
+        cfg.gridDim = dim3((unsigned)(segs.max_tiles * g.ns), (unsigned)n_proj);
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = s2;
         cfg.stream = stream;
@@ -503,11 +541,17 @@ lora_status_t tc_decode_fwd(void *y, float *H_save, const void *x, void *ws, con
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        const float *ch = hfin;
-        if (cudaLaunchKernelEx(&cfg, dec_expand_kernel, static_cast<uint16_t *>(y), ch, g, tab, segs) != cudaSuccess)
-            return LORA_ERR_CUDA;
+        if (cudaLaunchKernelEx(&cfg, dec_expand_kernel, ps, g, segs) != cudaSuccess) return LORA_ERR_CUDA;
     }
     return LORA_OK;
+}
+
+lora_status_t tc_decode_fwd(void *y, float *H_save, const void *x, void *ws, const lora_adapter_table &tab,
+                            const lora_segments &segs, cudaStream_t stream)
+{
+    void *ys[1] = {y};
+    float *hs[1] = {H_save};
+    return tc_decode_multi(1, ys, hs, x, ws, &tab, segs, stream);
 }
 
 }  // namespace lora

@@ -107,6 +107,34 @@ lora_status_t run_fwd(void *y, float *H_save, const void *x, void *ws, const lor
     return marked(marks, stream, [&] { return tc_expand_bf16(y, hi, lo, rw, tab, segs, stream); });
 }
 
+size_t multi_workspace_bytes(int32_t n_proj, const lora_adapter_table *tabs, int32_t T)
+{
+    size_t need = 0;
+    int32_t r_max = 0;
+    for (int32_t p = 0; p < n_proj; ++p) {
+        r_max = tabs[p].r_max > r_max ? tabs[p].r_max : r_max;
+        const size_t one = packed_workspace_bytes(T, tabs[p].r_max);  // the per-projection path
+        need = one > need ? one : need;
+    }
+    if (T <= kDecodeMaxTokens) {  // the shared decode launches: one h buffer per projection
+        const size_t dec = (size_t)n_proj * decode_workspace_bytes(T, r_max);
+        need = dec > need ? dec : need;
+    }
+    return need;
+}
+
+lora_status_t run_multi_fwd(int32_t n_proj, void *const *y, float *const *H_save, const void *x, void *ws,
+                            const lora_adapter_table *tabs, const lora_segments &segs, cudaStream_t stream)
+{
+    if (segs.n_tokens <= kDecodeMaxTokens) return tc_decode_multi(n_proj, y, H_save, x, ws, tabs, segs, stream);
+    for (int32_t p = 0; p < n_proj; ++p) {  // large batches: the packed kernels, one projection after another
+        const lora_status_t st =
+            run_fwd(y[p], H_save != nullptr ? H_save[p] : nullptr, x, ws, tabs[p], segs, stream, nullptr);
+        if (st != LORA_OK) return st;
+    }
+    return LORA_OK;
+}
+
 lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X, const float *H_saved, void *ws,
                       const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream, Marks *marks)
 {

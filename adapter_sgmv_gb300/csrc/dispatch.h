@@ -24,6 +24,10 @@ lora_status_t run_expand(void *y, const float *H, const lora_adapter_table &tab,
 // ws: packed_workspace_bytes(T, r_max) bytes
 lora_status_t run_fwd(void *y, float *H_save, const void *x, void *ws, const lora_adapter_table &tab,
                       const lora_segments &segs, cudaStream_t stream, Marks *marks = nullptr);
+// several projections reading the same x (tables share d_in and the adapter count)
+size_t multi_workspace_bytes(int32_t n_proj, const lora_adapter_table *tabs, int32_t T);
+lora_status_t run_multi_fwd(int32_t n_proj, void *const *y, float *const *H_save, const void *x, void *ws,
+                            const lora_adapter_table *tabs, const lora_segments &segs, cudaStream_t stream);
 lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X, const float *H_saved, void *ws,
                       const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream,
                       Marks *marks = nullptr);

@@ -231,6 +231,36 @@ lora_status_t lora_adamw_step(const lora_adapter_table *table, float *wA, float 
     return run_adamw(*table, wA, wB, gA, gB, mA, vA, mB, vB, lr, step, beta1, beta2, eps, weight_decay, st);
 }
 
+size_t lora_multi_workspace_bytes(int32_t n_proj, const lora_adapter_table *tables, int32_t n_tokens)
+{
+    if (tables == nullptr || n_proj < 1 || n_proj > LORA_MAX_PROJECTIONS || n_tokens < 0 || n_tokens > kMaxTokens)
+        return 0;
+    for (int32_t p = 0; p < n_proj; ++p)
+        if (check_table(&tables[p]) != LORA_OK) return 0;
+    return multi_workspace_bytes(n_proj, tables, n_tokens);
+}
+
+lora_status_t lora_multi_fwd(int32_t n_proj, void *const *y, float *const *H_save, const void *x,
+                             const lora_adapter_table *tables, const lora_segments *segs, void *ws, size_t ws_bytes,
+                             lora_stream_t stream)
+{
+    if (y == nullptr || tables == nullptr || x == nullptr) return LORA_ERR_INVALID_ARG;
+    if (n_proj < 1 || n_proj > LORA_MAX_PROJECTIONS) return LORA_ERR_SHAPE;
+    for (int32_t p = 0; p < n_proj; ++p) {
+        LORA_TRY(check_table(&tables[p]));
+        LORA_TRY(check_segs(segs, &tables[p]));
+        if (tables[p].d_in != tables[0].d_in) return LORA_ERR_SHAPE;
+        if (y[p] == nullptr) return LORA_ERR_INVALID_ARG;
+        if (!aligned16(y[p]) || (H_save != nullptr && H_save[p] != nullptr && !aligned16(H_save[p])))
+            return LORA_ERR_ALIGNMENT;
+    }
+    if (!aligned16(x) || (ws && !aligned16(ws))) return LORA_ERR_ALIGNMENT;
+    const size_t need = multi_workspace_bytes(n_proj, tables, segs->n_tokens);
+    if (need > 0 && (ws == nullptr || ws_bytes < need)) return LORA_ERR_WORKSPACE_TOO_SMALL;
+    LORA_TRY(check_device());
+    return run_multi_fwd(n_proj, y, H_save, x, ws, tables, *segs, reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t lora_fused_base_workspace_bytes(const lora_adapter_table *table, int32_t n_tokens)
 {
     if (check_table(table) != LORA_OK || n_tokens < 0) return 0;

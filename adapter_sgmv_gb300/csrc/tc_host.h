@@ -67,9 +67,15 @@ lora_status_t tc_da(float *dA, const void *X, const uint16_t *dh_bf16, int32_t r
 // (fp32 h in ws), then the expand as a programmatic dependent launch; H_save
 // may be null.  ws: decode_workspace_bytes(T, r_max) bytes.
 constexpr int32_t kDecodeSlices = 16;  // most slices of d_in (CTAs per cluster)
+constexpr int32_t kMaxProjections = LORA_MAX_PROJECTIONS;
 size_t decode_workspace_bytes(int32_t T, int32_t r_max);
 lora_status_t tc_decode_fwd(void *y, float *H_save, const void *x, void *ws, const lora_adapter_table &tab,
                             const lora_segments &segs, cudaStream_t stream);
+// n_proj projections reading the same x in the same two launches (tables
+// share d_in and the adapter count); H_save may be null, or hold null entries.
+// ws: n_proj * decode_workspace_bytes(T, largest r_max) bytes.
+lora_status_t tc_decode_multi(int32_t n_proj, void *const *y, float *const *H_save, const void *x, void *ws,
+                              const lora_adapter_table *tabs, const lora_segments &segs, cudaStream_t stream);
 
 // Base projection plus packed delta in one persistent launch (segment-sorted
 // batches): y = x W^T + s_i (x A_i^T) B_i^T, H (fp32, may be null) = x A_i^T.

@@ -451,6 +451,89 @@ def time_decode(dev, stream, reps: int = 50):
     return out
 
 
+QWEN3_4B_SHARED_X = {"qkv": ((4096, 1024, 1024), 32), "gate_up": ((9728, 9728), 32)}
+
+
+def time_decode_multi(dev, stream, reps: int = 50) -> dict:
+    """A decode layer's projections that read the same x (Qwen3-4B: hidden
+    2560 -> q 4096 / k 1024 / v 1024, and -> gate / up 9728), 256 one-token
+    requests over 8 adapters of rank 32: one lora_multi_fwd call against one
+    lora_packed_fwd call per projection, each replayed from a CUDA graph over
+    rotating buffer sets larger than 3x L2 (as in time_decode)."""
+    import torch
+
+    import adapter_sgmv_gb300 as lora
+
+    hbm, _, _ = measured_peaks()
+    out = {}
+    base = wl.decode(0)  # ids: one token per request, adapter uniform over 8
+    ids = torch.from_numpy(base.ids).to(dev)
+    segs = lora.lora_build_segments(ids=ids, n_adapters=base.n_adapters)
+    for name, (d_outs, r) in QWEN3_4B_SHARED_X.items():
+        specs = [wl.Spec(f"{name}{p}", 2560, d, np.full(8, r, np.int32), np.full(8, 2.0 * r), base.ids, False,
+                         seed=p, with_bwd=False) for p, d in enumerate(d_outs)]
+        nbytes = sum(decode_bytes(s) for s in specs) - (len(specs) - 1) * 2 * base.n_tokens * 2560
+        n_sets = max(2, int(3 * L2_BYTES / nbytes) + 1)
+        sets = []
+        for q in range(n_sets):
+            x = None
+            tabs, ys, wss = [], [], []
+            for p, s in enumerate(specs):
+                s_q = wl.Spec(s.name, s.d_in, s.d_out, s.ranks, s.alphas, s.ids, False, seed=100 * q + p,
+                              with_bwd=False)
+                inp = wl.device_inputs(s_q, dev, y0="randn", need=("A", "B", "x", "y0"))
+                x = inp["x"] if x is None else x
+                tabs.append(lora.AdapterTable(inp["A"], inp["B"], s.ranks.tolist(), torch.from_numpy(s.scales),
+                                              s.d_in, s.d_out))
+                ys.append(inp["y0"])
+                wss.append(lora.workspace(tabs[-1], s.n_tokens, dev))
+            ws_m = torch.empty(lora.lora_multi_workspace_bytes(tabs, base.n_tokens), dtype=torch.uint8, device=dev)
+            sets.append((x, tabs, ys, wss, ws_m))
+
+        def multi(k):
+            x, tabs, ys, _, ws_m = sets[k % n_sets]
+            lora.lora_multi_fwd(ys, None, x, tabs, segs, ws_m, stream=stream)
+
+        def separate(k):
+            x, tabs, ys, wss, _ = sets[k % n_sets]
+            for tab, y, ws in zip(tabs, ys, wss):
+                lora.lora_packed_fwd(y, None, x, tab, segs, ws, stream=stream)
+
+        res = {}
+        for label, fn in (("multi", multi), ("separate", separate)):
+            with torch.cuda.stream(stream):
+                for k in range(n_sets):
+                    fn(k)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for k in range(reps):
+                    fn(k)
+            times = []
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    g.replay()
+                torch.cuda.synchronize()
+                for _ in range(20):
+                    s0 = torch.cuda.Event(enable_timing=True)
+                    s1 = torch.cuda.Event(enable_timing=True)
+                    s0.record(stream)
+                    g.replay()
+                    s1.record(stream)
+                    s1.synchronize()
+                    times.append(s0.elapsed_time(s1) / reps)
+            res[label] = statistics.median(times)
+            del g
+        gbs = nbytes / (res["multi"] * 1e-3) / 1e9
+        out[name] = {"projections": [f"2560x{d}" for d in d_outs], "us_per_call": round(res["multi"] * 1e3, 3),
+                     "us_separate_calls": round(res["separate"] * 1e3, 3),
+                     "speedup": round(res["separate"] / res["multi"], 3), "bytes": nbytes, "GB/s": round(gbs, 1),
+                     "frac_of_hbm": round(gbs / hbm, 4)}
+        del sets
+        torch.cuda.empty_cache()
+    return out
+
+
 def time_adamw(spec: wl.Spec, dev, stream, reps: int = 20) -> dict:
     """The fused per-adapter AdamW step (masters, moments, bf16 refresh) on
     the workload's adapter table, rotating over enough buffer sets to exceed
@@ -618,7 +701,8 @@ def run_ours(args, rank, world, dev):
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)
     if args.decode_only:  # the decode measurement alone (profiling runs)
-        return {"decode_sgmv": time_decode(dev, stream)} if rank == 0 else None
+        return ({"decode_sgmv": time_decode(dev, stream), "decode_multi_projection": time_decode_multi(dev, stream)}
+                if rank == 0 else None)
     spec = wl.packed4096(tokens_per_adapter=args.tokens_per_adapter)
     work = Workload(spec, dev)
     torch.cuda.synchronize()
@@ -675,6 +759,7 @@ def run_ours(args, rank, world, dev):
 
     e2e_ms, h2d, d2h = time_e2e(work, max(3, args.steps // 2), 2, stream) if not args.no_e2e else (None, 0, 0)
     decode = time_decode(dev, stream) if rank == 0 and not args.no_decode else None
+    decode_multi = time_decode_multi(dev, stream) if rank == 0 and not args.no_decode else None
     others = None
     if rank == 0 and not args.no_sweep:
         del work
@@ -722,6 +807,7 @@ def run_ours(args, rank, world, dev):
         "gpu_launches": kernels_per_step(spec) * args.steps,
         "clocks": clk.summary(),
         "decode_sgmv": decode,
+        "decode_multi_projection": decode_multi,
         "adamw_step": adamw,
         "fused_base_lora": fused,
         "other_workloads": others,
