@@ -23,7 +23,7 @@ __all__ = [
     "lora_segments_bytes", "lora_build_segments", "lora_workspace_bytes", "lora_sgmv_shrink",
     "lora_sgmv_expand", "lora_packed_fwd", "lora_packed_bwd", "lora_packed_fwd_marked", "lora_packed_bwd_marked",
     "lora_packed_bwd_noalloc", "lora_adamw_step", "lora_fused_base_workspace_bytes", "lora_fused_base_fwd",
-    "lora_multi_workspace_bytes", "lora_multi_fwd",
+    "lora_multi_workspace_bytes", "lora_multi_fwd", "lora_plan_pack",
     "lora_query_status", "lora_reset_status",
     "STATUS",
 ]
@@ -54,6 +54,23 @@ class c_segments(ctypes.Structure):
                 ("tiles", ctypes.c_void_p), ("n_tiles", ctypes.c_void_p), ("status", ctypes.c_void_p),
                 ("scratch", ctypes.c_void_p), ("scratch_words", ctypes.c_int64), ("max_spans", ctypes.c_int32),
                 ("reserved", ctypes.c_int32), ("spans", ctypes.c_void_p), ("n_spans", ctypes.c_void_p)]
+
+
+class c_plan_config(ctypes.Structure):
+    _fields_ = [("rank", ctypes.c_int32), ("tokens_per_step", ctypes.c_int32), ("steps", ctypes.c_int64),
+                ("mem_bytes", ctypes.c_int64)]
+
+
+class c_plan_cost(ctypes.Structure):
+    _fields_ = [("step_overhead_s", ctypes.c_double), ("base_s_per_token", ctypes.c_double),
+                ("lora_s_per_token", ctypes.c_double), ("lora_s_per_token_rank", ctypes.c_double),
+                ("gpu_mem_bytes", ctypes.c_int64), ("job_mem_bytes", ctypes.c_int64),
+                ("mem_unit_bytes", ctypes.c_int64), ("n_gpus", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class c_plan_job(ctypes.Structure):
+    _fields_ = [("gpu", ctypes.c_int32), ("n_configs", ctypes.c_int32), ("start_s", ctypes.c_double),
+                ("duration_s", ctypes.c_double), ("step_s", ctypes.c_double)]
 
 
 _lib = None
@@ -88,6 +105,9 @@ SIGNATURES = {
     "lora_fused_base_workspace_bytes": (_SZ, [ctypes.POINTER(c_table), _I32]),
     "lora_fused_base_fwd": (_I32, [_P, _P, _P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments), _P, _SZ,
                                    _P]),
+    "lora_plan_pack": (_I32, [ctypes.POINTER(c_plan_config), _I32, ctypes.POINTER(c_plan_cost),
+                              ctypes.POINTER(_I32), ctypes.POINTER(c_plan_job), ctypes.POINTER(_I32),
+                              ctypes.POINTER(ctypes.c_double)]),
     "lora_query_status": (_I32, [ctypes.POINTER(c_segments), _P]),
     "lora_reset_status": (_I32, [ctypes.POINTER(c_segments), _P]),
 }
@@ -367,6 +387,29 @@ def lora_fused_base_fwd(y, H_save, x, W, table: AdapterTable, segs: Segments, ws
     _check(lib().lora_fused_base_fwd(_ptr(y), _ptr(H_save), _ptr(x), _ptr(W), ctypes.byref(table.c),
                                      ctypes.byref(segs.c), _ptr(ws), wsb, _stream(stream)), "lora_fused_base_fwd")
     return y
+
+
+def lora_plan_pack(configs, cost: dict) -> dict:
+    """Packing planner (host).  configs: sequence of dicts with rank,
+    tokens_per_step, steps, mem_bytes; cost: dict with the lora_plan_cost
+    fields.  Returns {"job_of": [...], "jobs": [{gpu, n_configs, start_s,
+    duration_s, step_s}, ...], "makespan_s": float}."""
+    n = len(configs)
+    arr = (c_plan_config * n)(*[c_plan_config(int(c["rank"]), int(c["tokens_per_step"]), int(c["steps"]),
+                                              int(c["mem_bytes"])) for c in configs])
+    cc = c_plan_cost(float(cost.get("step_overhead_s", 0.0)), float(cost.get("base_s_per_token", 0.0)),
+                     float(cost.get("lora_s_per_token", 0.0)), float(cost.get("lora_s_per_token_rank", 0.0)),
+                     int(cost["gpu_mem_bytes"]), int(cost.get("job_mem_bytes", 0)),
+                     int(cost.get("mem_unit_bytes", 1 << 20)), int(cost.get("n_gpus", 1)), 0)
+    job_of = (_I32 * n)()
+    jobs = (c_plan_job * n)()
+    nj = _I32(0)
+    mk = ctypes.c_double(0.0)
+    _check(lib().lora_plan_pack(arr, n, ctypes.byref(cc), job_of, jobs, ctypes.byref(nj), ctypes.byref(mk)),
+           "lora_plan_pack")
+    return {"job_of": list(job_of), "makespan_s": mk.value,
+            "jobs": [{"gpu": j.gpu, "n_configs": j.n_configs, "start_s": j.start_s, "duration_s": j.duration_s,
+                      "step_s": j.step_s} for j in jobs[:nj.value]]}
 
 
 def lora_query_status(segs: Segments, stream=None) -> int:

@@ -337,6 +337,63 @@ LORA_API lora_status_t lora_fused_base_fwd(void *y, float *H_save, const void *x
                                            void *ws, size_t ws_bytes, lora_stream_t stream);
 
 /*
+ * Packing planner (host only, no GPU work): group LoRA fine-tuning
+ * configurations into packed jobs and place the jobs on a pool of GPUs
+ * (PLoRA technical summary, "1. LoRA Packing Planner (Offline)": minimise the
+ * completion time of a set of configurations on a fixed pool, a 0-1 knapsack
+ * variant solved round by round, with a cost model for memory and throughput).
+ * Cost model: a job step of the packed set S takes
+ *     t(S) = step_overhead_s + sum_{c in S} tokens_per_step_c * w_c,
+ *     w_c  = base_s_per_token + lora_s_per_token + lora_s_per_token_rank * rank_c
+ * and the job runs max_{c in S} steps_c steps.  Each round makes the next job
+ * from the configurations not yet placed: the set whose memory fits one GPU
+ * (job_mem_bytes + sum of mem_bytes, counted in whole mem_unit_bytes units,
+ * each configuration's size rounded up) and that trains the most tokens per
+ * second, sum_c steps_c tokens_per_step_c / (max_c steps_c * t(S)), found
+ * exactly (Dinkelbach iterations over 0-1 knapsacks).  Jobs are then placed
+ * longest first, each on the GPU that frees first (lowest index on ties); a
+ * job uses one GPU.
+ *   configs    n_configs entries (host); n_configs in [1, 4096]
+ *   job_of     out, host int32 [n_configs]: the job of every configuration
+ *              (jobs numbered in the order the rounds made them)
+ *   jobs       out, host array with room for n_configs jobs
+ *   n_jobs     out: jobs made;  makespan_s  out: predicted completion time
+ * Errors: LORA_ERR_INVALID_ARG (NULL, negative cost terms, a zero-time step),
+ * LORA_ERR_SHAPE (a configuration that does not fit one GPU alone, sizes out
+ * of range, a memory budget of more than 2^20 units).
+ */
+typedef struct lora_plan_config {
+    int32_t rank;             /* LoRA rank */
+    int32_t tokens_per_step;  /* tokens of its batch in every training step */
+    int64_t steps;            /* training steps it needs */
+    int64_t mem_bytes;        /* device memory it adds to a job (adapter state, optimizer, activations) */
+} lora_plan_config;
+
+typedef struct lora_plan_cost {
+    double step_overhead_s;        /* fixed time of one job step */
+    double base_s_per_token;       /* frozen base model, forward + backward, per token */
+    double lora_s_per_token;       /* LoRA path per token, rank-independent part */
+    double lora_s_per_token_rank;  /* LoRA path per token and unit of rank */
+    int64_t gpu_mem_bytes;         /* memory of one GPU */
+    int64_t job_mem_bytes;         /* memory of every job besides its configurations */
+    int64_t mem_unit_bytes;        /* granularity of the memory budget */
+    int32_t n_gpus;                /* GPUs in the pool */
+    int32_t reserved;
+} lora_plan_cost;
+
+typedef struct lora_plan_job {
+    int32_t gpu;        /* GPU of the pool the job runs on */
+    int32_t n_configs;  /* configurations packed into it */
+    double start_s;     /* predicted start */
+    double duration_s;  /* predicted duration: steps x step time */
+    double step_s;      /* predicted time of one step */
+} lora_plan_job;
+
+LORA_API lora_status_t lora_plan_pack(const lora_plan_config *configs, int32_t n_configs,
+                                      const lora_plan_cost *cost, int32_t *job_of, lora_plan_job *jobs,
+                                      int32_t *n_jobs, double *makespan_s);
+
+/*
  * Packed backward without a workspace, for callers that cannot allocate device
  * memory (no cudaMalloc, no allocator of their own to draw scratch from).  The
  * pages have no counterpart to this call; it exists only for such callers.
