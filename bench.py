@@ -647,6 +647,70 @@ def time_fused_base(spec: wl.Spec, dev, stream, reps: int = 10) -> dict:
     return out
 
 
+def packing_plan(spec: wl.Spec, ms_step: float, fused: dict | None, dev, stream) -> dict | None:
+    """The packing planner (lora_plan_pack) on a PLoRA-sized search space, its
+    cost model taken from this run's measurements of one 4096 -> 4096
+    projection: the LoRA path's time per token from the packed step above
+    (its rank term from the step's algorithmic bytes, 8 B per token and unit
+    of rank, at the measured bandwidth), the fixed time of a step from the
+    intercept against a 1024-token step of the same workload, and the frozen
+    base's time per token from cuBLAS (forward GEMM + input-gradient GEMM,
+    2x the base GEMM measured beside the fused layer).  The model: 32 layers
+    x 7 such projections (a 7B-class dense model, 4096 wide), frozen bf16
+    weights 14 GB + 4 GB of workspace per job; 120 configurations = ranks
+    {8..128} x tokens per step {1024..8192} x 6 learning rates (the rate does
+    not change the cost), each trained on 20 M tokens; 8 GPUs of 280 GB."""
+    import torch
+
+    import adapter_sgmv_gb300 as lora
+
+    if fused is None:
+        return None
+    T = spec.n_tokens
+    small = Workload(wl.packed4096(tokens_per_adapter=128), dev)  # T = 1024
+    start, end, _, _ = time_steps(small, 10, 3, stream)
+    torch.cuda.synchronize()
+    ms_small = start.elapsed_time(end) / 10
+    del small
+    per_tok = ms_step * 1e-3 / T
+    sb = step_bytes(spec)
+    gbs = (sb["fwd"] + sb["bwd"]) / (ms_step * 1e-3)
+    rank_coef = 8.0 / gbs
+    counts = np.bincount(spec.ids, minlength=spec.n_adapters)
+    mean_rank = float((counts * spec.ranks).sum()) / T
+    proj = 32 * 7  # projections per model step
+    cost = {"step_overhead_s": proj * max(0.0, ms_small * 1e-3 - 1024 * per_tok),
+            "base_s_per_token": proj * 2 * fused["cublas_base_ms"] * 1e-3 / T,
+            "lora_s_per_token": proj * (per_tok - mean_rank * rank_coef),
+            "lora_s_per_token_rank": proj * rank_coef,
+            "gpu_mem_bytes": 280 << 30, "job_mem_bytes": 18 << 30, "mem_unit_bytes": 64 << 20, "n_gpus": 8}
+    configs = []
+    for r in (8, 16, 32, 64, 128):
+        for tok in (1024, 2048, 4096, 8192):
+            for _ in range(6):
+                mem = proj * r * 8192 * 18 + tok * 4096 * 2 * 32 * 12  # adapter state (bf16, fp32 master,
+                configs.append({"rank": r, "tokens_per_step": tok, "steps": 20_000_000 // tok,  # moments, grad)
+                                "mem_bytes": mem})                                                # + activations
+    t0 = time.perf_counter()
+    plan = lora.lora_plan_pack(configs, cost)
+    plan_ms = (time.perf_counter() - t0) * 1e3
+    w = lambda c: cost["base_s_per_token"] + cost["lora_s_per_token"] + cost["lora_s_per_token_rank"] * c["rank"]
+    alone = sorted((c["steps"] * (cost["step_overhead_s"] + c["tokens_per_step"] * w(c)) for c in configs),
+                   reverse=True)
+    free = [0.0] * cost["n_gpus"]
+    for d in alone:  # one configuration per job, longest first on the GPU that frees first
+        g = min(range(len(free)), key=lambda q: (free[q], q))
+        free[g] += d
+    sizes = [j["n_configs"] for j in plan["jobs"]]
+    return {"configs": len(configs), "gpus": cost["n_gpus"], "jobs": len(plan["jobs"]),
+            "configs_per_job": [min(sizes), max(sizes)], "makespan_h": round(plan["makespan_s"] / 3600, 3),
+            "one_config_per_job_makespan_h": round(max(free) / 3600, 3),
+            "speedup_vs_one_config_per_job": round(max(free) / plan["makespan_s"], 3),
+            "planner_ms": round(plan_ms, 1),
+            "cost_model": {k: (float(f"{v:.4g}") if isinstance(v, float) else v) for k, v in cost.items()},
+            "small_step_ms": round(ms_small, 4)}
+
+
 def cpu_baseline(spec: wl.Spec, target_s: float = 10.0):
     """The fp64 oracle on a bounded sample of the same workload (first tokens of
     every adapter), on this host's cores; tokens/s."""
@@ -773,6 +837,7 @@ def run_ours(args, rank, world, dev):
         others["skewed4096x14336_N32"] = time_config(wl.skewed(), dev, stream)
     adamw = time_adamw(spec, dev, stream) if rank == 0 else None
     fused = time_fused_base(spec, dev, stream) if rank == 0 and not args.no_fused else None
+    plan = packing_plan(spec, ms_step, fused, dev, stream) if rank == 0 and not args.no_plan else None
     cpu = cpu_baseline(spec, args.cpu_seconds) if rank == 0 and not args.no_cpu else None
 
     if rank != 0:
@@ -810,6 +875,7 @@ def run_ours(args, rank, world, dev):
         "decode_multi_projection": decode_multi,
         "adamw_step": adamw,
         "fused_base_lora": fused,
+        "packing_plan": plan,
         "other_workloads": others,
         "cpu_baseline": cpu,
     }
@@ -870,6 +936,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="skip the adapter-count sweep and the skewed batch")
     ap.add_argument("--no-fused", action="store_true", help="skip the fused base + delta layer forward")
+    ap.add_argument("--no-plan", action="store_true", help="skip the packing planner run")
     ap.add_argument("--decode-only", action="store_true", help="time only the decode batch (profiling runs)")
     ap.add_argument("--tokens-per-adapter", type=int, default=4096,
                     help="tokens per adapter of the packed batch (4096 is the benchmarked workload; "
