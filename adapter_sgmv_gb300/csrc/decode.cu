@@ -19,7 +19,11 @@
 // The expand kernel is launched as a programmatic dependent of the shrink: its
 // CTAs start while the shrink runs and fetch their B_i^T block and the y rows
 // they update (inputs the shrink does not write) before waiting for the shrink
-// grid to complete; h is then read from L2.
+// grid to complete; h is then read from L2.  The shrink is itself launched as
+// a programmatic dependent of whatever precedes it on the stream: back-to-back
+// decode calls (the layers of a decode step) overlap one call's routing reads
+// and weight prefetch with the previous call's expand, and wait for it before
+// reading x or writing h.
 //
 // Several projections that read the same x (q / k / v, gate / up) go through
 // the same two launches: blockIdx.y selects the projection, each with its own
@@ -236,6 +240,10 @@ __global__ void __launch_bounds__(kThreads, 2) dec_shrink_kernel(const uint16_t 
         if (c < nchunks) load_a(c, c);
     if (threadIdx.x < rows16) tok[threadIdx.x] = (int)threadIdx.x < rows ? D.my_tok : -1;
     __syncthreads();
+    // launched as a programmatic dependent of the previous call's expand: the
+    // routing and the weights above are not written by it, but x may be its
+    // output and the h buffer its input, so everything past here waits for it
+    pdl_wait();
     for (int c = 0; c < stages - 1; ++c) {
         if (c < nchunks) load_x(c, c);
         cp_async_commit();
@@ -356,6 +364,7 @@ __global__ void __launch_bounds__(kThreads, 2) dec_shrink_kernel(const uint16_t 
 __global__ void __launch_bounds__(kThreads, 2) dec_expand_kernel(const __grid_constant__ ProjSet ps, Geom g,
                                                               lora_segments segs)
 {
+    pdl_launch_dependents();  // a following decode call may start its own prologue
     const int32_t ti = blockIdx.x / g.ns, nsl = blockIdx.x % g.ns;
     const lora_adapter_table &tab = ps.tab[blockIdx.y];
     uint16_t *__restrict__ y = ps.y[blockIdx.y];
@@ -520,13 +529,15 @@ lora_status_t tc_decode_multi(int32_t n_proj, void *const *y, float *const *H_sa
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = s1;
         cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = (unsigned)g.ks;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlaps the previous call's tail
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 2;
         if (cudaLaunchKernelEx(&cfg, dec_shrink_kernel, static_cast<const uint16_t *>(x), ps, g, segs) != cudaSuccess)
             return LORA_ERR_CUDA;
     }
