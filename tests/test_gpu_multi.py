@@ -108,3 +108,12 @@ def test_multi_rejects_mismatched_tables():
     with pytest.raises(lora.LoraError) as e:
         lora.lora_multi_fwd([y0[0]] * 9, None, x, [tables[0]] * 9, segs, ws)
     assert e.value.status == 2  # more than LORA_MAX_PROJECTIONS
+
+
+def test_attention_projections_low_rank():
+    # ranks <= 32: the decode buffers sized for a rank-padded 32
+    ids = np.random.default_rng(8).integers(0, 8, 256).astype(np.int32)
+    specs = [_projection("q", 4096, [32, 16, 8, 32, 24, 32, 16, 8], ids, seed=11),
+             _projection("k", 1024, [8, 16, 32, 8, 16, 32, 8, 16], ids, seed=12),
+             _projection("v", 1024, [32] * 8, ids, seed=13)]
+    _check(specs)
