@@ -754,6 +754,17 @@ def cpu_baseline(spec: wl.Spec, target_s: float = 10.0):
             "one_thread": {"value": round(n1 / dt1, 2), "sample": f"{n1} tokens, {dt1:.1f} s"}}
 
 
+def max_over_ranks(ms: float, device) -> float:
+    """The slowest rank's time (every rank gets it): the job's clock when the
+    replicas run side by side."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(ms)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_ours(args, rank, world, dev):
     import torch
     import torch.distributed as dist
@@ -793,9 +804,7 @@ def run_ours(args, rank, world, dev):
     t_fwd = [e[1].elapsed_time(e[2]) for e in ev]
     t_bwd = [e[2].elapsed_time(e[3]) for e in ev]
     if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, dev)
     ms_step = total_ms / args.steps
     T = spec.n_tokens
     value = world * T * args.steps / (total_ms * 1e-3)
