@@ -112,11 +112,8 @@ double best_with_leader(const std::vector<Item> &items, const std::vector<int> &
     return N / D;
 }
 
-}  // namespace
-
-extern "C" LORA_API lora_status_t lora_plan_pack(const lora_plan_config *configs, int32_t n_configs,
-                                                 const lora_plan_cost *cost, int32_t *job_of, lora_plan_job *jobs,
-                                                 int32_t *n_jobs, double *makespan_s)
+lora_status_t plan_pack(const lora_plan_config *configs, int32_t n_configs, const lora_plan_cost *cost,
+                        int32_t *job_of, lora_plan_job *jobs, int32_t *n_jobs, double *makespan_s)
 {
     if (configs == nullptr || cost == nullptr || job_of == nullptr || jobs == nullptr || n_jobs == nullptr ||
         makespan_s == nullptr)
@@ -130,6 +127,8 @@ extern "C" LORA_API lora_status_t lora_plan_pack(const lora_plan_config *configs
     const int64_t cap64 = budget / cost->mem_unit_bytes;
     if (cap64 > (1 << 20)) return LORA_ERR_SHAPE;  // the knapsack table would be too large: use a coarser unit
     const int32_t cap = (int32_t)cap64;
+    // the knapsack's choice table holds n_configs x (budget + 1) bytes
+    if ((int64_t)n_configs * (cap64 + 1) > (int64_t(1) << 28)) return LORA_ERR_SHAPE;
     const double t0 = cost->step_overhead_s;
 
     std::vector<Item> items(n_configs);
@@ -200,4 +199,19 @@ extern "C" LORA_API lora_status_t lora_plan_pack(const lora_plan_config *configs
     *n_jobs = nj;
     *makespan_s = makespan;
     return LORA_OK;
+}
+
+}  // namespace
+
+// The planner is host code: any allocation failure is reported as a status,
+// never thrown across the C boundary.
+extern "C" LORA_API lora_status_t lora_plan_pack(const lora_plan_config *configs, int32_t n_configs,
+                                                 const lora_plan_cost *cost, int32_t *job_of, lora_plan_job *jobs,
+                                                 int32_t *n_jobs, double *makespan_s)
+{
+    try {
+        return plan_pack(configs, n_configs, cost, job_of, jobs, n_jobs, makespan_s);
+    } catch (...) {
+        return LORA_ERR_SHAPE;
+    }
 }

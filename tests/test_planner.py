@@ -137,3 +137,11 @@ def test_planner_rejects_a_config_larger_than_a_gpu():
     with pytest.raises(lora.LoraError) as e:
         lora.lora_plan_pack([cfg(8, 1024, 10, 61 * GB)], cost)
     assert e.value.status == 2
+
+
+def test_planner_rejects_a_knapsack_table_too_large():
+    # 4096 configurations over a 2^20-unit budget would need a 4 GB choice table
+    cost = {"gpu_mem_bytes": (1 << 20) * 1024, "mem_unit_bytes": 1024, "base_s_per_token": 1e-5}
+    with pytest.raises(lora.LoraError) as e:
+        lora.lora_plan_pack([cfg(8, 1024, 10, 4096)] * 4096, cost)
+    assert e.value.status == 2
