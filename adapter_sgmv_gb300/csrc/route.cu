@@ -227,6 +227,85 @@ __global__ void route_tiles_kernel(const int32_t *__restrict__ offs, int32_t n_c
     emit_pieces(seg_start, N, perm, LORA_SPAN_TOKENS, s.spans, s.n_spans, s.max_spans, base);
 }
 
+// ---------------------------------------------------------------- sorted input, one launch
+// For tokens already grouped by adapter the permutation is the identity and
+// every piece is a run of consecutive tokens, so the whole builder is one
+// launch: block 0 (1024 threads) resets the status word, checks the offsets,
+// and cuts the tiles and spans with the per-adapter piece bases kept in shared
+// memory; the other blocks write perm[t] = t.  Used when N + 1 offsets fit the
+// shared-memory table (kSortedSmemAdapters).
+constexpr int32_t kSortedSmemAdapters = 4095;  // two tables of N + 1 ints: 32 KB of static shared memory
+
+__device__ void emit_sorted_pieces(const int32_t *off, int32_t N, int32_t len, int32_t *out, int32_t *n_out,
+                                   int32_t max_out, int32_t *base)
+{
+    int32_t carry = 0;
+    for (int32_t i0 = 0; i0 < N; i0 += blockDim.x) {
+        const int32_t i = i0 + threadIdx.x;
+        const int32_t n = i < N ? off[i + 1] - off[i] : 0;
+        const int32_t cnt = n > 0 ? (n + len - 1) / len : 0;
+        int32_t tot;
+        const int32_t e = block_exclusive_scan(cnt, &tot);
+        if (i < N) base[i] = carry + e;
+        carry += tot;
+    }
+    if (threadIdx.x == 0) base[N] = carry;
+    __syncthreads();
+    const int32_t total = min(carry, max_out);
+    for (int32_t q = threadIdx.x; q < total; q += blockDim.x) {
+        int32_t lo = 0, hi = N;
+        while (hi - lo > 1) {
+            const int32_t mid = (lo + hi) >> 1;
+            if (base[mid] <= q) lo = mid;
+            else hi = mid;
+        }
+        const int32_t j = q - base[lo];
+        const int32_t b = off[lo] + j * len;
+        const int32_t rows = min(len, off[lo + 1] - off[lo] - j * len);
+        reinterpret_cast<int4 *>(out)[q] = make_int4(lo, b, rows, 1);
+    }
+    if (threadIdx.x == 0) *n_out = total;
+    __syncthreads();  // base is reused by the next call
+}
+
+__global__ void __launch_bounds__(1024) route_sorted_one_kernel(const int32_t *__restrict__ seg_offsets, int32_t T,
+                                                                int32_t N, lora_segments s)
+{
+    if (blockIdx.x > 0) {
+        const int64_t stride = (int64_t)(gridDim.x - 1) * blockDim.x;
+        for (int64_t t = (blockIdx.x - 1) * (int64_t)blockDim.x + threadIdx.x; t < T; t += stride)
+            s.perm[t] = (int32_t)t;
+        return;
+    }
+    __shared__ int32_t off[kSortedSmemAdapters + 1];
+    __shared__ int32_t base[kSortedSmemAdapters + 1];
+    __shared__ int bad;
+    if (threadIdx.x == 0) bad = 0;
+    __syncthreads();
+    for (int32_t i = threadIdx.x; i <= N; i += blockDim.x) {
+        const int32_t v = seg_offsets[i];
+        off[i] = v;
+        if ((i == 0 && v != 0) || (i == N && v != T) || v < 0 || v > T) bad = 1;
+    }
+    __syncthreads();
+    for (int32_t i = threadIdx.x; i < N; i += blockDim.x)
+        if (off[i + 1] < off[i]) bad = 1;
+    __syncthreads();
+    if (bad) {  // inconsistent segments: no work, the status says why
+        for (int32_t i = threadIdx.x; i <= N; i += blockDim.x) s.seg_start[i] = 0;
+        if (threadIdx.x == 0) {
+            *s.status = LORA_ERR_BAD_SEGMENTS;
+            *s.n_tiles = 0;
+            *s.n_spans = 0;
+        }
+        return;
+    }
+    if (threadIdx.x == 0) *s.status = LORA_OK;
+    for (int32_t i = threadIdx.x; i <= N; i += blockDim.x) s.seg_start[i] = off[i];
+    emit_sorted_pieces(off, N, LORA_TILE_M, s.tiles, s.n_tiles, s.max_tiles, base);
+    emit_sorted_pieces(off, N, LORA_SPAN_TOKENS, s.spans, s.n_spans, s.max_spans, base);
+}
+
 // ---------------------------------------------------------------- host side
 SegLayout seg_layout(int32_t T, int32_t N)
 {
@@ -279,6 +358,14 @@ lora_status_t build_segments(const int32_t *ids, const int32_t *seg_offsets, int
     s.spans = w + L.off_spans;
     s.n_spans = w + L.off_nspans;
 
+    if (seg_offsets != nullptr && N <= kSortedSmemAdapters) {
+        const int64_t perm_blocks = ((int64_t)T + 1023) / 1024;
+        const int blocks = 1 + (int)(perm_blocks < 296 ? perm_blocks : 296);
+        route_sorted_one_kernel<<<blocks, 1024, 0, stream>>>(seg_offsets, T, N, s);
+        if (cudaGetLastError() != cudaSuccess) return LORA_ERR_CUDA;
+        *out = s;
+        return LORA_OK;
+    }
     if (cudaMemsetAsync(s.status, 0, 4, stream) != cudaSuccess) return LORA_ERR_CUDA;
     if (seg_offsets != nullptr) {
         const int threads = 256;

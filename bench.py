@@ -230,7 +230,7 @@ class Workload:
 
 def kernels_per_step(spec: wl.Spec) -> int:
     """Kernels the library launches per step (builder + forward + backward)."""
-    build = 2 if spec.sorted else 6
+    build = 1 if spec.sorted and spec.n_adapters <= 4095 else 6  # sorted offsets: one launch
     return build + 2 + 4
 
 
