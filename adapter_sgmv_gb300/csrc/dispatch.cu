@@ -55,7 +55,7 @@ void mark(Marks *m, cudaStream_t stream)
 constexpr int kMaxDevices = 64;
 struct Side {
     cudaStream_t s[2];
-    cudaEvent_t ev[3];
+    cudaEvent_t ev[4];
     bool ready;
 };
 Side g_side[kMaxDevices];
@@ -146,29 +146,35 @@ lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void
         return LORA_ERR_CUDA;
     if (dA != nullptr && cudaMemsetAsync(dA, 0, (size_t)tab.sum_r * tab.d_in * sizeof(float), stream) != cudaSuccess)
         return LORA_ERR_CUDA;
-    lora_status_t st;
-    if (H_saved == nullptr) {
-        st = marked(marks, stream, [&] { return tc_shrink(X, tab, segs, nullptr, hb, nullptr, rw, stream); });
-        if (st == LORA_OK)
-            st = marked(marks, stream, [&] { return tc_dh(dY, tab, segs, dhb, nullptr, nullptr, rw, stream); });
-    } else {
-        st = marked(marks, stream, [&] { return tc_dh(dY, tab, segs, dhb, H_saved, hb, rw, stream); });
-    }
-    if (st != LORA_OK) return st;
-    // dB, dA and dX read only what the steps above wrote: fork them
+    lora_status_t st = LORA_OK;
+    // dB needs only dY and the bf16 rows of H, so it runs beside case i (dh);
+    // dA and dX need dh.  Side stream B: [H to bf16], dB; the caller's stream:
+    // [the shrink, when H is not saved], dh, dX; side stream A: dA after dh.
+    // (a marked call runs everything one after another on the caller's
+    // stream, so that each event pair brackets one kernel alone)
     std::lock_guard<std::mutex> lock(g_side_mu);
-    // (a marked call runs them one after another on the caller's stream, so that
-    // each event pair brackets one kernel alone)
     Side *sd = (marks == nullptr && (dB != nullptr || dA != nullptr)) ? side_for_device() : nullptr;
     cudaStream_t sB = sd != nullptr ? sd->s[0] : stream, sA = sd != nullptr ? sd->s[1] : stream;
-    if (sd != nullptr) {
-        if (cudaEventRecord(sd->ev[0], stream) != cudaSuccess) return LORA_ERR_CUDA;
-        if ((dB != nullptr && cudaStreamWaitEvent(sB, sd->ev[0], 0) != cudaSuccess) ||
-            (dA != nullptr && cudaStreamWaitEvent(sA, sd->ev[0], 0) != cudaSuccess))
+    if (H_saved == nullptr)
+        st = marked(marks, stream, [&] { return tc_shrink(X, tab, segs, nullptr, hb, nullptr, rw, stream); });
+    if (st != LORA_OK) return st;
+    if (sd != nullptr && dB != nullptr) {  // fork B once the outputs are zeroed (and H recomputed)
+        if (cudaEventRecord(sd->ev[0], stream) != cudaSuccess || cudaStreamWaitEvent(sB, sd->ev[0], 0) != cudaSuccess)
             return LORA_ERR_CUDA;
     }
-    if (dB != nullptr) st = marked(marks, sB, [&] { return tc_db(dB, dY, hb, rw, tab, segs, sB); });
-    if (st == LORA_OK && dA != nullptr) st = marked(marks, sA, [&] { return tc_da(dA, X, dhb, rw, tab, segs, sA); });
+    if (dB != nullptr) {
+        if (H_saved != nullptr)
+            st = marked(marks, sB, [&] { return tc_h_to_bf16(H_saved, hb, rw, tab, segs, sB); });
+        if (st == LORA_OK) st = marked(marks, sB, [&] { return tc_db(dB, dY, hb, rw, tab, segs, sB); });
+        if (st != LORA_OK) return st;
+    }
+    st = marked(marks, stream, [&] { return tc_dh(dY, tab, segs, dhb, nullptr, nullptr, rw, stream); });
+    if (st != LORA_OK) return st;
+    if (sd != nullptr && dA != nullptr) {  // fork A after dh
+        if (cudaEventRecord(sd->ev[3], stream) != cudaSuccess || cudaStreamWaitEvent(sA, sd->ev[3], 0) != cudaSuccess)
+            return LORA_ERR_CUDA;
+    }
+    if (dA != nullptr) st = marked(marks, sA, [&] { return tc_da(dA, X, dhb, rw, tab, segs, sA); });
     if (st == LORA_OK && dX != nullptr)
         st = marked(marks, stream, [&] { return tc_dx(dX, dhb, rw, tab, segs, stream); });
     if (sd != nullptr) {  // join: the caller's stream waits for both side streams

@@ -46,6 +46,10 @@ lora_status_t tc_shrink(const void *x, const lora_adapter_table &tab, const lora
 lora_status_t tc_dh(const void *dY, const lora_adapter_table &tab, const lora_segments &segs, uint16_t *dh_bf16,
                     const float *h_saved, uint16_t *h_bf16, int32_t rw, cudaStream_t stream);
 
+// A saved fp32 H (by token) converted to the bf16 hand-off rows (by perm
+// position) that cases iii reads; the same values case i writes as its hi.
+lora_status_t tc_h_to_bf16(const float *H, uint16_t *hb, int32_t rw, const lora_adapter_table &tab,
+                           const lora_segments &segs, cudaStream_t stream);
 // case ii.  y += s_i B_i h from the bf16 hand-off buffers (lo may be null).
 lora_status_t tc_expand_bf16(void *y, const uint16_t *hi, const uint16_t *lo, int32_t rw,
                              const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream);

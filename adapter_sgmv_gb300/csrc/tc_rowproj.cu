@@ -326,6 +326,54 @@ lora_status_t launch_rowproj(const void *act, const void *w, int32_t d, const Ro
 
 }  // namespace
 
+namespace {
+
+// A saved fp32 H (by token, stride r_max) to the bf16 hand-off rows (by perm
+// position, stride rw, zero beyond each adapter's rank): one CTA per tile,
+// one thread per (row, 8 columns).  It runs beside case i (dh), so its CTAs
+// are kept small (1024-thread CTAs converted faster alone but crowded out dh's).
+__global__ void __launch_bounds__(256) h_to_bf16_kernel(const float *__restrict__ H, uint16_t *__restrict__ hb,
+                                                        int32_t rw, lora_adapter_table tab, lora_segments segs)
+{
+    const int32_t n_tiles = *segs.n_tiles;
+    const int32_t r_max = tab.r_max;
+    const bool vec = (r_max & 3) == 0 && (reinterpret_cast<uintptr_t>(H) & 15u) == 0;
+    for (int32_t ti = blockIdx.x; ti < n_tiles; ti += gridDim.x) {
+        const Tile T = load_tile(segs.tiles, ti);
+        const AdapterInfo ad = load_adapter(tab, T.adapter, nullptr);
+        const int32_t r = ad.ok ? ad.rank : 0;
+        for (int32_t i = threadIdx.x; i < T.rows * (rw / 8); i += blockDim.x) {
+            const int32_t m = i / (rw / 8), k = 8 * (i % (rw / 8));
+            const int64_t p = (int64_t)T.begin + m;
+            const float *src = H + (int64_t)segs.perm[p] * r_max;
+            float f[8];
+            if (vec && k + 8 <= r) {  // two 16-byte loads
+                const float4 a = __ldcs(reinterpret_cast<const float4 *>(src + k));
+                const float4 b = __ldcs(reinterpret_cast<const float4 *>(src + k + 4));
+                f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+                f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = k + e < r ? src[k + e] : 0.f;
+            }
+            *reinterpret_cast<uint4 *>(hb + p * rw + k) = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
+                                                                     pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+        }
+    }
+}
+
+}  // namespace
+
+lora_status_t tc_h_to_bf16(const float *H, uint16_t *hb, int32_t rw, const lora_adapter_table &tab,
+                           const lora_segments &segs, cudaStream_t stream)
+{
+    if (segs.n_tokens == 0 || segs.max_tiles == 0) return LORA_OK;
+    const int sms = sm_count();
+    const int grid = segs.max_tiles < 4 * sms ? segs.max_tiles : 4 * sms;
+    h_to_bf16_kernel<<<grid, 256, 0, stream>>>(H, hb, rw, tab, segs);
+    return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+}
+
 lora_status_t tc_shrink(const void *x, const lora_adapter_table &tab, const lora_segments &segs, float *H,
                         uint16_t *hi, uint16_t *lo, int32_t rw, cudaStream_t stream)
 {

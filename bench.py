@@ -53,8 +53,8 @@ def step_bytes(spec: wl.Spec) -> dict:
 
 # kernels of a step in launch order (forward, then backward with H saved), and
 # the kernel template each one runs
-STEP_KERNELS = (("shrink", "tc_rowproj"), ("expand", "tc_colproj"), ("dh", "tc_rowproj"), ("dB", "tc_tokred"),
-                ("dA", "tc_tokred"), ("dX", "tc_colproj"))
+STEP_KERNELS = (("shrink", "tc_rowproj"), ("expand", "tc_colproj"), ("hconv", "h_to_bf16"), ("dB", "tc_tokred"),
+                ("dh", "tc_rowproj"), ("dA", "tc_tokred"), ("dX", "tc_colproj"))
 
 
 def kernel_bytes(spec: wl.Spec) -> dict:
@@ -65,7 +65,9 @@ def kernel_bytes(spec: wl.Spec) -> dict:
     counts = np.bincount(spec.ids, minlength=spec.n_adapters)
     th = int((counts * spec.ranks).sum())           # sum_i T_i r_i
     r = int(spec.sum_r)
+    rw = 64 if spec.r_max <= 64 else 128
     return {"shrink": 2 * T * di + 2 * r * di + 4 * th, "expand": 4 * T * do + 2 * r * do + 4 * th,
+            "hconv": 4 * T * int(spec.r_max) + 2 * T * rw,
             "dh": 2 * T * do + 2 * r * do + 4 * th, "dB": 2 * T * do + 4 * th + 4 * r * do,
             "dA": 2 * T * di + 4 * th + 4 * r * di, "dX": 4 * T * di + 2 * r * di + 4 * th}
 
@@ -231,7 +233,7 @@ class Workload:
 def kernels_per_step(spec: wl.Spec) -> int:
     """Kernels the library launches per step (builder + forward + backward)."""
     build = 1 if spec.sorted and spec.n_adapters <= 4095 else 6  # sorted offsets: one launch
-    return build + 2 + 4
+    return build + 2 + 5  # forward: shrink, expand; backward: H to bf16, dB, dh, dA, dX
 
 
 def time_steps(work: Workload, steps: int, warmup: int, stream, per_kernel: bool = False):
@@ -875,7 +877,7 @@ def run_ours(args, rank, world, dev):
         "kernels_ms": per_kernel,
         "kernels_note": ("from a second pass of the same steps with an event pair around every kernel "
                          f"({round(mstart.elapsed_time(mend) / args.steps, 4)} ms per step with the pairs, "
-                         "where the backward's dB, dA and dX run one after another instead of side by side)"),
+                         "where the backward's kernels run one after another instead of dB next to dh and dA next to dX)"),
         "e2e": ({"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                  "d2h_bytes_per_step": d2h} if e2e_ms is not None else None),
         "gpu_launches": kernels_per_step(spec) * args.steps,

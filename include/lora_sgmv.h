@@ -235,10 +235,12 @@ LORA_API lora_status_t lora_packed_bwd(void *dX, float *dA, float *dB, const voi
  *   n_recorded  out, may be NULL: events recorded (2 x kernels launched)
  * Kernel order.  Forward: case i (shrink), case ii (expand); a batch of at
  * most 512 tokens gets one pair around its two decode launches.  Backward:
- * [case i shrink, when H_saved is NULL], case i (dh), case iii (dB, if
- * requested), case iv (dA, if requested), case ii (dX, if requested).  The
- * zeroing of dA / dB precedes the first pair.  The plain backward runs dB and
- * dA on two internal streams next to dX; the marked one runs all of its
+ * [case i shrink, when H_saved is NULL], [the bf16 copy of H_saved, when
+ * given and dB is requested], case iii (dB, if requested), case i (dh), case
+ * iv (dA, if requested), case ii (dX, if requested).  The
+ * zeroing of dA / dB precedes the first pair.  The plain backward runs dB (with
+ * the bf16 copy of H) on an internal stream next to dh, and dA on another
+ * next to dX; the marked one runs all of its
  * kernels one after another on `stream`, so that each pair brackets one
  * kernel alone.
  * Errors: those of the unmarked call; LORA_ERR_INVALID_ARG when n_events < 0

@@ -46,10 +46,10 @@ def test_marked_calls_match_plain_calls(T, fwd_kernels):
     dX2 = case.inp["dX0"].clone()
     dA2 = torch.full_like(dA1, float("nan"))
     dB2 = torch.full_like(dB1, float("nan"))
-    evb = _events(8)
+    evb = _events(10)
     nb = lora.lora_packed_bwd_marked(dX2, dA2, dB2, case.inp["dY"], case.inp["x"], H2, case.table, case.segs,
                                      case.ws, evb)
-    assert nb == 8  # dh, dB, dA, dX
+    assert nb == 10  # H to bf16, dB, dh, dA, dX
     torch.cuda.synchronize()
     assert lora.lora_query_status(case.segs) == 0
     for a, b in ((y1, y2), (H1, H2), (dX1, dX2), (dA1, dA2), (dB1, dB2)):
