@@ -155,35 +155,39 @@ lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void
     std::lock_guard<std::mutex> lock(g_side_mu);
     Side *sd = (marks == nullptr && (dB != nullptr || dA != nullptr)) ? side_for_device() : nullptr;
     cudaStream_t sB = sd != nullptr ? sd->s[0] : stream, sA = sd != nullptr ? sd->s[1] : stream;
+    // fork: the side stream waits for what the caller's stream has issued so far
+    auto fork = [&](cudaEvent_t ev, cudaStream_t side) {
+        return cudaEventRecord(ev, stream) == cudaSuccess && cudaStreamWaitEvent(side, ev, 0) == cudaSuccess;
+    };
+    bool forked_B = false, forked_A = false;
     if (H_saved == nullptr)
         st = marked(marks, stream, [&] { return tc_shrink(X, tab, segs, nullptr, hb, nullptr, rw, stream); });
-    if (st != LORA_OK) return st;
-    if (sd != nullptr && dB != nullptr) {  // fork B once the outputs are zeroed (and H recomputed)
-        if (cudaEventRecord(sd->ev[0], stream) != cudaSuccess || cudaStreamWaitEvent(sB, sd->ev[0], 0) != cudaSuccess)
-            return LORA_ERR_CUDA;
+    if (st == LORA_OK && sd != nullptr && dB != nullptr) {  // fork B once the outputs are zeroed (and H recomputed)
+        forked_B = fork(sd->ev[0], sB);
+        if (!forked_B) st = LORA_ERR_CUDA;
     }
-    if (dB != nullptr) {
+    if (st == LORA_OK && dB != nullptr) {
         if (H_saved != nullptr)
             st = marked(marks, sB, [&] { return tc_h_to_bf16(H_saved, hb, rw, tab, segs, sB); });
         if (st == LORA_OK) st = marked(marks, sB, [&] { return tc_db(dB, dY, hb, rw, tab, segs, sB); });
-        if (st != LORA_OK) return st;
     }
-    st = marked(marks, stream, [&] { return tc_dh(dY, tab, segs, dhb, nullptr, nullptr, rw, stream); });
-    if (st != LORA_OK) return st;
-    if (sd != nullptr && dA != nullptr) {  // fork A after dh
-        if (cudaEventRecord(sd->ev[3], stream) != cudaSuccess || cudaStreamWaitEvent(sA, sd->ev[3], 0) != cudaSuccess)
-            return LORA_ERR_CUDA;
+    if (st == LORA_OK)
+        st = marked(marks, stream, [&] { return tc_dh(dY, tab, segs, dhb, nullptr, nullptr, rw, stream); });
+    if (st == LORA_OK && sd != nullptr && dA != nullptr) {  // fork A after dh
+        forked_A = fork(sd->ev[3], sA);
+        if (!forked_A) st = LORA_ERR_CUDA;
     }
-    if (dA != nullptr) st = marked(marks, sA, [&] { return tc_da(dA, X, dhb, rw, tab, segs, sA); });
+    if (st == LORA_OK && dA != nullptr) st = marked(marks, sA, [&] { return tc_da(dA, X, dhb, rw, tab, segs, sA); });
     if (st == LORA_OK && dX != nullptr)
         st = marked(marks, stream, [&] { return tc_dx(dX, dhb, rw, tab, segs, stream); });
-    if (sd != nullptr) {  // join: the caller's stream waits for both side streams
-        if ((dB != nullptr && (cudaEventRecord(sd->ev[1], sB) != cudaSuccess ||
-                               cudaStreamWaitEvent(stream, sd->ev[1], 0) != cudaSuccess)) ||
-            (dA != nullptr && (cudaEventRecord(sd->ev[2], sA) != cudaSuccess ||
-                               cudaStreamWaitEvent(stream, sd->ev[2], 0) != cudaSuccess)))
-            return LORA_ERR_CUDA;
-    }
+    // join: the caller's stream waits for every side stream that was forked,
+    // after an error too, so that no work of this call outlives it unordered
+    // with the caller's stream (and a capture is never left with an open fork)
+    auto join = [&](cudaEvent_t ev, cudaStream_t side) {
+        return cudaEventRecord(ev, side) == cudaSuccess && cudaStreamWaitEvent(stream, ev, 0) == cudaSuccess;
+    };
+    if (forked_B && !join(sd->ev[1], sB) && st == LORA_OK) st = LORA_ERR_CUDA;
+    if (forked_A && !join(sd->ev[2], sA) && st == LORA_OK) st = LORA_ERR_CUDA;
     return st;
 }
 
