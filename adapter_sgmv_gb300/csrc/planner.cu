@@ -22,6 +22,16 @@
 //                functions is maximised by Dinkelbach iterations, each one an
 //                exact 0-1 knapsack over the memory budget (dynamic
 //                programming in whole memory units);
+//   makespan     a round's job can be long enough to set the pool's
+//                completion time alone (a GPU with a large memory budget packs
+//                many configurations into it), so jobs are cut into balanced
+//                parts where that finishes the pool sooner: for a cap D on a
+//                job's duration, every job is cut into the fewest parts that
+//                each end within D (configurations dealt, largest step cost
+//                first, to the part with the least cost so far); the caps
+//                tried are the part durations themselves, plus every job cut
+//                into single configurations, and the plan that ends first
+//                under the placement below is kept (ties keep fewer jobs);
 //   placement    the jobs, longest first, each on the GPU that frees first.
 //
 // The parallelism degree of a job is one GPU: the library's jobs run on a
@@ -112,6 +122,68 @@ double best_with_leader(const std::vector<Item> &items, const std::vector<int> &
     return N / D;
 }
 
+// One part of a cut job: its configurations (ascending), step time and duration.
+struct Part {
+    std::vector<int> m;
+    double step, dur;
+};
+
+// `set` (ascending) cut into g parts: configurations dealt, largest step cost
+// first (ties: lower index), each to the part with the least cost so far
+// (ties: fewer configurations, then the lower part index).  A part's step
+// time adds its costs in ascending configuration order, as a round's job does,
+// so one part reproduces the uncut job exactly.
+std::vector<Part> cut_job(const std::vector<Item> &items, const std::vector<int> &set, int g, double t0)
+{
+    std::vector<int> order(set);
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return items[a].cost > items[b].cost; });
+    std::vector<double> load(g, 0.0);
+    std::vector<Part> parts(g);
+    for (int c : order) {
+        int p = 0;
+        for (int q = 1; q < g; ++q)
+            if (load[q] < load[p] || (load[q] == load[p] && parts[q].m.size() < parts[p].m.size())) p = q;
+        load[p] += items[c].cost;
+        parts[p].m.push_back(c);
+    }
+    for (Part &P : parts) {
+        std::sort(P.m.begin(), P.m.end());
+        double c_sum = 0.0;
+        int64_t smax = 0;
+        for (int k : P.m) {
+            c_sum += items[k].cost;
+            smax = std::max(smax, items[k].steps);
+        }
+        P.step = t0 + c_sum;
+        P.dur = (double)smax * (t0 + c_sum);
+    }
+    return parts;
+}
+
+// Longest job first (stable), each on the GPU that frees first (lowest index
+// on ties); returns the completion time of the pool.
+double place(const std::vector<double> &dur, int32_t n_gpus, std::vector<int32_t> *gpu, std::vector<double> *start)
+{
+    const int32_t nj = (int32_t)dur.size();
+    std::vector<int32_t> order(nj);
+    for (int32_t j = 0; j < nj; ++j) order[j] = j;
+    std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return dur[a] > dur[b]; });
+    std::vector<double> free_at(n_gpus, 0.0);
+    double makespan = 0.0;
+    if (gpu) gpu->assign(nj, 0);
+    if (start) start->assign(nj, 0.0);
+    for (int32_t j : order) {
+        int32_t g = 0;
+        for (int32_t q = 1; q < n_gpus; ++q)
+            if (free_at[q] < free_at[g]) g = q;
+        if (gpu) (*gpu)[j] = g;
+        if (start) (*start)[j] = free_at[g];
+        free_at[g] += dur[j];
+        makespan = std::max(makespan, free_at[g]);
+    }
+    return makespan;
+}
+
 lora_status_t plan_pack(const lora_plan_config *configs, int32_t n_configs, const lora_plan_cost *cost,
                         int32_t *job_of, lora_plan_job *jobs, int32_t *n_jobs, double *makespan_s)
 {
@@ -146,7 +218,6 @@ lora_status_t plan_pack(const lora_plan_config *configs, int32_t n_configs, cons
     // rounds: the best remaining set becomes the next job
     std::vector<char> placed(n_configs, 0);
     std::vector<std::vector<int>> sets;
-    std::vector<double> dur, step;
     int32_t left = n_configs;
     std::vector<int> cand, s, best;
     while (left > 0) {
@@ -163,38 +234,79 @@ lora_status_t plan_pack(const lora_plan_config *configs, int32_t n_configs, cons
             }
         }
         if (best.empty()) return LORA_ERR_SHAPE;
-        double c_sum = 0.0;
-        int64_t smax = 0;
-        for (int k : best) {
-            placed[k] = 1;
-            job_of[k] = (int32_t)sets.size();
-            c_sum += items[k].cost;
-            smax = std::max(smax, items[k].steps);
-        }
+        for (int k : best) placed[k] = 1;
         left -= (int32_t)best.size();
-        step.push_back(t0 + c_sum);
-        dur.push_back((double)smax * (t0 + c_sum));
         sets.push_back(best);
     }
 
-    // placement: longest job first, on the GPU that frees first (lowest index on ties)
-    const int32_t nj = (int32_t)sets.size();
-    std::vector<int32_t> order(nj);
-    for (int32_t j = 0; j < nj; ++j) order[j] = j;
-    std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return dur[a] > dur[b]; });
-    std::vector<double> free_at(cost->n_gpus, 0.0);
-    double makespan = 0.0;
-    for (int32_t j : order) {
-        int32_t g = 0;
-        for (int32_t q = 1; q < cost->n_gpus; ++q)
-            if (free_at[q] < free_at[g]) g = q;
-        jobs[j].gpu = g;
-        jobs[j].n_configs = (int32_t)sets[j].size();
-        jobs[j].start_s = free_at[g];
-        jobs[j].duration_s = dur[j];
-        jobs[j].step_s = step[j];
-        free_at[g] += dur[j];
-        makespan = std::max(makespan, free_at[g]);
+    // makespan: every job cut into g = 1 .. |S| parts; the longest part of each
+    // cut is a cap to try
+    const int32_t n_sets = (int32_t)sets.size();
+    std::vector<std::vector<std::vector<Part>>> cuts(n_sets);
+    std::vector<std::vector<double>> longest(n_sets);
+    std::vector<double> caps;
+    for (int32_t j = 0; j < n_sets; ++j) {
+        for (int g = 1; g <= (int)sets[j].size(); ++g) {
+            cuts[j].push_back(cut_job(items, sets[j], g, t0));
+            double d = 0.0;
+            for (const Part &P : cuts[j].back()) d = std::max(d, P.dur);
+            longest[j].push_back(d);
+            caps.push_back(d);
+        }
+    }
+    std::sort(caps.begin(), caps.end(), [](double a, double b) { return a > b; });
+    caps.erase(std::unique(caps.begin(), caps.end()), caps.end());
+    // the plans in the order they are tried: uncut, each cap from the largest
+    // down, every job cut into single configurations; a plan is kept only if it
+    // ends strictly sooner than the best so far
+    std::vector<int> g_of(n_sets, 1), best_g(n_sets, 1);
+    auto durations = [&](const std::vector<int> &gs) {
+        std::vector<double> d;
+        for (int32_t j = 0; j < n_sets; ++j)
+            for (const Part &P : cuts[j][gs[j] - 1]) d.push_back(P.dur);
+        return d;
+    };
+    double best_mk = place(durations(best_g), cost->n_gpus, nullptr, nullptr);
+    for (size_t k = 0; k <= caps.size(); ++k) {
+        bool ok = true;
+        for (int32_t j = 0; j < n_sets && ok; ++j) {
+            const int n = (int)sets[j].size();
+            if (k == caps.size()) {
+                g_of[j] = n;
+                continue;
+            }
+            int g = 1;
+            while (g <= n && longest[j][g - 1] > caps[k]) ++g;
+            if (g > n) ok = false;
+            g_of[j] = g;
+        }
+        if (!ok) continue;
+        const double mk = place(durations(g_of), cost->n_gpus, nullptr, nullptr);
+        if (mk < best_mk) {
+            best_mk = mk;
+            best_g = g_of;
+        }
+    }
+
+    // the kept plan: jobs in round order, a job's parts in part order
+    std::vector<double> dur;
+    std::vector<const Part *> parts;
+    for (int32_t j = 0; j < n_sets; ++j)
+        for (const Part &P : cuts[j][best_g[j] - 1]) {
+            parts.push_back(&P);
+            dur.push_back(P.dur);
+        }
+    std::vector<int32_t> gpu;
+    std::vector<double> start;
+    const double makespan = place(dur, cost->n_gpus, &gpu, &start);
+    const int32_t nj = (int32_t)parts.size();
+    for (int32_t j = 0; j < nj; ++j) {
+        for (int c : parts[j]->m) job_of[c] = j;
+        jobs[j].gpu = gpu[j];
+        jobs[j].n_configs = (int32_t)parts[j]->m.size();
+        jobs[j].start_s = start[j];
+        jobs[j].duration_s = parts[j]->dur;
+        jobs[j].step_s = parts[j]->step;
     }
     *n_jobs = nj;
     *makespan_s = makespan;

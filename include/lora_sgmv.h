@@ -352,18 +352,27 @@ LORA_API lora_status_t lora_fused_base_fwd(void *y, float *H_save, const void *x
  * (job_mem_bytes + sum of mem_bytes, counted in whole mem_unit_bytes units,
  * each configuration's size rounded up) and that trains the most tokens per
  * second, sum_c steps_c tokens_per_step_c / (max_c steps_c * t(S)), found
- * exactly (Dinkelbach iterations over 0-1 knapsacks).  Jobs are then placed
+ * exactly (Dinkelbach iterations over 0-1 knapsacks).  A round's job may
+ * then be cut into balanced parts where that ends the pool's work sooner: for
+ * a cap D on a job's duration every job is cut into the fewest parts that each
+ * end within D (configurations dealt, largest step cost first, to the part
+ * with the least cost so far); the caps tried are the parts' own durations,
+ * plus every job cut into single configurations, and the plan that ends
+ * first is kept (the uncut plan on ties, then fewer jobs).  Jobs are placed
  * longest first, each on the GPU that frees first (lowest index on ties); a
- * job uses one GPU.
+ * job uses one GPU.  The plan never ends later than the uncut rounds' jobs
+ * or than one configuration per job under the same placement.
  *   configs    n_configs entries (host); n_configs in [1, 4096]
  *   job_of     out, host int32 [n_configs]: the job of every configuration
- *              (jobs numbered in the order the rounds made them)
+ *              (jobs numbered in the order the rounds made them, the parts
+ *              of a cut job one after another)
  *   jobs       out, host array with room for n_configs jobs
  *   n_jobs     out: jobs made;  makespan_s  out: predicted completion time
  * Work grows as n_configs^3 x budget units (per round, per choice of the
- * longest configuration, a knapsack pass per Dinkelbach iteration): meant for
- * search spaces of a few hundred configurations and budgets of a few
- * thousand units (120 configurations, 4200 units: ~0.1 s).
+ * longest configuration, a knapsack pass per Dinkelbach iteration), plus
+ * |S|^3 for cutting a job of |S| configurations: meant for search spaces of a
+ * few hundred configurations and budgets of a few thousand units (120
+ * configurations, 4200 units: ~0.2 s).
  * Errors: LORA_ERR_INVALID_ARG (NULL, negative cost terms, a zero-time step),
  * LORA_ERR_SHAPE (a configuration that does not fit one GPU alone, sizes out
  * of range, a memory budget of more than 2^20 units, n_configs x (budget

@@ -16,6 +16,14 @@ readings stated in the library's header:
                units, each size rounded up) and maximises
                rate(S) = sum_c steps_c tok_c / (max_c steps_c * t(S)),
                found here by enumerating every subset
+  makespan     each round's job cut into g = 1 .. |S| parts (configurations
+               dealt, largest step cost first, ties by index, to the part
+               with the least cost so far, ties to the part with fewer
+               configurations, then the lower part); for every cap D among
+               the cuts' longest parts, from the largest down, each job takes
+               its smallest g whose parts all end within D; last, every job
+               cut into single configurations.  The first plan (uncut) and
+               then every plan that ends strictly sooner is kept.
   placement    jobs longest first (stable), each on the GPU that frees first
                (lowest index on ties)
 
@@ -59,18 +67,67 @@ def plan(configs, cost):
         sets.append(sorted(best))
         left = [c for c in left if c not in best]
     t0 = cost.get("step_overhead_s", 0.0)
-    step = [t0 + sum(configs[c]["tokens_per_step"] * _w(configs[c], cost) for c in s) for s in sets]
-    dur = [max(configs[c]["steps"] for c in s) * st for s, st in zip(sets, step)]
-    order = sorted(range(len(sets)), key=lambda j: -dur[j])  # stable: ties keep creation order
-    free = [0.0] * cost.get("n_gpus", 1)
-    jobs = [None] * len(sets)
-    for j in order:
-        g = min(range(len(free)), key=lambda q: (free[q], q))
-        jobs[j] = {"gpu": g, "n_configs": len(sets[j]), "start_s": free[g], "duration_s": dur[j], "step_s": step[j]}
-        free[g] += dur[j]
+    n_gpus = cost.get("n_gpus", 1)
+
+    def job_cost(c):
+        return configs[c]["tokens_per_step"] * _w(configs[c], cost)
+
+    def part(members):
+        members = sorted(members)
+        c_sum = 0.0
+        for c in members:  # ascending order, like the rounds' step time
+            c_sum += job_cost(c)
+        return {"m": members, "step": t0 + c_sum, "dur": max(configs[c]["steps"] for c in members) * (t0 + c_sum)}
+
+    def cut(s, g):
+        bins, load = [[] for _ in range(g)], [0.0] * g
+        for c in sorted(s, key=lambda c: -job_cost(c)):  # stable: equal costs keep index order
+            p = min(range(g), key=lambda q: (load[q], len(bins[q]), q))
+            load[p] += job_cost(c)
+            bins[p].append(c)
+        return [part(b) for b in bins]
+
+    def place(durs):
+        order = sorted(range(len(durs)), key=lambda j: -durs[j])  # stable: ties keep job order
+        free = [0.0] * n_gpus
+        where = [None] * len(durs)
+        for j in order:
+            g = min(range(n_gpus), key=lambda q: (free[q], q))
+            where[j] = (g, free[g])
+            free[g] += durs[j]
+        return max(free), where
+
+    cuts = [[cut(s, g) for g in range(1, len(s) + 1)] for s in sets]
+    longest = [[max(p["dur"] for p in c) for c in cj] for cj in cuts]
+    caps = sorted({d for lj in longest for d in lj}, reverse=True)
+
+    def plan_of(gs):
+        return [p for j, g in enumerate(gs) for p in cuts[j][g - 1]]
+
+    best_g = [1] * len(sets)
+    best_mk = place([p["dur"] for p in plan_of(best_g)])[0]
+    tries = []
+    for D in caps:
+        gs = []
+        for j in range(len(sets)):
+            g = next((g for g in range(1, len(sets[j]) + 1) if longest[j][g - 1] <= D), None)
+            gs.append(g)
+        if None not in gs:
+            tries.append(gs)
+    tries.append([len(s) for s in sets])
+    for gs in tries:
+        mk = place([p["dur"] for p in plan_of(gs)])[0]
+        if mk < best_mk:
+            best_mk, best_g = mk, gs
+
+    parts = plan_of(best_g)
+    makespan, where = place([p["dur"] for p in parts])
+    jobs = [{"gpu": g, "n_configs": len(p["m"]), "start_s": st, "duration_s": p["dur"], "step_s": p["step"]}
+            for p, (g, st) in zip(parts, where)]
     job_of = [0] * len(configs)
-    for j, s in enumerate(sets):
-        for c in s:
+    for j, p in enumerate(parts):
+        for c in p["m"]:
             job_of[c] = j
-    return {"job_of": job_of, "jobs": jobs, "makespan_s": max(free), "sets": sets,
-            "rates": [rate(s, configs, cost) for s in sets], "lower_bound_s": math.fsum(dur) / len(free)}
+    return {"job_of": job_of, "jobs": jobs, "makespan_s": makespan, "sets": sets, "parts": [p["m"] for p in parts],
+            "rates": [rate(s, configs, cost) for s in sets],
+            "lower_bound_s": math.fsum(p["dur"] for p in parts) / n_gpus}

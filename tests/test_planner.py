@@ -6,10 +6,14 @@ configurations pack when a step has a fixed overhead; a memory budget that
 fits only two of three configurations picks the pair with the best rate; a
 short configuration does not ride along with a long one when it would waste
 the job's steps; longest-first placement of durations 5, 4, 3 on two GPUs
-ends at 7.  Parity: the library's plan equals the exhaustive search on
-random instances (partitions and predicted times).  Invariants at the size of
-PLoRA's 120-configuration search space: every configuration placed once,
-memory budget kept, makespan above the work / GPUs bound."""
+ends at 7; a four-configuration job is cut in two across two GPUs (41 s ->
+21 s), never on one GPU, and a cut into three that ends no sooner is not
+taken.  Parity: the library's plan equals the exhaustive search on random
+instances (partitions and predicted times), including grouped instances on
+2-8 GPUs where the cuts decide the plan, which never ends later than the
+uncut jobs or one configuration per job.  Invariants at the size of PLoRA's
+120-configuration search space: every configuration placed once, memory
+budget kept, makespan above the work / GPUs bound."""
 import math
 
 import numpy as np
@@ -71,6 +75,38 @@ def test_longest_first_placement_on_two_gpus():
     assert [j["gpu"] for j in p["jobs"]] == [0, 1, 1]
 
 
+def test_a_job_is_cut_across_gpus_when_that_ends_sooner():
+    # four identical configs (1 s of tokens per step, 10 steps), t0 = 0.1, two GPUs.
+    # The round packs all four: rate 4000 / (10 * 4.1) = 97.6 beats 3000 / 31 = 96.8.
+    # Uncut the job takes 41 s; in two parts {0,2} {1,3} each takes 10 * 2.1 = 21 s,
+    # one per GPU -> 21; in four parts 11 s each, two per GPU -> 22.  Two parts win.
+    cost = {"step_overhead_s": 0.1, "base_s_per_token": 0.01, "gpu_mem_bytes": 10 * GB, "mem_unit_bytes": GB,
+            "n_gpus": 2}
+    c = [cfg(8, 100, 10, GB)] * 4
+    p = oplan.plan(c, cost)
+    assert p["sets"] == [[0, 1, 2, 3]]
+    assert p["parts"] == [[0, 2], [1, 3]] and p["job_of"] == [0, 1, 0, 1]
+    assert math.isclose(p["makespan_s"], 21.0, rel_tol=1e-12)
+    assert [j["gpu"] for j in p["jobs"]] == [0, 1]
+    got = lora.lora_plan_pack(c, cost)
+    assert got["job_of"] == p["job_of"] and math.isclose(got["makespan_s"], 21.0, rel_tol=1e-12)
+
+
+def test_one_gpu_never_cuts_and_ties_keep_fewer_jobs():
+    c = [cfg(8, 100, 10, GB)] * 4
+    base = {"step_overhead_s": 0.1, "base_s_per_token": 0.01, "gpu_mem_bytes": 10 * GB, "mem_unit_bytes": GB}
+    # one GPU: a cut only adds step overhead -> one job of 41 s
+    p = oplan.plan(c, dict(base, n_gpus=1))
+    assert p["parts"] == [[0, 1, 2, 3]] and math.isclose(p["makespan_s"], 41.0, rel_tol=1e-12)
+    # three GPUs: parts {0,3} {1} {2} (21, 11, 11 s) end at 21 like two parts -> the two parts stay
+    p = oplan.plan(c, dict(base, n_gpus=3))
+    assert p["parts"] == [[0, 2], [1, 3]] and math.isclose(p["makespan_s"], 21.0, rel_tol=1e-12)
+    for n in (1, 3):
+        got = lora.lora_plan_pack(c, dict(base, n_gpus=n))
+        want = oplan.plan(c, dict(base, n_gpus=n))
+        assert got["job_of"] == want["job_of"] and math.isclose(got["makespan_s"], want["makespan_s"])
+
+
 # ---------------------------------------------------------------- library vs oracle
 def random_instance(rng, m):
     configs = [cfg(int(rng.choice([8, 16, 32, 64, 128])), int(rng.integers(256, 8192)), int(rng.integers(50, 2000)),
@@ -95,6 +131,57 @@ def test_library_plan_equals_exhaustive_search(seed):
         for k in ("start_s", "duration_s", "step_s"):
             assert math.isclose(g[k], w[k], rel_tol=1e-12, abs_tol=1e-12), k
     assert math.isclose(got["makespan_s"], want["makespan_s"], rel_tol=1e-12)
+
+
+def grouped_instance(rng, m):
+    # configurations in a few groups of equal steps (one dataset, a few batch
+    # sizes), a large memory budget and several GPUs: rounds pack whole groups,
+    # and cutting them across the GPUs decides the makespan
+    toks = [int(t) for t in rng.choice([512, 1024, 2048, 4096], size=int(rng.integers(1, 4)), replace=False)]
+    configs = []
+    for _ in range(m):
+        tok = toks[int(rng.integers(0, len(toks)))]
+        configs.append(cfg(int(rng.choice([8, 16, 32, 64, 128])), tok, 4 * (1 << 20) // tok,
+                           int(rng.integers(1, 12)) * (GB // 4)))
+    cost = {"step_overhead_s": float(rng.uniform(0.005, 0.05)), "base_s_per_token": float(rng.uniform(2e-6, 1e-5)),
+            "lora_s_per_token": float(rng.uniform(0.0, 2e-6)), "lora_s_per_token_rank": float(rng.uniform(0.0, 1e-8)),
+            "gpu_mem_bytes": 280 * GB, "job_mem_bytes": 24 * GB, "mem_unit_bytes": GB // 4,
+            "n_gpus": int(rng.integers(2, 9))}
+    return configs, cost
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_library_plan_equals_exhaustive_search_with_cuts(seed):
+    rng = np.random.default_rng(100 + seed)
+    configs, cost = grouped_instance(rng, int(rng.integers(2, 11)))
+    want = oplan.plan(configs, cost)
+    got = lora.lora_plan_pack(configs, cost)
+    assert got["job_of"] == want["job_of"]
+    assert [(j["gpu"], j["n_configs"]) for j in got["jobs"]] == [(j["gpu"], j["n_configs"]) for j in want["jobs"]]
+    for g, w in zip(got["jobs"], want["jobs"]):
+        for k in ("start_s", "duration_s", "step_s"):
+            assert math.isclose(g[k], w[k], rel_tol=1e-12, abs_tol=1e-12), k
+    assert math.isclose(got["makespan_s"], want["makespan_s"], rel_tol=1e-12)
+    # never later than the uncut rounds' jobs, nor than one configuration per job
+    uncut = oplan.plan(configs, dict(cost))
+    uncut_mk = _lpt([max(configs[c]["steps"] for c in s) * (cost["step_overhead_s"] + sum(
+        configs[c]["tokens_per_step"] * _w(configs[c], cost) for c in s)) for s in uncut["sets"]], cost["n_gpus"])
+    singles_mk = _lpt([c["steps"] * (cost["step_overhead_s"] + c["tokens_per_step"] * _w(c, cost)) for c in configs],
+                      cost["n_gpus"])
+    assert want["makespan_s"] <= uncut_mk * (1 + 1e-12) and want["makespan_s"] <= singles_mk * (1 + 1e-12)
+
+
+def _w(c, cost):
+    return cost.get("base_s_per_token", 0.0) + cost.get("lora_s_per_token", 0.0) + \
+        cost.get("lora_s_per_token_rank", 0.0) * c["rank"]
+
+
+def _lpt(durs, n_gpus):
+    free = [0.0] * n_gpus
+    for d in sorted(durs, reverse=True):
+        g = min(range(n_gpus), key=lambda q: (free[q], q))
+        free[g] += d
+    return max(free)
 
 
 def test_plora_sized_search_space_invariants():
