@@ -17,6 +17,18 @@ LORA_DEV void set_status(int32_t *status, int32_t code)
     if (status != nullptr) atomicCAS(status, (int32_t)LORA_OK, code);
 }
 
+// ---------------------------------------------------------------- chained launches
+// A kernel launched with programmatic stream serialisation may start while
+// the kernel before it in the stream is still running.  pdl_wait() returns
+// once that kernel has completed and its writes are visible; a dependent
+// kernel reads nothing an earlier kernel may have written before it.
+// pdl_launch_dependents() lets the next such kernel start; it is issued only
+// after this kernel's own pdl_wait() (or by a kernel that is not itself a
+// dependent), so a dependent that starts early knows that every kernel before
+// its predecessor has completed.
+LORA_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+LORA_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- bf16 words
 // bf16 is carried as raw 16-bit words; widening is exact, narrowing rounds to
 // nearest-even (NaN stays NaN).

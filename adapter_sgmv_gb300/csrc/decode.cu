@@ -19,11 +19,11 @@
 // The expand kernel is launched as a programmatic dependent of the shrink: its
 // CTAs start while the shrink runs and fetch their B_i^T block and the y rows
 // they update (inputs the shrink does not write) before waiting for the shrink
-// grid to complete; h is then read from L2.  The shrink is itself launched as
-// a programmatic dependent of whatever precedes it on the stream: back-to-back
-// decode calls (the layers of a decode step) overlap one call's routing reads
-// and weight prefetch with the previous call's expand, and wait for it before
-// reading x or writing h.
+// grid to complete; h is then read from L2.  The shrink is an ordinary
+// launch: it reads the routing and A_i before anything else, and the kernel
+// before it on the stream may have written them (a routing build, an
+// optimizer step that refreshed A_i); only a completed predecessor is
+// visible without a grid-dependency wait.
 //
 // Several projections that read the same x (q / k / v, gate / up) go through
 // the same two launches: blockIdx.y selects the projection, each with its own
@@ -130,9 +130,6 @@ LORA_DEV float4 ld_cluster_f4(uint32_t saddr, uint32_t rank)
     return v;
 }
 
-LORA_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-LORA_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // A work item's tile, its adapter's table entry and the token of row
 // threadIdx.x, read in two rounds of memory latency instead of four: the tile
 // alongside the tile count, the table entry alongside the token.  For a tile
@@ -184,7 +181,10 @@ __global__ void __launch_bounds__(kThreads, 2) dec_shrink_kernel(const uint16_t 
                                                               const __grid_constant__ ProjSet ps, Geom g,
                                                               lora_segments segs)
 {
-    pdl_launch_dependents();  // the expand may start its own loads now
+    // an ordinary launch: everything earlier on the stream is complete and
+    // visible.  The expand, a programmatic dependent of this grid, may start
+    // its own loads of B and y now (this kernel writes neither)
+    pdl_launch_dependents();
     const int32_t ti = blockIdx.x / g.ks, sl = blockIdx.x % g.ks;
     const lora_adapter_table &tab = ps.tab[blockIdx.y];
     float *__restrict__ hfin = ps.hfin[blockIdx.y];
@@ -240,10 +240,6 @@ __global__ void __launch_bounds__(kThreads, 2) dec_shrink_kernel(const uint16_t 
         if (c < nchunks) load_a(c, c);
     if (threadIdx.x < rows16) tok[threadIdx.x] = (int)threadIdx.x < rows ? D.my_tok : -1;
     __syncthreads();
-    // launched as a programmatic dependent of the previous call's expand: the
-    // routing and the weights above are not written by it, but x may be its
-    // output and the h buffer its input, so everything past here waits for it
-    pdl_wait();
     for (int c = 0; c < stages - 1; ++c) {
         if (c < nchunks) load_x(c, c);
         cp_async_commit();
@@ -364,7 +360,6 @@ __global__ void __launch_bounds__(kThreads, 2) dec_shrink_kernel(const uint16_t 
 __global__ void __launch_bounds__(kThreads, 2) dec_expand_kernel(const __grid_constant__ ProjSet ps, Geom g,
                                                               lora_segments segs)
 {
-    pdl_launch_dependents();  // a following decode call may start its own prologue
     const int32_t ti = blockIdx.x / g.ns, nsl = blockIdx.x % g.ns;
     const lora_adapter_table &tab = ps.tab[blockIdx.y];
     uint16_t *__restrict__ y = ps.y[blockIdx.y];
@@ -529,15 +524,17 @@ lora_status_t tc_decode_multi(int32_t n_proj, void *const *y, float *const *H_sa
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = s1;
         cfg.stream = stream;
-        cudaLaunchAttribute attr[2];
+        // an ordinary (not programmatic) launch: the shrink reads the routing
+        // and A_i, which the kernel before it may have written (a routing
+        // build, an optimizer step), and only a completed predecessor is
+        // guaranteed visible without a grid-dependency wait
+        cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = (unsigned)g.ks;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
-        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlaps the previous call's tail
-        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 2;
+        cfg.numAttrs = 1;
         if (cudaLaunchKernelEx(&cfg, dec_shrink_kernel, static_cast<const uint16_t *>(x), ps, g, segs) != cudaSuccess)
             return LORA_ERR_CUDA;
     }
