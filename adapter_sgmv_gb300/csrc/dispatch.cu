@@ -2,9 +2,9 @@
 //
 //   forward:  case i (shrink) writes H (optional fp32 copy for the caller) and
 //             its bf16 hi + lo split in perm order; case ii (expand) reads them.
-//   backward: case i (dh) writes bf16 dH in perm order and converts the saved
-//             H to bf16 in perm order (or case i recomputes it from X);
-//             case iii (dB), case iv (dA) and case ii (dX) read those.
+//   backward: a small kernel converts the saved H to bf16 in perm order (or
+//             case i recomputes it from X); case i (dh) writes bf16 dH in perm
+//             order; case iii (dB), case iv (dA) and case ii (dX) read those.
 #include <mutex>
 
 #include "dispatch.h"
@@ -172,7 +172,7 @@ lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void
         if (st == LORA_OK) st = marked(marks, sB, [&] { return tc_db(dB, dY, hb, rw, tab, segs, sB); });
     }
     if (st == LORA_OK)
-        st = marked(marks, stream, [&] { return tc_dh(dY, tab, segs, dhb, nullptr, nullptr, rw, stream); });
+        st = marked(marks, stream, [&] { return tc_dh(dY, tab, segs, dhb, rw, stream); });
     if (st == LORA_OK && sd != nullptr && dA != nullptr) {  // fork A after dh
         forked_A = fork(sd->ev[3], sA);
         if (!forked_A) st = LORA_ERR_CUDA;

@@ -17,8 +17,10 @@
 //    r_max <= 64 else 128, each half rounded up to 256 bytes) are rejected
 //    with LORA_ERR_WORKSPACE_TOO_SMALL before anything is launched.
 //  - All calls share the one array and the last call's contents stay in it.
-//    Nothing in it has to start at zero: every scratch row a kernel reads is
-//    written earlier in the same call.  Calls whose work overlaps on the GPU
+//    Nothing in it has to start at zero: every scratch value a product uses
+//    is written earlier in the same call (hand-off columns past a tile's rank
+//    rounded up to 16 may reach shared memory with the rest of a row, but no
+//    product reads them).  Calls whose work overlaps on the GPU
 //    (different streams, or different host threads, same device) race on the
 //    array: serialise them.
 //  - In host code the array's name stands for a host-side shadow, not a

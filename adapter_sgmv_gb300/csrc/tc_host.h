@@ -38,13 +38,14 @@ int sm_count();
 inline int32_t handoff_cols(int32_t r_max) { return r_max <= 64 ? 64 : 128; }
 
 // case i.  shrink: H[t, :] = A_i x_t.  Writes the fp32 H by token (H may be
-// null) and/or its bf16 hi (+ lo) split by perm position (null to skip).
+// null; zero past r_i) and/or its bf16 hi (+ lo) split by perm position (null
+// to skip; zero from r_i up to r_i rounded to 16, unwritten past that, where
+// no product reads).
 lora_status_t tc_shrink(const void *x, const lora_adapter_table &tab, const lora_segments &segs, float *H,
                         uint16_t *hi, uint16_t *lo, int32_t rw, cudaStream_t stream);
-// case i.  dh = s_i B_i^T dy as bf16 by perm position; when h_saved is given,
-// also converts it (fp32 by token) into h_bf16 (bf16 by perm position).
+// case i.  dh = s_i B_i^T dy as bf16 by perm position.
 lora_status_t tc_dh(const void *dY, const lora_adapter_table &tab, const lora_segments &segs, uint16_t *dh_bf16,
-                    const float *h_saved, uint16_t *h_bf16, int32_t rw, cudaStream_t stream);
+                    int32_t rw, cudaStream_t stream);
 
 // A saved fp32 H (by token) converted to the bf16 hand-off rows (by perm
 // position) that cases iii reads; the same values case i writes as its hi.

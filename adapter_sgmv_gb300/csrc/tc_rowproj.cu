@@ -13,13 +13,14 @@
 // 128-byte swizzle: TMA when the rows are consecutive tokens, else cp.async
 // gather) and the weight block; one thread issues tcgen05.mma (M = 128,
 // N = r_pad, K = 16) into a TMEM accumulator; four epilogue warps write
-//   - out_f32[t, :]  = c * acc   (fp32, stride r_max; optional)
+//   - out_f32[t, :]  = c * acc   (fp32, stride r_max; optional), zero in
+//     columns r_i .. r_max - 1
 //   - out_hi[p, :]   = bf16(c * acc), out_lo[p, :] = bf16(c * acc - hi)
-//     (row p = the token's position in perm, stride rw; both optional)
-//   - hin_bf16[p, :] = bf16(hin[t, :])  (optional: converts a saved fp32 H
-//     into the same hand-off format, for the backward)
-// with zeros in columns r_i .. end.  The perm-ordered bf16 rows are what the
-// case ii / iii / iv kernels read by TMA.
+//     (row p = the token's position in perm, stride rw; both optional), zero
+//     in columns r_i .. r_pad - 1 and not written past r_pad
+// The perm-ordered bf16 rows are what the case ii / iii / iv kernels read by
+// TMA; their products stop at r_pad.  A small kernel beside them converts a
+// saved fp32 H into the same hand-off rows for the backward.
 //
 // Warp roles (192 threads): 0 loads, 1 issues MMAs and owns TMEM, 2..5 epilogue.
 // Every wait is bounded (tc::mbar_wait).
@@ -70,8 +71,6 @@ LORA_DEV int32_t rpad16(int32_t r) { return (r + 15) & ~15; }
 struct RowOut {
     float *f32;           // [T, r_max] by token, or null
     uint16_t *hi, *lo;    // [T, rw] by perm position, or null
-    const float *hin;     // [T, r_max] fp32 by token to convert, or null
-    uint16_t *hin_bf16;   // [T, rw] by perm position
     int32_t rw;
     float scale_is_adapter;  // 1: c = s_i, 0: c = 1
 };
@@ -274,25 +273,14 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.tempty[acc]);
             ++acc_n;
-            if (!valid) continue;
-            // zero tails and the optional conversion of a saved fp32 H
-            if (row != nullptr)
+            // the fp32 output is zero past the rank rounded up to 16 (its
+            // contract); the hand-off rows are not written there, because every
+            // product that reads them stops at that rounded rank
+            if (!valid || row == nullptr) continue;
+            if (vec) {
+                for (int k = rp; k < r_max; k += 4) *reinterpret_cast<float4 *>(row + k) = make_float4(0.f, 0.f, 0.f, 0.f);
+            } else {
                 for (int k = rp; k < r_max; ++k) row[k] = 0.f;
-            const uint4 z = make_uint4(0, 0, 0, 0);
-            for (int k = rp; k < o.rw; k += 8) {
-                if (rhi != nullptr) *reinterpret_cast<uint4 *>(rhi + k) = z;
-                if (rlo != nullptr) *reinterpret_cast<uint4 *>(rlo + k) = z;
-            }
-            if (o.hin != nullptr) {
-                const float *src = o.hin + (int64_t)t * r_max;
-                uint16_t *dst = o.hin_bf16 + p * o.rw;
-                for (int k = 0; k < o.rw; k += 8) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 8; e += 2)
-                        w[e / 2] = pack_bf16(k + e < r ? src[k + e] : 0.f, k + e + 1 < r ? src[k + e + 1] : 0.f);
-                    *reinterpret_cast<uint4 *>(dst + k) = make_uint4(w[0], w[1], w[2], w[3]);
-                }
             }
         }
     }
@@ -342,8 +330,9 @@ __global__ void __launch_bounds__(256) h_to_bf16_kernel(const float *__restrict_
         const Tile T = load_tile(segs.tiles, ti);
         const AdapterInfo ad = load_adapter(tab, T.adapter, nullptr);
         const int32_t r = ad.ok ? ad.rank : 0;
-        for (int32_t i = threadIdx.x; i < T.rows * (rw / 8); i += blockDim.x) {
-            const int32_t m = i / (rw / 8), k = 8 * (i % (rw / 8));
+        const int32_t rp8 = (r + 15) / 16 * 2;  // 8-column pieces up to the rank rounded to 16; past it no product reads
+        for (int32_t i = threadIdx.x; i < T.rows * rp8; i += blockDim.x) {
+            const int32_t m = i / rp8, k = 8 * (i % rp8);
             const int64_t p = (int64_t)T.begin + m;
             const float *src = H + (int64_t)segs.perm[p] * r_max;
             float f[8];
@@ -377,14 +366,14 @@ lora_status_t tc_h_to_bf16(const float *H, uint16_t *hb, int32_t rw, const lora_
 lora_status_t tc_shrink(const void *x, const lora_adapter_table &tab, const lora_segments &segs, float *H,
                         uint16_t *hi, uint16_t *lo, int32_t rw, cudaStream_t stream)
 {
-    RowOut o{H, hi, lo, nullptr, nullptr, rw, 0.f};
+    RowOut o{H, hi, lo, rw, 0.f};
     return launch_rowproj(x, tab.A, tab.d_in, o, tab, segs, stream);
 }
 
 lora_status_t tc_dh(const void *dY, const lora_adapter_table &tab, const lora_segments &segs, uint16_t *dh_bf16,
-                    const float *h_saved, uint16_t *h_bf16, int32_t rw, cudaStream_t stream)
+                    int32_t rw, cudaStream_t stream)
 {
-    RowOut o{nullptr, dh_bf16, nullptr, h_saved, h_bf16, rw, 1.f};
+    RowOut o{nullptr, dh_bf16, nullptr, rw, 1.f};
     return launch_rowproj(dY, tab.B, tab.d_out, o, tab, segs, stream);
 }
 

@@ -82,7 +82,8 @@ class GpuCase:
     def dH_workspace(self):
         """dH as left in the workspace by the last backward, in token order
         (implementation detail, for diagnosis): the second hand-off buffer,
-        bf16 [T, rw] rows in perm order."""
+        bf16 [T, rw] rows in perm order, of which a row holds its adapter's
+        r_i columns (zero up to r_i rounded to 16, unwritten past that)."""
         s = self.spec
         rw = 64 if s.r_max <= 64 else 128
         region = ((s.n_tokens * rw * 2) + 255) & ~255
@@ -91,7 +92,11 @@ class GpuCase:
         perm = self.segs.perm[:n_valid].long()
         out = torch.zeros((s.n_tokens, s.r_max), dtype=torch.float32, device=self.device)
         out[perm] = dhb[:n_valid, :s.r_max].float()
-        return out
+        ids = np.asarray(s.ids)
+        ok = (ids >= 0) & (ids < s.n_adapters)
+        rank = np.where(ok, np.asarray(s.ranks)[np.where(ok, ids, 0)], 0)
+        keep = torch.arange(s.r_max, device=self.device)[None, :] < torch.from_numpy(rank).to(self.device)[:, None]
+        return torch.where(keep, out, torch.zeros_like(out))
 
 
 def oracle_all(spec: wl.Spec, host: dict, rows=None):
