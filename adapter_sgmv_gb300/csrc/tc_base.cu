@@ -183,15 +183,7 @@ LORA_DEV bool wait_ready(const int32_t *flag, volatile int32_t *abort_flag, int3
     }
 }
 
-LORA_DEV void tma_store_2d(const CUtensorMap *map, const void *smem_src, int32_t c0, int32_t c1)
-{
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
-                 "r"(smem_u32(smem_src)), "r"(c0), "r"(c1)
-                 : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
 LORA_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-LORA_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // The next claimed task from the CTA's ring (every consumer sees every task
 // in claim order); -1 at the end, -2 on abort.

@@ -95,13 +95,6 @@ LORA_DEV Item load_item(const lora_adapter_table &tab, const lora_segments &segs
     return I;
 }
 
-LORA_DEV void tma_store_2d(const CUtensorMap *map, const void *smem_src, int32_t c0, int32_t c1)
-{
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
-                 "r"(smem_u32(smem_src)), "r"(c0), "r"(c1)
-                 : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
 template <int N>
 LORA_DEV void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
 // Per store leader, the TMA stores whose shared-memory reads may still be
@@ -112,7 +105,6 @@ __host__ __device__ constexpr int store_lag() { return kEpi == 8 ? 0 : 1; }
 // Threads: producer and MMA warps, the epilogue, and the loader warps.
 template <bool kLoader, int kEpi>
 __host__ __device__ constexpr int threads_of() { return 64 + 32 * kEpi + (kLoader ? 128 : 0); }
-LORA_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 struct ColIn {
     const float *h32;  // loader variant: fp32 h by token, stride r_max

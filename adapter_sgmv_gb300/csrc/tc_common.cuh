@@ -116,6 +116,19 @@ LORA_DEV void tma_load_3d(void *smem_dst, const CUtensorMap *map, uint64_t *bar,
         : "memory");
 }
 
+// TMA store of one box from shared memory (its own bulk group); c0 must not
+// be negative and c0 * element size must be a multiple of 16 bytes.  Parts of
+// the box outside the tensor are not written.
+LORA_DEV void tma_store_2d(const CUtensorMap *map, const void *smem_src, int32_t c0, int32_t c1)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
+                 "r"(smem_u32(smem_src)), "r"(c0), "r"(c1)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// every bulk group this thread committed has completed (writes performed)
+LORA_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 LORA_DEV void prefetch_tensormap(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");

@@ -94,7 +94,6 @@ LORA_DEV void tma_reduce_add_2d(const CUtensorMap *map, const void *smem_src, in
 }
 LORA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 LORA_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-LORA_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kThreads, 1)
 tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_act3,
