@@ -857,11 +857,9 @@ def run_ours(args, rank, world, dev):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, shapes of the packed training batch)",
-        "config": {"workload": "packed4096: 4096->4096, N=8 ranks {8,16,16,32,32,64,64,128}, alpha 16/32, "
-                               f"8 sorted segments x {args.tokens_per_adapter} tokens (T={T}), fwd+bwd",
-                   "tokens_per_step": T, "d_in": spec.d_in, "d_out": spec.d_out, "adapters": spec.n_adapters,
-                   "l2": "inputs larger than L2 (x, dY, y 268 MB each); no flush",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": dict(workload_config(spec, args.tokens_per_adapter),
+                       l2="inputs larger than L2 (x, dY, y 268 MB each); no flush",
+                       parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
         "breakdown_ms": {"lora_build_segments": round(statistics.mean(t_build), 4),
                          "lora_packed_fwd": round(statistics.mean(t_fwd), 4),
                          "lora_packed_bwd": round(statistics.mean(t_bwd), 4)},
@@ -894,12 +892,19 @@ def run_ours(args, rank, world, dev):
 
 
 # ---------------------------------------------------------------------------- reference arm
+def workload_config(spec: wl.Spec, tokens_per_adapter: int) -> dict:
+    """The benchmarked workload, named the same way by both arms."""
+    return {"workload": "packed4096: 4096->4096, N=8 ranks {8,16,16,32,32,64,64,128}, alpha 16/32, "
+                        f"8 sorted segments x {tokens_per_adapter} tokens (T={spec.n_tokens}), fwd+bwd",
+            "tokens_per_step": spec.n_tokens, "d_in": spec.d_in, "d_out": spec.d_out, "adapters": spec.n_adapters}
+
+
 def run_reference(args):
     """The fp64 oracle (the only reference this method has) on the host cores:
     each step is a bounded sample of the same workload; tokens/s."""
     import oracle
 
-    spec = wl.packed4096()
+    spec = wl.packed4096(tokens_per_adapter=args.tokens_per_adapter)
     oracle.build()
     per = args.ref_tokens_per_adapter
     rows = np.concatenate([np.flatnonzero(spec.ids == i)[:per] for i in range(spec.n_adapters)])
@@ -928,7 +933,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
-        "config": {"workload": "packed4096 (bounded sample per step)", "tokens_per_step": n},
+        "config": dict(workload_config(spec, args.tokens_per_adapter), sample_tokens_per_step=n,
+                       parallelism="host cores"),
         "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
