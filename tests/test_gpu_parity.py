@@ -89,6 +89,22 @@ def test_zipf_runs_unsorted_small():
     full_check(spec)
 
 
+@pytest.mark.parametrize("route", ["auto", "ids"])
+def test_five_thousand_adapters_sorted(route):
+    # more adapters than the one-launch routing build holds (4095): sorted
+    # offsets take the build that scans in global memory, ids the counting
+    # sort; a quarter of the adapters empty, one spanning several tiles
+    rng = np.random.default_rng(11)
+    N = 5000
+    lens = rng.integers(0, 4, N)
+    lens[rng.random(N) < 0.25] = 0
+    lens[17] = 700
+    ids = np.repeat(np.arange(N, dtype=np.int32), lens)
+    ranks = rng.choice(np.array([1, 4, 8, 16, 40]), size=N).astype(np.int32)
+    spec = wl.custom("many", 64, 72, ranks, 2.0 * ranks, ids, seed=3)
+    full_check(spec, y0="randn", dX0="randn", route=route)
+
+
 def test_empty_adapters_get_zero_gradients():
     ids = np.array([0] * 40 + [3] * 70, np.int32)  # adapters 1 and 2 have no token
     spec = wl.custom("empty", 64, 96, [8, 16, 32, 16], [16.0] * 4, ids)

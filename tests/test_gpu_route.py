@@ -54,6 +54,7 @@ ID_CASES = {
     "sparse_many_adapters": lambda: (np.random.default_rng(1).integers(0, 3000, 2000).astype(np.int32), 3000),
     "runs_and_singletons": lambda: (np.concatenate([np.full(129, 1), [0], np.full(257, 1), [2, 0, 2]]).astype(np.int32), 3),
     "odd_length_random": lambda: (np.random.default_rng(2).integers(0, 7, 4099).astype(np.int32), 7),
+    "ten_thousand_adapters": lambda: (np.random.default_rng(3).integers(0, 10000, 5000).astype(np.int32), 10000),
 }
 
 
@@ -101,6 +102,41 @@ def test_route_from_sorted_offsets(offsets):
     perm = segs.perm.cpu().numpy()
     assert np.array_equal(perm, np.arange(T))
     check_tiles(segs, np.array(offsets), perm)
+
+
+def random_offsets(N, seed, max_len=9):
+    # segment lengths 0..max_len (a quarter of the adapters empty), first 0, last T
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(0, max_len + 1, N)
+    lens[rng.random(N) < 0.25] = 0
+    lens[rng.integers(0, N)] += 300  # one segment of several tiles
+    return np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("N", [4095, 4096, 9000])
+def test_route_from_sorted_offsets_many_adapters(N):
+    # 4095 adapters: the one-launch build at its shared-memory capacity; above
+    # it the build that scans the offsets in global memory
+    offsets = random_offsets(N, seed=N)
+    T = int(offsets[-1])
+    off = torch.from_numpy(offsets).cuda()
+    segs = lora.lora_build_segments(seg_offsets=off, n_tokens=T, n_adapters=N)
+    assert lora.lora_query_status(segs) == 0
+    assert np.array_equal(segs.seg_start.cpu().numpy(), offsets)
+    perm = segs.perm.cpu().numpy()
+    assert np.array_equal(perm, np.arange(T))
+    check_tiles(segs, offsets, perm)
+
+
+@pytest.mark.parametrize("N", [4095, 5000])
+def test_route_inconsistent_offsets_many_adapters(N):
+    offsets = random_offsets(N, seed=7 + N)
+    offsets[N // 2] = offsets[N // 2 + 1] + 1  # one segment ends before it starts
+    T = int(offsets[-1])
+    off = torch.from_numpy(offsets).cuda()
+    segs = lora.lora_build_segments(seg_offsets=off, n_tokens=T, n_adapters=N)
+    assert lora.lora_query_status(segs) == 9
+    assert int(segs.n_tiles.item()) == 0 and int(segs.n_spans.item()) == 0
 
 
 @pytest.mark.parametrize("offsets,T", [([0, 9, 5, 12], 12), ([1, 4, 12], 12), ([0, 4, 11], 12)])
