@@ -218,6 +218,14 @@ LORA_API lora_status_t lora_packed_fwd(void *y, float *H_save, const void *x,
  *   ws       device workspace of >= lora_workspace_bytes(table, T) bytes; it carries
  *            bf16 copies of H and dH between the four cases (the dB, dA and dX
  *            products consume bf16 H / dH with fp32 accumulation)
+ * Reproducibility: dX (and the forward's y and H) come out bit-identical from
+ * run to run.  dA and dB are summed over spans of up to LORA_SPAN_TOKENS
+ * tokens, each span's fp32 partial added into the zeroed output as it
+ * finishes: for an adapter with at most two spans the result is still
+ * bit-identical (two additions to zero commute exactly); with more, the
+ * span partials may be added in a different order from run to run, so the
+ * last bits of dA / dB can differ (every order is within the same rounding
+ * of the exact sum).
  */
 LORA_API lora_status_t lora_packed_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X,
                               const float *H_saved, const lora_adapter_table *table,
