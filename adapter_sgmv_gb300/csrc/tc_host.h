@@ -34,7 +34,8 @@ bool make_tmap_f32_2d(CUtensorMap *map, const void *base, uint64_t cols, uint64_
 int sm_count();
 
 // Hand-off buffers between the kernels: bf16 [T, rw] rows in perm order (the
-// position of the token in its adapter's group), zero beyond each adapter's rank.
+// position of the token in its adapter's group), zero from each adapter's rank
+// up to the rank rounded to 16, unwritten past that (no product reads there).
 inline int32_t handoff_cols(int32_t r_max) { return r_max <= 64 ? 64 : 128; }
 
 // case i.  shrink: H[t, :] = A_i x_t.  Writes the fp32 H by token (H may be

@@ -317,7 +317,8 @@ lora_status_t launch_rowproj(const void *act, const void *w, int32_t d, const Ro
 namespace {
 
 // A saved fp32 H (by token, stride r_max) to the bf16 hand-off rows (by perm
-// position, stride rw, zero beyond each adapter's rank): one CTA per tile,
+// position, stride rw, zero from each adapter's rank up to the rank rounded to
+// 16, unwritten past that): one CTA per tile,
 // one thread per (row, 8 columns).  It runs beside case i (dh), so its CTAs
 // are kept small (1024-thread CTAs converted faster alone but crowded out dh's).
 __global__ void __launch_bounds__(256) h_to_bf16_kernel(const float *__restrict__ H, uint16_t *__restrict__ hb,
