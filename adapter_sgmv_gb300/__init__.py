@@ -24,7 +24,7 @@ __all__ = [
     "lora_sgmv_expand", "lora_packed_fwd", "lora_packed_bwd", "lora_packed_fwd_marked", "lora_packed_bwd_marked",
     "lora_packed_bwd_noalloc", "lora_adamw_step", "lora_fused_base_workspace_bytes", "lora_fused_base_fwd",
     "lora_multi_workspace_bytes", "lora_multi_fwd", "lora_plan_pack",
-    "lora_query_status", "lora_reset_status",
+    "lora_query_status", "lora_reset_status", "lora_check_wait_timeout",
     "STATUS",
 ]
 
@@ -110,6 +110,7 @@ SIGNATURES = {
                               ctypes.POINTER(ctypes.c_double)]),
     "lora_query_status": (_I32, [ctypes.POINTER(c_segments), _P]),
     "lora_reset_status": (_I32, [ctypes.POINTER(c_segments), _P]),
+    "lora_check_wait_timeout": (_I32, [_P, _P]),
 }
 
 
@@ -418,3 +419,9 @@ def lora_query_status(segs: Segments, stream=None) -> int:
 
 def lora_reset_status(segs: Segments, stream=None):
     _check(lib().lora_reset_status(ctypes.byref(segs.c), _stream(stream)), "lora_reset_status")
+
+
+def lora_check_wait_timeout(status, stream=None):
+    """Run the bounded pipeline wait against a barrier nothing completes; the
+    device int32 tensor ``status`` receives LORA_ERR_TIMEOUT (7) after ~2 s."""
+    _check(lib().lora_check_wait_timeout(_ptr(status), _stream(stream)), "lora_check_wait_timeout")

@@ -436,6 +436,18 @@ LORA_API lora_status_t lora_packed_bwd_noalloc(void *dX, float *dA, float *dB, c
                                                const float *H_saved, const lora_adapter_table *table,
                                                const lora_segments *segs, lora_stream_t stream);
 
+/*
+ * Diagnostic: runs the tensor-core kernels' bounded pipeline wait against a
+ * barrier that nothing completes (one CTA, two warps) and lets it give up:
+ * after about 2 s of SM clock (4e9 cycles) LORA_ERR_TIMEOUT is written to
+ * *status (device int32, 4-byte aligned; a nonzero value already there is
+ * kept) and the kernel returns.  Shows on a given GPU that a stalled pipeline
+ * ends with a status instead of a hang, and that the context stays usable.
+ * Stream-ordered; synchronise before reading *status.
+ * Errors: LORA_ERR_INVALID_ARG (NULL), LORA_ERR_ALIGNMENT, LORA_ERR_CUDA.
+ */
+LORA_API lora_status_t lora_check_wait_timeout(int32_t *status, lora_stream_t stream);
+
 /* Synchronise `stream` and return the device status word of `segs`. */
 LORA_API lora_status_t lora_query_status(const lora_segments *segs, lora_stream_t stream);
 

@@ -102,6 +102,8 @@ def test_host_side_rejections_return_before_any_cuda_call(L):
     assert L.lora_packed_bwd(None, None, None, None, 0x2000, None, ctypes.byref(t), ctypes.byref(s),
                              0x3000, 1 << 20, None) == 1
     assert L.lora_query_status(None, None) == 1
+    assert L.lora_check_wait_timeout(None, None) == 1
+    assert L.lora_check_wait_timeout(0x1002, None) == 3
 
 
 def test_binding_fails_loudly_without_the_library():
