@@ -121,3 +121,46 @@ def check_blocks(spec, got_dA, got_dB, ref_dA, ref_dB, adapters=None):
         errs[f"dA[{i}]"] = assert_close(got_dA[a0:a1], ref_dA[a0:a1], GRAD_TOL, f"dA_{i}")
         errs[f"dB[{i}]"] = assert_close(got_dB[a0:a1], ref_dB[a0:a1], GRAD_TOL, f"dB_{i}")
     return errs
+
+
+def worked_example(pad: int = 8) -> dict:
+    """The hand-worked two-adapter example of tests/golden/worked_two_adapters.json
+    as stacked arrays (A and B_i^T stacked by rank rows, dA / dB likewise), d_in
+    and d_out padded to ``pad`` with zero columns.  All values are small
+    integers (exact in bf16 / fp32 / fp64)."""
+    import json
+    import os
+
+    with open(os.path.join(os.path.dirname(__file__), "golden", "worked_two_adapters.json")) as f:
+        g = json.load(f)
+    ranks = np.asarray(g["ranks"], np.int32)
+    T = len(g["ids"])
+    sum_r = int(ranks.sum())
+    A = np.zeros((sum_r, pad))
+    B = np.zeros((sum_r, pad))
+    dA = np.zeros((sum_r, pad))
+    dB = np.zeros((sum_r, pad))
+    row = 0
+    for i, r in enumerate(ranks):
+        Ai = np.asarray(g["A_i"][str(i)], float)
+        Bi = np.asarray(g["B_i (d_out x r_i)"][str(i)], float)
+        dBi = np.asarray(g["expected"]["dB_i (d_out x r_i)"][str(i)], float)
+        dAi = np.asarray(g["expected"]["dA_i (r_i x d_in)"][str(i)], float)
+        A[row:row + r, :Ai.shape[1]] = Ai
+        B[row:row + r, :Bi.shape[0]] = Bi.T
+        dA[row:row + r, :dAi.shape[1]] = dAi
+        dB[row:row + r, :dBi.shape[0]] = dBi.T
+        row += r
+
+    def padded(key, width):
+        v = np.asarray(key, float)
+        out = np.zeros((v.shape[0], width))
+        out[:, :v.shape[1]] = v
+        return out
+
+    e = g["expected"]
+    return {"ranks": ranks, "alphas": np.asarray(g["alphas"], float), "scales": np.asarray(g["scales"], float),
+            "ids": np.asarray(g["ids"], np.int32), "A": A, "B": B, "x": padded(g["x"], pad),
+            "dY": padded(g["dy"], pad), "T": T, "r_max": int(ranks.max()),
+            "H": padded(e["H (T x r_max, zero past r_i)"], int(ranks.max())), "y": padded(e["y (y0 = 0)"], pad),
+            "dH": padded(e["dH"], int(ranks.max())), "dX": padded(e["dX (dX0 = 0)"], pad), "dA": dA, "dB": dB}

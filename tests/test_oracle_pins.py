@@ -461,3 +461,18 @@ def test_layer_forward_reduces_to_its_parts():
     assert np.array_equal(y, y_d) and np.array_equal(H, H_d)
     y0, _ = oracle.base_lora_fwd(P["tab"], P["ids"], W, np.zeros_like(P["A"]), P["B"], P["x"])
     close(y0, P["x"] @ W.T)
+
+
+# ---------------------------------------------------------------- hand-worked example
+def test_oracle_reproduces_the_hand_worked_example_exactly():
+    # tests/golden/worked_two_adapters.json: two adapters of rank 1 and 2, three
+    # unsorted tokens, every product worked out by hand in small integers
+    from lora_testlib import worked_example
+
+    g = worked_example()
+    tab = oracle.Table(g["ranks"], g["scales"])
+    y, H = oracle.fwd(tab, g["ids"], g["A"], g["B"], g["x"], np.zeros_like(g["y"]))
+    dH, dA, dB, dX = oracle.bwd(tab, g["ids"], g["A"], g["B"], g["x"], H, g["dY"], np.zeros_like(g["dX"]))
+    for name, got, want in (("y", y, g["y"]), ("H", H, g["H"]), ("dH", dH, g["dH"]), ("dA", dA, g["dA"]),
+                            ("dB", dB, g["dB"]), ("dX", dX, g["dX"])):
+        assert np.array_equal(got, want), name
