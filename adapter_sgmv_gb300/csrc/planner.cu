@@ -32,6 +32,8 @@
 //                tried are the part durations themselves, plus every job cut
 //                into single configurations, and the plan that ends first
 //                under the placement below is kept (ties keep fewer jobs);
+//                then, while it helps, one job at a time is cut into one part
+//                more or one fewer (the change that ends the pool soonest);
 //   placement    the jobs, longest first, each on the GPU that frees first.
 //
 // The parallelism degree of a job is one GPU: the library's jobs run on a
@@ -286,6 +288,30 @@ lora_status_t plan_pack(const lora_plan_config *configs, int32_t n_configs, cons
             best_mk = mk;
             best_g = g_of;
         }
+    }
+    // refinement: one job at a time cut into one part more or one fewer; the
+    // change that ends the pool soonest (strictly sooner than now; ties: the
+    // lower job, one more before one fewer) is taken, until none helps.  Every
+    // step shortens the makespan, so this ends; the bound only caps the work.
+    for (int32_t step = 0; step < 4 * n_configs; ++step) {
+        double cand_mk = best_mk;
+        std::vector<int> cand;
+        for (int32_t j = 0; j < n_sets; ++j) {
+            for (int dg : {1, -1}) {
+                const int g = best_g[j] + dg;
+                if (g < 1 || g > (int)sets[j].size()) continue;
+                std::vector<int> t = best_g;
+                t[j] = g;
+                const double mk = place(durations(t), cost->n_gpus, nullptr, nullptr);
+                if (mk < cand_mk) {
+                    cand_mk = mk;
+                    cand = t;
+                }
+            }
+        }
+        if (cand.empty()) break;
+        best_mk = cand_mk;
+        best_g = cand;
     }
 
     // the kept plan: jobs in round order, a job's parts in part order

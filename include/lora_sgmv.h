@@ -366,7 +366,9 @@ LORA_API lora_status_t lora_fused_base_fwd(void *y, float *H_save, const void *x
  * end within D (configurations dealt, largest step cost first, to the part
  * with the least cost so far); the caps tried are the parts' own durations,
  * plus every job cut into single configurations, and the plan that ends
- * first is kept (the uncut plan on ties, then fewer jobs).  Jobs are placed
+ * first is kept (the uncut plan on ties, then fewer jobs); then, while it
+ * helps, one job at a time is cut into one part more or one fewer (the change
+ * that ends the pool soonest, strictly sooner).  Jobs are placed
  * longest first, each on the GPU that frees first (lowest index on ties); a
  * job uses one GPU.  The plan never ends later than the uncut rounds' jobs
  * or than one configuration per job under the same placement.
@@ -380,7 +382,7 @@ LORA_API lora_status_t lora_fused_base_fwd(void *y, float *H_save, const void *x
  * longest configuration, a knapsack pass per Dinkelbach iteration), plus
  * |S|^3 for cutting a job of |S| configurations: meant for search spaces of a
  * few hundred configurations and budgets of a few thousand units (120
- * configurations, 4200 units: ~0.2 s).
+ * configurations, 4200 units: ~0.1-0.3 s).
  * Errors: LORA_ERR_INVALID_ARG (NULL, negative cost terms, a zero-time step),
  * LORA_ERR_SHAPE (a configuration that does not fit one GPU alone, sizes out
  * of range, a memory budget of more than 2^20 units, n_configs x (budget

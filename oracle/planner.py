@@ -23,7 +23,10 @@ readings stated in the library's header:
                the cuts' longest parts, from the largest down, each job takes
                its smallest g whose parts all end within D; last, every job
                cut into single configurations.  The first plan (uncut) and
-               then every plan that ends strictly sooner is kept.
+               then every plan that ends strictly sooner is kept.  Then, while
+               one exists, the plan one job away (that job cut into one part
+               more or one fewer) that ends soonest, strictly sooner than the
+               current one, replaces it.
   placement    jobs longest first (stable), each on the GPU that frees first
                (lowest index on ties)
 
@@ -119,6 +122,22 @@ def plan(configs, cost):
         mk = place([p["dur"] for p in plan_of(gs)])[0]
         if mk < best_mk:
             best_mk, best_g = mk, gs
+    # refinement: every plan one job away (one part more or one fewer); the one
+    # that ends soonest, if strictly sooner (ties: lower job, then one more part)
+    for _ in range(4 * len(configs)):
+        cand = None
+        for j in range(len(sets)):
+            for dg in (1, -1):
+                g = best_g[j] + dg
+                if 1 <= g <= len(sets[j]):
+                    t = list(best_g)
+                    t[j] = g
+                    mk = place([p["dur"] for p in plan_of(t)])[0]
+                    if mk < (best_mk if cand is None else cand[0]):
+                        cand = (mk, t)
+        if cand is None:
+            break
+        best_mk, best_g = cand
 
     parts = plan_of(best_g)
     makespan, where = place([p["dur"] for p in parts])

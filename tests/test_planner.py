@@ -8,7 +8,8 @@ short configuration does not ride along with a long one when it would waste
 the job's steps; longest-first placement of durations 5, 4, 3 on two GPUs
 ends at 7; a four-configuration job is cut in two across two GPUs (41 s ->
 21 s), never on one GPU, and a cut into three that ends no sooner is not
-taken.  Parity: the library's plan equals the exhaustive search on random
+taken; one job cut into one part more when no common cap helps (20 s ->
+19 s).  Parity: the library's plan equals the exhaustive search on random
 instances (partitions and predicted times), including grouped instances on
 2-8 GPUs where the cuts decide the plan, which never ends later than the
 uncut jobs or one configuration per job.  Invariants at the size of PLoRA's
@@ -105,6 +106,25 @@ def test_one_gpu_never_cuts_and_ties_keep_fewer_jobs():
         got = lora.lora_plan_pack(c, dict(base, n_gpus=n))
         want = oplan.plan(c, dict(base, n_gpus=n))
         assert got["job_of"] == want["job_of"] and math.isclose(got["makespan_s"], want["makespan_s"])
+
+
+def test_one_more_part_for_one_job_when_no_common_cap_helps():
+    # five configs (steps, step cost): c0 (1, 2), c1 (1, 1), c2 (2, 2), c3 (2, 2), c4 (2, 4); t0 = 3; two GPUs.
+    # Rounds: {0,1} rate 2 / (1 * 6) = 0.333, then {2,3} 4 / (2 * 7) = 0.286 (over {2,3,4} 6 / 22), then {4}.
+    # Uncut jobs 6, 14, 14 s -> 14 | 14 + 6 = 20.  Caps: 14 is the uncut plan; 10, 6 and 5 cannot hold {4}
+    # (14 s); every job cut into singles (5, 4, 10, 10, 14) ends at 23.  One job away: {0,1} in two parts
+    # (5 and 4 s) -> 14 + 5 | 14 + 4 = 19; {2,3} in two parts (10, 10) -> 20.  So {0}, {1}, {2,3}, {4}.
+    cost = {"step_overhead_s": 3.0, "lora_s_per_token_rank": 1.0, "gpu_mem_bytes": 10 * GB, "mem_unit_bytes": GB,
+            "n_gpus": 2}
+    c = [cfg(2, 1, 1, GB), cfg(1, 1, 1, GB), cfg(2, 1, 2, GB), cfg(2, 1, 2, GB), cfg(4, 1, 2, GB)]
+    p = oplan.plan(c, cost)
+    assert p["sets"] == [[0, 1], [2, 3], [4]]
+    assert p["parts"] == [[0], [1], [2, 3], [4]] and p["job_of"] == [0, 1, 2, 2, 3]
+    assert math.isclose(p["makespan_s"], 19.0, rel_tol=1e-12)
+    assert [(j["gpu"], j["start_s"], j["duration_s"]) for j in p["jobs"]] == [(0, 14.0, 5.0), (1, 14.0, 4.0),
+                                                                            (0, 0.0, 14.0), (1, 0.0, 14.0)]
+    got = lora.lora_plan_pack(c, cost)
+    assert got["job_of"] == p["job_of"] and math.isclose(got["makespan_s"], 19.0, rel_tol=1e-12)
 
 
 # ---------------------------------------------------------------- library vs oracle
