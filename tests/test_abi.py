@@ -26,7 +26,7 @@ def declared_functions():
     return sorted(set(re.findall(r"\b(lora_[a-z_]+)\s*\(", text)))
 
 
-def test_header_declares_the_north_star_calls():
+def test_header_declares_the_hot_path_calls():
     names = declared_functions()
     for n in ("lora_sgmv_shrink", "lora_sgmv_expand", "lora_packed_fwd", "lora_packed_bwd",
               "lora_build_segments"):
