@@ -21,7 +21,8 @@ from ._build import LIB_PATH, build as build_library  # noqa: F401
 __all__ = [
     "LoraError", "AdapterTable", "Segments", "lib", "lora_abi_version", "lora_status_string",
     "lora_segments_bytes", "lora_build_segments", "lora_workspace_bytes", "lora_sgmv_shrink",
-    "lora_sgmv_expand", "lora_packed_fwd", "lora_packed_bwd", "lora_packed_fwd_marked", "lora_packed_bwd_marked",
+    "lora_sgmv_expand", "lora_packed_fwd", "lora_packed_bwd", "lora_packed_bwd_concurrent", "SideStreams",
+    "lora_packed_fwd_marked", "lora_packed_bwd_marked",
     "lora_packed_bwd_noalloc", "lora_adamw_step", "lora_fused_base_workspace_bytes", "lora_fused_base_fwd",
     "lora_multi_workspace_bytes", "lora_multi_fwd", "lora_plan_pack",
     "lora_query_status", "lora_reset_status", "lora_check_wait_timeout",
@@ -54,6 +55,10 @@ class c_segments(ctypes.Structure):
                 ("tiles", ctypes.c_void_p), ("n_tiles", ctypes.c_void_p), ("status", ctypes.c_void_p),
                 ("scratch", ctypes.c_void_p), ("scratch_words", ctypes.c_int64), ("max_spans", ctypes.c_int32),
                 ("reserved", ctypes.c_int32), ("spans", ctypes.c_void_p), ("n_spans", ctypes.c_void_p)]
+
+
+class c_side_streams(ctypes.Structure):
+    _fields_ = [("stream", ctypes.c_void_p * 2), ("event", ctypes.c_void_p * 4)]
 
 
 class c_plan_config(ctypes.Structure):
@@ -91,6 +96,8 @@ SIGNATURES = {
     "lora_packed_fwd": (_I32, [_P, _P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments), _P, _SZ, _P]),
     "lora_packed_bwd": (_I32, [_P, _P, _P, _P, _P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments),
                                _P, _SZ, _P]),
+    "lora_packed_bwd_concurrent": (_I32, [_P, _P, _P, _P, _P, _P, ctypes.POINTER(c_table),
+                                          ctypes.POINTER(c_segments), _P, _SZ, ctypes.POINTER(c_side_streams), _P]),
     "lora_packed_fwd_marked": (_I32, [_P, _P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments), _P, _SZ,
                                       _P, ctypes.POINTER(_P), _I32, ctypes.POINTER(_I32)]),
     "lora_packed_bwd_marked": (_I32, [_P, _P, _P, _P, _P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments),
@@ -297,6 +304,32 @@ def lora_packed_bwd(dX, dA, dB, dY, X, H_saved, table: AdapterTable, segs: Segme
     _check(lib().lora_packed_bwd(_ptr(dX), _ptr(dA), _ptr(dB), _ptr(dY), _ptr(X), _ptr(H_saved),
                                  ctypes.byref(table.c), ctypes.byref(segs.c), _ptr(ws), wsb, _stream(stream)),
            "lora_packed_bwd")
+
+
+class SideStreams:
+    """Two CUDA streams and four events owned by the caller, on which
+    lora_packed_bwd_concurrent runs dB and dA beside dh and dX.  One set per
+    host thread that runs backward calls at the same time."""
+
+    def __init__(self, device=None):
+        import torch
+
+        self.streams = [torch.cuda.Stream(device) for _ in range(2)]
+        self.events = [torch.cuda.Event() for _ in range(4)]
+        for e in self.events:  # torch creates the event handle on first record
+            e.record(self.streams[0])
+        torch.cuda.current_stream(device).wait_stream(self.streams[0])
+        self.c = c_side_streams((ctypes.c_void_p * 2)(*[s.cuda_stream for s in self.streams]),
+                                (ctypes.c_void_p * 4)(*[e.cuda_event for e in self.events]))
+
+
+def lora_packed_bwd_concurrent(dX, dA, dB, dY, X, H_saved, table: AdapterTable, segs: Segments, ws,
+                               side: SideStreams, stream=None):
+    """lora_packed_bwd with dB and dA on the caller's side streams (same results)."""
+    wsb = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().lora_packed_bwd_concurrent(_ptr(dX), _ptr(dA), _ptr(dB), _ptr(dY), _ptr(X), _ptr(H_saved),
+                                            ctypes.byref(table.c), ctypes.byref(segs.c), _ptr(ws), wsb,
+                                            ctypes.byref(side.c), _stream(stream)), "lora_packed_bwd_concurrent")
 
 
 def _events(events, stream):

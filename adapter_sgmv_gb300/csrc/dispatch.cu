@@ -5,8 +5,6 @@
 //   backward: a small kernel converts the saved H to bf16 in perm order (or
 //             case i recomputes it from X); case i (dh) writes bf16 dH in perm
 //             order; case iii (dB), case iv (dA) and case ii (dX) read those.
-#include <mutex>
-
 #include "dispatch.h"
 #include "tc_host.h"
 
@@ -45,41 +43,6 @@ namespace {
 void mark(Marks *m, cudaStream_t stream)
 {
     if (m != nullptr && m->k < m->n) cudaEventRecord(static_cast<cudaEvent_t>(m->ev[m->k++]), stream);
-}
-
-// Two streams and three events per device on which the backward runs its
-// three independent products (dB, dA, dX) side by side, so that the tail of
-// one kernel's last wave overlaps the others.  Created on first use and kept;
-// the mutex also serialises the enqueue of each fork / join, so that calls
-// from several host threads never wait on each other's events.
-constexpr int kMaxDevices = 64;
-struct Side {
-    cudaStream_t s[2];
-    cudaEvent_t ev[4];
-    bool ready;
-};
-Side g_side[kMaxDevices];
-std::mutex g_side_mu;
-
-Side *side_for_device()  // called with g_side_mu held; nullptr: run serially
-{
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    Side &S = g_side[dev];
-    if (!S.ready) {
-        for (auto &st : S.s)
-            if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) {
-                cudaGetLastError();
-                return nullptr;
-            }
-        for (auto &e : S.ev)
-            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
-                cudaGetLastError();
-                return nullptr;
-            }
-        S.ready = true;
-    }
-    return &S;
 }
 
 // launch `f` between a pair of marks
@@ -136,7 +99,8 @@ lora_status_t run_multi_fwd(int32_t n_proj, void *const *y, float *const *H_save
 }
 
 lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X, const float *H_saved, void *ws,
-                      const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream, Marks *marks)
+                      const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream, Marks *marks,
+                      const SideStreams *side)
 {
     const int32_t rw = handoff_cols(tab.r_max);
     uint16_t *hb = static_cast<uint16_t *>(ws);
@@ -147,23 +111,23 @@ lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void
     if (dA != nullptr && cudaMemsetAsync(dA, 0, (size_t)tab.sum_r * tab.d_in * sizeof(float), stream) != cudaSuccess)
         return LORA_ERR_CUDA;
     lora_status_t st = LORA_OK;
-    // dB needs only dY and the bf16 rows of H, so it runs beside case i (dh);
-    // dA and dX need dh.  Side stream B: [H to bf16], dB; the caller's stream:
-    // [the shrink, when H is not saved], dh, dX; side stream A: dA after dh.
-    // (a marked call runs everything one after another on the caller's
-    // stream, so that each event pair brackets one kernel alone)
-    std::lock_guard<std::mutex> lock(g_side_mu);
-    Side *sd = (marks == nullptr && (dB != nullptr || dA != nullptr)) ? side_for_device() : nullptr;
-    cudaStream_t sB = sd != nullptr ? sd->s[0] : stream, sA = sd != nullptr ? sd->s[1] : stream;
+    // dB needs only dY and the bf16 rows of H, so with side streams it runs
+    // beside case i (dh); dA and dX need dh.  Side stream 0: [H to bf16], dB;
+    // the caller's stream: [the shrink, when H is not saved], dh, dX; side
+    // stream 1: dA after dh.  Without side streams (and in a marked call, so
+    // that each event pair brackets one kernel alone) everything runs one
+    // after another on the caller's stream.
+    const bool par = side != nullptr && marks == nullptr && (dB != nullptr || dA != nullptr);
+    cudaStream_t sB = par ? side->s[0] : stream, sA = par ? side->s[1] : stream;
     // fork: the side stream waits for what the caller's stream has issued so far
-    auto fork = [&](cudaEvent_t ev, cudaStream_t side) {
-        return cudaEventRecord(ev, stream) == cudaSuccess && cudaStreamWaitEvent(side, ev, 0) == cudaSuccess;
+    auto fork = [&](cudaEvent_t ev, cudaStream_t on) {
+        return cudaEventRecord(ev, stream) == cudaSuccess && cudaStreamWaitEvent(on, ev, 0) == cudaSuccess;
     };
     bool forked_B = false, forked_A = false;
     if (H_saved == nullptr)
         st = marked(marks, stream, [&] { return tc_shrink(X, tab, segs, nullptr, hb, nullptr, rw, stream); });
-    if (st == LORA_OK && sd != nullptr && dB != nullptr) {  // fork B once the outputs are zeroed (and H recomputed)
-        forked_B = fork(sd->ev[0], sB);
+    if (st == LORA_OK && par && dB != nullptr) {  // fork B once the outputs are zeroed (and H recomputed)
+        forked_B = fork(side->ev[0], sB);
         if (!forked_B) st = LORA_ERR_CUDA;
     }
     if (st == LORA_OK && dB != nullptr) {
@@ -173,8 +137,8 @@ lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void
     }
     if (st == LORA_OK)
         st = marked(marks, stream, [&] { return tc_dh(dY, tab, segs, dhb, rw, stream); });
-    if (st == LORA_OK && sd != nullptr && dA != nullptr) {  // fork A after dh
-        forked_A = fork(sd->ev[3], sA);
+    if (st == LORA_OK && par && dA != nullptr) {  // fork A after dh
+        forked_A = fork(side->ev[3], sA);
         if (!forked_A) st = LORA_ERR_CUDA;
     }
     if (st == LORA_OK && dA != nullptr) st = marked(marks, sA, [&] { return tc_da(dA, X, dhb, rw, tab, segs, sA); });
@@ -183,11 +147,11 @@ lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void
     // join: the caller's stream waits for every side stream that was forked,
     // after an error too, so that no work of this call outlives it unordered
     // with the caller's stream (and a capture is never left with an open fork)
-    auto join = [&](cudaEvent_t ev, cudaStream_t side) {
-        return cudaEventRecord(ev, side) == cudaSuccess && cudaStreamWaitEvent(stream, ev, 0) == cudaSuccess;
+    auto join = [&](cudaEvent_t ev, cudaStream_t on) {
+        return cudaEventRecord(ev, on) == cudaSuccess && cudaStreamWaitEvent(stream, ev, 0) == cudaSuccess;
     };
-    if (forked_B && !join(sd->ev[1], sB) && st == LORA_OK) st = LORA_ERR_CUDA;
-    if (forked_A && !join(sd->ev[2], sA) && st == LORA_OK) st = LORA_ERR_CUDA;
+    if (forked_B && !join(side->ev[1], sB) && st == LORA_OK) st = LORA_ERR_CUDA;
+    if (forked_A && !join(side->ev[2], sA) && st == LORA_OK) st = LORA_ERR_CUDA;
     return st;
 }
 

@@ -28,9 +28,16 @@ lora_status_t run_fwd(void *y, float *H_save, const void *x, void *ws, const lor
 size_t multi_workspace_bytes(int32_t n_proj, const lora_adapter_table *tabs, int32_t T);
 lora_status_t run_multi_fwd(int32_t n_proj, void *const *y, float *const *H_save, const void *x, void *ws,
                             const lora_adapter_table *tabs, const lora_segments &segs, cudaStream_t stream);
+// Caller-owned streams and events on which the backward may run its
+// independent products side by side (lora_packed_bwd_concurrent).
+struct SideStreams {
+    cudaStream_t s[2];
+    cudaEvent_t ev[4];
+};
+
 lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X, const float *H_saved, void *ws,
                       const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream,
-                      Marks *marks = nullptr);
+                      Marks *marks = nullptr, const SideStreams *side = nullptr);
 
 // one AdamW step over A and B^T (fp32 masters, moments) and their bf16 copies
 // in the table (adamw.cu)

@@ -28,18 +28,15 @@ lora_status_t build_segments(const int32_t *ids, const int32_t *seg_offsets, int
                              void *storage, size_t storage_bytes, lora_segments *out,
                              cudaStream_t stream);
 
-// generic SIMT kernels (any rank, any routing), each launch stream-ordered
-lora_status_t simt_shrink(float *H, const void *x, const lora_adapter_table &tab,
-                          const lora_segments &segs, cudaStream_t stream);
-lora_status_t simt_dh(float *dH, const void *dY, const lora_adapter_table &tab,
-                      const lora_segments &segs, cudaStream_t stream);
-lora_status_t simt_expand(void *y, const float *H, const lora_adapter_table &tab,
-                          const lora_segments &segs, cudaStream_t stream);
-lora_status_t simt_dx(void *dX, const float *dH, const lora_adapter_table &tab,
-                      const lora_segments &segs, cudaStream_t stream);
-lora_status_t simt_db(float *dB, const void *dY, const float *H, const lora_adapter_table &tab,
-                      const lora_segments &segs, cudaStream_t stream);
-lora_status_t simt_da(float *dA, const float *dH, const void *X, const lora_adapter_table &tab,
-                      const lora_segments &segs, cudaStream_t stream);
+// Host-side argument checks shared by the entry points (lora_sgmv.cu,
+// noalloc.cu): each returns LORA_OK or the status to report, before anything
+// is launched.
+bool aligned16(const void *p);
+bool aligned4(const void *p);
+lora_status_t check_table(const lora_adapter_table *t);
+// segs against the table (t may be null to check segs alone)
+lora_status_t check_segs(const lora_segments *s, const lora_adapter_table *t);
+// the current device is an sm_103 GPU (the library holds code for sm_103a only)
+lora_status_t check_device();
 
 }  // namespace lora

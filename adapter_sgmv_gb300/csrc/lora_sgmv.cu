@@ -12,7 +12,7 @@
 
 using namespace lora;
 
-namespace {
+namespace lora {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -34,14 +34,20 @@ lora_status_t check_table(const lora_adapter_table *t)
     return LORA_OK;
 }
 
+// Every pointer the kernels dereference must be present: the tile and span
+// counts are read on the device before anything else.
 lora_status_t check_segs(const lora_segments *s, const lora_adapter_table *t)
 {
     if (s == nullptr) return LORA_ERR_INVALID_ARG;
     if (s->perm == nullptr || s->seg_start == nullptr || s->tiles == nullptr || s->n_tiles == nullptr ||
-        s->status == nullptr)
+        s->status == nullptr || s->spans == nullptr || s->n_spans == nullptr)
         return LORA_ERR_INVALID_ARG;
-    if (s->n_tokens < 0 || s->n_tokens > kMaxTokens || s->max_tiles < 0) return LORA_ERR_SHAPE;
+    if (s->n_tokens < 0 || s->n_tokens > kMaxTokens || s->n_adapters < 1 || s->max_tiles < 0 || s->max_spans < 0)
+        return LORA_ERR_SHAPE;
     if (t != nullptr && s->n_adapters != t->n_adapters) return LORA_ERR_SHAPE;
+    if (!aligned4(s->perm) || !aligned4(s->seg_start) || !aligned16(s->tiles) || !aligned16(s->spans) ||
+        !aligned4(s->n_tiles) || !aligned4(s->n_spans) || !aligned4(s->status))
+        return LORA_ERR_ALIGNMENT;
     return LORA_OK;
 }
 
@@ -55,6 +61,10 @@ lora_status_t check_device()
     if (major != 10 || minor != 3) return LORA_ERR_UNSUPPORTED;  // built for sm_103a only
     return LORA_OK;
 }
+
+}  // namespace lora
+
+namespace {
 
 size_t workspace_bytes(const lora_adapter_table *t, int32_t T) { return packed_workspace_bytes(T, t->r_max); }
 
@@ -82,7 +92,7 @@ lora_status_t packed_fwd(void *y, float *H_save, const void *x, const lora_adapt
 
 lora_status_t packed_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X, const float *H_saved,
                          const lora_adapter_table *table, const lora_segments *segs, void *ws, size_t ws_bytes,
-                         lora_stream_t stream, Marks *marks)
+                         lora_stream_t stream, Marks *marks, const SideStreams *side = nullptr)
 {
     LORA_TRY(check_table(table));
     LORA_TRY(check_segs(segs, table));
@@ -94,7 +104,7 @@ lora_status_t packed_bwd(void *dX, float *dA, float *dB, const void *dY, const v
     if (need > 0 && (ws == nullptr || ws_bytes < need)) return LORA_ERR_WORKSPACE_TOO_SMALL;
     LORA_TRY(check_device());
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return run_bwd(dX, dA, dB, dY, X, H_saved, ws, *table, *segs, st, marks);
+    return run_bwd(dX, dA, dB, dY, X, H_saved, ws, *table, *segs, st, marks, side);
 }
 
 }  // namespace
@@ -186,6 +196,27 @@ lora_status_t lora_packed_bwd(void *dX, float *dA, float *dB, const void *dY, co
                               const lora_segments *segs, void *ws, size_t ws_bytes, lora_stream_t stream)
 {
     return packed_bwd(dX, dA, dB, dY, X, H_saved, table, segs, ws, ws_bytes, stream, nullptr);
+}
+
+lora_status_t lora_packed_bwd_concurrent(void *dX, float *dA, float *dB, const void *dY, const void *X,
+                                         const float *H_saved, const lora_adapter_table *table,
+                                         const lora_segments *segs, void *ws, size_t ws_bytes,
+                                         const lora_side_streams *side, lora_stream_t stream)
+{
+    if (side == nullptr) return LORA_ERR_INVALID_ARG;
+    SideStreams sd;
+    for (int i = 0; i < 2; ++i) {
+        if (side->stream[i] == nullptr || side->stream[i] == stream) return LORA_ERR_INVALID_ARG;
+        sd.s[i] = reinterpret_cast<cudaStream_t>(side->stream[i]);
+    }
+    if (side->stream[0] == side->stream[1]) return LORA_ERR_INVALID_ARG;
+    for (int i = 0; i < 4; ++i) {
+        if (side->event[i] == nullptr) return LORA_ERR_INVALID_ARG;
+        for (int j = 0; j < i; ++j)
+            if (side->event[j] == side->event[i]) return LORA_ERR_INVALID_ARG;
+        sd.ev[i] = static_cast<cudaEvent_t>(side->event[i]);
+    }
+    return packed_bwd(dX, dA, dB, dY, X, H_saved, table, segs, ws, ws_bytes, stream, nullptr, &sd);
 }
 
 lora_status_t lora_packed_fwd_marked(void *y, float *H_save, const void *x, const lora_adapter_table *table,

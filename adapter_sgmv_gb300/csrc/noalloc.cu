@@ -57,8 +57,6 @@ void *scratch_address()
     return g_addr[dev];
 }
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 }  // namespace lora
 
@@ -69,29 +67,18 @@ extern "C" LORA_API lora_status_t lora_packed_bwd_noalloc(void *dX, float *dA, f
                                                           const lora_adapter_table *table,
                                                           const lora_segments *segs, lora_stream_t stream)
 {
-    if (table == nullptr || segs == nullptr || dY == nullptr || X == nullptr) return LORA_ERR_INVALID_ARG;
-    if (table->rank == nullptr || table->row_off == nullptr || table->scale == nullptr || table->A == nullptr ||
-        table->B == nullptr || segs->perm == nullptr || segs->tiles == nullptr || segs->status == nullptr)
-        return LORA_ERR_INVALID_ARG;
-    if (table->n_adapters < 1 || table->n_adapters > kMaxAdapters || table->r_max < 1 ||
-        table->r_max > LORA_MAX_RANK || table->d_in < 8 || table->d_in > kMaxDim || (table->d_in % 8) != 0 ||
-        table->d_out < 8 || table->d_out > kMaxDim || (table->d_out % 8) != 0 || table->sum_r < table->r_max ||
-        (int64_t)table->sum_r > (int64_t)table->n_adapters * table->r_max)
-        return LORA_ERR_SHAPE;
-    if (segs->n_adapters != table->n_adapters || segs->n_tokens < 0 || segs->n_tokens > kMaxTokens)
-        return LORA_ERR_SHAPE;
+    // the checks lora_packed_bwd makes, in the same order, so that a caller
+    // error gives the same status here and never reaches the device
+    lora_status_t st = check_table(table);
+    if (st == LORA_OK) st = check_segs(segs, table);
+    if (st != LORA_OK) return st;
+    if (dY == nullptr || X == nullptr) return LORA_ERR_INVALID_ARG;
     if (!aligned16(dY) || !aligned16(X) || (dX && !aligned16(dX)) || (dA && !aligned16(dA)) ||
-        (dB && !aligned16(dB)) || (H_saved && !aligned16(H_saved)) || !aligned16(table->A) ||
-        !aligned16(table->B))
+        (dB && !aligned16(dB)) || (H_saved && !aligned16(H_saved)))
         return LORA_ERR_ALIGNMENT;
-    const int32_t T = segs->n_tokens;
-    if (packed_workspace_bytes(T, table->r_max) > kScratchBytes) return LORA_ERR_WORKSPACE_TOO_SMALL;
-    int dev = 0, major = 0, minor = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-        return LORA_ERR_CUDA;
-    if (major != 10 || minor != 3) return LORA_ERR_UNSUPPORTED;
+    if (packed_workspace_bytes(segs->n_tokens, table->r_max) > kScratchBytes) return LORA_ERR_WORKSPACE_TOO_SMALL;
+    st = check_device();
+    if (st != LORA_OK) return st;
     void *base = scratch_address();
     if (base == nullptr) return LORA_ERR_CUDA;
     return run_bwd(dX, dA, dB, dY, X, H_saved, base, *table, *segs, reinterpret_cast<cudaStream_t>(stream));

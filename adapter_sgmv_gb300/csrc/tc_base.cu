@@ -8,7 +8,8 @@
 // Engine"); the delta rides on the base GEMM's accumulators instead of
 // making another pass over y.
 //
-// Work is a list of tasks, handed out round-robin to one CTA per SM:
+// Work is a list of tasks that the CTAs (one per SM) claim in index order
+// from a global atomic counter:
 //   h task (routing tile m of up to 128 tokens of adapter i): h = x A_i^T
 //     accumulated in TMEM over d_in (M = 128, N = r_i rounded up to 16), then
 //     written as fp32 H (optional, for the backward) and as bf16 s_i h to a

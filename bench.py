@@ -197,6 +197,7 @@ class Workload:
         self.dX = self.inp["dX0"]
         self.dA = torch.empty((spec.sum_r, spec.d_in), dtype=torch.float32, device=dev)
         self.dB = torch.empty((spec.sum_r, spec.d_out), dtype=torch.float32, device=dev)
+        self.side = lora.SideStreams(dev)  # the backward's dB / dA run on these beside dh / dX
         self.segs = None
 
     def build(self, stream=None):
@@ -223,8 +224,8 @@ class Workload:
         x = self.inp["x"] if x is None else x
         dY = self.inp["dY"] if dY is None else dY
         if events is None:
-            lora.lora_packed_bwd(self.dX, self.dA, self.dB, dY, x, self.H, self.table, self.segs, self.ws,
-                                 stream=stream)
+            lora.lora_packed_bwd_concurrent(self.dX, self.dA, self.dB, dY, x, self.H, self.table, self.segs, self.ws,
+                                            self.side, stream=stream)
         else:
             lora.lora_packed_bwd_marked(self.dX, self.dA, self.dB, dY, x, self.H, self.table, self.segs, self.ws,
                                         events, stream=stream)
@@ -270,6 +271,25 @@ def time_steps(work: Workload, steps: int, warmup: int, stream, per_kernel: bool
     return start, end, ev, (kev if per_kernel else None)
 
 
+def kernel_times(work: Workload, steps: int, stream, hbm: float) -> dict:
+    """Each kernel's mean duration over `steps` steps in which the library
+    records an event pair around every kernel of the packed calls (the
+    backward's kernels then run one after another on `stream`), with its
+    algorithmic bytes and the fraction of the HBM peak they reach."""
+    import torch
+
+    _, _, _, kev = time_steps(work, steps, 1, stream, per_kernel=True)
+    torch.cuda.synchronize()
+    kb = kernel_bytes(work.spec)
+    out = {}
+    for j, (use, tmpl) in enumerate(STEP_KERNELS):
+        ms = statistics.mean(row[2 * j].elapsed_time(row[2 * j + 1]) for row in kev)
+        gbs = kb[use] / (ms * 1e-3) / 1e9
+        out[use] = {"kernel": tmpl, "ms": round(ms, 4), "bytes": kb[use], "GB/s": round(gbs, 1),
+                    "frac_of_hbm": round(gbs / hbm, 4)}
+    return out
+
+
 def time_config(spec: wl.Spec, dev, stream, steps: int = 10, warmup: int = 3, sequential: bool = False) -> dict:
     """One full step (build + fwd + bwd) of another workload: ms and tokens/s.
     With `sequential`, the same step is also timed as one single-adapter step
@@ -284,7 +304,8 @@ def time_config(spec: wl.Spec, dev, stream, steps: int = 10, warmup: int = 3, se
     hbm, _, _ = measured_peaks()
     out = {"tokens": spec.n_tokens, "ms_per_step": round(ms, 4), "tokens/s": round(spec.n_tokens / (ms * 1e-3), 1),
            "GB/s": round((by["fwd"] + by["bwd"]) / (ms * 1e-3) / 1e9, 1),
-           "frac_of_hbm": round((by["fwd"] + by["bwd"]) / (ms * 1e-3) / 1e9 / hbm, 4)}
+           "frac_of_hbm": round((by["fwd"] + by["bwd"]) / (ms * 1e-3) / 1e9 / hbm, 4),
+           "kernels_ms": kernel_times(work, steps, stream, hbm)}
     del work
     torch.cuda.empty_cache()
     if sequential:
@@ -780,6 +801,9 @@ def run_ours(args, rank, world, dev):
     if args.decode_only:  # the decode measurement alone (profiling runs)
         return ({"decode_sgmv": time_decode(dev, stream), "decode_multi_projection": time_decode_multi(dev, stream)}
                 if rank == 0 else None)
+    if args.only is not None:  # one workload's steps alone (profiling runs)
+        return {"workload": args.only, **time_config(named_workload(args.only), dev, stream, steps=args.steps,
+                                                       warmup=args.warmup)} if rank == 0 else None
     spec = wl.packed4096(tokens_per_adapter=args.tokens_per_adapter)
     work = Workload(spec, dev)
     torch.cuda.synchronize()
@@ -892,6 +916,16 @@ def run_ours(args, rank, world, dev):
 
 
 # ---------------------------------------------------------------------------- reference arm
+def named_workload(name: str) -> wl.Spec:
+    if name == "packed4096":
+        return wl.packed4096()
+    if name == "skewed":
+        return wl.skewed()
+    if name.startswith("sweep") and name[5:].isdigit():
+        return wl.sweep(int(name[5:]))
+    raise SystemExit(f"unknown workload {name!r}")
+
+
 def workload_config(spec: wl.Spec, tokens_per_adapter: int) -> dict:
     """The benchmarked workload, named the same way by both arms."""
     return {"workload": "packed4096: 4096->4096, N=8 ranks {8,16,16,32,32,64,64,128}, alpha 16/32, "
@@ -955,6 +989,9 @@ def main():
     ap.add_argument("--no-fused", action="store_true", help="skip the fused base + delta layer forward")
     ap.add_argument("--no-plan", action="store_true", help="skip the packing planner run")
     ap.add_argument("--decode-only", action="store_true", help="time only the decode batch (profiling runs)")
+    ap.add_argument("--only", default=None, metavar="WORKLOAD",
+                    help="time only this workload's steps and print its figures (profiling runs): packed4096, "
+                         "skewed, sweep2 .. sweep32")
     ap.add_argument("--tokens-per-adapter", type=int, default=4096,
                     help="tokens per adapter of the packed batch (4096 is the benchmarked workload; "
                          "smaller values give the small profiling case)")

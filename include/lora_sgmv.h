@@ -22,9 +22,13 @@
  *
  * Conventions shared by every entry point.
  *  - Ownership: the caller allocates and frees every buffer (inputs, outputs,
- *    segment storage, workspace).  The library never allocates or frees
- *    device memory, keeps no global mutable state and never synchronises,
- *    except lora_query_status.  Every call is stream-ordered on `stream`.
+ *    segment storage, workspace) and every stream and event.  The library
+ *    never allocates or frees device memory, never creates streams or events,
+ *    keeps no mutable state between calls (the one exception is the fixed
+ *    scratch array of lora_packed_bwd_noalloc, described there) and never
+ *    synchronises, except lora_query_status.  Every call is stream-ordered on
+ *    `stream`; calls on different streams share nothing but what the caller
+ *    passes them.
  *  - Pointers marked "device" must be device (or managed) memory, 16-byte
  *    aligned.  bf16 tensors are passed as raw 16-bit words (IEEE bfloat16).
  *  - Errors found on the host (NULL pointer, size out of range, misalignment,
@@ -233,6 +237,39 @@ LORA_API lora_status_t lora_packed_bwd(void *dX, float *dA, float *dB, const voi
                               lora_stream_t stream);
 
 /*
+ * lora_packed_bwd with its independent products side by side on two streams
+ * the caller owns.  dB needs only dY and H, so it (with the bf16 copy of a
+ * saved H) runs on side->stream[0] beside case i (dh) on `stream`; dA needs dh
+ * and runs on side->stream[1] beside case ii (dX) on `stream`.  The tails of
+ * one kernel's last wave then overlap the next kernel, which a single stream
+ * cannot do.  Results are those of lora_packed_bwd, bit for bit.
+ *   side  host struct: two distinct streams on the current device, neither of
+ *         them `stream`, and four distinct events (cudaEvent_t, timing may be
+ *         disabled), all created and destroyed by the caller.  The call records
+ *         the events and makes the streams wait on them (fork after the zeroing
+ *         of dA / dB, join before it returns: on return, `stream` is ordered
+ *         after everything the call enqueued on the side streams, also when a
+ *         launch failed).  Work the caller enqueues on the side streams after
+ *         the call is not ordered with it.  The streams and events may be
+ *         reused by the next call; two calls in flight at once (from different
+ *         host threads) must use different side streams and events.  Under
+ *         stream capture of `stream` the side streams join the capture through
+ *         the fork and leave it at the join.
+ * Errors: those of lora_packed_bwd; LORA_ERR_INVALID_ARG when side is NULL,
+ * a stream or event is NULL, the side streams coincide with each other or
+ * with `stream`, or two events coincide.
+ */
+typedef struct lora_side_streams {
+    lora_stream_t stream[2];
+    void *event[4];
+} lora_side_streams;
+
+LORA_API lora_status_t lora_packed_bwd_concurrent(void *dX, float *dA, float *dB, const void *dY, const void *X,
+                                                  const float *H_saved, const lora_adapter_table *table,
+                                                  const lora_segments *segs, void *ws, size_t ws_bytes,
+                                                  const lora_side_streams *side, lora_stream_t stream);
+
+/*
  * Measurement variants of lora_packed_fwd / lora_packed_bwd: the same checks,
  * kernels and results, and in addition CUDA events are recorded on `stream`
  * around each kernel launch: events[2k] before and events[2k + 1] after the
@@ -246,11 +283,9 @@ LORA_API lora_status_t lora_packed_bwd(void *dX, float *dA, float *dB, const voi
  * [case i shrink, when H_saved is NULL], [the bf16 copy of H_saved, when
  * given and dB is requested], case iii (dB, if requested), case i (dh), case
  * iv (dA, if requested), case ii (dX, if requested).  The
- * zeroing of dA / dB precedes the first pair.  The plain backward runs dB (with
- * the bf16 copy of H) on an internal stream next to dh, and dA on another
- * next to dX; the marked one runs all of its
- * kernels one after another on `stream`, so that each pair brackets one
- * kernel alone.
+ * zeroing of dA / dB precedes the first pair.  Like lora_packed_bwd, the
+ * marked backward runs all of its kernels one after another on `stream`, so
+ * that each pair brackets one kernel alone.
  * Errors: those of the unmarked call; LORA_ERR_INVALID_ARG when n_events < 0
  * or events is NULL with n_events > 0.
  */

@@ -71,12 +71,18 @@ class GpuCase:
         lora.lora_packed_fwd(y, H, self.inp["x"], self.table, self.segs, self.ws)
         return y, H
 
-    def bwd(self, H=None):
+    def bwd(self, H=None, side=None):
+        """Packed backward; with ``side`` (lora.SideStreams) the concurrent
+        variant, dB and dA on the side streams (the bench's configuration)."""
         s = self.spec
         dX = self.inp["dX0"].clone()
         dA = torch.full((s.sum_r, s.d_in), float("nan"), dtype=torch.float32, device=self.device)
         dB = torch.full((s.sum_r, s.d_out), float("nan"), dtype=torch.float32, device=self.device)
-        lora.lora_packed_bwd(dX, dA, dB, self.inp["dY"], self.inp["x"], H, self.table, self.segs, self.ws)
+        if side is None:
+            lora.lora_packed_bwd(dX, dA, dB, self.inp["dY"], self.inp["x"], H, self.table, self.segs, self.ws)
+        else:
+            lora.lora_packed_bwd_concurrent(dX, dA, dB, self.inp["dY"], self.inp["x"], H, self.table, self.segs,
+                                            self.ws, side)
         return dX, dA, dB
 
     def dH_workspace(self):

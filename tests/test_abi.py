@@ -79,6 +79,14 @@ def test_workspace_bytes_and_table_checks(L):
         assert L.lora_workspace_bytes(ctypes.byref(tb), 64) == 0, bad
 
 
+def fake_segs(**kw):
+    f = dict(n_tokens=64, n_adapters=4, max_tiles=5, sorted=1, perm=0x1000, seg_start=0x2000, tiles=0x3000,
+             n_tiles=0x4000, status=0x5000, scratch=0x6000, scratch_words=0, max_spans=5, reserved=0,
+             spans=0x7000, n_spans=0x8000)
+    f.update(kw)
+    return lora.c_segments(*[f[k] for k, _ in lora.c_segments._fields_])
+
+
 def test_host_side_rejections_return_before_any_cuda_call(L):
     segs = lora.c_segments()
     # no storage / no output struct
@@ -90,11 +98,11 @@ def test_host_side_rejections_return_before_any_cuda_call(L):
     # storage too small
     assert L.lora_build_segments(0x1000, None, 4, 2, 0x3000, 16, ctypes.byref(segs), None) == 5
     t = fake_table()
-    s = lora.c_segments(64, 4, 5, 1, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0)
+    s = fake_segs()
     assert L.lora_sgmv_shrink(None, 0x1000, ctypes.byref(t), ctypes.byref(s), None) == 1
     assert L.lora_sgmv_shrink(0x1004, 0x1000, ctypes.byref(t), ctypes.byref(s), None) == 3
     assert L.lora_sgmv_expand(0x1000, 0x2000, None, ctypes.byref(s), None) == 1
-    s_bad = lora.c_segments(64, 3, 5, 1, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0)
+    s_bad = fake_segs(n_adapters=3)
     assert L.lora_sgmv_expand(0x1000, 0x2000, ctypes.byref(t), ctypes.byref(s_bad), None) == 2
     assert L.lora_packed_fwd(0x1000, None, 0x2000, ctypes.byref(t), ctypes.byref(s), None, 0, None) == 5
     assert L.lora_packed_bwd(None, None, None, 0x1000, 0x2000, None, ctypes.byref(t), ctypes.byref(s),
@@ -102,8 +110,43 @@ def test_host_side_rejections_return_before_any_cuda_call(L):
     assert L.lora_packed_bwd(None, None, None, None, 0x2000, None, ctypes.byref(t), ctypes.byref(s),
                              0x3000, 1 << 20, None) == 1
     assert L.lora_query_status(None, None) == 1
+    # segments missing a pointer the kernels read on the device, or with a
+    # negative capacity: rejected on the host by every entry point
+    for bad, code in ((dict(n_tiles=0), 1), (dict(spans=0), 1), (dict(n_spans=0), 1), (dict(status=0), 1),
+                      (dict(max_tiles=-1), 2), (dict(max_spans=-1), 2), (dict(tiles=0x3008), 3)):
+        sb = fake_segs(**bad)
+        assert L.lora_sgmv_shrink(0x1000, 0x1000, ctypes.byref(t), ctypes.byref(sb), None) == code, bad
+        assert L.lora_packed_fwd(0x1000, None, 0x2000, ctypes.byref(t), ctypes.byref(sb), 0x3000, 1 << 20,
+                                 None) == code, bad
+        assert L.lora_packed_bwd(None, None, None, 0x1000, 0x2000, None, ctypes.byref(t), ctypes.byref(sb),
+                                 0x3000, 1 << 20, None) == code, bad
     assert L.lora_check_wait_timeout(None, None) == 1
     assert L.lora_check_wait_timeout(0x1002, None) == 3
+
+
+def test_noalloc_backward_checks_its_arguments_like_the_workspace_backward(L):
+    """The entry point without a workspace makes the same host-side checks as
+    lora_packed_bwd, in the same order: a malformed table or segment struct is
+    a status code, never a launch that dereferences it on the device."""
+    t = fake_table()
+    s = fake_segs()
+    call = lambda tb, sg, dY=0x1000, X=0x2000, dX=None: L.lora_packed_bwd_noalloc(
+        dX, None, None, dY, X, None, ctypes.byref(tb) if tb is not None else None,
+        ctypes.byref(sg) if sg is not None else None, None)
+    ws_call = lambda tb, sg, dY=0x1000, X=0x2000, dX=None: L.lora_packed_bwd(
+        dX, None, None, dY, X, None, ctypes.byref(tb) if tb is not None else None,
+        ctypes.byref(sg) if sg is not None else None, 0x3000, 1 << 20, None)
+    cases = [(None, s, {}), (t, None, {}),
+             (fake_table(rank=0), s, {}), (fake_table(row_off=0x20002), s, {}), (fake_table(scale=0x30001), s, {}),
+             (fake_table(d_in=12), s, {}), (fake_table(sum_r=8), s, {}),
+             (t, fake_segs(n_tiles=0), {}), (t, fake_segs(seg_start=0), {}), (t, fake_segs(spans=0), {}),
+             (t, fake_segs(max_tiles=-1), {}), (t, fake_segs(max_spans=-1), {}), (t, fake_segs(n_adapters=3), {}),
+             (t, fake_segs(n_tokens=-1), {}), (t, fake_segs(perm=0x1002), {}),
+             (t, s, dict(dY=None)), (t, s, dict(X=0x2008)), (t, s, dict(dX=0x4004))]
+    for tb, sg, kw in cases:
+        got = call(tb, sg, **kw)
+        assert got in (1, 2, 3), (tb, sg, kw, got)
+        assert got == ws_call(tb, sg, **kw), (tb, sg, kw)
 
 
 def test_binding_fails_loudly_without_the_library():

@@ -3,8 +3,9 @@ packed backward) against the fp64 oracle: ranks anywhere in 1..128 (odd ones
 included), hidden sizes that are multiples of 8 but not of 64, 1 to 40
 adapters, batches on both sides of the decode / packed boundary (512 tokens),
 sorted and unsorted routing, adapters without tokens.  Every case checks y,
-H, dH, dX element by element and dA / dB per adapter block, and that two runs
-give the same bits."""
+H, dH, dX element by element (with y0 = dX0 = 0, so the tolerance applies to
+the delta itself) and dA / dB per adapter block, and that two runs give the
+same bits."""
 import numpy as np
 import pytest
 import torch
@@ -42,7 +43,7 @@ def draw(seed):
 @pytest.mark.parametrize("seed", range(16))
 def test_random_shapes_match_oracle(seed):
     spec = draw(seed)
-    host = wl.host_inputs(spec, y0="randn", dX0="randn")
+    host = wl.host_inputs(spec, y0="zero", dX0="zero")  # pure delta: the tolerance binds the delta itself
     case = GpuCase(spec, host)
     y, H = case.fwd()
     dX, dA, dB = case.bwd(H)
