@@ -96,6 +96,8 @@ SIGNATURES = {
     "lora_packed_fwd": (_I32, [_P, _P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments), _P, _SZ, _P]),
     "lora_packed_bwd": (_I32, [_P, _P, _P, _P, _P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments),
                                _P, _SZ, _P]),
+    "lora_side_streams_create": (_I32, [ctypes.POINTER(c_side_streams)]),
+    "lora_side_streams_destroy": (_I32, [ctypes.POINTER(c_side_streams)]),
     "lora_packed_bwd_concurrent": (_I32, [_P, _P, _P, _P, _P, _P, ctypes.POINTER(c_table),
                                           ctypes.POINTER(c_segments), _P, _SZ, ctypes.POINTER(c_side_streams), _P]),
     "lora_packed_fwd_marked": (_I32, [_P, _P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments), _P, _SZ,
@@ -308,19 +310,23 @@ def lora_packed_bwd(dX, dA, dB, dY, X, H_saved, table: AdapterTable, segs: Segme
 
 class SideStreams:
     """Two CUDA streams and four events owned by the caller, on which
-    lora_packed_bwd_concurrent runs dB and dA beside dh and dX.  One set per
-    host thread that runs backward calls at the same time."""
+    lora_packed_bwd_concurrent runs dB and dA beside dh and dX; made on the
+    current device by lora_side_streams_create (fresh streams, so they never
+    coincide with a stream torch hands out) and released when the object is
+    collected.  One set per host thread that runs backward calls at the same
+    time."""
 
     def __init__(self, device=None):
         import torch
 
-        self.streams = [torch.cuda.Stream(device) for _ in range(2)]
-        self.events = [torch.cuda.Event() for _ in range(4)]
-        for e in self.events:  # torch creates the event handle on first record
-            e.record(self.streams[0])
-        torch.cuda.current_stream(device).wait_stream(self.streams[0])
-        self.c = c_side_streams((ctypes.c_void_p * 2)(*[s.cuda_stream for s in self.streams]),
-                                (ctypes.c_void_p * 4)(*[e.cuda_event for e in self.events]))
+        self.c = c_side_streams()
+        with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+            _check(lib().lora_side_streams_create(ctypes.byref(self.c)), "lora_side_streams_create")
+
+    def __del__(self):
+        if getattr(self, "c", None) is not None and _lib is not None:
+            _lib.lora_side_streams_destroy(ctypes.byref(self.c))
+            self.c = None
 
 
 def lora_packed_bwd_concurrent(dX, dA, dB, dY, X, H_saved, table: AdapterTable, segs: Segments, ws,

@@ -198,6 +198,46 @@ lora_status_t lora_packed_bwd(void *dX, float *dA, float *dB, const void *dY, co
     return packed_bwd(dX, dA, dB, dY, X, H_saved, table, segs, ws, ws_bytes, stream, nullptr);
 }
 
+lora_status_t lora_side_streams_destroy(lora_side_streams *side)
+{
+    if (side == nullptr) return LORA_ERR_INVALID_ARG;
+    bool ok = true;
+    for (auto &st : side->stream) {
+        if (st != nullptr && cudaStreamDestroy(reinterpret_cast<cudaStream_t>(st)) != cudaSuccess) ok = false;
+        st = nullptr;
+    }
+    for (auto &ev : side->event) {
+        if (ev != nullptr && cudaEventDestroy(static_cast<cudaEvent_t>(ev)) != cudaSuccess) ok = false;
+        ev = nullptr;
+    }
+    return ok ? LORA_OK : LORA_ERR_CUDA;
+}
+
+lora_status_t lora_side_streams_create(lora_side_streams *side)
+{
+    if (side == nullptr) return LORA_ERR_INVALID_ARG;
+    *side = lora_side_streams{};
+    for (auto &st : side->stream) {
+        cudaStream_t s = nullptr;
+        if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) {
+            cudaGetLastError();
+            lora_side_streams_destroy(side);
+            return LORA_ERR_CUDA;
+        }
+        st = reinterpret_cast<lora_stream_t>(s);
+    }
+    for (auto &ev : side->event) {
+        cudaEvent_t e = nullptr;
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            lora_side_streams_destroy(side);
+            return LORA_ERR_CUDA;
+        }
+        ev = e;
+    }
+    return LORA_OK;
+}
+
 lora_status_t lora_packed_bwd_concurrent(void *dX, float *dA, float *dB, const void *dY, const void *X,
                                          const float *H_saved, const lora_adapter_table *table,
                                          const lora_segments *segs, void *ws, size_t ws_bytes,

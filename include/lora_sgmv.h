@@ -23,8 +23,9 @@
  * Conventions shared by every entry point.
  *  - Ownership: the caller allocates and frees every buffer (inputs, outputs,
  *    segment storage, workspace) and every stream and event.  The library
- *    never allocates or frees device memory, never creates streams or events,
- *    keeps no mutable state between calls (the one exception is the fixed
+ *    never allocates or frees device memory, creates streams and events only
+ *    when asked to (lora_side_streams_create), keeps no mutable state between
+ *    calls (the one exception is the fixed
  *    scratch array of lora_packed_bwd_noalloc, described there) and never
  *    synchronises, except lora_query_status.  Every call is stream-ordered on
  *    `stream`; calls on different streams share nothing but what the caller
@@ -245,7 +246,9 @@ LORA_API lora_status_t lora_packed_bwd(void *dX, float *dA, float *dB, const voi
  * cannot do.  Results are those of lora_packed_bwd, bit for bit.
  *   side  host struct: two distinct streams on the current device, neither of
  *         them `stream`, and four distinct events (cudaEvent_t, timing may be
- *         disabled), all created and destroyed by the caller.  The call records
+ *         disabled), owned by the caller: made by lora_side_streams_create (or
+ *         by the caller's own runtime calls) and released with
+ *         lora_side_streams_destroy.  The call records
  *         the events and makes the streams wait on them (fork after the zeroing
  *         of dA / dB, join before it returns: on return, `stream` is ordered
  *         after everything the call enqueued on the side streams, also when a
@@ -263,6 +266,17 @@ typedef struct lora_side_streams {
     lora_stream_t stream[2];
     void *event[4];
 } lora_side_streams;
+
+/* Create a lora_side_streams set on the current device: two new non-blocking
+ * streams and four events with timing disabled, owned by the caller (these
+ * two calls are the only ones that create or destroy CUDA objects).  On error
+ * nothing is left allocated and *side is zeroed.  Errors: LORA_ERR_INVALID_ARG
+ * (NULL), LORA_ERR_CUDA. */
+LORA_API lora_status_t lora_side_streams_create(lora_side_streams *side);
+/* Destroy a set made by lora_side_streams_create (NULL members are skipped;
+ * work still queued on the streams completes first, as cudaStreamDestroy
+ * guarantees) and zero *side. */
+LORA_API lora_status_t lora_side_streams_destroy(lora_side_streams *side);
 
 LORA_API lora_status_t lora_packed_bwd_concurrent(void *dX, float *dA, float *dB, const void *dY, const void *X,
                                                   const float *H_saved, const lora_adapter_table *table,

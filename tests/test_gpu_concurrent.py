@@ -67,24 +67,58 @@ def test_concurrent_backward_equals_serial_backward_bitwise(saved):
 
 
 def test_concurrent_backward_rejects_bad_side_streams():
+    import ctypes
+
     spec = spec_of(0, T=64)
     case = GpuCase(spec, wl.host_inputs(spec))
     _, H = case.fwd()
     side = lora.SideStreams()
     cur = torch.cuda.current_stream()
-    bad = lora.SideStreams()
-    bad.c.stream[1] = bad.c.stream[0]  # the two side streams coincide
-    with pytest.raises(lora.LoraError):
-        run_bwd(case, H, bad)
-    bad2 = lora.SideStreams()
-    bad2.c.stream[0] = cur.cuda_stream  # a side stream is the caller's stream
-    with pytest.raises(lora.LoraError):
-        run_bwd(case, H, bad2)
-    bad3 = lora.SideStreams()
-    bad3.c.event[3] = bad3.c.event[0]  # two events coincide
-    with pytest.raises(lora.LoraError):
-        run_bwd(case, H, bad3)
-    run_bwd(case, H, side)  # a good set still works afterwards
+
+    def call_with(c):  # a modified copy of the owned set; the set itself stays intact
+        s = spec
+        dX = case.inp["dX0"].clone()
+        dA = torch.empty((s.sum_r, s.d_in), dtype=torch.float32, device="cuda")
+        dB = torch.empty((s.sum_r, s.d_out), dtype=torch.float32, device="cuda")
+        P = lambda t: ctypes.c_void_p(t.data_ptr())
+        return lora.lib().lora_packed_bwd_concurrent(
+            P(dX), P(dA), P(dB), P(case.inp["dY"]), P(case.inp["x"]), P(H), ctypes.byref(case.table.c),
+            ctypes.byref(case.segs.c), P(case.ws), case.ws.numel(), ctypes.byref(c), ctypes.c_void_p(cur.cuda_stream))
+
+    def copy():
+        c = lora.c_side_streams()
+        ctypes.memmove(ctypes.addressof(c), ctypes.addressof(side.c), ctypes.sizeof(c))
+        return c
+
+    bad = copy()
+    bad.stream[1] = bad.stream[0]  # the two side streams coincide
+    assert call_with(bad) == 1
+    bad = copy()
+    bad.stream[0] = cur.cuda_stream  # a side stream is the caller's stream
+    assert call_with(bad) == 1
+    bad = copy()
+    bad.event[3] = bad.event[0]  # two events coincide
+    assert call_with(bad) == 1
+    bad = copy()
+    bad.event[2] = None
+    assert call_with(bad) == 1
+    assert call_with(copy()) == 0  # the intact set works
+    run_bwd(case, H, side)
+    torch.cuda.synchronize()
+    assert lora.lora_query_status(case.segs) == 0
+
+
+def test_side_streams_are_fresh_and_distinct():
+    """Sets made by lora_side_streams_create never coincide with each other or
+    with streams torch hands out (torch's stream pool recycles its streams)."""
+    pool = [torch.cuda.Stream() for _ in range(40)]
+    sets = [lora.SideStreams() for _ in range(6)]
+    handles = [h for st in sets for h in st.c.stream]
+    assert len(set(handles)) == len(handles)
+    assert not set(handles) & {p.cuda_stream for p in pool}
+    events = [h for st in sets for h in st.c.event]
+    assert len(set(events)) == len(events) and all(events)
+    del sets
     torch.cuda.synchronize()
 
 

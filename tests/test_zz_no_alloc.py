@@ -51,15 +51,18 @@ def test_noalloc_backward_matches_workspace_backward_twice(name):
     host = wl.host_inputs(spec, dX0="randn")
     case = GpuCase(spec, host)
     y, H = case.fwd()
-    ref = outputs(case, lambda dX, dA, dB, h: lora.lora_packed_bwd(dX, dA, dB, case.inp["dY"], case.inp["x"], h,
-                                                                  case.table, case.segs, case.ws), H)
+    # the reference per mode: a saved H (here from the decode-size forward) and
+    # an H recomputed by the backward's own shrink may differ in their last bits
+    ws_bwd = lambda dX, dA, dB, h: lora.lora_packed_bwd(dX, dA, dB, case.inp["dY"], case.inp["x"], h, case.table,
+                                                        case.segs, case.ws)
+    refs = {True: outputs(case, ws_bwd, H), False: outputs(case, ws_bwd, None)}
     orc = oracle_all(spec, host)
     for call in range(2):
         for saved in (H, None):
             tag = f"call {call}, H {'saved' if saved is not None else 'recomputed'}"
             got = outputs(case, lambda dX, dA, dB, h: lora.lora_packed_bwd_noalloc(
                 dX, dA, dB, case.inp["dY"], case.inp["x"], h, case.table, case.segs), saved)
-            for g, r, what in zip(got, ref, ("dX", "dA", "dB")):
+            for g, r, what in zip(got, refs[saved is not None], ("dX", "dA", "dB")):
                 assert torch.equal(g, r), f"{what} ({tag}) differs from lora_packed_bwd"
             assert_close(dev_to_f64(got[0]), orc["dX"], GRAD_TOL, f"dX ({tag})")
             check_blocks(spec, dev_to_f64(got[1]), dev_to_f64(got[2]), orc["dA"], orc["dB"])
