@@ -34,7 +34,6 @@ using namespace tc;
 
 constexpr int kWStages = 2;
 constexpr int kYStages = 6;
-constexpr int kLagY = 2;
 constexpr int kNC = 128;                              // columns per MMA chunk
 constexpr int kNPart = 1024;                          // columns per work item
 constexpr uint32_t kWBytes = kNC * LORA_MAX_RANK * 2;  // one weight chunk
@@ -127,11 +126,12 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
     // stores, i.e. after stage g + kStoreLag (four warps: one leader for both
     // halves) or g + 2 kStoreLag (eight: one leader per half) is worked on; TMA
     // stages arrive when issued, so the producer can fill that stage once an
-    // earlier one is freed.  A gathered stage is released kLagY stages after it
-    // was issued and is freed without a store.  Tiles of the two kinds never
-    // share an item, and every item ends with its stores drained.
-    static_assert(kLagY < kYStages && (kEpi / 4) * kStoreLag < kYStages,
-                  "y-stage ring too shallow for the arrive and store lags");
+    // earlier one is freed.  A gathered stage completes once the copies of every
+    // producer lane have landed (each lane's arrival is triggered by its own
+    // copies, the lane never waits for them) and is freed without a store.
+    // Tiles of the two kinds never share an item, and every item ends with its
+    // stores drained.
+    static_assert((kEpi / 4) * kStoreLag < kYStages, "y-stage ring too shallow for the store lag");
     extern __shared__ uint8_t smem_raw[];
     const Smem S = carve(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -182,7 +182,6 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
         }
         uint32_t gw = 0, gy = 0, na = 0;
         bool ok = true;
-        ArriveQueue<kLagY, kYStages> aq;
         for (int32_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const Item I = load_item(tab, segs, it, n_parts, d);
             if (!I.ad.ok) continue;
@@ -271,12 +270,16 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
                             }
                         }
                     }
-                    aq.issued(S.yfull, gy, !contiguous);
+                    // every lane's arrival: at once for a TMA stage, once its copies
+                    // have landed for a gathered one (the lane does not wait for them)
+                    if (contiguous)
+                        mbar_arrive(&S.yfull[s]);
+                    else
+                        cp_async_mbar_arrive(&S.yfull[s]);
                     ++gy;
                 }
             }
         }
-        aq.drain(S.yfull);
         if (!ok && lane == 0) {  // aborted: let issued copies land before the CTA leaves
             for (uint32_t u = gy > (uint32_t)kYStages ? gy - kYStages : 0u; u < gy; ++u) {
                 uint64_t t0 = globaltimer_ns();

@@ -154,6 +154,15 @@ LORA_DEV void cp_async_16(void *smem_dst, const void *gmem_src, bool pred)
                  : "memory");
 }
 LORA_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Arrive on `bar` once every cp.async this thread has issued so far has
+// completed.  The arrive does not raise the barrier's pending count: it is one
+// of the arrivals the barrier was initialised with, so the thread never waits
+// for its own copies.  Consumers that read the stage with ordinary loads see
+// the data once the barrier's phase completes.
+LORA_DEV void cp_async_mbar_arrive(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 template <int N>
 LORA_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 

@@ -164,6 +164,30 @@ def test_decode_path_full_tiles_rank_128_ragged_edges():
     full_check(spec, y0="randn")
 
 
+@pytest.mark.parametrize("route", ["ids", "auto"])
+def test_decode_path_ragged_edges(route):
+    # a decode-size batch (T <= 512): an adapter spanning two tiles, ragged
+    # tiles, ranks 1 and 33 (padding to 16 and 48), d_in = 3000 (slices of 256,
+    # the last 184 wide) and d_out = 1000 (four 256-column expand slices, the
+    # last 232 wide)
+    ranks = [64, 48, 8, 1, 33]
+    lengths = [200, 150, 100, 40, 10]
+    rng = np.random.default_rng(9)
+    ids = np.concatenate([np.full(n, i, np.int32) for i, n in enumerate(lengths)])
+    if route == "ids":
+        ids = rng.permutation(ids)
+    spec = wl.custom("decode_edges2", 3000, 1000, ranks, [2.0 * r for r in ranks], ids)
+    full_check(spec, y0="zero")
+    host = wl.host_inputs(spec, y0="randn")
+    case = GpuCase(spec, host)
+    y1, H1 = case.fwd()
+    y2, H2 = case.fwd()
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2) and torch.equal(H1, H2)
+    ref = oracle_all(spec, host)
+    assert_close(dev_to_f64(y1), ref["y"], FWD_TOL, "y (accumulated)")
+
+
 @pytest.mark.parametrize("proj", [0, 1, 2])
 def test_decode_batch_shrink_expand(proj):
     spec = wl.decode(proj)
