@@ -7,21 +7,19 @@
 // the step is bound by latency (the working set is a few MB).  Two launches,
 // each over all adapters, chained by programmatic dependent launch:
 //
-//   shrink  a cluster per tile of <= 128 tokens of one adapter; CTA s of the
-//           cluster takes slice s of d_in:
-//           P_s[t, k] = sum_{j in slice s} x[t, j] A_i[k, j]   (fp32, shared memory)
-//           then the cluster adds the slices through distributed shared
-//           memory, h[t, k] = sum_s P_s[t, k], each CTA a share of the rows,
-//           and writes h (fp32) for the expand
+//   shrink  a CTA per (tile of <= 128 tokens of one adapter, slice s of d_in):
+//           P_s[t, k] = sum_{j in slice s} x[t, j] A_i[k, j]   (fp32)
+//           written to the workspace; no CTA waits for another
 //   expand  work item = (tile, 256-column slice of d_out)
+//           h[t, k]   = sum_s P_s[t, k]   (slice order, the same in every item)
 //           y[t, o]  += s_i sum_k h[t, k] B_i[o, k]
 //
 // The expand kernel is launched as a programmatic dependent of the shrink: its
 // CTAs start while the shrink runs and fetch their B_i^T block and the y rows
 // they update (inputs the shrink does not write) before waiting for the shrink
-// grid to complete; h is then read from L2.  The shrink is an ordinary
-// launch: it reads the routing and A_i before anything else, and the kernel
-// before it on the stream may have written them (a routing build, an
+// grid to complete; the partials are then read from L2.  The shrink is an
+// ordinary launch: it reads the routing and A_i before anything else, and the
+// kernel before it on the stream may have written them (a routing build, an
 // optimizer step that refreshed A_i); only a completed predecessor is
 // visible without a grid-dependency wait.
 //
@@ -63,7 +61,7 @@ struct ProjSet {
     lora_adapter_table tab[kMaxProjections];
     uint16_t *y[kMaxProjections];
     float *H[kMaxProjections];     // fp32 H by token, or null
-    float *hfin[kMaxProjections];  // [T, rp_cap] fp32 h hand-off
+    float *part[kMaxProjections];  // [ks, T, rp_cap] fp32 slice partials of h
     int32_t n;
 };
 
@@ -71,7 +69,7 @@ struct Geom {
     int32_t rows_cap;  // tile rows the shared buffers hold (multiple of 16, <= 128)
     int32_t rp_cap;    // rank rows they hold: the largest r_max rounded up to 16
     int32_t kw;        // shrink: columns per slice of d_in (multiple of kKC)
-    int32_t ks;        // shrink: slices of d_in = CTAs per cluster (<= kDecodeSlices)
+    int32_t ks;        // shrink: slices of d_in (<= kDecodeSlices)
     int32_t stages;    // shrink: stages of rows_cap + rp_cap rows the ring holds (>= 2)
     int32_t ns;        // expand: slices of the widest d_out
 };
@@ -111,23 +109,12 @@ LORA_DEV void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint3
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// hardware cluster barrier; every CTA of a cluster reaches each one (a cluster
-// shares its tile, so early exits are cluster-wide)
-LORA_DEV void cluster_sync()
+// two floats to bf16 (nearest-even) in one word, `lo` in the low half
+LORA_DEV uint32_t cvt_bf16x2(float lo, float hi)
 {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// 16 bytes of CTA `rank`'s shared memory at this CTA's shared address `saddr`
-LORA_DEV float4 ld_cluster_f4(uint32_t saddr, uint32_t rank)
-{
-    uint32_t ra;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(saddr), "r"(rank));
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(ra)
-                 : "memory");
-    return v;
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
 }
 
 // A work item's tile, its adapter's table entry and the token of row
@@ -187,8 +174,7 @@ __global__ void __launch_bounds__(kThreads, 2) dec_shrink_kernel(const uint16_t 
     pdl_launch_dependents();
     const int32_t ti = blockIdx.x / g.ks, sl = blockIdx.x % g.ks;
     const lora_adapter_table &tab = ps.tab[blockIdx.y];
-    float *__restrict__ hfin = ps.hfin[blockIdx.y];
-    float *__restrict__ H_save = ps.H[blockIdx.y];
+    float *__restrict__ part = ps.part[blockIdx.y];
     const DecTile D = dec_tile(tab, segs, ti);
     if (!D.run || !D.ad.ok) return;
     const Tile &T = D.T;
@@ -299,9 +285,10 @@ __global__ void __launch_bounds__(kThreads, 2) dec_shrink_kernel(const uint16_t 
         }
     }
     __syncthreads();
-    // this CTA's slice partial: the k-groups added in a fixed order into the
-    // first [rows16 x rp] block of P (the result does not depend on timing)
-    for (int i = threadIdx.x; i < rows16 * (rp / 4); i += kThreads) {
+    // this CTA's slice partial: the k-groups added in a fixed order (the result
+    // does not depend on timing), rows of the tile in perm order, to the workspace
+    float *pout = part + ((int64_t)sl * segs.n_tokens + T.begin) * g.rp_cap;
+    for (int i = threadIdx.x; i < rows * (rp / 4); i += kThreads) {
         const int m = i / (rp / 4), k4 = i % (rp / 4);
         float4 v = *reinterpret_cast<const float4 *>(P + m * rp + 4 * k4);
         for (int q = 1; q < kg; ++q) {
@@ -311,46 +298,8 @@ __global__ void __launch_bounds__(kThreads, 2) dec_shrink_kernel(const uint16_t 
             v.z += u.z;
             v.w += u.w;
         }
-        *reinterpret_cast<float4 *>(P + m * rp + 4 * k4) = v;
+        *reinterpret_cast<float4 *>(pout + (int64_t)m * g.rp_cap + 4 * k4) = v;
     }
-    cluster_sync();  // every slice partial of the tile is complete
-    // CTA sl adds rows sl, sl + ks, ... over the cluster in rank order
-    const int32_t r_max = tab.r_max;
-    const int my_rows = rows > sl ? (rows - sl + g.ks - 1) / g.ks : 0;
-    for (int i = threadIdx.x; i < my_rows * (rp / 4); i += kThreads) {
-        const int m = sl + g.ks * (i / (rp / 4)), k4 = i % (rp / 4);
-        const uint32_t sa = smem_u32(P + m * rp + 4 * k4);
-        float4 v[kDecodeSlices];
-#pragma unroll
-        for (int q = 0; q < kDecodeSlices; ++q)
-            if (q < g.ks) v[q] = ld_cluster_f4(sa, (uint32_t)q);
-        float e[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int q = 0; q < kDecodeSlices; ++q) {
-            if (q < g.ks) {
-                e[0] += v[q].x;
-                e[1] += v[q].y;
-                e[2] += v[q].z;
-                e[3] += v[q].w;
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (4 * k4 + u >= r) e[u] = 0.f;
-        *reinterpret_cast<float4 *>(hfin + ((int64_t)T.begin + m) * g.rp_cap + 4 * k4) = make_float4(e[0], e[1], e[2], e[3]);
-        if (H_save != nullptr) {
-            const int32_t t = tok[m];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (4 * k4 + u < r_max) H_save[(int64_t)t * r_max + 4 * k4 + u] = e[u];
-        }
-    }
-    if (H_save != nullptr)  // columns r_pad .. r_max - 1 of this CTA's rows
-        for (int i = threadIdx.x; i < my_rows * r_max; i += kThreads) {
-            const int m = sl + g.ks * (i / r_max), k = i % r_max;
-            if (k >= rp) H_save[(int64_t)tok[m] * r_max + k] = 0.f;
-        }
-    cluster_sync();  // no CTA leaves while another may still read its partial
 }
 
 // ------------------------------------------------------------------ expand
@@ -363,7 +312,8 @@ __global__ void __launch_bounds__(kThreads, 2) dec_expand_kernel(const __grid_co
     const int32_t ti = blockIdx.x / g.ns, nsl = blockIdx.x % g.ns;
     const lora_adapter_table &tab = ps.tab[blockIdx.y];
     uint16_t *__restrict__ y = ps.y[blockIdx.y];
-    const float *__restrict__ hfin = ps.hfin[blockIdx.y];
+    const float *__restrict__ part = ps.part[blockIdx.y];
+    float *__restrict__ H_save = ps.H[blockIdx.y];
     if (nsl * kNW >= tab.d_out) return;  // a narrower projection has fewer slices
     // the routing was complete before the shrink started, so it can be read
     // before the wait; so can B and y, which the shrink does not write
@@ -400,18 +350,51 @@ __global__ void __launch_bounds__(kThreads, 2) dec_expand_kernel(const __grid_co
     }
     cp_async_commit();
 
-    pdl_wait();  // the shrink grid has completed and h is visible
+    pdl_wait();  // the shrink grid has completed and its partials are visible
 
+    // h = the slice partials added in slice order (every item of the tile
+    // adds them alike); the tile's first item also writes the fp32 H
+    const int32_t T_all = segs.n_tokens, r_max = tab.r_max;
+    const bool write_h = H_save != nullptr && nsl == 0;
     for (int i = threadIdx.x; i < rows16 * (rp / 4); i += kThreads) {
         const int m = i / (rp / 4), k4 = i % (rp / 4);
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (m < rows) v = __ldcg(reinterpret_cast<const float4 *>(hfin + ((int64_t)T.begin + m) * g.rp_cap + 4 * k4));
-        const uint32_t h01 = pack_bf16(v.x, v.y), h23 = pack_bf16(v.z, v.w);
-        const uint32_t l01 = pack_bf16(v.x - bf16lo(h01), v.y - bf16hi(h01));
-        const uint32_t l23 = pack_bf16(v.z - bf16lo(h23), v.w - bf16hi(h23));
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
+        if (m < rows) {
+            const float *src = part + ((int64_t)T.begin + m) * g.rp_cap + 4 * k4;
+            float4 v[kDecodeSlices];
+#pragma unroll
+            for (int q = 0; q < kDecodeSlices; ++q)
+                if (q < g.ks) v[q] = __ldcg(reinterpret_cast<const float4 *>(src + (int64_t)q * T_all * g.rp_cap));
+#pragma unroll
+            for (int q = 0; q < kDecodeSlices; ++q) {
+                if (q < g.ks) {
+                    e[0] += v[q].x;
+                    e[1] += v[q].y;
+                    e[2] += v[q].z;
+                    e[3] += v[q].w;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (4 * k4 + u >= r) e[u] = 0.f;
+            if (write_h) {
+                float *hrow = H_save + (int64_t)tok[m] * r_max;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (4 * k4 + u < r_max) hrow[4 * k4 + u] = e[u];
+            }
+        }
+        const uint32_t h01 = cvt_bf16x2(e[0], e[1]), h23 = cvt_bf16x2(e[2], e[3]);
+        const uint32_t l01 = cvt_bf16x2(e[0] - bf16lo(h01), e[1] - bf16hi(h01));
+        const uint32_t l23 = cvt_bf16x2(e[2] - bf16lo(h23), e[3] - bf16hi(h23));
         *reinterpret_cast<uint2 *>(hh + m * hs + 4 * k4) = make_uint2(h01, h23);
         *reinterpret_cast<uint2 *>(hl + m * hs + 4 * k4) = make_uint2(l01, l23);
     }
+    if (write_h)  // columns r_pad .. r_max - 1
+        for (int i = threadIdx.x; i < rows * r_max; i += kThreads) {
+            const int m = i / r_max, k = i % r_max;
+            if (k >= rp) H_save[(int64_t)tok[m] * r_max + k] = 0.f;
+        }
     tc::cp_async_wait<0>();
     __syncthreads();
 
@@ -446,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 2) dec_expand_kernel(const __grid_co
             for (int hf = 0; hf < 2; ++hf) {
                 uint32_t *p = reinterpret_cast<uint32_t *>(ys + (row + 8 * hf) * kYStride + col);
                 const uint32_t w = *p;
-                *p = pack_bf16(bf16lo(w) + c * acc[n][2 * hf], bf16hi(w) + c * acc[n][2 * hf + 1]);
+                *p = cvt_bf16x2(bf16lo(w) + c * acc[n][2 * hf], bf16hi(w) + c * acc[n][2 * hf + 1]);
             }
         }
     }
@@ -458,6 +441,13 @@ __global__ void __launch_bounds__(kThreads, 2) dec_expand_kernel(const __grid_co
             *reinterpret_cast<uint4 *>(y + (int64_t)tok[m] * d_out + o) =
                 *reinterpret_cast<const uint4 *>(ys + m * kYStride + 8 * p);
     }
+}
+
+// slices of d_in of at least 256 columns, at most kDecodeSlices of them
+int32_t slice_width(int32_t d_in)
+{
+    const int32_t per = (d_in + kDecodeSlices - 1) / kDecodeSlices;
+    return std::max<int32_t>(2 * kKC, ((per + kKC - 1) / kKC) * kKC);
 }
 
 Geom make_geom(const ProjSet &ps, const lora_segments &segs)
@@ -472,10 +462,7 @@ Geom make_geom(const ProjSet &ps, const lora_segments &segs)
     }
     g.rows_cap = std::min<int32_t>(LORA_TILE_M, (T + 15) & ~15);
     g.rp_cap = (r_max + 15) & ~15;
-    // slices of at least 256 columns, at most kDecodeSlices of them (one CTA
-    // of the tile's cluster each)
-    const int32_t per = (tab.d_in + kDecodeSlices - 1) / kDecodeSlices;
-    g.kw = std::max<int32_t>(2 * kKC, ((per + kKC - 1) / kKC) * kKC);
+    g.kw = slice_width(tab.d_in);
     g.ks = (tab.d_in + g.kw - 1) / g.kw;
     // as many stages as the slice has chunks, within ~100 KB (two CTAs of the
     // two kernels then fit one SM), at least two
@@ -491,9 +478,11 @@ Geom make_geom(const ProjSet &ps, const lora_segments &segs)
 
 }  // namespace
 
-size_t decode_workspace_bytes(int32_t T, int32_t r_max)
+size_t decode_workspace_bytes(int32_t T, int32_t r_max, int32_t d_in)
 {
-    return (size_t)T * (size_t)((r_max + 15) & ~15) * sizeof(float);
+    const int32_t kw = slice_width(d_in);
+    const size_t ks = (size_t)((d_in + kw - 1) / kw);
+    return ks * (size_t)T * (size_t)((r_max + 15) & ~15) * sizeof(float);
 }
 
 lora_status_t tc_decode_multi(int32_t n_proj, void *const *y, float *const *H_save, const void *x, void *ws,
@@ -505,17 +494,16 @@ lora_status_t tc_decode_multi(int32_t n_proj, void *const *y, float *const *H_sa
     ps.n = n_proj;
     int32_t r_max = 0;
     for (int p = 0; p < n_proj; ++p) r_max = std::max(r_max, tabs[p].r_max);
-    const size_t per = decode_workspace_bytes(segs.n_tokens, r_max);
+    const size_t per = decode_workspace_bytes(segs.n_tokens, r_max, tabs[0].d_in);
     for (int p = 0; p < n_proj; ++p) {
         ps.tab[p] = tabs[p];
         ps.y[p] = static_cast<uint16_t *>(y[p]);
         ps.H[p] = H_save != nullptr ? H_save[p] : nullptr;
-        ps.hfin[p] = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + (size_t)p * per);
+        ps.part[p] = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + (size_t)p * per);
     }
     const Geom g = make_geom(ps, segs);
     const size_t s1 = shrink_smem(g), s2 = expand_smem(g);
     if (cudaFuncSetAttribute(dec_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1) != cudaSuccess ||
-        cudaFuncSetAttribute(dec_shrink_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
         cudaFuncSetAttribute(dec_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2) != cudaSuccess)
         return LORA_ERR_CUDA;
     {
@@ -528,13 +516,6 @@ lora_status_t tc_decode_multi(int32_t n_proj, void *const *y, float *const *H_sa
         // and A_i, which the kernel before it may have written (a routing
         // build, an optimizer step), and only a completed predecessor is
         // guaranteed visible without a grid-dependency wait
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)g.ks;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
         if (cudaLaunchKernelEx(&cfg, dec_shrink_kernel, static_cast<const uint16_t *>(x), ps, g, segs) != cudaSuccess)
             return LORA_ERR_CUDA;
     }

@@ -19,10 +19,10 @@ size_t handoff_region_bytes(int32_t T, int32_t r_max)
 // batches up to this many tokens take the decode kernels
 constexpr int32_t kDecodeMaxTokens = 512;
 
-size_t packed_workspace_bytes(int32_t T, int32_t r_max)
+size_t packed_workspace_bytes(int32_t T, int32_t r_max, int32_t d_in)
 {
     const size_t packed = 2 * handoff_region_bytes(T, r_max);
-    const size_t decode = T <= kDecodeMaxTokens ? decode_workspace_bytes(T, r_max) : 0;
+    const size_t decode = T <= kDecodeMaxTokens ? decode_workspace_bytes(T, r_max, d_in) : 0;
     return packed > decode ? packed : decode;
 }
 
@@ -76,11 +76,11 @@ size_t multi_workspace_bytes(int32_t n_proj, const lora_adapter_table *tabs, int
     int32_t r_max = 0;
     for (int32_t p = 0; p < n_proj; ++p) {
         r_max = tabs[p].r_max > r_max ? tabs[p].r_max : r_max;
-        const size_t one = packed_workspace_bytes(T, tabs[p].r_max);  // the per-projection path
+        const size_t one = packed_workspace_bytes(T, tabs[p].r_max, tabs[p].d_in);  // the per-projection path
         need = one > need ? one : need;
     }
     if (T <= kDecodeMaxTokens) {  // the shared decode launches: one h buffer per projection
-        const size_t dec = (size_t)n_proj * decode_workspace_bytes(T, r_max);
+        const size_t dec = (size_t)n_proj * decode_workspace_bytes(T, r_max, tabs[0].d_in);
         need = dec > need ? dec : need;
     }
     return need;

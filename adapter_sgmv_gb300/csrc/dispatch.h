@@ -5,9 +5,11 @@
 
 namespace lora {
 
-// Workspace of the packed calls: two bf16 hand-off buffers [T, rw] (see tc_host.h).
+// Workspace of the packed calls: two bf16 hand-off buffers [T, rw] (see
+// tc_host.h), or for a decode-size forward the shrink's fp32 slice partials,
+// whichever is larger.
 size_t handoff_region_bytes(int32_t T, int32_t r_max);
-size_t packed_workspace_bytes(int32_t T, int32_t r_max);
+size_t packed_workspace_bytes(int32_t T, int32_t r_max, int32_t d_in);
 
 // Optional CUDA events recorded around each kernel of a call (measurement):
 // ev[2k] before and ev[2k + 1] after the k-th kernel, while room is left.
@@ -21,7 +23,7 @@ lora_status_t run_shrink(float *H, const void *x, const lora_adapter_table &tab,
                          cudaStream_t stream);
 lora_status_t run_expand(void *y, const float *H, const lora_adapter_table &tab, const lora_segments &segs,
                          cudaStream_t stream);
-// ws: packed_workspace_bytes(T, r_max) bytes
+// ws: packed_workspace_bytes(T, r_max, d_in) bytes
 lora_status_t run_fwd(void *y, float *H_save, const void *x, void *ws, const lora_adapter_table &tab,
                       const lora_segments &segs, cudaStream_t stream, Marks *marks = nullptr);
 // several projections reading the same x (tables share d_in and the adapter count)

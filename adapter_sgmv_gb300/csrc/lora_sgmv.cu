@@ -66,7 +66,7 @@ lora_status_t check_device()
 
 namespace {
 
-size_t workspace_bytes(const lora_adapter_table *t, int32_t T) { return packed_workspace_bytes(T, t->r_max); }
+size_t workspace_bytes(const lora_adapter_table *t, int32_t T) { return packed_workspace_bytes(T, t->r_max, t->d_in); }
 
 
 #define LORA_TRY(expr)                          \

@@ -76,7 +76,8 @@ extern "C" LORA_API lora_status_t lora_packed_bwd_noalloc(void *dX, float *dA, f
     if (!aligned16(dY) || !aligned16(X) || (dX && !aligned16(dX)) || (dA && !aligned16(dA)) ||
         (dB && !aligned16(dB)) || (H_saved && !aligned16(H_saved)))
         return LORA_ERR_ALIGNMENT;
-    if (packed_workspace_bytes(segs->n_tokens, table->r_max) > kScratchBytes) return LORA_ERR_WORKSPACE_TOO_SMALL;
+    // the backward's scratch: the two bf16 hand-off copies (of H and dH)
+    if (2 * handoff_region_bytes(segs->n_tokens, table->r_max) > kScratchBytes) return LORA_ERR_WORKSPACE_TOO_SMALL;
     st = check_device();
     if (st != LORA_OK) return st;
     void *base = scratch_address();

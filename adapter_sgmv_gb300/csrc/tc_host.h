@@ -69,17 +69,18 @@ lora_status_t tc_db(float *dB, const void *dY, const uint16_t *h_bf16, int32_t r
 lora_status_t tc_da(float *dA, const void *X, const uint16_t *dh_bf16, int32_t rw, const lora_adapter_table &tab,
                     const lora_segments &segs, cudaStream_t stream);
 
-// decode-sized batches: the shrink split over d_in across a cluster per tile
-// (fp32 h in ws), then the expand as a programmatic dependent launch; H_save
-// may be null.  ws: decode_workspace_bytes(T, r_max) bytes.
-constexpr int32_t kDecodeSlices = 16;  // most slices of d_in (CTAs per cluster)
+// decode-sized batches: the shrink split over d_in, one CTA per (tile, slice),
+// its fp32 partials in ws, then the expand as a programmatic dependent launch
+// that adds them; H_save may be null.  ws: decode_workspace_bytes(T, r_max,
+// d_in) bytes.
+constexpr int32_t kDecodeSlices = 16;  // most slices of d_in
 constexpr int32_t kMaxProjections = LORA_MAX_PROJECTIONS;
-size_t decode_workspace_bytes(int32_t T, int32_t r_max);
+size_t decode_workspace_bytes(int32_t T, int32_t r_max, int32_t d_in);
 lora_status_t tc_decode_fwd(void *y, float *H_save, const void *x, void *ws, const lora_adapter_table &tab,
                             const lora_segments &segs, cudaStream_t stream);
 // n_proj projections reading the same x in the same two launches (tables
 // share d_in and the adapter count); H_save may be null, or hold null entries.
-// ws: n_proj * decode_workspace_bytes(T, largest r_max) bytes.
+// ws: n_proj * decode_workspace_bytes(T, largest r_max, d_in) bytes.
 lora_status_t tc_decode_multi(int32_t n_proj, void *const *y, float *const *H_save, const void *x, void *ws,
                               const lora_adapter_table *tabs, const lora_segments &segs, cudaStream_t stream);
 

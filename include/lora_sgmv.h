@@ -203,8 +203,10 @@ LORA_API lora_status_t lora_sgmv_expand(void *y, const float *H, const lora_adap
  *   x       device bf16 [T, d_in]
  *   ws      device workspace of >= lora_workspace_bytes(table, T) bytes (may be
  *           NULL when that is 0); it carries H from the shrink to the expand:
- *           as bf16 hi + lo (~16 significant bits), or in fp32 for batches of at
- *           most 512 tokens; contents need not be preserved after the call
+ *           as bf16 hi + lo (~16 significant bits), or, for batches of at most
+ *           512 tokens, as fp32 partial sums over slices of d_in that the
+ *           expand adds in a fixed order; contents need not be preserved after
+ *           the call
  */
 LORA_API lora_status_t lora_packed_fwd(void *y, float *H_save, const void *x,
                               const lora_adapter_table *table, const lora_segments *segs,
@@ -475,8 +477,8 @@ LORA_API lora_status_t lora_plan_pack(const lora_plan_config *configs, int32_t n
  * Same arguments and results as lora_packed_bwd minus ws / ws_bytes: the bf16
  * H / dH hand-off scratch lives in a fixed 8 MiB array inside the library's device
  * memory (held by every GPU that loads the library until exit), so it needs
- * lora_workspace_bytes(table, T) <= 8 MiB (2 * T * 64 bf16 when r_max <= 64,
- * 2 * T * 128 otherwise, each half rounded up to 256 bytes), otherwise
+ * 2 * T * 64 bf16 when r_max <= 64, 2 * T * 128 otherwise (each half rounded
+ * up to 256 bytes) to be at most 8 MiB, otherwise
  * LORA_ERR_WORKSPACE_TOO_SMALL is returned and nothing runs.  Allocates
  * nothing.  All calls share the array: calls that overlap on the GPU race and
  * must be serialised by the caller.  The first call on a device resolves the
