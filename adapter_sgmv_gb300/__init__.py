@@ -21,7 +21,8 @@ from ._build import LIB_PATH, build as build_library  # noqa: F401
 __all__ = [
     "LoraError", "AdapterTable", "Segments", "lib", "lora_abi_version", "lora_status_string",
     "lora_segments_bytes", "lora_build_segments", "lora_workspace_bytes", "lora_sgmv_shrink",
-    "lora_sgmv_expand", "lora_packed_fwd", "lora_packed_bwd", "lora_packed_bwd_concurrent", "SideStreams",
+    "lora_sgmv_expand", "lora_packed_fwd", "lora_packed_bwd", "lora_packed_bwd_concurrent", "lora_packed_bwd_ex", "SideStreams",
+    "LORA_BWD_DETERMINISTIC",
     "lora_packed_fwd_marked", "lora_packed_bwd_marked",
     "lora_packed_bwd_noalloc", "lora_adamw_step", "lora_fused_base_workspace_bytes", "lora_fused_base_fwd",
     "lora_multi_workspace_bytes", "lora_multi_fwd", "lora_plan_pack",
@@ -98,6 +99,8 @@ SIGNATURES = {
                                _P, _SZ, _P]),
     "lora_side_streams_create": (_I32, [ctypes.POINTER(c_side_streams)]),
     "lora_side_streams_destroy": (_I32, [ctypes.POINTER(c_side_streams)]),
+    "lora_packed_bwd_ex": (_I32, [_P, _P, _P, _P, _P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments), _P,
+                                  _SZ, ctypes.POINTER(c_side_streams), ctypes.c_uint32, _P]),
     "lora_packed_bwd_concurrent": (_I32, [_P, _P, _P, _P, _P, _P, ctypes.POINTER(c_table),
                                           ctypes.POINTER(c_segments), _P, _SZ, ctypes.POINTER(c_side_streams), _P]),
     "lora_packed_fwd_marked": (_I32, [_P, _P, _P, ctypes.POINTER(c_table), ctypes.POINTER(c_segments), _P, _SZ,
@@ -336,6 +339,22 @@ def lora_packed_bwd_concurrent(dX, dA, dB, dY, X, H_saved, table: AdapterTable, 
     _check(lib().lora_packed_bwd_concurrent(_ptr(dX), _ptr(dA), _ptr(dB), _ptr(dY), _ptr(X), _ptr(H_saved),
                                             ctypes.byref(table.c), ctypes.byref(segs.c), _ptr(ws), wsb,
                                             ctypes.byref(side.c), _stream(stream)), "lora_packed_bwd_concurrent")
+
+
+LORA_BWD_DETERMINISTIC = 1
+
+
+def lora_packed_bwd_ex(dX, dA, dB, dY, X, H_saved, table: AdapterTable, segs: Segments, ws, side=None,
+                       deterministic=False, stream=None):
+    """Packed backward with options: dB / dA on the caller's side streams
+    (``side``: SideStreams) and/or dA / dB summed in a fixed span order
+    (``deterministic``: bit-identical from run to run)."""
+    wsb = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().lora_packed_bwd_ex(_ptr(dX), _ptr(dA), _ptr(dB), _ptr(dY), _ptr(X), _ptr(H_saved),
+                                    ctypes.byref(table.c), ctypes.byref(segs.c), _ptr(ws), wsb,
+                                    None if side is None else ctypes.byref(side.c),
+                                    LORA_BWD_DETERMINISTIC if deterministic else 0, _stream(stream)),
+           "lora_packed_bwd_ex")
 
 
 def _events(events, stream):

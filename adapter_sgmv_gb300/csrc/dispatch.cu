@@ -19,10 +19,18 @@ size_t handoff_region_bytes(int32_t T, int32_t r_max)
 // batches up to this many tokens take the decode kernels
 constexpr int32_t kDecodeMaxTokens = 512;
 
-size_t packed_workspace_bytes(int32_t T, int32_t r_max, int32_t d_in)
+size_t ticket_region_bytes(const lora_adapter_table &tab, int32_t T)
 {
-    const size_t packed = 2 * handoff_region_bytes(T, r_max);
-    const size_t decode = T <= kDecodeMaxTokens ? decode_workspace_bytes(T, r_max, d_in) : 0;
+    const SegLayout L = seg_layout(T, tab.n_adapters);
+    if (!L.ok) return 0;
+    const int64_t words = (int64_t)L.max_spans * (tokred_ranges(tab.d_out) + tokred_ranges(tab.d_in));
+    return (size_t)((words * 4 + 255) & ~int64_t(255));
+}
+
+size_t packed_workspace_bytes(const lora_adapter_table &tab, int32_t T)
+{
+    const size_t packed = 2 * handoff_region_bytes(T, tab.r_max) + ticket_region_bytes(tab, T);
+    const size_t decode = T <= kDecodeMaxTokens ? decode_workspace_bytes(T, tab.r_max, tab.d_in) : 0;
     return packed > decode ? packed : decode;
 }
 
@@ -76,7 +84,7 @@ size_t multi_workspace_bytes(int32_t n_proj, const lora_adapter_table *tabs, int
     int32_t r_max = 0;
     for (int32_t p = 0; p < n_proj; ++p) {
         r_max = tabs[p].r_max > r_max ? tabs[p].r_max : r_max;
-        const size_t one = packed_workspace_bytes(T, tabs[p].r_max, tabs[p].d_in);  // the per-projection path
+        const size_t one = packed_workspace_bytes(tabs[p], T);  // the per-projection path
         need = one > need ? one : need;
     }
     if (T <= kDecodeMaxTokens) {  // the shared decode launches: one h buffer per projection
@@ -100,11 +108,20 @@ lora_status_t run_multi_fwd(int32_t n_proj, void *const *y, float *const *H_save
 
 lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X, const float *H_saved, void *ws,
                       const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream, Marks *marks,
-                      const SideStreams *side)
+                      const SideStreams *side, bool ordered)
 {
     const int32_t rw = handoff_cols(tab.r_max);
+    const size_t hreg = handoff_region_bytes(segs.n_tokens, tab.r_max);
     uint16_t *hb = static_cast<uint16_t *>(ws);
-    uint16_t *dhb = reinterpret_cast<uint16_t *>(static_cast<char *>(ws) + handoff_region_bytes(segs.n_tokens, tab.r_max));
+    uint16_t *dhb = reinterpret_cast<uint16_t *>(static_cast<char *>(ws) + hreg);
+    // ordered mode: tickets of dB, then of dA, after the hand-off regions
+    int32_t *tk_B = nullptr, *tk_A = nullptr;
+    if (ordered && (dA != nullptr || dB != nullptr)) {
+        tk_B = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + 2 * hreg);
+        tk_A = tk_B + (int64_t)segs.max_spans * tokred_ranges(tab.d_out);
+        if (cudaMemsetAsync(tk_B, 0, ticket_region_bytes(tab, segs.n_tokens), stream) != cudaSuccess)
+            return LORA_ERR_CUDA;
+    }
     // dA and dB are sums over token spans added into zeroed outputs
     if (dB != nullptr && cudaMemsetAsync(dB, 0, (size_t)tab.sum_r * tab.d_out * sizeof(float), stream) != cudaSuccess)
         return LORA_ERR_CUDA;
@@ -133,7 +150,7 @@ lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void
     if (st == LORA_OK && dB != nullptr) {
         if (H_saved != nullptr)
             st = marked(marks, sB, [&] { return tc_h_to_bf16(H_saved, hb, rw, tab, segs, sB); });
-        if (st == LORA_OK) st = marked(marks, sB, [&] { return tc_db(dB, dY, hb, rw, tab, segs, sB); });
+        if (st == LORA_OK) st = marked(marks, sB, [&] { return tc_db(dB, dY, hb, rw, tk_B, tab, segs, sB); });
     }
     if (st == LORA_OK)
         st = marked(marks, stream, [&] { return tc_dh(dY, tab, segs, dhb, rw, stream); });
@@ -141,7 +158,7 @@ lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void
         forked_A = fork(side->ev[3], sA);
         if (!forked_A) st = LORA_ERR_CUDA;
     }
-    if (st == LORA_OK && dA != nullptr) st = marked(marks, sA, [&] { return tc_da(dA, X, dhb, rw, tab, segs, sA); });
+    if (st == LORA_OK && dA != nullptr) st = marked(marks, sA, [&] { return tc_da(dA, X, dhb, rw, tk_A, tab, segs, sA); });
     if (st == LORA_OK && dX != nullptr)
         st = marked(marks, stream, [&] { return tc_dx(dX, dhb, rw, tab, segs, stream); });
     // join: the caller's stream waits for every side stream that was forked,

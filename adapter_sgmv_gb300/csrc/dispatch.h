@@ -9,7 +9,10 @@ namespace lora {
 // tc_host.h), or for a decode-size forward the shrink's fp32 slice partials,
 // whichever is larger.
 size_t handoff_region_bytes(int32_t T, int32_t r_max);
-size_t packed_workspace_bytes(int32_t T, int32_t r_max, int32_t d_in);
+// the ordered backward's tickets (one int per adapter's first span and column
+// range of dB and of dA), zeroed at the start of every ordered call
+size_t ticket_region_bytes(const lora_adapter_table &tab, int32_t T);
+size_t packed_workspace_bytes(const lora_adapter_table &tab, int32_t T);
 
 // Optional CUDA events recorded around each kernel of a call (measurement):
 // ev[2k] before and ev[2k + 1] after the k-th kernel, while room is left.
@@ -23,7 +26,7 @@ lora_status_t run_shrink(float *H, const void *x, const lora_adapter_table &tab,
                          cudaStream_t stream);
 lora_status_t run_expand(void *y, const float *H, const lora_adapter_table &tab, const lora_segments &segs,
                          cudaStream_t stream);
-// ws: packed_workspace_bytes(T, r_max, d_in) bytes
+// ws: packed_workspace_bytes(tab, T) bytes
 lora_status_t run_fwd(void *y, float *H_save, const void *x, void *ws, const lora_adapter_table &tab,
                       const lora_segments &segs, cudaStream_t stream, Marks *marks = nullptr);
 // several projections reading the same x (tables share d_in and the adapter count)
@@ -39,7 +42,7 @@ struct SideStreams {
 
 lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X, const float *H_saved, void *ws,
                       const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream,
-                      Marks *marks = nullptr, const SideStreams *side = nullptr);
+                      Marks *marks = nullptr, const SideStreams *side = nullptr, bool ordered = false);
 
 // one AdamW step over A and B^T (fp32 masters, moments) and their bf16 copies
 // in the table (adamw.cu)

@@ -66,7 +66,7 @@ lora_status_t check_device()
 
 namespace {
 
-size_t workspace_bytes(const lora_adapter_table *t, int32_t T) { return packed_workspace_bytes(T, t->r_max, t->d_in); }
+size_t workspace_bytes(const lora_adapter_table *t, int32_t T) { return packed_workspace_bytes(*t, T); }
 
 
 #define LORA_TRY(expr)                          \
@@ -92,7 +92,7 @@ lora_status_t packed_fwd(void *y, float *H_save, const void *x, const lora_adapt
 
 lora_status_t packed_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X, const float *H_saved,
                          const lora_adapter_table *table, const lora_segments *segs, void *ws, size_t ws_bytes,
-                         lora_stream_t stream, Marks *marks, const SideStreams *side = nullptr)
+                         lora_stream_t stream, Marks *marks, const SideStreams *side = nullptr, bool ordered = false)
 {
     LORA_TRY(check_table(table));
     LORA_TRY(check_segs(segs, table));
@@ -104,7 +104,25 @@ lora_status_t packed_bwd(void *dX, float *dA, float *dB, const void *dY, const v
     if (need > 0 && (ws == nullptr || ws_bytes < need)) return LORA_ERR_WORKSPACE_TOO_SMALL;
     LORA_TRY(check_device());
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return run_bwd(dX, dA, dB, dY, X, H_saved, ws, *table, *segs, st, marks, side);
+    return run_bwd(dX, dA, dB, dY, X, H_saved, ws, *table, *segs, st, marks, side, ordered);
+}
+
+// the caller's side streams and events, checked: distinct, none of them `stream`
+lora_status_t side_streams_of(const lora_side_streams *side, lora_stream_t stream, SideStreams *out)
+{
+    SideStreams &sd = *out;
+    for (int i = 0; i < 2; ++i) {
+        if (side->stream[i] == nullptr || side->stream[i] == stream) return LORA_ERR_INVALID_ARG;
+        sd.s[i] = reinterpret_cast<cudaStream_t>(side->stream[i]);
+    }
+    if (side->stream[0] == side->stream[1]) return LORA_ERR_INVALID_ARG;
+    for (int i = 0; i < 4; ++i) {
+        if (side->event[i] == nullptr) return LORA_ERR_INVALID_ARG;
+        for (int j = 0; j < i; ++j)
+            if (side->event[j] == side->event[i]) return LORA_ERR_INVALID_ARG;
+        sd.ev[i] = static_cast<cudaEvent_t>(side->event[i]);
+    }
+    return LORA_OK;
 }
 
 }  // namespace
@@ -245,18 +263,19 @@ lora_status_t lora_packed_bwd_concurrent(void *dX, float *dA, float *dB, const v
 {
     if (side == nullptr) return LORA_ERR_INVALID_ARG;
     SideStreams sd;
-    for (int i = 0; i < 2; ++i) {
-        if (side->stream[i] == nullptr || side->stream[i] == stream) return LORA_ERR_INVALID_ARG;
-        sd.s[i] = reinterpret_cast<cudaStream_t>(side->stream[i]);
-    }
-    if (side->stream[0] == side->stream[1]) return LORA_ERR_INVALID_ARG;
-    for (int i = 0; i < 4; ++i) {
-        if (side->event[i] == nullptr) return LORA_ERR_INVALID_ARG;
-        for (int j = 0; j < i; ++j)
-            if (side->event[j] == side->event[i]) return LORA_ERR_INVALID_ARG;
-        sd.ev[i] = static_cast<cudaEvent_t>(side->event[i]);
-    }
+    LORA_TRY(side_streams_of(side, stream, &sd));
     return packed_bwd(dX, dA, dB, dY, X, H_saved, table, segs, ws, ws_bytes, stream, nullptr, &sd);
+}
+
+lora_status_t lora_packed_bwd_ex(void *dX, float *dA, float *dB, const void *dY, const void *X, const float *H_saved,
+                                 const lora_adapter_table *table, const lora_segments *segs, void *ws,
+                                 size_t ws_bytes, const lora_side_streams *side, uint32_t flags, lora_stream_t stream)
+{
+    if ((flags & ~(uint32_t)LORA_BWD_DETERMINISTIC) != 0) return LORA_ERR_INVALID_ARG;
+    SideStreams sd;
+    if (side != nullptr) LORA_TRY(side_streams_of(side, stream, &sd));
+    return packed_bwd(dX, dA, dB, dY, X, H_saved, table, segs, ws, ws_bytes, stream, nullptr,
+                      side != nullptr ? &sd : nullptr, (flags & LORA_BWD_DETERMINISTIC) != 0);
 }
 
 lora_status_t lora_packed_fwd_marked(void *y, float *H_save, const void *x, const lora_adapter_table *table,

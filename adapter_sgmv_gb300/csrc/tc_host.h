@@ -63,11 +63,14 @@ lora_status_t tc_dx(void *dX, const uint16_t *dh_bf16, int32_t rw, const lora_ad
                     const lora_segments &segs, cudaStream_t stream);
 
 // cases iii / iv, output [sum_r, d] accumulated into (the caller zeroes it):
-// dB[row_off + k, o] and dA[row_off + k, j].
-lora_status_t tc_db(float *dB, const void *dY, const uint16_t *h_bf16, int32_t rw, const lora_adapter_table &tab,
-                    const lora_segments &segs, cudaStream_t stream);
-lora_status_t tc_da(float *dA, const void *X, const uint16_t *dh_bf16, int32_t rw, const lora_adapter_table &tab,
-                    const lora_segments &segs, cudaStream_t stream);
+// dB[row_off + k, o] and dA[row_off + k, j].  tickets: null, or
+// tokred_ranges(d) x segs.max_spans zeroed ints for the ordered mode (each
+// adapter's span partials added in span order: bit-reproducible sums).
+int32_t tokred_ranges(int32_t d);
+lora_status_t tc_db(float *dB, const void *dY, const uint16_t *h_bf16, int32_t rw, int32_t *tickets,
+                    const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream);
+lora_status_t tc_da(float *dA, const void *X, const uint16_t *dh_bf16, int32_t rw, int32_t *tickets,
+                    const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream);
 
 // decode-sized batches: the shrink split over d_in, one CTA per (tile, slice),
 // its fp32 partials in ws, then the expand as a programmatic dependent launch

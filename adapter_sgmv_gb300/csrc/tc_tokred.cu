@@ -43,7 +43,7 @@ constexpr size_t kSmemBytes = 1024 + kStages * (size_t)kStageBytes + 4 * (size_t
 
 struct Smem {
     uint8_t *act, *h, *red;
-    uint64_t *full, *empty, *tfull, *tempty, *done;
+    uint64_t *full, *empty, *tfull, *tempty, *done, *tk_go, *tk_done;
     uint32_t *tmem_holder;
     volatile int32_t *abort;
 };
@@ -61,7 +61,9 @@ LORA_DEV Smem carve(uint8_t *raw)
     s.tfull = bars + 2 * kStages;
     s.tempty = s.tfull + 1;
     s.done = s.tempty + 1;
-    s.tmem_holder = reinterpret_cast<uint32_t *>(s.done + 1);
+    s.tk_go = s.done + 1;
+    s.tk_done = s.tk_go + 1;
+    s.tmem_holder = reinterpret_cast<uint32_t *>(s.tk_done + 1);
     s.abort = reinterpret_cast<volatile int32_t *>(s.tmem_holder + 1);
     return s;
 }
@@ -93,6 +95,36 @@ LORA_DEV void tma_reduce_add_2d(const CUtensorMap *map, const void *smem_src, in
                  : "memory");
 }
 LORA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// orders memory accesses between the generic and the async proxy (all state spaces)
+LORA_DEV void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
+// Ordered adds.  An item of the ordered mode adds its span's partial only
+// after the partials of the adapter's earlier spans (same column range) are in
+// the output: the span's ticket holds the number of spans already added.  The
+// wait is bounded like every pipeline wait; on time-out the CTA's abort flag
+// and LORA_ERR_TIMEOUT are set.  Items are taken in index order by every CTA
+// and an earlier span of the same adapter and range has the lower index, so
+// the unfinished item with the lowest index can always proceed.
+LORA_DEV bool wait_ticket(const int32_t *tk, int32_t want, volatile int32_t *abort_flag, int32_t *status)
+{
+    const long long t0 = clock64();
+    for (;;) {
+        int32_t v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(tk) : "memory");
+        if (v == want) return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitLimitCycles) {
+            *abort_flag = 1;
+            set_status(status, LORA_ERR_TIMEOUT);
+            return false;
+        }
+        __nanosleep(128);
+    }
+}
+LORA_DEV void release_ticket(int32_t *tk, int32_t v)
+{
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(tk), "r"(v) : "memory");
+}
 LORA_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -100,7 +132,7 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
                  const __grid_constant__ CUtensorMap map_h,
                  const __grid_constant__ CUtensorMap map_g, const uint16_t *__restrict__ act, int32_t d,
                  const uint16_t *__restrict__ hbuf, int32_t rw, float use_scale, int32_t blocks3,
-                 lora_adapter_table tab, lora_segments segs)
+                 int32_t *__restrict__ tickets, lora_adapter_table tab, lora_segments segs)
 {
     extern __shared__ uint8_t smem_raw[];
     const Smem S = carve(smem_raw);
@@ -114,6 +146,8 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
         mbar_init(S.tfull, 1);
         mbar_init(S.tempty, 4);
         mbar_init(S.done, 1);
+        mbar_init(S.tk_go, 1);    // ordered mode: the ticket says the earlier spans are added
+        mbar_init(S.tk_done, 4);  // ordered mode: every epilogue warp's adds are complete
         *S.abort = 0;
         fence_barrier_init();
     }
@@ -268,7 +302,7 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
         // zero there); rows and columns past G's edge are clipped by the TMA.
         const uint32_t lane_base = 32u * (warp & 3);
         float *red = reinterpret_cast<float *>(S.red + (warp - 2) * kRedBytes);
-        uint32_t nitem = 0;
+        uint32_t nitem = 0, n_ord = 0;
         for (int32_t it = blockIdx.x; it < n_items; it += gridDim.x) {
             const Item I = load_item(tab, segs, it, n_ranges, d);
             if (!I.ad.ok) continue;
@@ -276,6 +310,25 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
             if (!mbar_wait_warp(S.tfull, nitem & 1u, S.abort, segs.status)) break;
             tc_fence_after();
             const float c = use_scale != 0.f ? I.ad.scale : 1.0f;
+            // ordered mode, adapters of three spans or more (with two, the two adds
+            // to zero commute exactly): span j of the adapter, its ticket
+            int32_t *tk = nullptr;
+            int32_t tj = 0;
+            if (tickets != nullptr) {
+                const int32_t g0 = segs.seg_start[I.span.adapter], g1 = segs.seg_start[I.span.adapter + 1];
+                if (g1 - g0 > 2 * LORA_SPAN_TOKENS) {
+                    tj = (I.span.begin - g0) / LORA_SPAN_TOKENS;
+                    tk = tickets + (int64_t)(it / n_ranges - tj) * n_ranges + it % n_ranges;
+                }
+            }
+            if (tk != nullptr) {
+                if (warp == 2 && lane == 0 && wait_ticket(tk, tj, S.abort, segs.status)) {
+                    fence_proxy_async_all();
+                    mbar_arrive(S.tk_go);
+                }
+                if (!mbar_wait_warp(S.tk_go, n_ord & 1u, S.abort, segs.status)) break;
+                if (lane == 0) fence_proxy_async_all();
+            }
             for (int q = 0; q < 4; ++q) {
                 if (q >= I.n_chunks) break;
                 if (lane == 0) bulk_wait_read0();  // the previous chunk's reductions have read the block
@@ -301,6 +354,18 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
             __syncwarp();
             if (lane == 0) mbar_arrive(S.tempty);
             ++nitem;
+            if (tk != nullptr) {  // the span's adds are complete in every warp: pass the ticket on
+                if (lane == 0) {
+                    bulk_wait0();
+                    fence_proxy_async_all();
+                    mbar_arrive(S.tk_done);
+                }
+                if (warp == 2) {
+                    if (!mbar_wait_warp(S.tk_done, n_ord & 1u, S.abort, segs.status)) break;
+                    if (lane == 0) release_ticket(tk, tj + 1);
+                }
+                ++n_ord;
+            }
         }
         if (lane == 0) bulk_wait0();
         __syncwarp();
@@ -315,7 +380,8 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
 }
 
 lora_status_t launch_tokred(float *G, const void *act, int32_t d, const uint16_t *hbuf, int32_t rw, float use_scale,
-                            const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream)
+                            int32_t *tickets, const lora_adapter_table &tab, const lora_segments &segs,
+                            cudaStream_t stream)
 {
     if (segs.n_tokens == 0 || segs.max_spans == 0) return LORA_OK;
     CUtensorMap map_act, map_act3, map_h, map_g;
@@ -338,22 +404,24 @@ lora_status_t launch_tokred(float *G, const void *act, int32_t d, const uint16_t
     if (!blocks3) map_act3 = map_act;
     tc_tokred_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_act, map_act3, map_h, map_g,
                                                              static_cast<const uint16_t *>(act), d, hbuf, rw,
-                                                             use_scale, blocks3, tab, segs);
+                                                             use_scale, blocks3, tickets, tab, segs);
     return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
 }  // namespace
 
-lora_status_t tc_db(float *dB, const void *dY, const uint16_t *h_bf16, int32_t rw, const lora_adapter_table &tab,
-                    const lora_segments &segs, cudaStream_t stream)
+int32_t tokred_ranges(int32_t d) { return (d + kRange - 1) / kRange; }
+
+lora_status_t tc_db(float *dB, const void *dY, const uint16_t *h_bf16, int32_t rw, int32_t *tickets,
+                    const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream)
 {
-    return launch_tokred(dB, dY, tab.d_out, h_bf16, rw, 1.f, tab, segs, stream);
+    return launch_tokred(dB, dY, tab.d_out, h_bf16, rw, 1.f, tickets, tab, segs, stream);
 }
 
-lora_status_t tc_da(float *dA, const void *X, const uint16_t *dh_bf16, int32_t rw, const lora_adapter_table &tab,
-                    const lora_segments &segs, cudaStream_t stream)
+lora_status_t tc_da(float *dA, const void *X, const uint16_t *dh_bf16, int32_t rw, int32_t *tickets,
+                    const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream)
 {
-    return launch_tokred(dA, X, tab.d_in, dh_bf16, rw, 0.f, tab, segs, stream);
+    return launch_tokred(dA, X, tab.d_in, dh_bf16, rw, 0.f, tickets, tab, segs, stream);
 }
 
 }  // namespace lora

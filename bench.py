@@ -198,6 +198,7 @@ class Workload:
         self.dA = torch.empty((spec.sum_r, spec.d_in), dtype=torch.float32, device=dev)
         self.dB = torch.empty((spec.sum_r, spec.d_out), dtype=torch.float32, device=dev)
         self.side = lora.SideStreams(dev)  # the backward's dB / dA run on these beside dh / dX
+        self.deterministic = False  # dA / dB summed in a fixed span order (lora_packed_bwd_ex)
         self.segs = None
 
     def build(self, stream=None):
@@ -223,7 +224,10 @@ class Workload:
 
         x = self.inp["x"] if x is None else x
         dY = self.inp["dY"] if dY is None else dY
-        if events is None:
+        if events is None and self.deterministic:
+            lora.lora_packed_bwd_ex(self.dX, self.dA, self.dB, dY, x, self.H, self.table, self.segs, self.ws,
+                                    side=self.side, deterministic=True, stream=stream)
+        elif events is None:
             lora.lora_packed_bwd_concurrent(self.dX, self.dA, self.dB, dY, x, self.H, self.table, self.segs, self.ws,
                                             self.side, stream=stream)
         else:
@@ -856,6 +860,12 @@ def run_ours(args, rank, world, dev):
     dom_bytes = templates[dom]["bytes"] / templates[dom]["launches"]
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
 
+    # the same steps with the ordered (bit-reproducible) dA / dB sums
+    work.deterministic = True
+    dstart, dend, _, _ = time_steps(work, args.steps, 2, stream)
+    torch.cuda.synchronize()
+    work.deterministic = False
+    det_ms = dstart.elapsed_time(dend) / args.steps
     e2e_ms, h2d, d2h = time_e2e(work, max(3, args.steps // 2), 2, stream) if not args.no_e2e else (None, 0, 0)
     decode = time_decode(dev, stream) if rank == 0 and not args.no_decode else None
     decode_multi = time_decode_multi(dev, stream) if rank == 0 and not args.no_decode else None
@@ -896,6 +906,9 @@ def run_ours(args, rank, world, dev):
                      "bytes_per_launch": int(dom_bytes), "ms_per_launch": round(dom_ms, 4),
                      "launches_per_step": templates[dom]["launches"],
                      "tensor_frac_at_this_time": round(step_flops(spec) / (ms_step * 1e-3) / 1e12 / tflops, 4)},
+        "deterministic_bwd": {"ms_per_step": round(det_ms, 4), "extra_ms": round(det_ms - ms_step, 4),
+                              "note": "lora_packed_bwd_ex with LORA_BWD_DETERMINISTIC: dA / dB bit-identical "
+                                      "run to run (every adapter here has four spans of 1024 tokens)"},
         "kernels_ms": per_kernel,
         "kernels_note": ("from a second pass of the same steps with an event pair around every kernel "
                          f"({round(mstart.elapsed_time(mend) / args.steps, 4)} ms per step with the pairs, "

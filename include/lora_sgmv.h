@@ -232,7 +232,8 @@ LORA_API lora_status_t lora_packed_fwd(void *y, float *H_save, const void *x,
  * bit-identical (two additions to zero commute exactly); with more, the
  * span partials may be added in a different order from run to run, so the
  * last bits of dA / dB can differ (every order is within the same rounding
- * of the exact sum).
+ * of the exact sum).  lora_packed_bwd_ex with LORA_BWD_DETERMINISTIC fixes
+ * the order.
  */
 LORA_API lora_status_t lora_packed_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X,
                               const float *H_saved, const lora_adapter_table *table,
@@ -284,6 +285,29 @@ LORA_API lora_status_t lora_packed_bwd_concurrent(void *dX, float *dA, float *dB
                                                   const float *H_saved, const lora_adapter_table *table,
                                                   const lora_segments *segs, void *ws, size_t ws_bytes,
                                                   const lora_side_streams *side, lora_stream_t stream);
+
+/*
+ * The packed backward with options: lora_packed_bwd when side is NULL and
+ * flags is 0, lora_packed_bwd_concurrent when side is given.
+ *   side   NULL, or the caller's side streams and events (see
+ *          lora_packed_bwd_concurrent)
+ *   flags  0 or LORA_BWD_DETERMINISTIC: dA and dB come out bit-identical from
+ *          run to run for every adapter.  The partial sum of each span of
+ *          LORA_SPAN_TOKENS tokens is added into the output in span order (for
+ *          adapters of more than two spans, a span's adds wait, within the
+ *          launch and for a bounded time, until the previous span's adds are
+ *          complete; a wait that gives up sets LORA_ERR_TIMEOUT on the device).
+ *          Uses ticket counters at the end of the workspace, which
+ *          lora_workspace_bytes includes, zeroed by the call.  The pages give no
+ *          summation order; this mode fixes one.
+ * Errors: those of lora_packed_bwd / lora_packed_bwd_concurrent;
+ * LORA_ERR_INVALID_ARG for unknown flag bits.
+ */
+#define LORA_BWD_DETERMINISTIC 1u
+LORA_API lora_status_t lora_packed_bwd_ex(void *dX, float *dA, float *dB, const void *dY, const void *X,
+                                          const float *H_saved, const lora_adapter_table *table,
+                                          const lora_segments *segs, void *ws, size_t ws_bytes,
+                                          const lora_side_streams *side, uint32_t flags, lora_stream_t stream);
 
 /*
  * Measurement variants of lora_packed_fwd / lora_packed_bwd: the same checks,
