@@ -22,8 +22,11 @@
 // TMA; their products stop at r_pad.  A small kernel beside them converts a
 // saved fp32 H into the same hand-off rows for the backward.
 //
-// Warp roles (192 threads): 0 loads, 1 issues MMAs and owns TMEM, 2..5 epilogue.
-// Every wait is bounded (tc::mbar_wait).
+// Warp roles (352 threads): 0..5 load, warp w filling every stage of ring
+// slot w (a gathered stage's copies are waited for by the warp that issued
+// them, which makes them visible to the tensor cores and releases the stage at
+// once, so all six stages can be in flight); 6 issues MMAs and owns TMEM;
+// 7..10 epilogue.  Every wait is bounded (tc::mbar_wait).
 #include "internal.h"
 #include "tc_common.cuh"
 #include "tc_host.h"
@@ -34,8 +37,9 @@ namespace {
 using namespace tc;
 
 constexpr int kStages = 6;
-constexpr int kLag = 3;            // cp.async groups kept in flight per producer lane
-constexpr int kThreads = 192;
+constexpr int kProd = kStages;     // producer warps, one per ring slot
+constexpr int kMmaWarp = kProd;
+constexpr int kThreads = 32 * (kProd + 1 + 4);
 constexpr uint32_t kActBytes = 128 * 64 * 2;
 constexpr uint32_t kWBytes = LORA_MAX_RANK * 64 * 2;
 constexpr uint32_t kStageBytes = kActBytes + kWBytes;
@@ -86,7 +90,7 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(&S.full[i], 33);  // lane 0's expect-tx arrive + one per producer lane
+            mbar_init(&S.full[i], 33);  // lane 0's expect-tx arrive + one per lane of the slot's producer warp
             mbar_init(&S.empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -97,7 +101,7 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
         *S.abort = 0;
         fence_barrier_init();
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tmem_alloc(S.tmem_holder, kTmemCols);
         tmem_relinquish();
     }
@@ -108,23 +112,29 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
     const int32_t n_tiles = *segs.n_tiles;
     const int32_t nk = (d + 63) / 64;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
+    if (warp < kProd) {
+        // ------------------------------------------------------------ producers
+        // Stage g of the whole sequence goes to ring slot g % kStages = warp.
+        if (lane == 0 && warp == 0) {
             prefetch_tensormap(&map_act);
             prefetch_tensormap(&map_w.m16);
             prefetch_tensormap(&map_w.m32);
             prefetch_tensormap(&map_w.m64);
         }
-        uint32_t g = 0;
+        uint32_t g = 0, last = 0xffffffffu;
         bool ok = true;
-        ArriveQueue<kLag, kStages> aq;
         for (int32_t ti = blockIdx.x; ti < n_tiles && ok; ti += gridDim.x) {
             const Tile T = load_tile(segs.tiles, ti);
             const AdapterInfo ad = load_adapter(tab, T.adapter, segs.status);
             if (!ad.ok) continue;
             const int32_t rp = rpad16(ad.rank);
             const bool contiguous = (T.flags & 1) != 0;
+            // this warp's first stage of the tile, and whether it has one at all
+            const uint32_t k0 = (uint32_t)((warp - (int)(g % kStages) + kStages) % kStages);
+            if ((int32_t)k0 >= nk) {
+                g += (uint32_t)nk;
+                continue;
+            }
             const int32_t t0 = segs.perm[T.begin];
             int32_t tok[32];  // rows (lane >> 3) + 4 q of a gathered tile
             if (!contiguous) {
@@ -134,8 +144,9 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
                     tok[q] = m < T.rows ? segs.perm[T.begin + m] : -1;
                 }
             }
-            for (int32_t kb = 0; kb < nk; ++kb) {
-                const uint32_t s = g % kStages, ph = (g / kStages) & 1u;
+            for (int32_t kb = (int32_t)k0; kb < nk; kb += kStages) {
+                const uint32_t gs = g + (uint32_t)kb;
+                const uint32_t s = gs % kStages, ph = (gs / kStages) & 1u;
                 if (!mbar_wait(&S.empty[s], ph ^ 1u, S.abort, segs.status)) {
                     ok = false;
                     break;
@@ -158,21 +169,23 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
                         const uint16_t *src = v ? act + (int64_t)tok[q] * d + j0 + 8 * c : act;
                         cp_async_16(act_s + sw128_offset(m, c), src, v);
                     }
+                    // this lane's copies have landed; visible to the tensor cores
+                    cp_async_commit();
+                    cp_async_wait<0>();
+                    fence_proxy_async();
                 }
-                aq.issued(S.full, g, !contiguous);
-                ++g;
+                mbar_arrive(&S.full[s]);
+                last = gs;
+            }
+            g += (uint32_t)nk;
+        }
+        if (!ok && lane == 0 && last != 0xffffffffu) {  // aborted: let the last stage's TMA copies land
+            uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&S.full[last % kStages], (last / kStages) & 1u) &&
+                   globaltimer_ns() - t0 < kWaitLimitNs / 8) {
             }
         }
-        aq.drain(S.full);
-        if (!ok && lane == 0) {  // aborted: let issued TMA copies land before the CTA leaves
-            for (uint32_t u = g > (uint32_t)kStages ? g - kStages : 0u; u < g; ++u) {
-                uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(&S.full[u % kStages], (u / kStages) & 1u) &&
-                       globaltimer_ns() - t0 < kWaitLimitNs / 8) {
-                }
-            }
-        }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             uint32_t g = 0, acc_n = 0;
@@ -287,7 +300,7 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
     }

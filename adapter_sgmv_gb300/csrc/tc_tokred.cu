@@ -18,7 +18,10 @@
 // warp's 32 x r_pad block in shared memory and adds it into the
 // zero-initialised output with TMA bulk reductions (spans of an adapter sum).
 //
-// Warp roles (192 threads): 0 loads, 1 MMA + TMEM owner, 2..5 epilogue.
+// Warp roles (288 threads): 0..3 load, warp w filling every stage of ring slot
+// w (a gathered stage's copies are waited for by the warp that issued them,
+// which makes them visible to the tensor cores and releases the stage at once,
+// so all four stages can be in flight); 4 MMA + TMEM owner; 5..8 epilogue.
 #include "internal.h"
 #include "tc_common.cuh"
 #include "tc_host.h"
@@ -28,9 +31,11 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 192;
 constexpr int kStages = 4;
-constexpr int kLag = 2;
+constexpr int kProd = kStages;  // producer warps, one per ring slot
+constexpr int kMmaWarp = kProd;
+constexpr int kEpi0 = kProd + 1;  // first epilogue warp
+constexpr int kThreads = 32 * (kProd + 1 + 4);
 constexpr int kTok = 32;                                  // tokens per stage
 constexpr int kRange = 512;                               // columns of d per work item
 constexpr uint32_t kActBytes = kTok * kRange * 2;         // 8 boxes of [64 cols x 32 tokens]
@@ -151,7 +156,7 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
         *S.abort = 0;
         fence_barrier_init();
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tmem_alloc(S.tmem_holder, kTmemCols);
         tmem_relinquish();
     }
@@ -162,32 +167,41 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
     const int32_t n_ranges = (d + kRange - 1) / kRange;
     const int32_t n_items = *segs.n_spans * n_ranges;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
+    if (warp < kProd) {
+        // ------------------------------------------------------------ producers
+        // Stage g of the whole sequence goes to ring slot g % kStages = warp.
+        if (lane == 0 && warp == 0) {
             prefetch_tensormap(blocks3 ? &map_act3 : &map_act);
             prefetch_tensormap(&map_h);
         }
-        uint32_t g = 0;
+        uint32_t g = 0, last = 0xffffffffu;
         bool ok = true;
-        ArriveQueue<kLag, kStages> aq;
         for (int32_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const Item I = load_item(tab, segs, it, n_ranges, d);
             if (!I.ad.ok) continue;
+            // this warp's first stage of the item, and whether it has one at all
+            const int32_t st0 = (warp - (int)(g % kStages) + kStages) % kStages;
+            if (st0 >= I.n_stages) {
+                g += (uint32_t)I.n_stages;
+                continue;
+            }
             const int32_t rp = rpad16(I.ad.rank);
             const int natoms = (rp + 63) / 64;
             const int32_t p0 = I.span.begin;
             const bool contiguous = (I.span.flags & 1) != 0;
             const int32_t t0 = segs.perm[p0];
-            for (int32_t st = 0; st < I.n_stages; ++st) {
-                const uint32_t s = g % kStages, ph = (g / kStages) & 1u;
+            for (int32_t st = st0; st < I.n_stages; st += kStages) {
+                const uint32_t gs = g + (uint32_t)st;
+                const uint32_t s = gs % kStages, ph = (gs / kStages) & 1u;
+                // a gathered stage: lane m holds the token of row m (loaded before the wait)
+                const int valid = min(kTok, I.span.rows - kTok * st);  // rows of this stage in the span
+                const int32_t tl = !contiguous && lane < valid ? segs.perm[p0 + kTok * st + lane] : -1;
                 if (!mbar_wait(&S.empty[s], ph ^ 1u, S.abort, segs.status)) {
                     ok = false;
                     break;
                 }
                 uint8_t *act_s = S.act + s * kActBytes;
                 uint8_t *h_s = S.h + s * kHBytes;
-                const int valid = min(kTok, I.span.rows - kTok * st);  // rows of this stage in the span
                 const bool h_tma = valid == kTok;
                 if (lane == 0) {
                     // a 3-D box always moves all eight blocks (past d: zero-filled)
@@ -209,10 +223,9 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
                 }
                 if (!contiguous) {
                     // token row m, 16-byte chunk c of the 512 columns: box b = c / 8 holds
-                    // columns 64 b .. 64 b + 63 as a [32 x 128 B] 128-byte-swizzled block.
-                    // Lane m reads row m's token once; lanes take chunks lane, lane + 32.
+                    // columns 64 b .. 64 b + 63 as a [32 x 128 B] 128-byte-swizzled block;
+                    // lanes take chunks lane, lane + 32
                     const int nch = I.n_chunks * 16;
-                    const int32_t tl = lane < valid ? segs.perm[p0 + kTok * st + lane] : -1;
 #pragma unroll 4
                     for (int m = 0; m < kTok; ++m) {
                         const int32_t t = __shfl_sync(0xffffffffu, tl, m);
@@ -238,20 +251,23 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
                         cp_async_16(h_s + (c >> 3) * kBox + sw128_offset((uint32_t)m, (uint32_t)(c & 7)), src, v);
                     }
                 }
-                aq.issued(S.full, g, !contiguous || !h_tma);
-                ++g;
-            }
-        }
-        aq.drain(S.full);
-        if (!ok && lane == 0) {
-            for (uint32_t u = g > (uint32_t)kStages ? g - kStages : 0u; u < g; ++u) {
-                uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(&S.full[u % kStages], (u / kStages) & 1u) &&
-                       globaltimer_ns() - t0 < kWaitLimitNs / 8) {
+                if (!contiguous || !h_tma) {  // this lane's copies have landed; visible to the tensor cores
+                    cp_async_commit();
+                    cp_async_wait<0>();
+                    fence_proxy_async();
                 }
+                mbar_arrive(&S.full[s]);
+                last = gs;
+            }
+            g += (uint32_t)I.n_stages;
+        }
+        if (!ok && lane == 0 && last != 0xffffffffu) {  // aborted: let the last stage's TMA copies land
+            uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&S.full[last % kStages], (last / kStages) & 1u) &&
+                   globaltimer_ns() - t0 < kWaitLimitNs / 8) {
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             uint32_t g = 0, nitem = 0;
@@ -301,7 +317,7 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
         // reductions of [16 x 32].  Rows k in [r_i, r_pad) add exact zeros (h is
         // zero there); rows and columns past G's edge are clipped by the TMA.
         const uint32_t lane_base = 32u * (warp & 3);
-        float *red = reinterpret_cast<float *>(S.red + (warp - 2) * kRedBytes);
+        float *red = reinterpret_cast<float *>(S.red + (warp - kEpi0) * kRedBytes);
         uint32_t nitem = 0, n_ord = 0;
         for (int32_t it = blockIdx.x; it < n_items; it += gridDim.x) {
             const Item I = load_item(tab, segs, it, n_ranges, d);
@@ -322,7 +338,7 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
                 }
             }
             if (tk != nullptr) {
-                if (warp == 2 && lane == 0 && wait_ticket(tk, tj, S.abort, segs.status)) {
+                if (warp == kEpi0 && lane == 0 && wait_ticket(tk, tj, S.abort, segs.status)) {
                     fence_proxy_async_all();
                     mbar_arrive(S.tk_go);
                 }
@@ -360,7 +376,7 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
                     fence_proxy_async_all();
                     mbar_arrive(S.tk_done);
                 }
-                if (warp == 2) {
+                if (warp == kEpi0) {
                     if (!mbar_wait_warp(S.tk_done, n_ord & 1u, S.abort, segs.status)) break;
                     if (lane == 0) release_ticket(tk, tj + 1);
                 }
@@ -373,7 +389,7 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
     }
