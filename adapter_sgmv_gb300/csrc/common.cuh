@@ -31,23 +31,18 @@ LORA_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---------------------------------------------------------------- bf16 words
 // bf16 is carried as raw 16-bit words; widening is exact, narrowing rounds to
-// nearest-even (NaN stays NaN).
+// nearest-even (cvt.rn: NaN stays NaN).
 LORA_DEV float bf16_to_f32(uint16_t h) { return __uint_as_float(((uint32_t)h) << 16); }
-
-LORA_DEV uint16_t f32_to_bf16(float f)
-{
-    uint32_t u = __float_as_uint(f);
-    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0u) return (uint16_t)0x7fc0u;
-    u += 0x7fffu + ((u >> 16) & 1u);
-    return (uint16_t)(u >> 16);
-}
 
 // two bf16 packed in a 32-bit word: low half is the lower-addressed element
 LORA_DEV float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 LORA_DEV float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+// one instruction for both halves (the epilogues round millions of elements)
 LORA_DEV uint32_t pack_bf16(float lo, float hi)
 {
-    return (uint32_t)f32_to_bf16(lo) | ((uint32_t)f32_to_bf16(hi) << 16);
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
 }
 
 // ---------------------------------------------------------------- work tiles

@@ -109,14 +109,6 @@ LORA_DEV void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint3
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// two floats to bf16 (nearest-even) in one word, `lo` in the low half
-LORA_DEV uint32_t cvt_bf16x2(float lo, float hi)
-{
-    uint32_t d;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
-    return d;
-}
-
 // A work item's tile, its adapter's table entry and the token of row
 // threadIdx.x, read in two rounds of memory latency instead of four: the tile
 // alongside the tile count, the table entry alongside the token.  For a tile
@@ -384,9 +376,9 @@ __global__ void __launch_bounds__(kThreads, 2) dec_expand_kernel(const __grid_co
                     if (4 * k4 + u < r_max) hrow[4 * k4 + u] = e[u];
             }
         }
-        const uint32_t h01 = cvt_bf16x2(e[0], e[1]), h23 = cvt_bf16x2(e[2], e[3]);
-        const uint32_t l01 = cvt_bf16x2(e[0] - bf16lo(h01), e[1] - bf16hi(h01));
-        const uint32_t l23 = cvt_bf16x2(e[2] - bf16lo(h23), e[3] - bf16hi(h23));
+        const uint32_t h01 = pack_bf16(e[0], e[1]), h23 = pack_bf16(e[2], e[3]);
+        const uint32_t l01 = pack_bf16(e[0] - bf16lo(h01), e[1] - bf16hi(h01));
+        const uint32_t l23 = pack_bf16(e[2] - bf16lo(h23), e[3] - bf16hi(h23));
         *reinterpret_cast<uint2 *>(hh + m * hs + 4 * k4) = make_uint2(h01, h23);
         *reinterpret_cast<uint2 *>(hl + m * hs + 4 * k4) = make_uint2(l01, l23);
     }
@@ -429,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 2) dec_expand_kernel(const __grid_co
             for (int hf = 0; hf < 2; ++hf) {
                 uint32_t *p = reinterpret_cast<uint32_t *>(ys + (row + 8 * hf) * kYStride + col);
                 const uint32_t w = *p;
-                *p = cvt_bf16x2(bf16lo(w) + c * acc[n][2 * hf], bf16hi(w) + c * acc[n][2 * hf + 1]);
+                *p = pack_bf16(bf16lo(w) + c * acc[n][2 * hf], bf16hi(w) + c * acc[n][2 * hf + 1]);
             }
         }
     }
