@@ -27,9 +27,36 @@ size_t ticket_region_bytes(const lora_adapter_table &tab, int32_t T)
     return (size_t)((words * 4 + 255) & ~int64_t(255));
 }
 
+size_t part_region_bytes(const lora_adapter_table &tab, int32_t T)
+{
+    const SegLayout L = seg_layout(T, tab.n_adapters);
+    if (!L.ok) return 0;
+    const int32_t a = rowproj_splits(L.max_tiles, tab.d_in), b = rowproj_splits(L.max_tiles, tab.d_out);
+    const int32_t sp = a > b ? a : b;
+    if (sp <= 1) return 0;
+    const int64_t bytes = (int64_t)sp * T * rowproj_part_ld(tab.r_max) * 4;
+    return (size_t)((bytes + 255) & ~int64_t(255));
+}
+
+namespace {
+// case i's partials in the workspace, when the workspace holds them
+float *part_region(void *ws, size_t ws_bytes, const lora_adapter_table &tab, int32_t T)
+{
+    const size_t off = 2 * handoff_region_bytes(T, tab.r_max) + ticket_region_bytes(tab, T);
+    const size_t need = part_region_bytes(tab, T);
+    if (need == 0 || ws_bytes < off + need) return nullptr;
+    return reinterpret_cast<float *>(static_cast<char *>(ws) + off);
+}
+}  // namespace
+
+size_t bwd_workspace_bytes(const lora_adapter_table &tab, int32_t T)
+{
+    return 2 * handoff_region_bytes(T, tab.r_max) + ticket_region_bytes(tab, T) + part_region_bytes(tab, T);
+}
+
 size_t packed_workspace_bytes(const lora_adapter_table &tab, int32_t T)
 {
-    const size_t packed = 2 * handoff_region_bytes(T, tab.r_max) + ticket_region_bytes(tab, T);
+    const size_t packed = bwd_workspace_bytes(tab, T);
     const size_t decode = T <= kDecodeMaxTokens ? decode_workspace_bytes(T, tab.r_max, tab.d_in) : 0;
     return packed > decode ? packed : decode;
 }
@@ -37,7 +64,7 @@ size_t packed_workspace_bytes(const lora_adapter_table &tab, int32_t T)
 lora_status_t run_shrink(float *H, const void *x, const lora_adapter_table &tab, const lora_segments &segs,
                          cudaStream_t stream)
 {
-    return tc_shrink(x, tab, segs, H, nullptr, nullptr, 0, stream);
+    return tc_shrink(x, tab, segs, H, nullptr, nullptr, 0, nullptr, stream);  // no workspace: not split
 }
 
 lora_status_t run_expand(void *y, const float *H, const lora_adapter_table &tab, const lora_segments &segs,
@@ -65,7 +92,7 @@ lora_status_t marked(Marks *m, cudaStream_t stream, F f)
 
 }  // namespace
 
-lora_status_t run_fwd(void *y, float *H_save, const void *x, void *ws, const lora_adapter_table &tab,
+lora_status_t run_fwd(void *y, float *H_save, const void *x, void *ws, size_t ws_bytes, const lora_adapter_table &tab,
                       const lora_segments &segs, cudaStream_t stream, Marks *marks)
 {
     if (segs.n_tokens <= kDecodeMaxTokens)  // one pair of marks around both decode launches
@@ -73,7 +100,9 @@ lora_status_t run_fwd(void *y, float *H_save, const void *x, void *ws, const lor
     const int32_t rw = handoff_cols(tab.r_max);
     uint16_t *hi = static_cast<uint16_t *>(ws);
     uint16_t *lo = reinterpret_cast<uint16_t *>(static_cast<char *>(ws) + handoff_region_bytes(segs.n_tokens, tab.r_max));
-    lora_status_t st = marked(marks, stream, [&] { return tc_shrink(x, tab, segs, H_save, hi, lo, rw, stream); });
+    float *part = part_region(ws, ws_bytes, tab, segs.n_tokens);
+    lora_status_t st =
+        marked(marks, stream, [&] { return tc_shrink(x, tab, segs, H_save, hi, lo, rw, part, stream); });
     if (st != LORA_OK) return st;
     return marked(marks, stream, [&] { return tc_expand_bf16(y, hi, lo, rw, tab, segs, stream); });
 }
@@ -95,25 +124,27 @@ size_t multi_workspace_bytes(int32_t n_proj, const lora_adapter_table *tabs, int
 }
 
 lora_status_t run_multi_fwd(int32_t n_proj, void *const *y, float *const *H_save, const void *x, void *ws,
-                            const lora_adapter_table *tabs, const lora_segments &segs, cudaStream_t stream)
+                            size_t ws_bytes, const lora_adapter_table *tabs, const lora_segments &segs,
+                            cudaStream_t stream)
 {
     if (segs.n_tokens <= kDecodeMaxTokens) return tc_decode_multi(n_proj, y, H_save, x, ws, tabs, segs, stream);
     for (int32_t p = 0; p < n_proj; ++p) {  // large batches: the packed kernels, one projection after another
         const lora_status_t st =
-            run_fwd(y[p], H_save != nullptr ? H_save[p] : nullptr, x, ws, tabs[p], segs, stream, nullptr);
+            run_fwd(y[p], H_save != nullptr ? H_save[p] : nullptr, x, ws, ws_bytes, tabs[p], segs, stream, nullptr);
         if (st != LORA_OK) return st;
     }
     return LORA_OK;
 }
 
 lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X, const float *H_saved, void *ws,
-                      const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream, Marks *marks,
-                      const SideStreams *side, bool ordered)
+                      size_t ws_bytes, const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream,
+                      Marks *marks, const SideStreams *side, bool ordered)
 {
     const int32_t rw = handoff_cols(tab.r_max);
     const size_t hreg = handoff_region_bytes(segs.n_tokens, tab.r_max);
     uint16_t *hb = static_cast<uint16_t *>(ws);
     uint16_t *dhb = reinterpret_cast<uint16_t *>(static_cast<char *>(ws) + hreg);
+    float *part = part_region(ws, ws_bytes, tab, segs.n_tokens);  // case i split along d (few tiles)
     // ordered mode: tickets of dB, then of dA, after the hand-off regions
     int32_t *tk_B = nullptr, *tk_A = nullptr;
     if (ordered && (dA != nullptr || dB != nullptr)) {
@@ -142,7 +173,7 @@ lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void
     };
     bool forked_B = false, forked_A = false;
     if (H_saved == nullptr)
-        st = marked(marks, stream, [&] { return tc_shrink(X, tab, segs, nullptr, hb, nullptr, rw, stream); });
+        st = marked(marks, stream, [&] { return tc_shrink(X, tab, segs, nullptr, hb, nullptr, rw, part, stream); });
     if (st == LORA_OK && par && dB != nullptr) {  // fork B once the outputs are zeroed (and H recomputed)
         forked_B = fork(side->ev[0], sB);
         if (!forked_B) st = LORA_ERR_CUDA;
@@ -153,7 +184,7 @@ lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void
         if (st == LORA_OK) st = marked(marks, sB, [&] { return tc_db(dB, dY, hb, rw, tk_B, tab, segs, sB); });
     }
     if (st == LORA_OK)
-        st = marked(marks, stream, [&] { return tc_dh(dY, tab, segs, dhb, rw, stream); });
+        st = marked(marks, stream, [&] { return tc_dh(dY, tab, segs, dhb, rw, part, stream); });
     if (st == LORA_OK && par && dA != nullptr) {  // fork A after dh
         forked_A = fork(side->ev[3], sA);
         if (!forked_A) st = LORA_ERR_CUDA;

@@ -12,6 +12,10 @@ size_t handoff_region_bytes(int32_t T, int32_t r_max);
 // the ordered backward's tickets (one int per adapter's first span and column
 // range of dB and of dA), zeroed at the start of every ordered call
 size_t ticket_region_bytes(const lora_adapter_table &tab, int32_t T);
+// case i's partials for batches of few tiles (zero bytes otherwise), after the tickets
+size_t part_region_bytes(const lora_adapter_table &tab, int32_t T);
+// what the backward uses of the workspace: hand-off copies, tickets, partials
+size_t bwd_workspace_bytes(const lora_adapter_table &tab, int32_t T);
 size_t packed_workspace_bytes(const lora_adapter_table &tab, int32_t T);
 
 // Optional CUDA events recorded around each kernel of a call (measurement):
@@ -26,13 +30,15 @@ lora_status_t run_shrink(float *H, const void *x, const lora_adapter_table &tab,
                          cudaStream_t stream);
 lora_status_t run_expand(void *y, const float *H, const lora_adapter_table &tab, const lora_segments &segs,
                          cudaStream_t stream);
-// ws: packed_workspace_bytes(tab, T) bytes
-lora_status_t run_fwd(void *y, float *H_save, const void *x, void *ws, const lora_adapter_table &tab,
+// ws: ws_bytes >= 2 * handoff_region_bytes bytes; case i is split along d
+// only when ws_bytes reaches packed_workspace_bytes(tab, T)
+lora_status_t run_fwd(void *y, float *H_save, const void *x, void *ws, size_t ws_bytes, const lora_adapter_table &tab,
                       const lora_segments &segs, cudaStream_t stream, Marks *marks = nullptr);
 // several projections reading the same x (tables share d_in and the adapter count)
 size_t multi_workspace_bytes(int32_t n_proj, const lora_adapter_table *tabs, int32_t T);
 lora_status_t run_multi_fwd(int32_t n_proj, void *const *y, float *const *H_save, const void *x, void *ws,
-                            const lora_adapter_table *tabs, const lora_segments &segs, cudaStream_t stream);
+                            size_t ws_bytes, const lora_adapter_table *tabs, const lora_segments &segs,
+                            cudaStream_t stream);
 // Caller-owned streams and events on which the backward may run its
 // independent products side by side (lora_packed_bwd_concurrent).
 struct SideStreams {
@@ -41,7 +47,7 @@ struct SideStreams {
 };
 
 lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X, const float *H_saved, void *ws,
-                      const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream,
+                      size_t ws_bytes, const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream,
                       Marks *marks = nullptr, const SideStreams *side = nullptr, bool ordered = false);
 
 // one AdamW step over A and B^T (fp32 masters, moments) and their bf16 copies

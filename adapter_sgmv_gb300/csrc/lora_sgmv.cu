@@ -87,7 +87,7 @@ lora_status_t packed_fwd(void *y, float *H_save, const void *x, const lora_adapt
     if (need > 0 && (ws == nullptr || ws_bytes < need)) return LORA_ERR_WORKSPACE_TOO_SMALL;
     LORA_TRY(check_device());
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return run_fwd(y, H_save, x, ws, *table, *segs, st, marks);
+    return run_fwd(y, H_save, x, ws, ws_bytes, *table, *segs, st, marks);
 }
 
 lora_status_t packed_bwd(void *dX, float *dA, float *dB, const void *dY, const void *X, const float *H_saved,
@@ -104,7 +104,7 @@ lora_status_t packed_bwd(void *dX, float *dA, float *dB, const void *dY, const v
     if (need > 0 && (ws == nullptr || ws_bytes < need)) return LORA_ERR_WORKSPACE_TOO_SMALL;
     LORA_TRY(check_device());
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return run_bwd(dX, dA, dB, dY, X, H_saved, ws, *table, *segs, st, marks, side, ordered);
+    return run_bwd(dX, dA, dB, dY, X, H_saved, ws, ws_bytes, *table, *segs, st, marks, side, ordered);
 }
 
 // the caller's side streams and events, checked: distinct, none of them `stream`
@@ -348,7 +348,7 @@ lora_status_t lora_multi_fwd(int32_t n_proj, void *const *y, float *const *H_sav
     const size_t need = multi_workspace_bytes(n_proj, tables, segs->n_tokens);
     if (need > 0 && (ws == nullptr || ws_bytes < need)) return LORA_ERR_WORKSPACE_TOO_SMALL;
     LORA_TRY(check_device());
-    return run_multi_fwd(n_proj, y, H_save, x, ws, tables, *segs, reinterpret_cast<cudaStream_t>(stream));
+    return run_multi_fwd(n_proj, y, H_save, x, ws, ws_bytes, tables, *segs, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t lora_fused_base_workspace_bytes(const lora_adapter_table *table, int32_t n_tokens)

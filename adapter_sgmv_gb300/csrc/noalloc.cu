@@ -2,7 +2,8 @@
 // cannot allocate device memory.
 //
 // lora_packed_bwd takes its scratch (the bf16 hand-off copies of H and dH,
-// T x 64 or T x 128 each) from a caller-provided workspace.  Some callers have no way to get
+// T x 64 or T x 128 each, and for batches of few tiles fp32 partial sums) from
+// a caller-provided workspace.  Some callers have no way to get
 // one: code that runs where cudaMalloc is not allowed or not wanted (inside a
 // custom allocator's own callbacks, in a plugin that must not touch the host
 // framework's memory pool, in a process whose device memory is fully reserved
@@ -13,8 +14,10 @@
 // Costs and rules:
 //  - The array is a file-scope __device__ variable of kScratchBytes (8 MiB);
 //    every GPU that loads the library holds it until the process exits.
-//  - Problems whose scratch exceeds it (2 * T * rw * 2 bytes, rw = 64 when
-//    r_max <= 64 else 128, each half rounded up to 256 bytes) are rejected
+//  - The scratch is laid out as lora_packed_bwd lays out its workspace, so the
+//    two compute the same bits.  Problems whose backward scratch exceeds the
+//    array (2 * T * rw * 2 bytes, rw = 64 when r_max <= 64 else 128, each half
+//    rounded up to 256 bytes, plus counters and partial sums) are rejected
 //    with LORA_ERR_WORKSPACE_TOO_SMALL before anything is launched.
 //  - All calls share the one array and the last call's contents stay in it.
 //    Nothing in it has to start at zero: every scratch value a product uses
@@ -76,11 +79,13 @@ extern "C" LORA_API lora_status_t lora_packed_bwd_noalloc(void *dX, float *dA, f
     if (!aligned16(dY) || !aligned16(X) || (dX && !aligned16(dX)) || (dA && !aligned16(dA)) ||
         (dB && !aligned16(dB)) || (H_saved && !aligned16(H_saved)))
         return LORA_ERR_ALIGNMENT;
-    // the backward's scratch: the two bf16 hand-off copies (of H and dH)
-    if (2 * handoff_region_bytes(segs->n_tokens, table->r_max) > kScratchBytes) return LORA_ERR_WORKSPACE_TOO_SMALL;
+    // the backward's scratch, laid out as in lora_packed_bwd's workspace: the two
+    // bf16 hand-off copies (of H and dH), then counters and partial sums
+    if (bwd_workspace_bytes(*table, segs->n_tokens) > kScratchBytes) return LORA_ERR_WORKSPACE_TOO_SMALL;
     st = check_device();
     if (st != LORA_OK) return st;
     void *base = scratch_address();
     if (base == nullptr) return LORA_ERR_CUDA;
-    return run_bwd(dX, dA, dB, dY, X, H_saved, base, *table, *segs, reinterpret_cast<cudaStream_t>(stream));
+    return run_bwd(dX, dA, dB, dY, X, H_saved, base, kScratchBytes, *table, *segs,
+                   reinterpret_cast<cudaStream_t>(stream));
 }

@@ -42,11 +42,16 @@ inline int32_t handoff_cols(int32_t r_max) { return r_max <= 64 ? 64 : 128; }
 // null; zero past r_i) and/or its bf16 hi (+ lo) split by perm position (null
 // to skip; zero from r_i up to r_i rounded to 16, unwritten past that, where
 // no product reads).
+// part: null, or rowproj_splits(max_tiles, d) x T x rowproj_part_ld(r_max)
+// floats of scratch, with which a batch of few tiles is cut along d into
+// parts whose partials a second small kernel adds.
 lora_status_t tc_shrink(const void *x, const lora_adapter_table &tab, const lora_segments &segs, float *H,
-                        uint16_t *hi, uint16_t *lo, int32_t rw, cudaStream_t stream);
+                        uint16_t *hi, uint16_t *lo, int32_t rw, float *part, cudaStream_t stream);
 // case i.  dh = s_i B_i^T dy as bf16 by perm position.
 lora_status_t tc_dh(const void *dY, const lora_adapter_table &tab, const lora_segments &segs, uint16_t *dh_bf16,
-                    int32_t rw, cudaStream_t stream);
+                    int32_t rw, float *part, cudaStream_t stream);
+int32_t rowproj_splits(int32_t max_tiles, int32_t d);
+int32_t rowproj_part_ld(int32_t r_max);
 
 // A saved fp32 H (by token) converted to the bf16 hand-off rows (by perm
 // position) that cases iii reads; the same values case i writes as its hi.

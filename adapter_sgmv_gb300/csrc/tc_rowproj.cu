@@ -77,7 +77,16 @@ struct RowOut {
     uint16_t *hi, *lo;    // [T, rw] by perm position, or null
     int32_t rw;
     float scale_is_adapter;  // 1: c = s_i, 0: c = 1
+    // split along d (few tiles): the kernel writes fp32 partials c * acc of
+    // each part to part[(q * T + p) * part_ld + k], k < r_pad, and a combine
+    // kernel adds them in part order and writes the outputs above
+    int32_t splits;
+    int32_t part_ld;
+    float *part;
 };
+
+// the k-blocks [lo, hi) of part q of a d of nk blocks cut into `splits` parts
+LORA_DEV int32_t part_lo(int32_t q, int32_t nk, int32_t splits) { return (int32_t)((int64_t)q * nk / splits); }
 
 __global__ void __launch_bounds__(kThreads, 1)
 tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_constant__ WMaps map_w,
@@ -109,7 +118,7 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *S.tmem_holder;
-    const int32_t n_tiles = *segs.n_tiles;
+    const int32_t n_units = *segs.n_tiles * o.splits;  // (tile, part of d)
     const int32_t nk = (d + 63) / 64;
 
     if (warp < kProd) {
@@ -123,16 +132,18 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
         }
         uint32_t g = 0, last = 0xffffffffu;
         bool ok = true;
-        for (int32_t ti = blockIdx.x; ti < n_tiles && ok; ti += gridDim.x) {
+        for (int32_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            const int32_t ti = u / o.splits, q = u % o.splits;
+            const int32_t kb_lo = part_lo(q, nk, o.splits), kb_n = part_lo(q + 1, nk, o.splits) - kb_lo;
             const Tile T = load_tile(segs.tiles, ti);
             const AdapterInfo ad = load_adapter(tab, T.adapter, segs.status);
             if (!ad.ok) continue;
             const int32_t rp = rpad16(ad.rank);
             const bool contiguous = (T.flags & 1) != 0;
-            // this warp's first stage of the tile, and whether it has one at all
+            // this warp's first stage of the unit, and whether it has one at all
             const uint32_t k0 = (uint32_t)((warp - (int)(g % kStages) + kStages) % kStages);
-            if ((int32_t)k0 >= nk) {
-                g += (uint32_t)nk;
+            if ((int32_t)k0 >= kb_n) {
+                g += (uint32_t)kb_n;
                 continue;
             }
             const int32_t t0 = segs.perm[T.begin];
@@ -144,8 +155,9 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
                     tok[q] = m < T.rows ? segs.perm[T.begin + m] : -1;
                 }
             }
-            for (int32_t kb = (int32_t)k0; kb < nk; kb += kStages) {
-                const uint32_t gs = g + (uint32_t)kb;
+            for (int32_t kq = (int32_t)k0; kq < kb_n; kq += kStages) {
+                const int32_t kb = kb_lo + kq;
+                const uint32_t gs = g + (uint32_t)kq;
                 const uint32_t s = gs % kStages, ph = (gs / kStages) & 1u;
                 if (!mbar_wait(&S.empty[s], ph ^ 1u, S.abort, segs.status)) {
                     ok = false;
@@ -177,7 +189,7 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
                 mbar_arrive(&S.full[s]);
                 last = gs;
             }
-            g += (uint32_t)nk;
+            g += (uint32_t)kb_n;
         }
         if (!ok && lane == 0 && last != 0xffffffffu) {  // aborted: let the last stage's TMA copies land
             uint64_t t0 = globaltimer_ns();
@@ -190,7 +202,9 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
         if (lane == 0) {
             uint32_t g = 0, acc_n = 0;
             bool ok = true;
-            for (int32_t ti = blockIdx.x; ti < n_tiles && ok; ti += gridDim.x) {
+            for (int32_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                const int32_t ti = u / o.splits, q = u % o.splits;
+                const int32_t kb_lo = part_lo(q, nk, o.splits), kb_hi = part_lo(q + 1, nk, o.splits);
                 const Tile T = load_tile(segs.tiles, ti);
                 const AdapterInfo ad = load_adapter(tab, T.adapter, segs.status);
                 if (!ad.ok) continue;
@@ -200,7 +214,7 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
                 tc_fence_after();
                 const uint32_t idesc = make_idesc_bf16(128, rp, false, false);
                 const uint32_t d_tmem = tmem_base + acc * 128u;
-                for (int32_t kb = 0; kb < nk; ++kb) {
+                for (int32_t kb = kb_lo; kb < kb_hi; ++kb) {
                     const uint32_t s = g % kStages, ph = (g / kStages) & 1u;
                     if (!mbar_wait(&S.full[s], ph, S.abort, segs.status)) {
                         ok = false;
@@ -212,7 +226,8 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         umma_bf16(d_tmem, make_desc(a_base + 32u * k, 16, 1024, kSwizzle128),
-                                  make_desc(w_base + 32u * k, 16, 1024, kSwizzle128), idesc, (kb | k) != 0 ? 1u : 0u);
+                                  make_desc(w_base + 32u * k, 16, 1024, kSwizzle128), idesc,
+                                  (kb != kb_lo || k != 0) ? 1u : 0u);
                     umma_commit(&S.empty[s]);
                     ++g;
                 }
@@ -232,7 +247,8 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
         const int32_t r_max = tab.r_max;
         const bool vec = (r_max & 3) == 0;
         uint32_t acc_n = 0;
-        for (int32_t ti = blockIdx.x; ti < n_tiles; ti += gridDim.x) {
+        for (int32_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+            const int32_t ti = u / o.splits, q = u % o.splits;
             const Tile T = load_tile(segs.tiles, ti);
             const AdapterInfo ad = load_adapter(tab, T.adapter, segs.status);
             if (!ad.ok) continue;
@@ -245,9 +261,11 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
             const int64_t p = (int64_t)T.begin + m;
             const int32_t t = valid ? segs.perm[p] : -1;
             const float c = o.scale_is_adapter != 0.f ? ad.scale : 1.0f;
-            float *row = o.f32 != nullptr ? o.f32 + (int64_t)(t < 0 ? 0 : t) * r_max : nullptr;
-            uint16_t *rhi = o.hi != nullptr ? o.hi + p * o.rw : nullptr;
-            uint16_t *rlo = o.lo != nullptr ? o.lo + p * o.rw : nullptr;
+            const bool whole = o.splits == 1;  // else this unit's part goes to the partials
+            float *row = whole && o.f32 != nullptr ? o.f32 + (int64_t)(t < 0 ? 0 : t) * r_max : nullptr;
+            uint16_t *rhi = whole && o.hi != nullptr ? o.hi + p * o.rw : nullptr;
+            uint16_t *rlo = whole && o.lo != nullptr ? o.lo + p * o.rw : nullptr;
+            float *prow = whole ? nullptr : o.part + ((int64_t)q * segs.n_tokens + p) * o.part_ld;
             for (int c0 = 0; c0 < rp; c0 += 16) {
                 uint32_t v[16];
                 tmem_ld16(tmem_base + (lane_base << 16) + acc * 128u + (uint32_t)c0, v);
@@ -256,6 +274,11 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
                 float f[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) f[e] = (c0 + e < r) ? c * __uint_as_float(v[e]) : 0.f;
+                if (prow != nullptr) {
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4)
+                        *reinterpret_cast<float4 *>(prow + c0 + e) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+                }
                 if (row != nullptr) {
                     if (vec && c0 + 16 <= r_max) {
 #pragma unroll
@@ -306,10 +329,55 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
     }
 }
 
-lora_status_t launch_rowproj(const void *act, const void *w, int32_t d, const RowOut &o,
-                             const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream)
+// Split case i: the parts' partials added in part order (the sum does not
+// depend on timing) and written as the unsplit epilogue writes them.  One CTA
+// per tile, one thread per (row, 4 columns).
+__global__ void __launch_bounds__(256) rowproj_combine_kernel(RowOut o, lora_adapter_table tab, lora_segments segs)
+{
+    const int32_t n_tiles = *segs.n_tiles, r_max = tab.r_max, T_all = segs.n_tokens;
+    for (int32_t ti = blockIdx.x; ti < n_tiles; ti += gridDim.x) {
+        const Tile T = load_tile(segs.tiles, ti);
+        const AdapterInfo ad = load_adapter(tab, T.adapter, nullptr);
+        if (!ad.ok) continue;
+        const int32_t r = ad.rank, rp = rpad16(r), n4 = rp / 4;
+        for (int32_t i = threadIdx.x; i < T.rows * n4; i += blockDim.x) {
+            const int32_t m = i / n4, k = 4 * (i % n4);
+            const int64_t p = (int64_t)T.begin + m;
+            float4 v = __ldcs(reinterpret_cast<const float4 *>(o.part + p * o.part_ld + k));
+            for (int32_t q = 1; q < o.splits; ++q) {
+                const float4 w = __ldcs(reinterpret_cast<const float4 *>(o.part + ((int64_t)q * T_all + p) * o.part_ld + k));
+                v.x += w.x;
+                v.y += w.y;
+                v.z += w.z;
+                v.w += w.w;
+            }
+            const float f[4] = {v.x, v.y, v.z, v.w};
+            if (o.f32 != nullptr) {
+                float *row = o.f32 + (int64_t)segs.perm[p] * r_max;
+                for (int e = 0; e < 4; ++e)
+                    if (k + e < r_max) row[k + e] = f[e];
+                if (k + 4 == rp)  // the row's zero tail past the rank rounded up to 16
+                    for (int32_t e = rp; e < r_max; ++e) row[e] = 0.f;
+            }
+            if (o.hi != nullptr) {
+                const uint32_t h01 = pack_bf16(f[0], f[1]), h23 = pack_bf16(f[2], f[3]);
+                *reinterpret_cast<uint2 *>(o.hi + p * o.rw + k) = make_uint2(h01, h23);
+                if (o.lo != nullptr)
+                    *reinterpret_cast<uint2 *>(o.lo + p * o.rw + k) =
+                        make_uint2(pack_bf16(f[0] - bf16lo(h01), f[1] - bf16hi(h01)),
+                                   pack_bf16(f[2] - bf16lo(h23), f[3] - bf16hi(h23)));
+            }
+        }
+    }
+}
+
+lora_status_t launch_rowproj(const void *act, const void *w, int32_t d, RowOut o, const lora_adapter_table &tab,
+                             const lora_segments &segs, float *part, cudaStream_t stream)
 {
     if (segs.n_tokens == 0 || segs.max_tiles == 0) return LORA_OK;
+    o.splits = part != nullptr ? rowproj_splits(segs.max_tiles, d) : 1;
+    o.part_ld = rowproj_part_ld(tab.r_max);
+    o.part = part;
     CUtensorMap map_act;
     WMaps map_w;
     if (!make_tmap_bf16_2d(&map_act, act, (uint64_t)d, (uint64_t)segs.n_tokens, 64, 128, true) ||
@@ -319,10 +387,17 @@ lora_status_t launch_rowproj(const void *act, const void *w, int32_t d, const Ro
         cudaSuccess)
         return LORA_ERR_CUDA;
     const int sms = sm_count();
-    const int grid = segs.max_tiles < sms ? segs.max_tiles : sms;
+    const int64_t units = (int64_t)segs.max_tiles * o.splits;
+    const int grid = units < sms ? (int)units : sms;
     tc_rowproj_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_act, map_w, static_cast<const uint16_t *>(act), d,
                                                               o, tab, segs);
-    return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return LORA_ERR_CUDA;
+    if (o.splits > 1) {
+        const int cgrid = segs.max_tiles < 4 * sms ? segs.max_tiles : 4 * sms;
+        rowproj_combine_kernel<<<cgrid, 256, 0, stream>>>(o, tab, segs);
+        if (cudaGetLastError() != cudaSuccess) return LORA_ERR_CUDA;
+    }
+    return LORA_OK;
 }
 
 }  // namespace
@@ -377,18 +452,29 @@ lora_status_t tc_h_to_bf16(const float *H, uint16_t *hb, int32_t rw, const lora_
     return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
-lora_status_t tc_shrink(const void *x, const lora_adapter_table &tab, const lora_segments &segs, float *H,
-                        uint16_t *hi, uint16_t *lo, int32_t rw, cudaStream_t stream)
+int32_t rowproj_splits(int32_t max_tiles, int32_t d)
 {
-    RowOut o{H, hi, lo, rw, 0.f};
-    return launch_rowproj(x, tab.A, tab.d_in, o, tab, segs, stream);
+    // 2 or 4 parts when there are too few tiles to fill GB300's 152 SMs, each
+    // at least 8 blocks of 64 columns deep (the choice depends on the sizes alone)
+    const int32_t nk = (d + 63) / 64;
+    int32_t sp = max_tiles <= 38 ? 4 : max_tiles <= 76 ? 2 : 1;
+    while (sp > 1 && nk < 8 * sp) sp /= 2;
+    return sp;
+}
+int32_t rowproj_part_ld(int32_t r_max) { return (r_max + 15) & ~15; }
+
+lora_status_t tc_shrink(const void *x, const lora_adapter_table &tab, const lora_segments &segs, float *H,
+                        uint16_t *hi, uint16_t *lo, int32_t rw, float *part, cudaStream_t stream)
+{
+    RowOut o{H, hi, lo, rw, 0.f, 1, 0, nullptr};
+    return launch_rowproj(x, tab.A, tab.d_in, o, tab, segs, part, stream);
 }
 
 lora_status_t tc_dh(const void *dY, const lora_adapter_table &tab, const lora_segments &segs, uint16_t *dh_bf16,
-                    int32_t rw, cudaStream_t stream)
+                    int32_t rw, float *part, cudaStream_t stream)
 {
-    RowOut o{nullptr, dh_bf16, nullptr, rw, 1.f};
-    return launch_rowproj(dY, tab.B, tab.d_out, o, tab, segs, stream);
+    RowOut o{nullptr, dh_bf16, nullptr, rw, 1.f, 1, 0, nullptr};
+    return launch_rowproj(dY, tab.B, tab.d_out, o, tab, segs, part, stream);
 }
 
 }  // namespace lora

@@ -500,9 +500,11 @@ LORA_API lora_status_t lora_plan_pack(const lora_plan_config *configs, int32_t n
  * pages have no counterpart to this call; it exists only for such callers.
  * Same arguments and results as lora_packed_bwd minus ws / ws_bytes: the bf16
  * H / dH hand-off scratch lives in a fixed 8 MiB array inside the library's device
- * memory (held by every GPU that loads the library until exit), so it needs
- * 2 * T * 64 bf16 when r_max <= 64, 2 * T * 128 otherwise (each half rounded
- * up to 256 bytes) to be at most 8 MiB, otherwise
+ * memory (held by every GPU that loads the library until exit), laid out as
+ * lora_packed_bwd lays out its workspace: two bf16 hand-off copies of
+ * T * 64 values when r_max <= 64, T * 128 otherwise (each rounded up to 256
+ * bytes), then a few counters and, for batches of few tiles, fp32 partial
+ * sums of case i; when all of it does not fit in 8 MiB
  * LORA_ERR_WORKSPACE_TOO_SMALL is returned and nothing runs.  Allocates
  * nothing.  All calls share the array: calls that overlap on the GPU race and
  * must be serialised by the caller.  The first call on a device resolves the

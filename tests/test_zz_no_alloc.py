@@ -85,8 +85,9 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
                                            ctypes.byref(segs.c), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == 5  # LORA_ERR_WORKSPACE_TOO_SMALL
     assert spec.n_tokens == T
-    # the largest batch of rank-128 adapters that fits: 2 * 16384 * 128 * 2 bytes = 8 MiB exactly
-    T = 16384
+    # a batch of rank-128 adapters that fits: two copies of 16256 x 128 bf16 (8,323,072 bytes)
+    # plus one 256-byte block of counters, below 8 MiB
+    T = 16256
     segs = lora.lora_build_segments(seg_offsets=torch.tensor([0, T], dtype=torch.int32, device=dev),
                                     n_tokens=T, n_adapters=1)
     st = lora.lib().lora_packed_bwd_noalloc(None, None, None, ctypes.c_void_p(dY.data_ptr()),
