@@ -37,7 +37,7 @@ constexpr int kMmaWarp = kProd;
 constexpr int kEpi0 = kProd + 1;  // first epilogue warp
 constexpr int kThreads = 32 * (kProd + 1 + 4);
 constexpr int kTok = 32;                                  // tokens per stage
-constexpr int kRange = 512;                               // columns of d per work item
+constexpr int kRange = 512;                               // most columns of d per work item
 constexpr uint32_t kActBytes = kTok * kRange * 2;         // 8 boxes of [64 cols x 32 tokens]
 constexpr uint32_t kBox = kTok * 64 * 2;                  // one [64 x 32] box
 constexpr uint32_t kHBytes = 2 * kBox;                    // h: up to 128 columns
@@ -82,13 +82,13 @@ struct Item {
 };
 
 LORA_DEV Item load_item(const lora_adapter_table &tab, const lora_segments &segs, int32_t it, int32_t n_ranges,
-                        int32_t d)
+                        int32_t d, int32_t rng)
 {
     Item I;
     I.span = load_tile(segs.spans, it / n_ranges);
     I.ad = load_adapter(tab, I.span.adapter, segs.status);
-    I.n_base = (it % n_ranges) * kRange;
-    I.n_chunks = min(4, (d - I.n_base + 127) / 128);
+    I.n_base = (it % n_ranges) * rng;
+    I.n_chunks = min(rng / 128, (d - I.n_base + 127) / 128);
     I.n_stages = (I.span.rows + kTok - 1) / kTok;
     return I;
 }
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_act3,
                  const __grid_constant__ CUtensorMap map_h,
                  const __grid_constant__ CUtensorMap map_g, const uint16_t *__restrict__ act, int32_t d,
-                 const uint16_t *__restrict__ hbuf, int32_t rw, float use_scale, int32_t blocks3,
+                 const uint16_t *__restrict__ hbuf, int32_t rw, float use_scale, int32_t blocks3, int32_t rng,
                  int32_t *__restrict__ tickets, lora_adapter_table tab, lora_segments segs)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -164,7 +164,7 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *S.tmem_holder;
-    const int32_t n_ranges = (d + kRange - 1) / kRange;
+    const int32_t n_ranges = (d + rng - 1) / rng;  // rng: 512 or, when spans are few, 128 columns
     const int32_t n_items = *segs.n_spans * n_ranges;
 
     if (warp < kProd) {
@@ -177,7 +177,7 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
         uint32_t g = 0, last = 0xffffffffu;
         bool ok = true;
         for (int32_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-            const Item I = load_item(tab, segs, it, n_ranges, d);
+            const Item I = load_item(tab, segs, it, n_ranges, d, rng);
             if (!I.ad.ok) continue;
             // this warp's first stage of the item, and whether it has one at all
             const int32_t st0 = (warp - (int)(g % kStages) + kStages) % kStages;
@@ -205,7 +205,7 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
                 const bool h_tma = valid == kTok;
                 if (lane == 0) {
                     // a 3-D box always moves all eight blocks (past d: zero-filled)
-                    const uint32_t act_bytes = blocks3 ? kActBytes : (uint32_t)I.n_chunks * 2u * kBox;
+                    const uint32_t act_bytes = blocks3 ? (uint32_t)(rng / 64) * kBox : (uint32_t)I.n_chunks * 2u * kBox;
                     const uint32_t bytes = (contiguous ? act_bytes : 0u) +
                                            (h_tma ? (uint32_t)natoms * kBox : 0u);
                     mbar_arrive_expect_tx(&S.full[s], bytes);
@@ -273,7 +273,7 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
             uint32_t g = 0, nitem = 0;
             bool ok = true;
             for (int32_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-                const Item I = load_item(tab, segs, it, n_ranges, d);
+                const Item I = load_item(tab, segs, it, n_ranges, d, rng);
                 if (!I.ad.ok) continue;
                 const uint32_t rp = (uint32_t)rpad16(I.ad.rank);
                 const uint32_t idesc = make_idesc_bf16(128, rp, true, true);
@@ -320,7 +320,7 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
         float *red = reinterpret_cast<float *>(S.red + (warp - kEpi0) * kRedBytes);
         uint32_t nitem = 0, n_ord = 0;
         for (int32_t it = blockIdx.x; it < n_items; it += gridDim.x) {
-            const Item I = load_item(tab, segs, it, n_ranges, d);
+            const Item I = load_item(tab, segs, it, n_ranges, d, rng);
             if (!I.ad.ok) continue;
             const int32_t rp = rpad16(I.ad.rank);
             if (!mbar_wait_warp(S.tfull, nitem & 1u, S.abort, segs.status)) break;
@@ -402,8 +402,13 @@ lora_status_t launch_tokred(float *G, const void *act, int32_t d, const uint16_t
     if (segs.n_tokens == 0 || segs.max_spans == 0) return LORA_OK;
     CUtensorMap map_act, map_act3, map_h, map_g;
     // d a multiple of 64: a stage's eight column blocks come in one 3-D copy
+    // 512-column items, or 128-column ones when 512-column items would leave
+    // half the SMs idle (few spans: a narrow batch of large adapters); in
+    // between, the wider items' fewer reads of h win
+    const int sms = sm_count();
+    const int32_t rng = 2 * (int64_t)segs.max_spans * ((d + kRange - 1) / kRange) < sms ? 128 : kRange;
     const int32_t blocks3 = (d % 64 == 0 && make_tmap_bf16_blocks(&map_act3, act, (uint64_t)d,
-                                                                   (uint64_t)segs.n_tokens, kTok, 8))
+                                                                   (uint64_t)segs.n_tokens, kTok, rng / 64))
                                 ? 1
                                 : 0;
     if (!make_tmap_bf16_2d(&map_act, act, (uint64_t)d, (uint64_t)segs.n_tokens, 64, kTok, true) ||
@@ -413,20 +418,19 @@ lora_status_t launch_tokred(float *G, const void *act, int32_t d, const uint16_t
     if (cudaFuncSetAttribute(tc_tokred_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
         cudaSuccess)
         return LORA_ERR_CUDA;
-    const int n_ranges = (d + kRange - 1) / kRange;
+    const int n_ranges = (d + rng - 1) / rng;
     const int64_t items = (int64_t)segs.max_spans * n_ranges;
-    const int sms = sm_count();
     const int grid = items < sms ? (int)items : sms;
     if (!blocks3) map_act3 = map_act;
     tc_tokred_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_act, map_act3, map_h, map_g,
                                                              static_cast<const uint16_t *>(act), d, hbuf, rw,
-                                                             use_scale, blocks3, tickets, tab, segs);
+                                                             use_scale, blocks3, rng, tickets, tab, segs);
     return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
 }  // namespace
 
-int32_t tokred_ranges(int32_t d) { return (d + kRange - 1) / kRange; }
+int32_t tokred_ranges(int32_t d) { return (d + 127) / 128; }  // the most column ranges of an item list
 
 lora_status_t tc_db(float *dB, const void *dY, const uint16_t *h_bf16, int32_t rw, int32_t *tickets,
                     const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream)
