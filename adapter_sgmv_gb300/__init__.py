@@ -16,7 +16,7 @@ from __future__ import annotations
 import ctypes
 import os
 
-from ._build import LIB_PATH, build as build_library  # noqa: F401
+from ._build import DEBUG_LIB_PATH, LIB_PATH, build as build_library  # noqa: F401
 
 __all__ = [
     "LoraError", "AdapterTable", "Segments", "lib", "lora_abi_version", "lora_status_string",
@@ -26,7 +26,8 @@ __all__ = [
     "lora_packed_fwd_marked", "lora_packed_bwd_marked",
     "lora_packed_bwd_noalloc", "lora_adamw_step", "lora_fused_base_workspace_bytes", "lora_fused_base_fwd",
     "lora_multi_workspace_bytes", "lora_multi_fwd", "lora_plan_pack",
-    "lora_query_status", "lora_reset_status", "lora_check_wait_timeout",
+    "lora_query_status", "lora_reset_status", "lora_check_wait_timeout", "lora_debug_checks",
+    "lora_query_index_check",
     "STATUS",
 ]
 
@@ -34,6 +35,7 @@ STATUS = {
     0: "LORA_OK", 1: "LORA_ERR_INVALID_ARG", 2: "LORA_ERR_SHAPE", 3: "LORA_ERR_ALIGNMENT",
     4: "LORA_ERR_BAD_ADAPTER_ID", 5: "LORA_ERR_WORKSPACE_TOO_SMALL", 6: "LORA_ERR_UNSUPPORTED",
     7: "LORA_ERR_TIMEOUT", 8: "LORA_ERR_BAD_TABLE", 9: "LORA_ERR_BAD_SEGMENTS", 10: "LORA_ERR_CUDA",
+    11: "LORA_ERR_INDEX",
 }
 
 
@@ -121,6 +123,8 @@ SIGNATURES = {
                               ctypes.POINTER(_I32), ctypes.POINTER(c_plan_job), ctypes.POINTER(_I32),
                               ctypes.POINTER(ctypes.c_double)]),
     "lora_query_status": (_I32, [ctypes.POINTER(c_segments), _P]),
+    "lora_query_index_check": (_I32, [ctypes.POINTER(c_segments), _P, ctypes.POINTER(_I32)]),
+    "lora_debug_checks": (_I32, []),
     "lora_reset_status": (_I32, [ctypes.POINTER(c_segments), _P]),
     "lora_check_wait_timeout": (_I32, [_P, _P]),
 }
@@ -473,6 +477,19 @@ def lora_plan_pack(configs, cost: dict) -> dict:
 
 def lora_query_status(segs: Segments, stream=None) -> int:
     return int(lib().lora_query_status(ctypes.byref(segs.c), _stream(stream)))
+
+
+def lora_debug_checks() -> bool:
+    """True when the loaded library is the debug build (device-side index checks)."""
+    return bool(lib().lora_debug_checks())
+
+
+def lora_query_index_check(segs: Segments, stream=None) -> tuple[int, int]:
+    """(status, where): the status word and, after LORA_ERR_INDEX in the debug
+    build, the failed check's source file number << 16 | line."""
+    where = _I32(0)
+    st = int(lib().lora_query_index_check(ctypes.byref(segs.c), _stream(stream), ctypes.byref(where)))
+    return st, int(where.value)
 
 
 def lora_reset_status(segs: Segments, stream=None):

@@ -34,6 +34,7 @@
 // commit round trips would cost more than the MMA time they save.  h enters
 // the expand as bf16 hi + lo (about 16 significant bits), y is updated in fp32
 // and rounded once.
+#define LORA_DBG_FILE 5
 #include <algorithm>
 
 #include "internal.h"
@@ -124,15 +125,18 @@ struct DecTile {
 LORA_DEV DecTile dec_tile(const lora_adapter_table &tab, const lora_segments &segs, int32_t ti)
 {
     DecTile d;
-    const int32_t n_tiles = *segs.n_tiles;
-    d.T = load_tile(segs.tiles, ti);
+    const int32_t n_tiles = N_TILES(segs);
+    d.run = ti < n_tiles;
+    d.T = d.run ? LOAD_TILE(segs, ti) : Tile{0, 0, 1, 0};
     const int32_t a = min(max(d.T.adapter, 0), tab.n_adapters - 1);
     const int32_t b = min(max(d.T.begin, 0), segs.n_tokens - 1);
     d.ad.rank = __ldg(tab.rank + a);
     d.ad.row_off = __ldg(tab.row_off + a);
     d.ad.scale = __ldg(tab.scale + a);
-    d.my_tok = segs.perm[min(b + (int32_t)threadIdx.x, segs.n_tokens - 1)];
-    d.run = ti < n_tiles;
+    // only a row of the tile has a token (perm past the valid entries is unwritten)
+    d.my_tok = d.run && (int32_t)threadIdx.x < d.T.rows
+                   ? PERM_AT(segs, min(b + (int32_t)threadIdx.x, segs.n_tokens - 1))
+                   : 0;
     d.ad.ok = d.ad.rank >= 1 && d.ad.rank <= tab.r_max && d.ad.row_off >= 0 &&
               (int64_t)d.ad.row_off + d.ad.rank <= (int64_t)tab.sum_r;
     if (d.run && !d.ad.ok) set_status(segs.status, LORA_ERR_BAD_TABLE);

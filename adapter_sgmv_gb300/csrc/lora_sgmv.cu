@@ -145,6 +145,7 @@ const char *lora_status_string(lora_status_t s)
     case LORA_ERR_BAD_TABLE: return "LORA_ERR_BAD_TABLE";
     case LORA_ERR_BAD_SEGMENTS: return "LORA_ERR_BAD_SEGMENTS";
     case LORA_ERR_CUDA: return "LORA_ERR_CUDA";
+    case LORA_ERR_INDEX: return "LORA_ERR_INDEX";
     }
     return "LORA_ERR_UNKNOWN";
 }
@@ -375,6 +376,20 @@ lora_status_t lora_fused_base_fwd(void *y, float *H_save, const void *x, const v
     return tc_base_fwd(y, H_save, x, W, ws, *table, *segs, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int32_t lora_debug_checks(void) { return LORA_DEBUG_CHECKS ? 1 : 0; }
+
+lora_status_t lora_query_index_check(const lora_segments *segs, lora_stream_t stream, int32_t *where)
+{
+    if (segs == nullptr || segs->status == nullptr || where == nullptr) return LORA_ERR_INVALID_ARG;
+    int32_t h[2] = {0, 0};
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(h, segs->status, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return LORA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return LORA_ERR_CUDA;
+    *where = h[1];
+    return static_cast<lora_status_t>(h[0]);
+}
+
 lora_status_t lora_query_status(const lora_segments *segs, lora_stream_t stream)
 {
     if (segs == nullptr || segs->status == nullptr) return LORA_ERR_INVALID_ARG;
@@ -389,7 +404,7 @@ lora_status_t lora_query_status(const lora_segments *segs, lora_stream_t stream)
 lora_status_t lora_reset_status(const lora_segments *segs, lora_stream_t stream)
 {
     if (segs == nullptr || segs->status == nullptr) return LORA_ERR_INVALID_ARG;
-    if (cudaMemsetAsync(segs->status, 0, sizeof(int32_t), reinterpret_cast<cudaStream_t>(stream)) !=
+    if (cudaMemsetAsync(segs->status, 0, 2 * sizeof(int32_t), reinterpret_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return LORA_ERR_CUDA;
     return LORA_OK;

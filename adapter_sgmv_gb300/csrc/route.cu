@@ -15,6 +15,7 @@
 // the first perm slot of adapter i's tokens of chunk c, and a token's rank
 // inside its chunk is the number of lower lanes with the same id
 // (__match_any_sync).  All of it is integer work and is bit-exact.
+#define LORA_DBG_FILE 1
 #include "common.cuh"
 #include "internal.h"
 
@@ -78,7 +79,7 @@ __global__ void route_hist_kernel(const int32_t *__restrict__ ids, int32_t T, in
 
 __global__ void route_scatter_kernel(const int32_t *__restrict__ ids, int32_t T, int32_t N,
                                      int32_t n_chunks, const int32_t *__restrict__ offs,
-                                     int32_t *__restrict__ perm)
+                                     int32_t *__restrict__ perm, int32_t *__restrict__ status)
 {
     const int32_t chunk = (int32_t)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
@@ -92,7 +93,7 @@ __global__ void route_scatter_kernel(const int32_t *__restrict__ ids, int32_t T,
     const uint32_t same = __match_any_sync(0xffffffffu, id);
     if (id >= 0) {
         const int32_t rank = __popc(same & ((1u << lane) - 1u));
-        perm[offs[(int64_t)id * n_chunks + chunk] + rank] = (int32_t)t;
+        perm[LORA_DBG_INDEX((int64_t)offs[(int64_t)id * n_chunks + chunk] + rank, T, status)] = (int32_t)t;
     }
 }
 
@@ -170,7 +171,7 @@ __global__ void route_sorted_kernel(const int32_t *__restrict__ seg_offsets, int
 // q by binary search (base[i] <= q < base[i+1]; empty adapters never match).
 __device__ void emit_pieces(const int32_t *__restrict__ seg_start, int32_t N, const int32_t *__restrict__ perm,
                             int32_t len, int32_t *__restrict__ out, int32_t *__restrict__ n_out, int32_t max_out,
-                            int32_t *__restrict__ base)
+                            int32_t *__restrict__ base, int32_t T, int32_t *__restrict__ status)
 {
     int32_t carry = 0;
     for (int32_t i0 = 0; i0 < N; i0 += blockDim.x) {
@@ -196,7 +197,10 @@ __device__ void emit_pieces(const int32_t *__restrict__ seg_start, int32_t N, co
         const int32_t n = seg_start[lo + 1] - seg_start[lo];
         const int32_t b = seg_start[lo] + j * len;
         const int32_t rows = min(len, n - j * len);
-        const int32_t contiguous = (perm[b + rows - 1] - perm[b] == rows - 1) ? 1 : 0;
+        const int32_t contiguous =
+            (perm[LORA_DBG_INDEX((int64_t)b + rows - 1, T, status)] - perm[LORA_DBG_INDEX(b, T, status)] == rows - 1)
+                ? 1
+                : 0;
         reinterpret_cast<int4 *>(out)[q] = make_int4(lo, b, rows, contiguous);
     }
     if (threadIdx.x == 0) *n_out = total;
@@ -223,8 +227,8 @@ __global__ void route_tiles_kernel(const int32_t *__restrict__ offs, int32_t n_c
         return;
     }
     int32_t *base = s.scratch + (s.scratch_words - (((int64_t)N + 1 + 63) & ~int64_t(63)));
-    emit_pieces(seg_start, N, perm, LORA_TILE_M, s.tiles, s.n_tiles, s.max_tiles, base);
-    emit_pieces(seg_start, N, perm, LORA_SPAN_TOKENS, s.spans, s.n_spans, s.max_spans, base);
+    emit_pieces(seg_start, N, perm, LORA_TILE_M, s.tiles, s.n_tiles, s.max_tiles, base, s.n_tokens, s.status);
+    emit_pieces(seg_start, N, perm, LORA_SPAN_TOKENS, s.spans, s.n_spans, s.max_spans, base, s.n_tokens, s.status);
 }
 
 // ---------------------------------------------------------------- sorted input, one launch
@@ -294,13 +298,17 @@ __global__ void __launch_bounds__(1024) route_sorted_one_kernel(const int32_t *_
     if (bad) {  // inconsistent segments: no work, the status says why
         for (int32_t i = threadIdx.x; i <= N; i += blockDim.x) s.seg_start[i] = 0;
         if (threadIdx.x == 0) {
-            *s.status = LORA_ERR_BAD_SEGMENTS;
+            s.status[0] = LORA_ERR_BAD_SEGMENTS;
+            s.status[1] = 0;
             *s.n_tiles = 0;
             *s.n_spans = 0;
         }
         return;
     }
-    if (threadIdx.x == 0) *s.status = LORA_OK;
+    if (threadIdx.x == 0) {
+        s.status[0] = LORA_OK;
+        s.status[1] = 0;  // the debug build's check site
+    }
     for (int32_t i = threadIdx.x; i <= N; i += blockDim.x) s.seg_start[i] = off[i];
     emit_sorted_pieces(off, N, LORA_TILE_M, s.tiles, s.n_tiles, s.max_tiles, base);
     emit_sorted_pieces(off, N, LORA_SPAN_TOKENS, s.spans, s.n_spans, s.max_spans, base);
@@ -366,7 +374,7 @@ lora_status_t build_segments(const int32_t *ids, const int32_t *seg_offsets, int
         *out = s;
         return LORA_OK;
     }
-    if (cudaMemsetAsync(s.status, 0, 4, stream) != cudaSuccess) return LORA_ERR_CUDA;
+    if (cudaMemsetAsync(s.status, 0, 8, stream) != cudaSuccess) return LORA_ERR_CUDA;
     if (seg_offsets != nullptr) {
         const int threads = 256;
         const int64_t work = (int64_t)(T > N + 1 ? T : N + 1);
@@ -386,7 +394,7 @@ lora_status_t build_segments(const int32_t *ids, const int32_t *seg_offsets, int
             scan_reduce_kernel<<<L.block_sums, kScanThreads, 0, stream>>>(hist, L.hist_words, bsum);
             scan_top_kernel<<<1, kScanThreads, 0, stream>>>(bsum, L.block_sums, total);
             scan_apply_kernel<<<L.block_sums, kScanThreads, 0, stream>>>(hist, L.hist_words, bsum);
-            route_scatter_kernel<<<blocks, threads, 0, stream>>>(ids, T, N, L.n_chunks, hist, s.perm);
+            route_scatter_kernel<<<blocks, threads, 0, stream>>>(ids, T, N, L.n_chunks, hist, s.perm, s.status);
             route_tiles_kernel<<<1, 1024, 0, stream>>>(hist, L.n_chunks, total, s.seg_start, N, s.perm, s);
         } else {  // empty batch: every group empty, no tiles
             if (cudaMemsetAsync(s.seg_start, 0, (size_t)(N + 1) * 4, stream) != cudaSuccess ||

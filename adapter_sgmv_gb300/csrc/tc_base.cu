@@ -31,6 +31,7 @@
 // Warp roles: 0 TMA producer, 1 MMA issuer + TMEM owner, 2..9 epilogue
 // (2..5 the first half's rows, 6..9 the second's, one TMEM sub-partition per
 // warp).
+#define LORA_DBG_FILE 6
 #include "internal.h"
 #include "tc_common.cuh"
 #include "tc_host.h"
@@ -143,10 +144,10 @@ LORA_DEV Pair load_pair(const lora_adapter_table &tab, const lora_segments &segs
 {
     Pair P;
     P.has1 = 2 * p + 1 < n_tiles;
-    P.t[0] = load_tile(segs.tiles, 2 * p);
+    P.t[0] = LOAD_TILE(segs, 2 * p);
     P.ad[0] = load_adapter(tab, P.t[0].adapter, nullptr);  // the h task reports a bad entry
     if (P.has1) {
-        P.t[1] = load_tile(segs.tiles, 2 * p + 1);
+        P.t[1] = LOAD_TILE(segs, 2 * p + 1);
         P.ad[1] = load_adapter(tab, P.t[1].adapter, nullptr);
     } else {
         P.t[1] = P.t[0];
@@ -235,7 +236,7 @@ tc_base_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *S.tmem_holder;
-    const int32_t n_tiles = *segs.n_tiles;
+    const int32_t n_tiles = N_TILES(segs);
     const int64_t total = n_tasks(n_tiles, args);
     const int32_t kb_n = (tab.d_in + 63) / 64;
 
@@ -269,7 +270,7 @@ tc_base_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
                     }
                     t = task_of(k, n_tiles, args);
                     if (t.kind == 2) break;
-                    if (t.kind == 1 && load_adapter(tab, load_tile(segs.tiles, t.m).adapter, segs.status).ok) break;
+                    if (t.kind == 1 && load_adapter(tab, LOAD_TILE(segs, t.m).adapter, segs.status).ok) break;
                 }
                 const uint32_t slot = i % kRing, ph = (i / kRing) & 1u;
                 if (!mbar_wait(&S.qempty[slot], ph ^ 1u, S.abort, segs.status)) break;
@@ -277,7 +278,7 @@ tc_base_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
                 mbar_arrive(&S.qfull[slot]);
                 if (k < 0) break;
                 if (t.kind == 1) {
-                    const Tile T = load_tile(segs.tiles, t.m);
+                    const Tile T = LOAD_TILE(segs, t.m);
                     const AdapterInfo ad = load_adapter(tab, T.adapter, nullptr);
                     const int32_t rp = rpad16(ad.rank);
                     for (int32_t kb = 0; kb < kb_n; ++kb) {
@@ -356,7 +357,7 @@ tc_base_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
             if (!mbar_wait(S.tempty, (u & 1u) ^ 1u, S.abort, segs.status)) return false;
             tc_fence_after();
             if (t.kind == 1) {
-                const AdapterInfo ad = load_adapter(tab, load_tile(segs.tiles, t.m).adapter, nullptr);
+                const AdapterInfo ad = load_adapter(tab, LOAD_TILE(segs, t.m).adapter, nullptr);
                 const int32_t rp = rpad16(ad.rank);
                 const uint32_t idesc = make_idesc_bf16(128, (uint32_t)rp, false, false);
                 for (int32_t kb = 0; kb < kb_n; ++kb) {
@@ -453,7 +454,7 @@ tc_base_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant_
             tc_fence_after();
             ++u;
             if (t.kind == 1) {
-                const Tile T = load_tile(segs.tiles, t.m);
+                const Tile T = LOAD_TILE(segs, t.m);
                 const AdapterInfo ad = load_adapter(tab, T.adapter, nullptr);
                 if (half == 0) {
                     // h of this warp's 32 rows: fp32 H by token and bf16 s_i h hand-off,

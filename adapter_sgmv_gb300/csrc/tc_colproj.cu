@@ -23,6 +23,7 @@
 // epilogue: warps 2..9 for sorted batches (both column halves of a chunk at
 // once), else 2..5; in the loader variant 2..5 epilogue and 6..9 fp32 -> bf16
 // conversion of the h block.
+#define LORA_DBG_FILE 3
 #include "internal.h"
 #include "tc_common.cuh"
 #include "tc_host.h"
@@ -86,7 +87,7 @@ LORA_DEV Item load_item(const lora_adapter_table &tab, const lora_segments &segs
                         int32_t d)
 {
     Item I;
-    I.tile = load_tile(segs.tiles, it / n_parts);
+    I.tile = LOAD_TILE(segs, it / n_parts);
     I.ad = load_adapter(tab, I.tile.adapter, segs.status);
     I.n_lo = (it % n_parts) * kNPart;
     I.n_hi = min(d, I.n_lo + kNPart);
@@ -166,7 +167,7 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
     tc_fence_after();
     const uint32_t tmem_base = *S.tmem_holder;
     const int32_t n_parts = (d + kNPart - 1) / kNPart;
-    const int32_t n_items = *segs.n_tiles * n_parts;
+    const int32_t n_items = N_TILES(segs) * n_parts;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -187,7 +188,7 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
             if (!I.ad.ok) continue;
             const int32_t rp = rpad16(I.ad.rank);
             const bool contiguous = (I.tile.flags & 1) != 0;
-            const int32_t t0 = segs.perm[I.tile.begin];
+            const int32_t t0 = PERM_AT(segs, I.tile.begin);
             if (!kLoader) {
                 if (!mbar_wait(S.aempty, (na & 1u) ^ 1u, S.abort, segs.status)) {
                     ok = false;
@@ -214,7 +215,7 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
 #pragma unroll
                 for (int i = 0; i < kTokRegs; ++i) {
                     const int m = kTokShfl ? lane + 32 * i : (lane >> 3) + 4 * i;
-                    tok[i] = m < I.tile.rows ? segs.perm[I.tile.begin + m] : -1;
+                    tok[i] = m < I.tile.rows ? PERM_AT(segs, I.tile.begin + m) : -1;
                 }
             }
             for (int32_t n0 = I.n_lo; n0 < I.n_hi && ok; n0 += kNC) {
@@ -357,7 +358,7 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
             if (!I.ad.ok) continue;
             const int32_t r = I.ad.rank, rp = rpad16(r);
             if (!mbar_wait_warp(S.aempty, (na & 1u) ^ 1u, S.abort, segs.status)) break;
-            const int32_t t = m < I.tile.rows ? segs.perm[I.tile.begin + m] : -1;
+            const int32_t t = m < I.tile.rows ? PERM_AT(segs, I.tile.begin + m) : -1;
             const float *hr = in.h32 + (int64_t)(t < 0 ? 0 : t) * r_max;
 #pragma unroll 4
             for (int kc = 0; kc < rp / 8; ++kc) {
@@ -400,8 +401,8 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
             const Item I = load_item(tab, segs, it, n_parts, d);
             if (!I.ad.ok) continue;
             const float c = in.use_scale != 0.f ? I.ad.scale : 1.0f;
-            const int32_t t = m < I.tile.rows ? segs.perm[I.tile.begin + m] : -1;
-            const int32_t t0 = segs.perm[I.tile.begin];
+            const int32_t t = m < I.tile.rows ? PERM_AT(segs, I.tile.begin + m) : -1;
+            const int32_t t0 = PERM_AT(segs, I.tile.begin);
             uint16_t *row = out + (int64_t)(t < 0 ? 0 : t) * d;
             for (int32_t n0 = I.n_lo; n0 < I.n_hi; n0 += kNC) {
                 const uint32_t acc = a % kAcc, aph = (a / kAcc) & 1u;

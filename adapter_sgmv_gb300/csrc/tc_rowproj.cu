@@ -27,6 +27,7 @@
 // them, which makes them visible to the tensor cores and releases the stage at
 // once, so all six stages can be in flight); 6 issues MMAs and owns TMEM;
 // 7..10 epilogue.  Every wait is bounded (tc::mbar_wait).
+#define LORA_DBG_FILE 2
 #include "internal.h"
 #include "tc_common.cuh"
 #include "tc_host.h"
@@ -118,7 +119,7 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *S.tmem_holder;
-    const int32_t n_units = *segs.n_tiles * o.splits;  // (tile, part of d)
+    const int32_t n_units = N_TILES(segs) * o.splits;  // (tile, part of d)
     const int32_t nk = (d + 63) / 64;
 
     if (warp < kProd) {
@@ -135,7 +136,7 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
         for (int32_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
             const int32_t ti = u / o.splits, q = u % o.splits;
             const int32_t kb_lo = part_lo(q, nk, o.splits), kb_n = part_lo(q + 1, nk, o.splits) - kb_lo;
-            const Tile T = load_tile(segs.tiles, ti);
+            const Tile T = LOAD_TILE(segs, ti);
             const AdapterInfo ad = load_adapter(tab, T.adapter, segs.status);
             if (!ad.ok) continue;
             const int32_t rp = rpad16(ad.rank);
@@ -146,13 +147,13 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
                 g += (uint32_t)kb_n;
                 continue;
             }
-            const int32_t t0 = segs.perm[T.begin];
+            const int32_t t0 = PERM_AT(segs, T.begin);
             int32_t tok[32];  // rows (lane >> 3) + 4 q of a gathered tile
             if (!contiguous) {
 #pragma unroll
                 for (int q = 0; q < 32; ++q) {
                     const int m = (lane >> 3) + 4 * q;
-                    tok[q] = m < T.rows ? segs.perm[T.begin + m] : -1;
+                    tok[q] = m < T.rows ? PERM_AT(segs, T.begin + m) : -1;
                 }
             }
             for (int32_t kq = (int32_t)k0; kq < kb_n; kq += kStages) {
@@ -205,7 +206,7 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
             for (int32_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
                 const int32_t ti = u / o.splits, q = u % o.splits;
                 const int32_t kb_lo = part_lo(q, nk, o.splits), kb_hi = part_lo(q + 1, nk, o.splits);
-                const Tile T = load_tile(segs.tiles, ti);
+                const Tile T = LOAD_TILE(segs, ti);
                 const AdapterInfo ad = load_adapter(tab, T.adapter, segs.status);
                 if (!ad.ok) continue;
                 const uint32_t rp = (uint32_t)rpad16(ad.rank);
@@ -249,7 +250,7 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
         uint32_t acc_n = 0;
         for (int32_t u = blockIdx.x; u < n_units; u += gridDim.x) {
             const int32_t ti = u / o.splits, q = u % o.splits;
-            const Tile T = load_tile(segs.tiles, ti);
+            const Tile T = LOAD_TILE(segs, ti);
             const AdapterInfo ad = load_adapter(tab, T.adapter, segs.status);
             if (!ad.ok) continue;
             const int32_t r = ad.rank, rp = rpad16(r);
@@ -259,7 +260,7 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
             const int m = (int)lane_base + lane;
             const bool valid = m < T.rows;
             const int64_t p = (int64_t)T.begin + m;
-            const int32_t t = valid ? segs.perm[p] : -1;
+            const int32_t t = valid ? PERM_AT(segs, p) : -1;
             const float c = o.scale_is_adapter != 0.f ? ad.scale : 1.0f;
             const bool whole = o.splits == 1;  // else this unit's part goes to the partials
             float *row = whole && o.f32 != nullptr ? o.f32 + (int64_t)(t < 0 ? 0 : t) * r_max : nullptr;
@@ -334,9 +335,9 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
 // per tile, one thread per (row, 4 columns).
 __global__ void __launch_bounds__(256) rowproj_combine_kernel(RowOut o, lora_adapter_table tab, lora_segments segs)
 {
-    const int32_t n_tiles = *segs.n_tiles, r_max = tab.r_max, T_all = segs.n_tokens;
+    const int32_t n_tiles = N_TILES(segs), r_max = tab.r_max, T_all = segs.n_tokens;
     for (int32_t ti = blockIdx.x; ti < n_tiles; ti += gridDim.x) {
-        const Tile T = load_tile(segs.tiles, ti);
+        const Tile T = LOAD_TILE(segs, ti);
         const AdapterInfo ad = load_adapter(tab, T.adapter, nullptr);
         if (!ad.ok) continue;
         const int32_t r = ad.rank, rp = rpad16(r), n4 = rp / 4;
@@ -353,7 +354,7 @@ __global__ void __launch_bounds__(256) rowproj_combine_kernel(RowOut o, lora_ada
             }
             const float f[4] = {v.x, v.y, v.z, v.w};
             if (o.f32 != nullptr) {
-                float *row = o.f32 + (int64_t)segs.perm[p] * r_max;
+                float *row = o.f32 + (int64_t)PERM_AT(segs, p) * r_max;
                 for (int e = 0; e < 4; ++e)
                     if (k + e < r_max) row[k + e] = f[e];
                 if (k + 4 == rp)  // the row's zero tail past the rank rounded up to 16
@@ -412,18 +413,18 @@ namespace {
 __global__ void __launch_bounds__(256) h_to_bf16_kernel(const float *__restrict__ H, uint16_t *__restrict__ hb,
                                                         int32_t rw, lora_adapter_table tab, lora_segments segs)
 {
-    const int32_t n_tiles = *segs.n_tiles;
+    const int32_t n_tiles = N_TILES(segs);
     const int32_t r_max = tab.r_max;
     const bool vec = (r_max & 3) == 0 && (reinterpret_cast<uintptr_t>(H) & 15u) == 0;
     for (int32_t ti = blockIdx.x; ti < n_tiles; ti += gridDim.x) {
-        const Tile T = load_tile(segs.tiles, ti);
+        const Tile T = LOAD_TILE(segs, ti);
         const AdapterInfo ad = load_adapter(tab, T.adapter, nullptr);
         const int32_t r = ad.ok ? ad.rank : 0;
         const int32_t rp8 = (r + 15) / 16 * 2;  // 8-column pieces up to the rank rounded to 16; past it no product reads
         for (int32_t i = threadIdx.x; i < T.rows * rp8; i += blockDim.x) {
             const int32_t m = i / rp8, k = 8 * (i % rp8);
             const int64_t p = (int64_t)T.begin + m;
-            const float *src = H + (int64_t)segs.perm[p] * r_max;
+            const float *src = H + (int64_t)PERM_AT(segs, p) * r_max;
             float f[8];
             if (vec && k + 8 <= r) {  // two 16-byte loads
                 const float4 a = __ldcs(reinterpret_cast<const float4 *>(src + k));

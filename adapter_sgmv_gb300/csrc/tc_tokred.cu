@@ -22,6 +22,7 @@
 // w (a gathered stage's copies are waited for by the warp that issued them,
 // which makes them visible to the tensor cores and releases the stage at once,
 // so all four stages can be in flight); 4 MMA + TMEM owner; 5..8 epilogue.
+#define LORA_DBG_FILE 4
 #include "internal.h"
 #include "tc_common.cuh"
 #include "tc_host.h"
@@ -85,7 +86,7 @@ LORA_DEV Item load_item(const lora_adapter_table &tab, const lora_segments &segs
                         int32_t d, int32_t rng)
 {
     Item I;
-    I.span = load_tile(segs.spans, it / n_ranges);
+    I.span = LOAD_SPAN(segs, it / n_ranges);
     I.ad = load_adapter(tab, I.span.adapter, segs.status);
     I.n_base = (it % n_ranges) * rng;
     I.n_chunks = min(rng / 128, (d - I.n_base + 127) / 128);
@@ -165,7 +166,7 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
     tc_fence_after();
     const uint32_t tmem_base = *S.tmem_holder;
     const int32_t n_ranges = (d + rng - 1) / rng;  // rng: 512 or, when spans are few, 128 columns
-    const int32_t n_items = *segs.n_spans * n_ranges;
+    const int32_t n_items = N_SPANS(segs) * n_ranges;
 
     if (warp < kProd) {
         // ------------------------------------------------------------ producers
@@ -189,13 +190,13 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
             const int natoms = (rp + 63) / 64;
             const int32_t p0 = I.span.begin;
             const bool contiguous = (I.span.flags & 1) != 0;
-            const int32_t t0 = segs.perm[p0];
+            const int32_t t0 = PERM_AT(segs, p0);
             for (int32_t st = st0; st < I.n_stages; st += kStages) {
                 const uint32_t gs = g + (uint32_t)st;
                 const uint32_t s = gs % kStages, ph = (gs / kStages) & 1u;
                 // a gathered stage: lane m holds the token of row m (loaded before the wait)
                 const int valid = min(kTok, I.span.rows - kTok * st);  // rows of this stage in the span
-                const int32_t tl = !contiguous && lane < valid ? segs.perm[p0 + kTok * st + lane] : -1;
+                const int32_t tl = !contiguous && lane < valid ? PERM_AT(segs, p0 + kTok * st + lane) : -1;
                 if (!mbar_wait(&S.empty[s], ph ^ 1u, S.abort, segs.status)) {
                     ok = false;
                     break;
@@ -334,7 +335,8 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
                 const int32_t g0 = segs.seg_start[I.span.adapter], g1 = segs.seg_start[I.span.adapter + 1];
                 if (g1 - g0 > 2 * LORA_SPAN_TOKENS) {
                     tj = (I.span.begin - g0) / LORA_SPAN_TOKENS;
-                    tk = tickets + (int64_t)(it / n_ranges - tj) * n_ranges + it % n_ranges;
+                    tk = tickets + LORA_DBG_INDEX((int64_t)(it / n_ranges - tj) * n_ranges + it % n_ranges,
+                                                  (int64_t)segs.max_spans * n_ranges, segs.status);
                 }
             }
             if (tk != nullptr) {

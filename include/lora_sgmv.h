@@ -38,6 +38,13 @@
  *    inconsistent adapter table, a bounded wait that gave up) are written to
  *    the device status word of the lora_segments in use; the kernels skip the
  *    offending work and never trap.  Read it with lora_query_status.
+ *  - Debug build (liblora_sgmv_debug.so, the same ABI; lora_debug_checks()
+ *    returns 1 there): every index the kernels read from the routing
+ *    metadata (tile and span entries and counts, perm, the slots derived from
+ *    them) is checked before it addresses memory.  An index out of range sets
+ *    LORA_ERR_INDEX and records where in status[1]; the access is redirected
+ *    to an in-range index, the results are unspecified and nothing traps.
+ *    The release build has no such checks (it trusts lora_build_segments).
  *  - Tokens whose id lies outside [0, N) belong to no adapter: their H / dH
  *    rows are not written and their y / dX rows are left unchanged.
  *  - y and dX accumulate (+=) and are rounded once to bf16 (nearest-even)
@@ -53,7 +60,7 @@
 extern "C" {
 #endif
 
-#define LORA_SGMV_ABI_VERSION 1
+#define LORA_SGMV_ABI_VERSION 2
 
 /* Exported entry points (the library is built with hidden default visibility). */
 #if defined(__GNUC__)
@@ -84,7 +91,9 @@ typedef enum lora_status {
     LORA_ERR_TIMEOUT = 7,              /* device: a bounded wait gave up */
     LORA_ERR_BAD_TABLE = 8,            /* device: rank / row offset inconsistent */
     LORA_ERR_BAD_SEGMENTS = 9,         /* device: segment offsets not monotone or not ending at T */
-    LORA_ERR_CUDA = 10                 /* a CUDA runtime call failed */
+    LORA_ERR_CUDA = 10,                /* a CUDA runtime call failed */
+    LORA_ERR_INDEX = 11                /* device, debug build only: an index read from the routing
+                                          metadata was out of range (status[1] says where) */
 } lora_status_t;
 
 /*
@@ -129,6 +138,8 @@ typedef struct lora_adapter_table {
  *                    adapter then begin; n_tiles[0] of them are valid
  *   spans[4*max_spans]  the same cut at LORA_SPAN_TOKENS tokens; n_spans[0] valid
  *   status[0]        device status word (an lora_status_t, LORA_OK when clean)
+ *   status[1]        debug build only: where the first failed index check sits
+ *                    (source file number << 16 | line; see lora_query_index_check), else 0
  */
 typedef struct lora_segments {
     int32_t n_tokens;
@@ -527,10 +538,21 @@ LORA_API lora_status_t lora_packed_bwd_noalloc(void *dX, float *dA, float *dB, c
  */
 LORA_API lora_status_t lora_check_wait_timeout(int32_t *status, lora_stream_t stream);
 
+/* 1 in the debug build (device-side index checks compiled in), else 0. */
+LORA_API int32_t lora_debug_checks(void);
+
+/* Synchronise `stream`, return the device status word of `segs` and store in
+ * *where (host int32) status[1]: in the debug build, after LORA_ERR_INDEX,
+ * the failed check's source file number << 16 | line (file numbers: 1
+ * route.cu, 2 tc_rowproj.cu, 3 tc_colproj.cu, 4 tc_tokred.cu, 5 decode.cu,
+ * 6 tc_base.cu, 7 dispatch.cu); else 0.  Errors: LORA_ERR_INVALID_ARG (NULL),
+ * LORA_ERR_CUDA. */
+LORA_API lora_status_t lora_query_index_check(const lora_segments *segs, lora_stream_t stream, int32_t *where);
+
 /* Synchronise `stream` and return the device status word of `segs`. */
 LORA_API lora_status_t lora_query_status(const lora_segments *segs, lora_stream_t stream);
 
-/* Clear the device status word (stream-ordered). */
+/* Clear the device status word and the debug build's check site (stream-ordered). */
 LORA_API lora_status_t lora_reset_status(const lora_segments *segs, lora_stream_t stream);
 
 #ifdef __cplusplus

@@ -44,8 +44,22 @@ def test_library_exports_every_declared_symbol(L):
     assert set(lora.SIGNATURES) == set(names)
 
 
+def test_debug_build_exports_the_same_symbols(L):
+    # the device-side index checks are a compile-time switch: same sources, same ABI
+    path = lora.build_library(debug=True)
+    D = ctypes.CDLL(path)
+    for n in declared_functions():
+        assert hasattr(D, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
+    assert sorted(set(re.findall(r"\bT (lora_\w+)", out))) == declared_functions()
+    D.lora_debug_checks.restype = ctypes.c_int32
+    assert D.lora_debug_checks() == 1
+    assert L.lora_debug_checks() == 0
+    assert lora.lora_debug_checks() is False
+
+
 def test_version_and_status_strings(L):
-    assert lora.lora_abi_version() == 1
+    assert lora.lora_abi_version() == 2
     for code, name in lora.STATUS.items():
         assert lora.lora_status_string(code) == name
     assert lora.lora_status_string(999) == "LORA_ERR_UNKNOWN"
