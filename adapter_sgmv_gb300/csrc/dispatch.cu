@@ -19,6 +19,20 @@ size_t handoff_region_bytes(int32_t T, int32_t r_max)
 // batches up to this many tokens take the decode kernels
 constexpr int32_t kDecodeMaxTokens = 512;
 
+// Work-claim counters, 256 bytes after the two hand-off regions: one int per
+// claiming launch of a call.  The kernel before a claiming one on the same
+// stream zeroes its counter (forward: the shrink zeroes the expand's;
+// backward: the bf16 copy of H, or the recomputing shrink, zeroes dB's, and
+// dh zeroes dA's and dX's), so no memset is needed.  Items are claimed at run
+// time when their costs differ (id-routed batches: gathered and TMA tiles,
+// tiles and spans of any length) and in the ordered backward (whose waits
+// rely on it); the uniform items of segment-sorted batches are split evenly
+// ahead of time (CTA b takes b, b + grid, ...), which ends every CTA's share
+// together where run-time claims would leave the last items to CTAs that are
+// still finishing others.
+constexpr size_t kClaimRegionBytes = 256;
+enum ClaimSlot { kClaimExpand = 0, kClaimDB = 1, kClaimDA = 2, kClaimDX = 3 };
+
 size_t ticket_region_bytes(const lora_adapter_table &tab, int32_t T)
 {
     const SegLayout L = seg_layout(T, tab.n_adapters);
@@ -26,6 +40,16 @@ size_t ticket_region_bytes(const lora_adapter_table &tab, int32_t T)
     const int64_t words = (int64_t)L.max_spans * (tokred_ranges(tab.d_out) + tokred_ranges(tab.d_in));
     return (size_t)((words * 4 + 255) & ~int64_t(255));
 }
+
+namespace {
+// the claim counters, when the workspace holds them (null: items by CTA index)
+int32_t *claim_region(void *ws, size_t ws_bytes, int32_t T, int32_t r_max)
+{
+    const size_t off = 2 * handoff_region_bytes(T, r_max);
+    if (ws_bytes < off + kClaimRegionBytes) return nullptr;
+    return reinterpret_cast<int32_t *>(static_cast<char *>(ws) + off);
+}
+}  // namespace
 
 size_t part_region_bytes(const lora_adapter_table &tab, int32_t T)
 {
@@ -42,7 +66,7 @@ namespace {
 // case i's partials in the workspace, when the workspace holds them
 float *part_region(void *ws, size_t ws_bytes, const lora_adapter_table &tab, int32_t T)
 {
-    const size_t off = 2 * handoff_region_bytes(T, tab.r_max) + ticket_region_bytes(tab, T);
+    const size_t off = 2 * handoff_region_bytes(T, tab.r_max) + kClaimRegionBytes + ticket_region_bytes(tab, T);
     const size_t need = part_region_bytes(tab, T);
     if (need == 0 || ws_bytes < off + need) return nullptr;
     return reinterpret_cast<float *>(static_cast<char *>(ws) + off);
@@ -51,7 +75,8 @@ float *part_region(void *ws, size_t ws_bytes, const lora_adapter_table &tab, int
 
 size_t bwd_workspace_bytes(const lora_adapter_table &tab, int32_t T)
 {
-    return 2 * handoff_region_bytes(T, tab.r_max) + ticket_region_bytes(tab, T) + part_region_bytes(tab, T);
+    return 2 * handoff_region_bytes(T, tab.r_max) + kClaimRegionBytes + ticket_region_bytes(tab, T) +
+           part_region_bytes(tab, T);
 }
 
 size_t packed_workspace_bytes(const lora_adapter_table &tab, int32_t T)
@@ -64,7 +89,7 @@ size_t packed_workspace_bytes(const lora_adapter_table &tab, int32_t T)
 lora_status_t run_shrink(float *H, const void *x, const lora_adapter_table &tab, const lora_segments &segs,
                          cudaStream_t stream)
 {
-    return tc_shrink(x, tab, segs, H, nullptr, nullptr, 0, nullptr, stream);  // no workspace: not split
+    return tc_shrink(x, tab, segs, H, nullptr, nullptr, 0, nullptr, nullptr, 0, stream);  // no workspace: not split
 }
 
 lora_status_t run_expand(void *y, const float *H, const lora_adapter_table &tab, const lora_segments &segs,
@@ -101,10 +126,13 @@ lora_status_t run_fwd(void *y, float *H_save, const void *x, void *ws, size_t ws
     uint16_t *hi = static_cast<uint16_t *>(ws);
     uint16_t *lo = reinterpret_cast<uint16_t *>(static_cast<char *>(ws) + handoff_region_bytes(segs.n_tokens, tab.r_max));
     float *part = part_region(ws, ws_bytes, tab, segs.n_tokens);
-    lora_status_t st =
-        marked(marks, stream, [&] { return tc_shrink(x, tab, segs, H_save, hi, lo, rw, part, stream); });
+    int32_t *claims = claim_region(ws, ws_bytes, segs.n_tokens, tab.r_max);
+    int32_t *c_expand = claims != nullptr ? claims + kClaimExpand : nullptr;
+    lora_status_t st = marked(
+        marks, stream, [&] { return tc_shrink(x, tab, segs, H_save, hi, lo, rw, part, c_expand, 1, stream); });
     if (st != LORA_OK) return st;
-    return marked(marks, stream, [&] { return tc_expand_bf16(y, hi, lo, rw, tab, segs, stream); });
+    int32_t *use = segs.sorted != 0 ? nullptr : c_expand;
+    return marked(marks, stream, [&] { return tc_expand_bf16(y, hi, lo, rw, use, tab, segs, stream); });
 }
 
 size_t multi_workspace_bytes(int32_t n_proj, const lora_adapter_table *tabs, int32_t T)
@@ -145,10 +173,16 @@ lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void
     uint16_t *hb = static_cast<uint16_t *>(ws);
     uint16_t *dhb = reinterpret_cast<uint16_t *>(static_cast<char *>(ws) + hreg);
     float *part = part_region(ws, ws_bytes, tab, segs.n_tokens);  // case i split along d (few tiles)
-    // ordered mode: tickets of dB, then of dA, after the hand-off regions
+    int32_t *claims = claim_region(ws, ws_bytes, segs.n_tokens, tab.r_max);
+    auto claim = [&](ClaimSlot k) { return claims != nullptr ? claims + k : nullptr; };
+    // the counters the launches claim from (null: items split ahead of time)
+    const bool dyn = segs.sorted == 0;
+    auto use = [&](ClaimSlot k, bool on) { return on ? claim(k) : nullptr; };
+    // ordered mode: tickets of dB, then of dA, after the claim counters
     int32_t *tk_B = nullptr, *tk_A = nullptr;
     if (ordered && (dA != nullptr || dB != nullptr)) {
-        tk_B = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + 2 * hreg);
+        if (claims == nullptr) return LORA_ERR_WORKSPACE_TOO_SMALL;
+        tk_B = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + 2 * hreg + kClaimRegionBytes);
         tk_A = tk_B + (int64_t)segs.max_spans * tokred_ranges(tab.d_out);
         if (cudaMemsetAsync(tk_B, 0, ticket_region_bytes(tab, segs.n_tokens), stream) != cudaSuccess)
             return LORA_ERR_CUDA;
@@ -173,25 +207,29 @@ lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void
     };
     bool forked_B = false, forked_A = false;
     if (H_saved == nullptr)
-        st = marked(marks, stream, [&] { return tc_shrink(X, tab, segs, nullptr, hb, nullptr, rw, part, stream); });
+        st = marked(marks, stream, [&] {
+            return tc_shrink(X, tab, segs, nullptr, hb, nullptr, rw, part, claim(kClaimDB), 1, stream);
+        });
     if (st == LORA_OK && par && dB != nullptr) {  // fork B once the outputs are zeroed (and H recomputed)
         forked_B = fork(side->ev[0], sB);
         if (!forked_B) st = LORA_ERR_CUDA;
     }
     if (st == LORA_OK && dB != nullptr) {
         if (H_saved != nullptr)
-            st = marked(marks, sB, [&] { return tc_h_to_bf16(H_saved, hb, rw, tab, segs, sB); });
-        if (st == LORA_OK) st = marked(marks, sB, [&] { return tc_db(dB, dY, hb, rw, tk_B, tab, segs, sB); });
+            st = marked(marks, sB, [&] { return tc_h_to_bf16(H_saved, hb, rw, claim(kClaimDB), 1, tab, segs, sB); });
+        if (st == LORA_OK)
+            st = marked(marks, sB, [&] { return tc_db(dB, dY, hb, rw, tk_B, use(kClaimDB, dyn || ordered), tab, segs, sB); });
     }
     if (st == LORA_OK)
-        st = marked(marks, stream, [&] { return tc_dh(dY, tab, segs, dhb, rw, part, stream); });
+        st = marked(marks, stream, [&] { return tc_dh(dY, tab, segs, dhb, rw, part, claim(kClaimDA), 2, stream); });
     if (st == LORA_OK && par && dA != nullptr) {  // fork A after dh
         forked_A = fork(side->ev[3], sA);
         if (!forked_A) st = LORA_ERR_CUDA;
     }
-    if (st == LORA_OK && dA != nullptr) st = marked(marks, sA, [&] { return tc_da(dA, X, dhb, rw, tk_A, tab, segs, sA); });
+    if (st == LORA_OK && dA != nullptr)
+        st = marked(marks, sA, [&] { return tc_da(dA, X, dhb, rw, tk_A, use(kClaimDA, dyn || ordered), tab, segs, sA); });
     if (st == LORA_OK && dX != nullptr)
-        st = marked(marks, stream, [&] { return tc_dx(dX, dhb, rw, tab, segs, stream); });
+        st = marked(marks, stream, [&] { return tc_dx(dX, dhb, rw, use(kClaimDX, dyn), tab, segs, stream); });
     // join: the caller's stream waits for every side stream that was forked,
     // after an error too, so that no work of this call outlives it unordered
     // with the caller's stream (and a capture is never left with an open fork)

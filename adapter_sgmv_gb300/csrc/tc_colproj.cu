@@ -49,6 +49,7 @@ struct Smem {
     uint64_t *wfull, *wempty, *yfull, *yempty, *ysync, *tfull, *tempty, *afull, *aempty, *done;
     uint32_t *tmem_holder;
     volatile int32_t *abort;
+    ClaimRing claims;  // items claimed at run time
 };
 
 LORA_DEV Smem carve(uint8_t *raw)
@@ -71,6 +72,9 @@ LORA_DEV Smem carve(uint8_t *raw)
     s.done = s.aempty + 1;
     s.tmem_holder = reinterpret_cast<uint32_t *>(s.done + 1);
     s.abort = reinterpret_cast<volatile int32_t *>(s.tmem_holder + 1);
+    s.claims.full = reinterpret_cast<uint64_t *>(s.tmem_holder + 8);
+    s.claims.empty = s.claims.full + kClaimSlots;
+    s.claims.slot = reinterpret_cast<volatile int32_t *>(s.claims.empty + kClaimSlots);
     return s;
 }
 
@@ -110,9 +114,12 @@ struct ColIn {
     const float *h32;  // loader variant: fp32 h by token, stride r_max
     float use_scale;   // 1: c = s_i, 0: c = 1
     int32_t split;     // 1: the A operand is hi + lo
+    int32_t *claim;    // kClaim: the work-claim counter, zero at launch
 };
 
-template <bool kLoader, int kEpi>
+// kClaim: items claimed at run time from in.claim (id-routed batches, whose
+// items differ in cost), else CTA b takes items b, b + gridDim.x, ...
+template <bool kLoader, int kEpi, bool kClaim>
 __global__ void __launch_bounds__(threads_of<kLoader, kEpi>(), 1)
 tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ CUtensorMap map_hi,
                   const __grid_constant__ CUtensorMap map_lo, const __grid_constant__ CUtensorMap map_y,
@@ -121,6 +128,7 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
     // epilogue warps: eight (sorted batches: every tile is a run of consecutive
     // tokens), else four; four when warps 6..9 convert the fp32 h block
     static_assert((kEpi == 4 || kEpi == 8) && !(kLoader && kEpi == 8), "epilogue of four or eight warps");
+    static_assert(!(kLoader && kClaim), "the loader variant takes its items by CTA index");
     constexpr int kHStep = kEpi / 4;
     constexpr int kStoreLag = store_lag<kEpi>();
     // A stage of a full tile is freed once its leader has issued kStoreLag more
@@ -137,6 +145,8 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
     const Smem S = carve(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool split = in.split != 0;
+    // the claimer's first item, claimed before the set-up so that its round trip overlaps it
+    const int32_t first = kClaim && warp == 0 && lane == 0 ? claim_first(in.claim) : 0;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kWStages; ++i) {
@@ -155,6 +165,11 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
         mbar_init(S.afull, kLoader ? 4 : 1);
         mbar_init(S.aempty, 1);
         mbar_init(S.done, 1);
+        if (kClaim)
+            for (int i = 0; i < kClaimSlots; ++i) {  // claimed by warp 0; read by the MMA thread and the epilogue
+                mbar_init(&S.claims.full[i], 1);
+                mbar_init(&S.claims.empty[i], 1 + kEpi);
+            }
         *S.abort = 0;
         fence_barrier_init();
     }
@@ -183,7 +198,19 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
         }
         uint32_t gw = 0, gy = 0, na = 0;
         bool ok = true;
-        for (int32_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        uint32_t q = 0;
+        for (int32_t it = blockIdx.x; (kClaim || it < n_items) && ok; it += gridDim.x, ++q) {
+            if (kClaim) {
+                bool got = true;
+                if (lane == 0) got = claim_next(S.claims, q, in.claim, first, &it, S.abort, segs.status);
+                got = __shfl_sync(0xffffffffu, got, 0);
+                it = __shfl_sync(0xffffffffu, it, 0);
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                if (it < 0 || it >= n_items) break;
+            }
             const Item I = load_item(tab, segs, it, n_parts, d);
             if (!I.ad.ok) continue;
             const int32_t rp = rpad16(I.ad.rank);
@@ -307,7 +334,12 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
             bool ok = true;
             const uint32_t idesc = make_idesc_bf16(128, kNC, false, true);
             const uint32_t abase = smem_u32(S.a);
-            for (int32_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+            uint32_t q = 0;
+            for (int32_t it = blockIdx.x; (kClaim || it < n_items) && ok; it += gridDim.x, ++q) {
+                if (kClaim) {
+                    if (!claim_read(S.claims, q, &it, S.abort, segs.status)) break;
+                    if (it < 0 || it >= n_items) break;
+                }
                 const Item I = load_item(tab, segs, it, n_parts, d);
                 if (!I.ad.ok) continue;
                 const int32_t rp = rpad16(I.ad.rank);
@@ -397,7 +429,16 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
         // oldest first; a stage goes back to the producer once its store has read it
         int32_t pend[kStoreLag + 1];
         int npend = 0;
-        for (int32_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        uint32_t q = 0;
+        for (int32_t it = blockIdx.x; (kClaim || it < n_items) && ok; it += gridDim.x, ++q) {
+            if (kClaim) {
+                if (q > 0) claim_release_warp(S.claims, q - 1);  // the previous item is done
+                if (!claim_read_warp(S.claims, q, &it, S.abort, segs.status, true)) break;
+                if (it < 0 || it >= n_items) {
+                    claim_release_warp(S.claims, q);
+                    break;
+                }
+            }
             const Item I = load_item(tab, segs, it, n_parts, d);
             if (!I.ad.ok) continue;
             const float c = in.use_scale != 0.f ? I.ad.scale : 1.0f;
@@ -502,7 +543,7 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
     }
 }
 
-template <bool kLoader, int kEpi>
+template <bool kLoader, int kEpi, bool kClaim>
 lora_status_t launch_colproj(uint16_t *out, int32_t d, const void *w, const uint16_t *hi, const uint16_t *lo,
                              int32_t rw, const ColIn &in, const lora_adapter_table &tab, const lora_segments &segs,
                              cudaStream_t stream)
@@ -526,46 +567,54 @@ lora_status_t launch_colproj(uint16_t *out, int32_t d, const void *w, const uint
         map_hi = map_y;
         map_lo = map_y;
     }
-    if (cudaFuncSetAttribute(tc_colproj_kernel<kLoader, kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(tc_colproj_kernel<kLoader, kEpi, kClaim>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
         return LORA_ERR_CUDA;
     const int n_parts = (d + kNPart - 1) / kNPart;
     const int64_t items = (int64_t)segs.max_tiles * n_parts;
     const int sms = sm_count();
     const int grid = items < sms ? (int)items : sms;
-    tc_colproj_kernel<kLoader, kEpi><<<grid, threads_of<kLoader, kEpi>(), kSmemBytes, stream>>>(map_w, map_hi, map_lo, map_y, out,
-                                                                                  d, in, tab, segs);
+    tc_colproj_kernel<kLoader, kEpi, kClaim><<<grid, threads_of<kLoader, kEpi>(), kSmemBytes, stream>>>(
+        map_w, map_hi, map_lo, map_y, out, d, in, tab, segs);
     return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
 }  // namespace
 
-lora_status_t tc_expand_bf16(void *y, const uint16_t *hi, const uint16_t *lo, int32_t rw,
+// Segment-sorted batches: every tile a run of consecutive tokens, eight
+// epilogue warps, items split ahead of time (they cost the same but for the
+// last tile of each adapter).  Id-routed batches: four epilogue warps, items
+// claimed at run time when a counter is given (gathered and TMA tiles, tiles
+// of any length).
+lora_status_t launch_bf16(uint16_t *out, int32_t d, const void *w, const uint16_t *hi, const uint16_t *lo, int32_t rw,
+                          const ColIn &in, const lora_adapter_table &tab, const lora_segments &segs,
+                          cudaStream_t stream)
+{
+    if (segs.sorted != 0) return launch_colproj<false, 8, false>(out, d, w, hi, lo, rw, in, tab, segs, stream);
+    if (in.claim != nullptr) return launch_colproj<false, 4, true>(out, d, w, hi, lo, rw, in, tab, segs, stream);
+    return launch_colproj<false, 4, false>(out, d, w, hi, lo, rw, in, tab, segs, stream);
+}
+
+lora_status_t tc_expand_bf16(void *y, const uint16_t *hi, const uint16_t *lo, int32_t rw, int32_t *claim,
                              const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream)
 {
-    ColIn in{nullptr, 1.f, lo != nullptr ? 1 : 0};
-    if (segs.sorted != 0)
-        return launch_colproj<false, 8>(static_cast<uint16_t *>(y), tab.d_out, tab.B, hi, lo, rw, in, tab, segs, stream);
-    return launch_colproj<false, 4>(static_cast<uint16_t *>(y), tab.d_out, tab.B, hi, lo, rw, in, tab, segs, stream);
+    const ColIn in{nullptr, 1.f, lo != nullptr ? 1 : 0, claim};
+    return launch_bf16(static_cast<uint16_t *>(y), tab.d_out, tab.B, hi, lo, rw, in, tab, segs, stream);
 }
 
 lora_status_t tc_expand_f32(void *y, const float *H, const lora_adapter_table &tab, const lora_segments &segs,
                             cudaStream_t stream)
 {
-    ColIn in{H, 1.f, 1};
-    return launch_colproj<true, 4>(static_cast<uint16_t *>(y), tab.d_out, tab.B, nullptr, nullptr, 0, in, tab, segs,
-                                stream);
+    const ColIn in{H, 1.f, 1, nullptr};
+    return launch_colproj<true, 4, false>(static_cast<uint16_t *>(y), tab.d_out, tab.B, nullptr, nullptr, 0, in, tab,
+                                          segs, stream);
 }
 
-lora_status_t tc_dx(void *dX, const uint16_t *dh_bf16, int32_t rw, const lora_adapter_table &tab,
+lora_status_t tc_dx(void *dX, const uint16_t *dh_bf16, int32_t rw, int32_t *claim, const lora_adapter_table &tab,
                     const lora_segments &segs, cudaStream_t stream)
 {
-    ColIn in{nullptr, 0.f, 0};
-    if (segs.sorted != 0)
-        return launch_colproj<false, 8>(static_cast<uint16_t *>(dX), tab.d_in, tab.A, dh_bf16, nullptr, rw, in, tab,
-                                        segs, stream);
-    return launch_colproj<false, 4>(static_cast<uint16_t *>(dX), tab.d_in, tab.A, dh_bf16, nullptr, rw, in, tab, segs,
-                                    stream);
+    const ColIn in{nullptr, 0.f, 0, claim};
+    return launch_bf16(static_cast<uint16_t *>(dX), tab.d_in, tab.A, dh_bf16, nullptr, rw, in, tab, segs, stream);
 }
 
 }  // namespace lora

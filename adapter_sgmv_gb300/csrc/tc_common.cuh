@@ -169,46 +169,82 @@ LORA_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) 
 // generic-proxy shared-memory writes -> visible to the async proxy (tcgen05.mma, TMA)
 LORA_DEV void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// ---------------------------------------------------------------- producer arrivals
-// A producer lane owes one arrive per pipeline stage on that stage's "full"
-// barrier (whose count includes one arrive per producer lane).  Stages filled
-// only by TMA are covered by the expect-tx bytes, so the lane arrives at once.
-// Stages with cp.async copies can only be released after the copies land:
-// their arrives are deferred by kLag stages (cp.async.wait_group keeps kLag
-// groups in flight) and flushed before any immediate arrive, so stages always
-// complete in order and no consumer waits on a stage behind a later one.
-template <int kLag, int kStages>
-struct ArriveQueue {
-    uint32_t q[kLag + 1];
-    int n = 0;
+// ---------------------------------------------------------------- work claims
+// The roles of a persistent CTA (producers, MMA issuer, epilogue) walk the
+// same sequence of work items.  Items split ahead of time: CTA b takes b,
+// b + gridDim.x, ..., which every role computes by itself.  Items claimed at
+// run time: one thread, the claimer, takes each next index from a counter in
+// global memory (zero when the launch starts) with atomicAdd and passes it to
+// the other roles through a ring of kClaimSlots slots in shared memory.  Items
+// then go out in index order to whichever CTA asks first, so items of uneven
+// cost spread evenly over the SMs, and every item below a claimed one is held
+// by a running CTA.  The last index a CTA passes on is >= n_items, which ends
+// every role's walk.
+//
+// The epilogue hands its slot back only when it comes for the next claim,
+// i.e. once it has finished the item: with two slots the claimer takes item
+// q + 1 only after the epilogue has finished item q - 1, so a CTA holds at
+// most one item beyond the one its epilogue works on (the producer's
+// look-ahead) and the last items go to CTAs that are about to be free.
+constexpr int kClaimSlots = 2;
 
-    LORA_DEV void drain(uint64_t *full)
-    {
-        if (n == 0) return;
-        cp_async_wait<0>();
-        fence_proxy_async();
-        for (int i = 0; i < n; ++i) mbar_arrive(&full[q[i] % kStages]);
-        n = 0;
-    }
-    // call once per stage g after issuing its copies; `gathered`: cp.async used
-    LORA_DEV void issued(uint64_t *full, uint32_t g, bool gathered)
-    {
-        if (!gathered) {
-            drain(full);
-            mbar_arrive(&full[g % kStages]);
-            return;
-        }
-        cp_async_commit();
-        q[n++] = g;
-        if (n > kLag) {
-            cp_async_wait<kLag>();
-            fence_proxy_async();
-            mbar_arrive(&full[q[0] % kStages]);
-            for (int i = 1; i < n; ++i) q[i - 1] = q[i];
-            --n;
-        }
-    }
+struct ClaimRing {
+    volatile int32_t *slot;  // [kClaimSlots]
+    uint64_t *full;          // [kClaimSlots], count 1: the claimer's arrive
+    uint64_t *empty;         // [kClaimSlots], count: one arrive per reader (a thread or a warp)
 };
+
+// the claimer's first item, taken before the CTA's set-up so that the
+// atomic's round trip overlaps it (0 without a counter: unused)
+LORA_DEV int32_t claim_first(int32_t *counter) { return counter != nullptr ? atomicAdd(counter, 1) : 0; }
+
+// claimer (one thread): the CTA's claim number q = 0, 1, ...; false on time-out
+LORA_DEV bool claim_next(const ClaimRing &R, uint32_t q, int32_t *counter, int32_t first, int32_t *it,
+                         volatile int32_t *abort_flag, int32_t *status)
+{
+    const uint32_t s = q % kClaimSlots;
+    if (!mbar_wait(&R.empty[s], ((q / kClaimSlots) & 1u) ^ 1u, abort_flag, status)) return false;
+    *it = q == 0 ? first : atomicAdd(counter, 1);
+    R.slot[s] = *it;
+    mbar_arrive(&R.full[s]);  // release: the slot is visible to a reader once its wait returns
+    return true;
+}
+
+// a reading thread: claim q of this CTA, its slot handed back at once; false on time-out
+LORA_DEV bool claim_read(const ClaimRing &R, uint32_t q, int32_t *it, volatile int32_t *abort_flag, int32_t *status)
+{
+    const uint32_t s = q % kClaimSlots;
+    if (!mbar_wait(&R.full[s], (q / kClaimSlots) & 1u, abort_flag, status)) return false;
+    *it = R.slot[s];
+    mbar_arrive(&R.empty[s]);
+    return true;
+}
+
+// a reading warp (every lane calls it and gets the same answer).  `keep`:
+// the slot is handed back later, by claim_release_warp(q), once the warp has
+// finished the item (the epilogue)
+LORA_DEV bool claim_read_warp(const ClaimRing &R, uint32_t q, int32_t *it, volatile int32_t *abort_flag,
+                              int32_t *status, bool keep = false)
+{
+    const uint32_t s = q % kClaimSlots;
+    if (!mbar_wait_warp(&R.full[s], (q / kClaimSlots) & 1u, abort_flag, status)) return false;
+    *it = R.slot[s];
+    __syncwarp();
+    if (!keep && (threadIdx.x & 31) == 0) mbar_arrive(&R.empty[s]);
+    return true;
+}
+LORA_DEV void claim_release_warp(const ClaimRing &R, uint32_t q)
+{
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&R.empty[q % kClaimSlots]);
+}
+
+// A kernel that runs before the claiming kernels of the same call, on the
+// same stream, zeroes their counters (block 0, before anything else).
+LORA_DEV void zero_claims(int32_t *claims, int32_t n)
+{
+    if (claims != nullptr && blockIdx.x == 0 && (int32_t)threadIdx.x < n) claims[threadIdx.x] = 0;
+}
 
 // ---------------------------------------------------------------- tcgen05
 // Shared-memory matrix descriptor (tcgen05 "matrix descriptor"):

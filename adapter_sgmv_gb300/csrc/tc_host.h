@@ -45,36 +45,42 @@ inline int32_t handoff_cols(int32_t r_max) { return r_max <= 64 ? 64 : 128; }
 // part: null, or rowproj_splits(max_tiles, d) x T x rowproj_part_ld(r_max)
 // floats of scratch, with which a batch of few tiles is cut along d into
 // parts whose partials a second small kernel adds.
+// zero_claims: null, or n_zero work-claim counters of kernels that follow on
+// the same stream in the same call, set to zero before anything else.
 lora_status_t tc_shrink(const void *x, const lora_adapter_table &tab, const lora_segments &segs, float *H,
-                        uint16_t *hi, uint16_t *lo, int32_t rw, float *part, cudaStream_t stream);
+                        uint16_t *hi, uint16_t *lo, int32_t rw, float *part, int32_t *zero_claims, int32_t n_zero,
+                        cudaStream_t stream);
 // case i.  dh = s_i B_i^T dy as bf16 by perm position.
 lora_status_t tc_dh(const void *dY, const lora_adapter_table &tab, const lora_segments &segs, uint16_t *dh_bf16,
-                    int32_t rw, float *part, cudaStream_t stream);
+                    int32_t rw, float *part, int32_t *zero_claims, int32_t n_zero, cudaStream_t stream);
 int32_t rowproj_splits(int32_t max_tiles, int32_t d);
 int32_t rowproj_part_ld(int32_t r_max);
 
 // A saved fp32 H (by token) converted to the bf16 hand-off rows (by perm
 // position) that cases iii reads; the same values case i writes as its hi.
-lora_status_t tc_h_to_bf16(const float *H, uint16_t *hb, int32_t rw, const lora_adapter_table &tab,
-                           const lora_segments &segs, cudaStream_t stream);
+lora_status_t tc_h_to_bf16(const float *H, uint16_t *hb, int32_t rw, int32_t *zero_claims, int32_t n_zero,
+                           const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream);
 // case ii.  y += s_i B_i h from the bf16 hand-off buffers (lo may be null).
-lora_status_t tc_expand_bf16(void *y, const uint16_t *hi, const uint16_t *lo, int32_t rw,
+// claim: null (CTA b takes items b, b + grid, ...) or a counter that is zero
+// when the kernel starts, from which items are claimed at run time.
+lora_status_t tc_expand_bf16(void *y, const uint16_t *hi, const uint16_t *lo, int32_t rw, int32_t *claim,
                              const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream);
 // case ii.  y += s_i B_i h from an fp32 H by token (converted in the kernel).
 lora_status_t tc_expand_f32(void *y, const float *H, const lora_adapter_table &tab, const lora_segments &segs,
                             cudaStream_t stream);
 // case ii.  dX += A_i^T dh from the bf16 hand-off buffer.
-lora_status_t tc_dx(void *dX, const uint16_t *dh_bf16, int32_t rw, const lora_adapter_table &tab,
+lora_status_t tc_dx(void *dX, const uint16_t *dh_bf16, int32_t rw, int32_t *claim, const lora_adapter_table &tab,
                     const lora_segments &segs, cudaStream_t stream);
 
 // cases iii / iv, output [sum_r, d] accumulated into (the caller zeroes it):
 // dB[row_off + k, o] and dA[row_off + k, j].  tickets: null, or
 // tokred_ranges(d) x segs.max_spans zeroed ints for the ordered mode (each
 // adapter's span partials added in span order: bit-reproducible sums).
+// claim: as for case ii.
 int32_t tokred_ranges(int32_t d);
-lora_status_t tc_db(float *dB, const void *dY, const uint16_t *h_bf16, int32_t rw, int32_t *tickets,
+lora_status_t tc_db(float *dB, const void *dY, const uint16_t *h_bf16, int32_t rw, int32_t *tickets, int32_t *claim,
                     const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream);
-lora_status_t tc_da(float *dA, const void *X, const uint16_t *dh_bf16, int32_t rw, int32_t *tickets,
+lora_status_t tc_da(float *dA, const void *X, const uint16_t *dh_bf16, int32_t rw, int32_t *tickets, int32_t *claim,
                     const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream);
 
 // decode-sized batches: the shrink split over d_in, one CTA per (tile, slice),

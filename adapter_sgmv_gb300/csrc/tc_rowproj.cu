@@ -84,6 +84,10 @@ struct RowOut {
     int32_t splits;
     int32_t part_ld;
     float *part;
+    // work-claim counters of the kernels that follow in the same call, zeroed
+    // here before anything else (null: none)
+    int32_t *zero_claims;
+    int32_t n_zero;
 };
 
 // the k-blocks [lo, hi) of part q of a d of nk blocks cut into `splits` parts
@@ -97,6 +101,7 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
     extern __shared__ uint8_t smem_raw[];
     const Smem S = carve(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    zero_claims(o.zero_claims, o.n_zero);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -411,8 +416,10 @@ namespace {
 // one thread per (row, 8 columns).  It runs beside case i (dh), so its CTAs
 // are kept small (1024-thread CTAs converted faster alone but crowded out dh's).
 __global__ void __launch_bounds__(256) h_to_bf16_kernel(const float *__restrict__ H, uint16_t *__restrict__ hb,
-                                                        int32_t rw, lora_adapter_table tab, lora_segments segs)
+                                                        int32_t rw, int32_t *zero, int32_t n_zero,
+                                                        lora_adapter_table tab, lora_segments segs)
 {
+    zero_claims(zero, n_zero);  // the counters of the kernels after this one in the call
     const int32_t n_tiles = N_TILES(segs);
     const int32_t r_max = tab.r_max;
     const bool vec = (r_max & 3) == 0 && (reinterpret_cast<uintptr_t>(H) & 15u) == 0;
@@ -443,13 +450,13 @@ __global__ void __launch_bounds__(256) h_to_bf16_kernel(const float *__restrict_
 
 }  // namespace
 
-lora_status_t tc_h_to_bf16(const float *H, uint16_t *hb, int32_t rw, const lora_adapter_table &tab,
-                           const lora_segments &segs, cudaStream_t stream)
+lora_status_t tc_h_to_bf16(const float *H, uint16_t *hb, int32_t rw, int32_t *zero_claims, int32_t n_zero,
+                           const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream)
 {
     if (segs.n_tokens == 0 || segs.max_tiles == 0) return LORA_OK;
     const int sms = sm_count();
     const int grid = segs.max_tiles < 4 * sms ? segs.max_tiles : 4 * sms;
-    h_to_bf16_kernel<<<grid, 256, 0, stream>>>(H, hb, rw, tab, segs);
+    h_to_bf16_kernel<<<grid, 256, 0, stream>>>(H, hb, rw, zero_claims, n_zero, tab, segs);
     return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
@@ -465,16 +472,17 @@ int32_t rowproj_splits(int32_t max_tiles, int32_t d)
 int32_t rowproj_part_ld(int32_t r_max) { return (r_max + 15) & ~15; }
 
 lora_status_t tc_shrink(const void *x, const lora_adapter_table &tab, const lora_segments &segs, float *H,
-                        uint16_t *hi, uint16_t *lo, int32_t rw, float *part, cudaStream_t stream)
+                        uint16_t *hi, uint16_t *lo, int32_t rw, float *part, int32_t *zero_claims, int32_t n_zero,
+                        cudaStream_t stream)
 {
-    RowOut o{H, hi, lo, rw, 0.f, 1, 0, nullptr};
+    RowOut o{H, hi, lo, rw, 0.f, 1, 0, nullptr, zero_claims, n_zero};
     return launch_rowproj(x, tab.A, tab.d_in, o, tab, segs, part, stream);
 }
 
 lora_status_t tc_dh(const void *dY, const lora_adapter_table &tab, const lora_segments &segs, uint16_t *dh_bf16,
-                    int32_t rw, float *part, cudaStream_t stream)
+                    int32_t rw, float *part, int32_t *zero_claims, int32_t n_zero, cudaStream_t stream)
 {
-    RowOut o{nullptr, dh_bf16, nullptr, rw, 1.f, 1, 0, nullptr};
+    RowOut o{nullptr, dh_bf16, nullptr, rw, 1.f, 1, 0, nullptr, zero_claims, n_zero};
     return launch_rowproj(dY, tab.B, tab.d_out, o, tab, segs, part, stream);
 }
 

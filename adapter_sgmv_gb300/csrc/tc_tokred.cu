@@ -52,6 +52,7 @@ struct Smem {
     uint64_t *full, *empty, *tfull, *tempty, *done, *tk_go, *tk_done;
     uint32_t *tmem_holder;
     volatile int32_t *abort;
+    ClaimRing claims;  // items claimed at run time
 };
 
 LORA_DEV Smem carve(uint8_t *raw)
@@ -71,6 +72,9 @@ LORA_DEV Smem carve(uint8_t *raw)
     s.tk_done = s.tk_go + 1;
     s.tmem_holder = reinterpret_cast<uint32_t *>(s.tk_done + 1);
     s.abort = reinterpret_cast<volatile int32_t *>(s.tmem_holder + 1);
+    s.claims.full = reinterpret_cast<uint64_t *>(s.tmem_holder + 8);
+    s.claims.empty = s.claims.full + kClaimSlots;
+    s.claims.slot = reinterpret_cast<volatile int32_t *>(s.claims.empty + kClaimSlots);
     return s;
 }
 
@@ -108,9 +112,11 @@ LORA_DEV void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "m
 // after the partials of the adapter's earlier spans (same column range) are in
 // the output: the span's ticket holds the number of spans already added.  The
 // wait is bounded like every pipeline wait; on time-out the CTA's abort flag
-// and LORA_ERR_TIMEOUT are set.  Items are taken in index order by every CTA
-// and an earlier span of the same adapter and range has the lower index, so
-// the unfinished item with the lowest index can always proceed.
+// and LORA_ERR_TIMEOUT are set.  The ordered mode claims its items at run
+// time, in index order, so every item below a claimed one is held by a
+// running CTA; an earlier span of the same adapter and range has the lower
+// index, and a CTA works through its claims in order, so the unfinished item
+// with the lowest index can always proceed.
 LORA_DEV bool wait_ticket(const int32_t *tk, int32_t want, volatile int32_t *abort_flag, int32_t *status)
 {
     const long long t0 = clock64();
@@ -133,16 +139,21 @@ LORA_DEV void release_ticket(int32_t *tk, int32_t v)
 }
 LORA_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
+// kClaim: items claimed at run time from `claim` (id-routed batches and the
+// ordered mode), else CTA b takes items b, b + gridDim.x, ...
+template <bool kClaim>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_act3,
                  const __grid_constant__ CUtensorMap map_h,
                  const __grid_constant__ CUtensorMap map_g, const uint16_t *__restrict__ act, int32_t d,
                  const uint16_t *__restrict__ hbuf, int32_t rw, float use_scale, int32_t blocks3, int32_t rng,
-                 int32_t *__restrict__ tickets, lora_adapter_table tab, lora_segments segs)
+                 int32_t *__restrict__ tickets, int32_t *claim, lora_adapter_table tab, lora_segments segs)
 {
     extern __shared__ uint8_t smem_raw[];
     const Smem S = carve(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the claimer's first item, claimed before the set-up so that its round trip overlaps it
+    const int32_t first = kClaim && warp == 0 && lane == 0 ? claim_first(claim) : 0;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -154,6 +165,11 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
         mbar_init(S.done, 1);
         mbar_init(S.tk_go, 1);    // ordered mode: the ticket says the earlier spans are added
         mbar_init(S.tk_done, 4);  // ordered mode: every epilogue warp's adds are complete
+        if (kClaim)
+            for (int i = 0; i < kClaimSlots; ++i) {  // claimed by producer warp 0, read by the other warps
+                mbar_init(&S.claims.full[i], 1);
+                mbar_init(&S.claims.empty[i], (kProd - 1) + 1 + 4);
+            }
         *S.abort = 0;
         fence_barrier_init();
     }
@@ -177,7 +193,23 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
         }
         uint32_t g = 0, last = 0xffffffffu;
         bool ok = true;
-        for (int32_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        uint32_t q = 0;
+        for (int32_t it = blockIdx.x; (kClaim || it < n_items) && ok; it += gridDim.x, ++q) {
+            if (kClaim) {
+                bool got = true;
+                if (warp == 0) {  // the claimer
+                    if (lane == 0) got = claim_next(S.claims, q, claim, first, &it, S.abort, segs.status);
+                    got = __shfl_sync(0xffffffffu, got, 0);
+                    it = __shfl_sync(0xffffffffu, it, 0);
+                } else {
+                    got = claim_read_warp(S.claims, q, &it, S.abort, segs.status);
+                }
+                if (!got) {
+                    ok = false;
+                    break;
+                }
+                if (it < 0 || it >= n_items) break;
+            }
             const Item I = load_item(tab, segs, it, n_ranges, d, rng);
             if (!I.ad.ok) continue;
             // this warp's first stage of the item, and whether it has one at all
@@ -273,7 +305,12 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
         if (lane == 0) {
             uint32_t g = 0, nitem = 0;
             bool ok = true;
-            for (int32_t it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+            uint32_t q = 0;
+            for (int32_t it = blockIdx.x; (kClaim || it < n_items) && ok; it += gridDim.x, ++q) {
+                if (kClaim) {
+                    if (!claim_read(S.claims, q, &it, S.abort, segs.status)) break;
+                    if (it < 0 || it >= n_items) break;
+                }
                 const Item I = load_item(tab, segs, it, n_ranges, d, rng);
                 if (!I.ad.ok) continue;
                 const uint32_t rp = (uint32_t)rpad16(I.ad.rank);
@@ -320,7 +357,16 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
         const uint32_t lane_base = 32u * (warp & 3);
         float *red = reinterpret_cast<float *>(S.red + (warp - kEpi0) * kRedBytes);
         uint32_t nitem = 0, n_ord = 0;
-        for (int32_t it = blockIdx.x; it < n_items; it += gridDim.x) {
+        uint32_t q = 0;
+        for (int32_t it = blockIdx.x; kClaim || it < n_items; it += gridDim.x, ++q) {
+            if (kClaim) {
+                if (q > 0) claim_release_warp(S.claims, q - 1);  // the previous item is done
+                if (!claim_read_warp(S.claims, q, &it, S.abort, segs.status, true)) break;
+                if (it < 0 || it >= n_items) {
+                    claim_release_warp(S.claims, q);
+                    break;
+                }
+            }
             const Item I = load_item(tab, segs, it, n_ranges, d, rng);
             if (!I.ad.ok) continue;
             const int32_t rp = rpad16(I.ad.rank);
@@ -398,9 +444,10 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
 }
 
 lora_status_t launch_tokred(float *G, const void *act, int32_t d, const uint16_t *hbuf, int32_t rw, float use_scale,
-                            int32_t *tickets, const lora_adapter_table &tab, const lora_segments &segs,
+                            int32_t *tickets, int32_t *claim, const lora_adapter_table &tab, const lora_segments &segs,
                             cudaStream_t stream)
 {
+    if (tickets != nullptr && claim == nullptr) return LORA_ERR_INVALID_ARG;  // the ordered adds need claimed items
     if (segs.n_tokens == 0 || segs.max_spans == 0) return LORA_OK;
     CUtensorMap map_act, map_act3, map_h, map_g;
     // d a multiple of 64: a stage's eight column blocks come in one 3-D copy
@@ -417,16 +464,23 @@ lora_status_t launch_tokred(float *G, const void *act, int32_t d, const uint16_t
         !make_tmap_bf16_2d(&map_h, hbuf, (uint64_t)rw, (uint64_t)segs.n_tokens, 64, kTok, true) ||
         !make_tmap_f32_2d(&map_g, G, (uint64_t)d, (uint64_t)tab.sum_r, 32, 16))
         return LORA_ERR_CUDA;
-    if (cudaFuncSetAttribute(tc_tokred_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(tc_tokred_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(tc_tokred_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+            cudaSuccess)
         return LORA_ERR_CUDA;
     const int n_ranges = (d + rng - 1) / rng;
     const int64_t items = (int64_t)segs.max_spans * n_ranges;
     const int grid = items < sms ? (int)items : sms;
+    // run-time claims balance uneven items once every CTA has several to
+    // take; with fewer than three per CTA (at most) the split by CTA index did
+    // better (skewed batch, dA: 50 against 55 us).  The ordered mode always
+    // claims: its waits rely on it.
+    if (tickets == nullptr && items < 3 * (int64_t)sms) claim = nullptr;
     if (!blocks3) map_act3 = map_act;
-    tc_tokred_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_act, map_act3, map_h, map_g,
-                                                             static_cast<const uint16_t *>(act), d, hbuf, rw,
-                                                             use_scale, blocks3, rng, tickets, tab, segs);
+    auto *kernel = claim != nullptr ? tc_tokred_kernel<true> : tc_tokred_kernel<false>;
+    kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_act, map_act3, map_h, map_g, static_cast<const uint16_t *>(act),
+                                                   d, hbuf, rw, use_scale, blocks3, rng, tickets, claim, tab, segs);
     return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
@@ -434,16 +488,16 @@ lora_status_t launch_tokred(float *G, const void *act, int32_t d, const uint16_t
 
 int32_t tokred_ranges(int32_t d) { return (d + 127) / 128; }  // the most column ranges of an item list
 
-lora_status_t tc_db(float *dB, const void *dY, const uint16_t *h_bf16, int32_t rw, int32_t *tickets,
+lora_status_t tc_db(float *dB, const void *dY, const uint16_t *h_bf16, int32_t rw, int32_t *tickets, int32_t *claim,
                     const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream)
 {
-    return launch_tokred(dB, dY, tab.d_out, h_bf16, rw, 1.f, tickets, tab, segs, stream);
+    return launch_tokred(dB, dY, tab.d_out, h_bf16, rw, 1.f, tickets, claim, tab, segs, stream);
 }
 
-lora_status_t tc_da(float *dA, const void *X, const uint16_t *dh_bf16, int32_t rw, int32_t *tickets,
+lora_status_t tc_da(float *dA, const void *X, const uint16_t *dh_bf16, int32_t rw, int32_t *tickets, int32_t *claim,
                     const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream)
 {
-    return launch_tokred(dA, X, tab.d_in, dh_bf16, rw, 0.f, tickets, tab, segs, stream);
+    return launch_tokred(dA, X, tab.d_in, dh_bf16, rw, 0.f, tickets, claim, tab, segs, stream);
 }
 
 }  // namespace lora

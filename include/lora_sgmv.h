@@ -189,7 +189,12 @@ LORA_API lora_status_t lora_build_segments(const int32_t *ids, const int32_t *se
                                   lora_segments *out, lora_stream_t stream);
 
 /* Bytes of device workspace lora_packed_fwd / lora_packed_bwd need for this
- * table and T tokens (0 when the sizes are out of range). */
+ * table and T tokens (0 when the sizes are out of range).  The workspace holds
+ * the hand-off rows between the kernels, the counters from which the
+ * persistent kernels claim their work items at run time (each zeroed inside
+ * the call by the kernel that runs before its user), and for the backward the
+ * ordered mode's tickets and case i's partial sums.  Nothing in it has to
+ * start at zero; calls that overlap on the GPU need separate workspaces. */
 LORA_API size_t lora_workspace_bytes(const lora_adapter_table *table, int32_t n_tokens);
 
 /*

@@ -86,7 +86,7 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     assert st == 5  # LORA_ERR_WORKSPACE_TOO_SMALL
     assert spec.n_tokens == T
     # a batch of rank-128 adapters that fits: two copies of 16256 x 128 bf16 (8,323,072 bytes)
-    # plus one 256-byte block of counters, below 8 MiB
+    # plus a 256-byte block of work-claim counters and one of tickets, below 8 MiB
     T = 16256
     segs = lora.lora_build_segments(seg_offsets=torch.tensor([0, T], dtype=torch.int32, device=dev),
                                     n_tokens=T, n_adapters=1)
