@@ -35,6 +35,7 @@ using namespace tc;
 
 constexpr int kWStages = 2;
 constexpr int kYStages = 6;
+constexpr int kLook = 2;  // gathered tiles: chunks of y an epilogue warp copies ahead (kLook + 1 <= kYStages / 2)
 constexpr int kNC = 128;                              // columns per MMA chunk
 constexpr int kNPart = 1024;                          // columns per work item
 constexpr uint32_t kWBytes = kNC * LORA_MAX_RANK * 2;  // one weight chunk
@@ -117,9 +118,11 @@ struct ColIn {
     int32_t *claim;    // kClaim: the work-claim counter, zero at launch
 };
 
+// kGather: tiles of non-consecutive tokens occur (id-routed batches); their
+// rows of y are copied into the stages by the epilogue warps that use them.
 // kClaim: items claimed at run time from in.claim (id-routed batches, whose
 // items differ in cost), else CTA b takes items b, b + gridDim.x, ...
-template <bool kLoader, int kEpi, bool kClaim>
+template <bool kLoader, int kEpi, bool kGather, bool kClaim>
 __global__ void __launch_bounds__(threads_of<kLoader, kEpi>(), 1)
 tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ CUtensorMap map_hi,
                   const __grid_constant__ CUtensorMap map_lo, const __grid_constant__ CUtensorMap map_y,
@@ -135,9 +138,10 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
     // stores, i.e. after stage g + kStoreLag (four warps: one leader for both
     // halves) or g + 2 kStoreLag (eight: one leader per half) is worked on; TMA
     // stages arrive when issued, so the producer can fill that stage once an
-    // earlier one is freed.  A gathered stage completes once the copies of every
-    // producer lane have landed (each lane's arrival is triggered by its own
-    // copies, the lane never waits for them) and is freed without a store.
+    // earlier one is freed.  The stages of a gathered tile are handed to the
+    // epilogue empty: each epilogue warp copies its own 32 rows of the chunk
+    // kLook chunks ahead of the one it works on (cp.async, its own copy groups,
+    // no barrier between warps), and the stage is freed without a store.
     // Tiles of the two kinds never share an item, and every item ends with its
     // stores drained.
     static_assert((kEpi / 4) * kStoreLag < kYStages, "y-stage ring too shallow for the store lag");
@@ -231,20 +235,6 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
                 }
                 ++na;
             }
-            // tokens of a gathered tile's rows, -1 past its end: in the 192-thread
-            // kernel the 32 rows (lane >> 3) + 4 q this lane copies sit in
-            // registers; in the 320-thread ones (a smaller register budget per
-            // thread) row lane + 32 i sits in tok[i] and is passed by shuffles
-            constexpr bool kTokShfl = threads_of<kLoader, kEpi>() > 192;
-            constexpr int kTokRegs = kTokShfl ? 4 : 32;
-            int32_t tok[kTokRegs];
-            if (!contiguous) {
-#pragma unroll
-                for (int i = 0; i < kTokRegs; ++i) {
-                    const int m = kTokShfl ? lane + 32 * i : (lane >> 3) + 4 * i;
-                    tok[i] = m < I.tile.rows ? PERM_AT(segs, I.tile.begin + m) : -1;
-                }
-            }
             for (int32_t n0 = I.n_lo; n0 < I.n_hi && ok; n0 += kNC) {
                 // weights of the chunk: A_i / B_i^T rows k, columns n0 .. n0+127, MN-major atoms
                 {
@@ -274,36 +264,9 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
                         mbar_arrive_expect_tx(&S.yfull[s], contiguous ? kYBytes : 0u);
                         if (contiguous) tma_load_2d(y_s, &map_y, &S.yfull[s], c0, t0);
                     }
-                    if (!contiguous) {
-                        const int c = lane & 7;
-                        const bool cin = c0 + 8 * c < d;
-                        // rows (lane >> 3) + 4 q, eight rows at a time
-#pragma unroll
-                        for (int qb = 0; qb < 32; qb += 8) {
-                            int32_t tk[8];
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                const int m = (lane >> 3) + 4 * (qb + j);
-                                if constexpr (kTokShfl)
-                                    tk[j] = __shfl_sync(0xffffffffu, tok[(qb >> 3) & (kTokRegs - 1)], m & 31);
-                                else
-                                    tk[j] = tok[(qb + j) & (kTokRegs - 1)];
-                            }
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                const int m = (lane >> 3) + 4 * (qb + j);
-                                const bool v = tk[j] >= 0 && cin;
-                                const uint16_t *src = v ? out + (int64_t)tk[j] * d + c0 + 8 * c : out;
-                                cp_async_16(y_s + sw128_offset(m, c), src, v);
-                            }
-                        }
-                    }
-                    // every lane's arrival: at once for a TMA stage, once its copies
-                    // have landed for a gathered one (the lane does not wait for them)
-                    if (contiguous)
-                        mbar_arrive(&S.yfull[s]);
-                    else
-                        cp_async_mbar_arrive(&S.yfull[s]);
+                    // every lane's arrival: a gathered tile's stage goes to the
+                    // epilogue warps empty (they copy their own rows into it)
+                    mbar_arrive(&S.yfull[s]);
                     ++gy;
                 }
             }
@@ -445,19 +408,66 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
             const int32_t t = m < I.tile.rows ? PERM_AT(segs, I.tile.begin + m) : -1;
             const int32_t t0 = PERM_AT(segs, I.tile.begin);
             uint16_t *row = out + (int64_t)(t < 0 ? 0 : t) * d;
+            // a gathered tile: this warp copies its own 32 rows of each chunk's
+            // halves into the chunk's stages, kLook chunks ahead; lane l copies
+            // 16 bytes (piece l & 7) of rows (l >> 3) + 4 q, q < 8, of the warp
+            const bool gathered = kGather && (I.tile.flags & 1) == 0;
+            const uint32_t a0 = a;
+            const int32_t n_chunks = (I.n_hi - I.n_lo + kNC - 1) / kNC;
+            int32_t tg[8];
+            auto copy_rows = [&](int32_t j) -> bool {
+                for (int h = hg; h < 2; h += kHStep) {
+                    const uint32_t gy = 2u * (a0 + (uint32_t)j) + (uint32_t)h;
+                    const uint32_t s = gy % kYStages, ph = (gy / kYStages) & 1u;
+                    if (!mbar_wait_warp(&S.yfull[s], ph, S.abort, segs.status)) return false;  // handed over
+                    uint8_t *y_s = S.y + s * kYBytes;
+                    const int32_t c0 = I.n_lo + j * kNC + 64 * h;
+                    const int cc = lane & 7;
+                    const bool cin = c0 + 8 * cc < d;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const bool v = tg[q] >= 0 && cin;
+                        cp_async_16(y_s + sw128_offset(lane_base + (uint32_t)((lane >> 3) + 4 * q), (uint32_t)cc),
+                                    v ? out + (int64_t)tg[q] * d + c0 + 8 * cc : out, v);
+                    }
+                }
+                cp_async_commit();
+                return true;
+            };
+            if (gathered) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) tg[q] = __shfl_sync(0xffffffffu, t, (lane >> 3) + 4 * q);
+                for (int32_t j = 0; j < kLook && j < n_chunks && ok; ++j) ok = copy_rows(j);
+                if (!ok) break;
+            }
             for (int32_t n0 = I.n_lo; n0 < I.n_hi; n0 += kNC) {
+                const int32_t j = (n0 - I.n_lo) / kNC;
+                if (gathered && j + kLook < n_chunks && !copy_rows(j + kLook)) {
+                    ok = false;
+                    break;
+                }
                 const uint32_t acc = a % kAcc, aph = (a / kAcc) & 1u;
                 if (!mbar_wait_warp(&S.tfull[acc], aph, S.abort, segs.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                if (gathered) {  // this warp's copies of chunk j have landed (later chunks' may not have)
+                    const int32_t later = min(kLook, n_chunks - 1 - j);
+                    if (later >= 2)
+                        cp_async_wait<2>();
+                    else if (later == 1)
+                        cp_async_wait<1>();
+                    else
+                        cp_async_wait<0>();
+                    __syncwarp();
+                }
 #pragma unroll 1
                 for (int h = hg; h < 2; h += kHStep) {
                     const int32_t c0 = n0 + 64 * h;
                     const uint32_t gy = 2u * a + (uint32_t)h;  // the producer fills two stages per chunk
                     const uint32_t s = gy % kYStages, ph = (gy / kYStages) & 1u;
-                    if (!mbar_wait_warp(&S.yfull[s], ph, S.abort, segs.status)) {
+                    if (!gathered && !mbar_wait_warp(&S.yfull[s], ph, S.abort, segs.status)) {
                         ok = false;
                         break;
                     }
@@ -543,7 +553,7 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
     }
 }
 
-template <bool kLoader, int kEpi, bool kClaim>
+template <bool kLoader, int kEpi, bool kGather, bool kClaim>
 lora_status_t launch_colproj(uint16_t *out, int32_t d, const void *w, const uint16_t *hi, const uint16_t *lo,
                              int32_t rw, const ColIn &in, const lora_adapter_table &tab, const lora_segments &segs,
                              cudaStream_t stream)
@@ -567,32 +577,31 @@ lora_status_t launch_colproj(uint16_t *out, int32_t d, const void *w, const uint
         map_hi = map_y;
         map_lo = map_y;
     }
-    if (cudaFuncSetAttribute(tc_colproj_kernel<kLoader, kEpi, kClaim>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(tc_colproj_kernel<kLoader, kEpi, kGather, kClaim>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
         return LORA_ERR_CUDA;
     const int n_parts = (d + kNPart - 1) / kNPart;
     const int64_t items = (int64_t)segs.max_tiles * n_parts;
     const int sms = sm_count();
     const int grid = items < sms ? (int)items : sms;
-    tc_colproj_kernel<kLoader, kEpi, kClaim><<<grid, threads_of<kLoader, kEpi>(), kSmemBytes, stream>>>(
+    tc_colproj_kernel<kLoader, kEpi, kGather, kClaim><<<grid, threads_of<kLoader, kEpi>(), kSmemBytes, stream>>>(
         map_w, map_hi, map_lo, map_y, out, d, in, tab, segs);
     return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
 }  // namespace
 
-// Segment-sorted batches: every tile a run of consecutive tokens, eight
-// epilogue warps, items split ahead of time (they cost the same but for the
-// last tile of each adapter).  Id-routed batches: four epilogue warps, items
-// claimed at run time when a counter is given (gathered and TMA tiles, tiles
-// of any length).
+// Segment-sorted batches: every tile a run of consecutive tokens, items split
+// ahead of time (they cost the same but for the last tile of each adapter).
+// Id-routed batches: gathered tiles too, items claimed at run time when a
+// counter is given (gathered and TMA tiles, tiles of any length).
 lora_status_t launch_bf16(uint16_t *out, int32_t d, const void *w, const uint16_t *hi, const uint16_t *lo, int32_t rw,
                           const ColIn &in, const lora_adapter_table &tab, const lora_segments &segs,
                           cudaStream_t stream)
 {
-    if (segs.sorted != 0) return launch_colproj<false, 8, false>(out, d, w, hi, lo, rw, in, tab, segs, stream);
-    if (in.claim != nullptr) return launch_colproj<false, 4, true>(out, d, w, hi, lo, rw, in, tab, segs, stream);
-    return launch_colproj<false, 4, false>(out, d, w, hi, lo, rw, in, tab, segs, stream);
+    if (segs.sorted != 0) return launch_colproj<false, 8, false, false>(out, d, w, hi, lo, rw, in, tab, segs, stream);
+    if (in.claim != nullptr) return launch_colproj<false, 8, true, true>(out, d, w, hi, lo, rw, in, tab, segs, stream);
+    return launch_colproj<false, 8, true, false>(out, d, w, hi, lo, rw, in, tab, segs, stream);
 }
 
 lora_status_t tc_expand_bf16(void *y, const uint16_t *hi, const uint16_t *lo, int32_t rw, int32_t *claim,
@@ -606,8 +615,8 @@ lora_status_t tc_expand_f32(void *y, const float *H, const lora_adapter_table &t
                             cudaStream_t stream)
 {
     const ColIn in{H, 1.f, 1, nullptr};
-    return launch_colproj<true, 4, false>(static_cast<uint16_t *>(y), tab.d_out, tab.B, nullptr, nullptr, 0, in, tab,
-                                          segs, stream);
+    return launch_colproj<true, 4, true, false>(static_cast<uint16_t *>(y), tab.d_out, tab.B, nullptr, nullptr, 0, in,
+                                                tab, segs, stream);
 }
 
 lora_status_t tc_dx(void *dX, const uint16_t *dh_bf16, int32_t rw, int32_t *claim, const lora_adapter_table &tab,
