@@ -10,8 +10,8 @@ multi-projection decode) runs on small ragged batches; the outputs go to
 OUT_DIR/<case>.npz with the status word and the check site after each case.
 The parent test runs the same cases on the release build and compares.
 
-Then two batches whose perm holds one token index past T (a corruption the
-builder never makes) run through the debug build's decode and packed paths;
+Then three batches whose perm holds one token index past T (a corruption the
+builder never makes) run through the debug build's decode, packed and one-launch forward paths;
 their x / y / H / dY / dX buffers carry 64 spare rows, so even an unchecked
 read or write of that row would stay inside its buffer.  The checks must
 report LORA_ERR_INDEX and where."""
@@ -40,6 +40,13 @@ def specs():
     out["ragged_sorted"] = wl.custom("ragged_sorted", 1032, 520, ranks, alphas, ids)
     out["ragged_ids"] = wl.custom("ragged_ids", 1032, 520, ranks, alphas,
                                   np.random.default_rng(11).permutation(ids), sorted_=False)
+    # enough tiles (87) that case i is not split: the forward runs as one launch
+    lengths2, ranks2 = [4000, 3000, 1500, 1, 1739, 0], [32, 128, 16, 64, 8, 16]
+    ids2 = np.concatenate([np.full(n, i, np.int32) for i, n in enumerate(lengths2)])
+    alphas2 = [2.0 * r for r in ranks2]
+    out["many_tiles_sorted"] = wl.custom("many_tiles_sorted", 256, 392, ranks2, alphas2, ids2)
+    out["many_tiles_ids"] = wl.custom("many_tiles_ids", 256, 392, ranks2, alphas2,
+                                      np.random.default_rng(13).permutation(ids2), sorted_=False)
     # decode-sized, unsorted (the decode kernels)
     dec_ranks = [16, 32, 8, 128, 24]
     out["decode_ids"] = wl.custom("decode_ids", 264, 392, dec_ranks, [2.0 * r for r in dec_ranks],
@@ -148,7 +155,7 @@ def main(out_dir):
         out, st, where = run_case(spec, host)
         np.savez(os.path.join(out_dir, f"{name}.npz"), **out)
         summary["cases"][name] = {"status": st, "where": where}
-    for name in ("decode_ids", "ragged_ids"):
+    for name in ("decode_ids", "ragged_ids", "many_tiles_ids"):
         spec = specs()[name]
         summary["corrupted"][name] = run_corrupted(spec, wl.host_inputs(spec))
     torch.cuda.synchronize()
