@@ -19,9 +19,8 @@ size_t handoff_region_bytes(int32_t T, int32_t r_max)
 // batches up to this many tokens take the decode kernels
 constexpr int32_t kDecodeMaxTokens = 512;
 
-// Work-claim counters after the two hand-off regions: one int per claiming
-// launch of a call, then (from int kFusedOff) the fused forward's task counter
-// and one ready count per routing tile.  The kernel before a claiming one on the same
+// Work-claim counters, 256 bytes after the two hand-off regions: one int per
+// claiming launch of a call.  The kernel before a claiming one on the same
 // stream zeroes its counter (forward: the shrink zeroes the expand's;
 // backward: the bf16 copy of H, or the recomputing shrink, zeroes dB's, and
 // dh zeroes dA's and dX's), so no memset is needed.  Items are claimed at run
@@ -31,15 +30,8 @@ constexpr int32_t kDecodeMaxTokens = 512;
 // ahead of time (CTA b takes b, b + grid, ...), which ends every CTA's share
 // together where run-time claims would leave the last items to CTAs that are
 // still finishing others.
+constexpr size_t kClaimRegionBytes = 256;
 enum ClaimSlot { kClaimExpand = 0, kClaimDB = 1, kClaimDA = 2, kClaimDX = 3 };
-constexpr int32_t kFusedOff = 16;
-
-size_t claim_region_bytes(int32_t T, int32_t n_adapters)
-{
-    const SegLayout L = seg_layout(T, n_adapters);
-    const int64_t words = kFusedOff + 1 + (L.ok ? L.max_tiles : 0);
-    return (size_t)((words * 4 + 255) & ~int64_t(255));
-}
 
 size_t ticket_region_bytes(const lora_adapter_table &tab, int32_t T)
 {
@@ -51,10 +43,10 @@ size_t ticket_region_bytes(const lora_adapter_table &tab, int32_t T)
 
 namespace {
 // the claim counters, when the workspace holds them (null: items by CTA index)
-int32_t *claim_region(void *ws, size_t ws_bytes, const lora_adapter_table &tab, int32_t T)
+int32_t *claim_region(void *ws, size_t ws_bytes, int32_t T, int32_t r_max)
 {
-    const size_t off = 2 * handoff_region_bytes(T, tab.r_max);
-    if (ws_bytes < off + claim_region_bytes(T, tab.n_adapters)) return nullptr;
+    const size_t off = 2 * handoff_region_bytes(T, r_max);
+    if (ws_bytes < off + kClaimRegionBytes) return nullptr;
     return reinterpret_cast<int32_t *>(static_cast<char *>(ws) + off);
 }
 }  // namespace
@@ -74,8 +66,7 @@ namespace {
 // case i's partials in the workspace, when the workspace holds them
 float *part_region(void *ws, size_t ws_bytes, const lora_adapter_table &tab, int32_t T)
 {
-    const size_t off =
-        2 * handoff_region_bytes(T, tab.r_max) + claim_region_bytes(T, tab.n_adapters) + ticket_region_bytes(tab, T);
+    const size_t off = 2 * handoff_region_bytes(T, tab.r_max) + kClaimRegionBytes + ticket_region_bytes(tab, T);
     const size_t need = part_region_bytes(tab, T);
     if (need == 0 || ws_bytes < off + need) return nullptr;
     return reinterpret_cast<float *>(static_cast<char *>(ws) + off);
@@ -84,8 +75,8 @@ float *part_region(void *ws, size_t ws_bytes, const lora_adapter_table &tab, int
 
 size_t bwd_workspace_bytes(const lora_adapter_table &tab, int32_t T)
 {
-    return 2 * handoff_region_bytes(T, tab.r_max) + claim_region_bytes(T, tab.n_adapters) +
-           ticket_region_bytes(tab, T) + part_region_bytes(tab, T);
+    return 2 * handoff_region_bytes(T, tab.r_max) + kClaimRegionBytes + ticket_region_bytes(tab, T) +
+           part_region_bytes(tab, T);
 }
 
 size_t packed_workspace_bytes(const lora_adapter_table &tab, int32_t T)
@@ -135,12 +126,7 @@ lora_status_t run_fwd(void *y, float *H_save, const void *x, void *ws, size_t ws
     uint16_t *hi = static_cast<uint16_t *>(ws);
     uint16_t *lo = reinterpret_cast<uint16_t *>(static_cast<char *>(ws) + handoff_region_bytes(segs.n_tokens, tab.r_max));
     float *part = part_region(ws, ws_bytes, tab, segs.n_tokens);
-    int32_t *claims = claim_region(ws, ws_bytes, tab, segs.n_tokens);
-    // one launch for both cases unless case i is split along d (few tiles) or
-    // each kernel is timed on its own
-    const bool split = part != nullptr && rowproj_splits(segs.max_tiles, tab.d_in) > 1;
-    if (!split && claims != nullptr && marks == nullptr)
-        return tc_fwd_fused(y, H_save, x, hi, lo, rw, claims + kFusedOff, tab, segs, stream);
+    int32_t *claims = claim_region(ws, ws_bytes, segs.n_tokens, tab.r_max);
     int32_t *c_expand = claims != nullptr ? claims + kClaimExpand : nullptr;
     lora_status_t st = marked(
         marks, stream, [&] { return tc_shrink(x, tab, segs, H_save, hi, lo, rw, part, c_expand, 1, stream); });
@@ -187,7 +173,7 @@ lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void
     uint16_t *hb = static_cast<uint16_t *>(ws);
     uint16_t *dhb = reinterpret_cast<uint16_t *>(static_cast<char *>(ws) + hreg);
     float *part = part_region(ws, ws_bytes, tab, segs.n_tokens);  // case i split along d (few tiles)
-    int32_t *claims = claim_region(ws, ws_bytes, tab, segs.n_tokens);
+    int32_t *claims = claim_region(ws, ws_bytes, segs.n_tokens, tab.r_max);
     auto claim = [&](ClaimSlot k) { return claims != nullptr ? claims + k : nullptr; };
     // the counters the launches claim from (null: items split ahead of time)
     const bool dyn = segs.sorted == 0;
@@ -196,8 +182,7 @@ lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void
     int32_t *tk_B = nullptr, *tk_A = nullptr;
     if (ordered && (dA != nullptr || dB != nullptr)) {
         if (claims == nullptr) return LORA_ERR_WORKSPACE_TOO_SMALL;
-        tk_B = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + 2 * hreg +
-                                           claim_region_bytes(segs.n_tokens, tab.n_adapters));
+        tk_B = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + 2 * hreg + kClaimRegionBytes);
         tk_A = tk_B + (int64_t)segs.max_spans * tokred_ranges(tab.d_out);
         if (cudaMemsetAsync(tk_B, 0, ticket_region_bytes(tab, segs.n_tokens), stream) != cudaSuccess)
             return LORA_ERR_CUDA;

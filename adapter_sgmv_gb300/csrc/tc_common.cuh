@@ -239,51 +239,6 @@ LORA_DEV void claim_release_warp(const ClaimRing &R, uint32_t q)
     if ((threadIdx.x & 31) == 0) mbar_arrive(&R.empty[q % kClaimSlots]);
 }
 
-// A count read early without ordering (ld_relaxed), then, once it is seen to
-// have reached its target, made an acquire for the TMA reads that follow:
-// the fence after the relaxed read that saw the writer's release orders the
-// writes the count stands for before those reads.
-LORA_DEV int32_t ld_relaxed(const int32_t *p)
-{
-    int32_t v;
-    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-LORA_DEV void acquire_for_tma()
-{
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-// Wait (bounded, like every pipeline wait) until *flag reaches `target`
-// (acquire), then order the TMA reads that follow after the writes the count
-// stands for.  Writers add to the flag after their stores with
-//   fence.proxy.async.global; __threadfence(); red.release.gpu.global.add
-LORA_DEV bool wait_count(const int32_t *flag, int32_t target, volatile int32_t *abort_flag, int32_t *status)
-{
-    long long t0 = 0;
-    for (uint32_t it = 0;; ++it) {
-        int32_t v;
-        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-        if (v >= target) {
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            return true;
-        }
-        if ((it & 63u) == 0u) {
-            if (*abort_flag) return false;
-            const long long now = clock64();
-            if (t0 == 0) {
-                t0 = now;
-            } else if (now - t0 > kWaitLimitCycles) {
-                *abort_flag = 1;
-                set_status(status, LORA_ERR_TIMEOUT);
-                return false;
-            }
-        }
-        __nanosleep(64);
-    }
-}
-
 // A kernel that runs before the claiming kernels of the same call, on the
 // same stream, zeroes their counters (block 0, before anything else).
 LORA_DEV void zero_claims(int32_t *claims, int32_t n)

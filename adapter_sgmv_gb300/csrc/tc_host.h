@@ -65,13 +65,6 @@ lora_status_t tc_h_to_bf16(const float *H, uint16_t *hb, int32_t rw, int32_t *ze
 // when the kernel starts, from which items are claimed at run time.
 lora_status_t tc_expand_bf16(void *y, const uint16_t *hi, const uint16_t *lo, int32_t rw, int32_t *claim,
                              const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream);
-// The packed forward in one persistent launch: case i for every tile, then
-// case ii for every item, tasks claimed in index order (no split along d).
-// counters: 1 + segs.max_tiles ints (the task counter and the tiles' ready
-// counts), zeroed by the call.
-lora_status_t tc_fwd_fused(void *y, float *H_save, const void *x, uint16_t *hi, uint16_t *lo, int32_t rw,
-                           int32_t *counters, const lora_adapter_table &tab, const lora_segments &segs,
-                           cudaStream_t stream);
 // case ii.  y += s_i B_i h from an fp32 H by token (converted in the kernel).
 lora_status_t tc_expand_f32(void *y, const float *H, const lora_adapter_table &tab, const lora_segments &segs,
                             cudaStream_t stream);

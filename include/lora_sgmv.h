@@ -550,8 +550,7 @@ LORA_API int32_t lora_debug_checks(void);
  * *where (host int32) status[1]: in the debug build, after LORA_ERR_INDEX,
  * the failed check's source file number << 16 | line (file numbers: 1
  * route.cu, 2 tc_rowproj.cu, 3 tc_colproj.cu, 4 tc_tokred.cu, 5 decode.cu,
- * 6 tc_base.cu, 8 tc_fwd.cu; the case i and ii kernel bodies count as the file
- * that includes them); else 0.  Errors: LORA_ERR_INVALID_ARG (NULL),
+ * 6 tc_base.cu, 7 dispatch.cu); else 0.  Errors: LORA_ERR_INVALID_ARG (NULL),
  * LORA_ERR_CUDA. */
 LORA_API lora_status_t lora_query_index_check(const lora_segments *segs, lora_stream_t stream, int32_t *where);
 

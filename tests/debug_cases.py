@@ -11,7 +11,7 @@ OUT_DIR/<case>.npz with the status word and the check site after each case.
 The parent test runs the same cases on the release build and compares.
 
 Then three batches whose perm holds one token index past T (a corruption the
-builder never makes) run through the debug build's decode, packed and one-launch forward paths;
+builder never makes) run through the debug build's decode and packed paths (split and not);
 their x / y / H / dY / dX buffers carry 64 spare rows, so even an unchecked
 read or write of that row would stay inside its buffer.  The checks must
 report LORA_ERR_INDEX and where."""
@@ -40,7 +40,7 @@ def specs():
     out["ragged_sorted"] = wl.custom("ragged_sorted", 1032, 520, ranks, alphas, ids)
     out["ragged_ids"] = wl.custom("ragged_ids", 1032, 520, ranks, alphas,
                                   np.random.default_rng(11).permutation(ids), sorted_=False)
-    # enough tiles (87) that case i is not split: the forward runs as one launch
+    # enough tiles (87) that case i is not split along d
     lengths2, ranks2 = [4000, 3000, 1500, 1, 1739, 0], [32, 128, 16, 64, 8, 16]
     ids2 = np.concatenate([np.full(n, i, np.int32) for i, n in enumerate(lengths2)])
     alphas2 = [2.0 * r for r in ranks2]

@@ -27,7 +27,7 @@ pytestmark = pytest.mark.gpu
 HERE = os.path.dirname(os.path.abspath(__file__))
 LORA_ERR_INDEX = 11
 FILE_NUMBER = {"route.cu": 1, "tc_rowproj.cu": 2, "tc_colproj.cu": 3, "tc_tokred.cu": 4, "decode.cu": 5,
-               "tc_base.cu": 6, "tc_fwd.cu": 8}
+               "tc_base.cu": 6}
 
 
 @pytest.fixture(scope="module")
@@ -85,8 +85,8 @@ def test_debug_build_reports_a_bad_perm_entry(debug_run):
     assert st == LORA_ERR_INDEX and where >> 16 == FILE_NUMBER["tc_rowproj.cu"] and where & 0xffff > 0, (st, where)
     st, where = c["ragged_ids"]["bwd"]
     assert st == LORA_ERR_INDEX and where >> 16 == FILE_NUMBER["tc_rowproj.cu"], (st, where)
-    # a batch of many tiles: the one-launch forward's case i phase reads it first
+    # a batch of many tiles (case i not split): the shrink reads it first
     st, where = c["many_tiles_ids"]["fwd"]
-    assert st == LORA_ERR_INDEX and where >> 16 == FILE_NUMBER["tc_fwd.cu"] and where & 0xffff > 0, (st, where)
+    assert st == LORA_ERR_INDEX and where >> 16 == FILE_NUMBER["tc_rowproj.cu"] and where & 0xffff > 0, (st, where)
     st, where = c["many_tiles_ids"]["bwd"]
     assert st == LORA_ERR_INDEX and where >> 16 == FILE_NUMBER["tc_rowproj.cu"], (st, where)

@@ -73,30 +73,3 @@ def test_marked_backward_with_fewer_events_than_kernels():
     torch.cuda.synchronize()
     assert n == 3
     assert torch.equal(dX1, dX2) and torch.equal(dA1, dA2) and torch.equal(dB1, dB2)
-
-
-@pytest.mark.parametrize("route", ["auto", "ids"])
-def test_one_launch_forward_matches_two_launches(route):
-    # 95 routing tiles: case i is not split along d, so the plain forward is the
-    # one-launch kernel, while the marked forward times case i and case ii as
-    # two launches; both compute the same bits
-    ranks = [16, 32, 128]
-    lengths = [6000, 3000, 3001]
-    ids = np.concatenate([np.full(n, i, np.int32) for i, n in enumerate(lengths)])
-    if route == "ids":
-        ids = np.random.default_rng(7).permutation(ids)
-    spec = wl.custom(f"onelaunch_{route}", 512, 1288, ranks, [32.0, 64.0, 16.0], ids)
-    case = GpuCase(spec, wl.host_inputs(spec, y0="randn", dX0="randn"), route=route)
-    y1, H1 = case.fwd()
-    y2 = case.inp["y0"].clone()
-    H2 = torch.zeros_like(H1)
-    ev = _events(4)
-    assert lora.lora_packed_fwd_marked(y2, H2, case.inp["x"], case.table, case.segs, case.ws, ev) == 4
-    torch.cuda.synchronize()
-    assert lora.lora_query_status(case.segs) == 0
-    assert torch.equal(H1, H2)
-    assert torch.equal(y1, y2)
-    # and repeated: the run-time order of the tasks changes nothing
-    y3, H3 = case.fwd()
-    torch.cuda.synchronize()
-    assert torch.equal(H1, H3) and torch.equal(y1, y3)
