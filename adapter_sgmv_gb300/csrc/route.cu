@@ -231,6 +231,121 @@ __global__ void route_tiles_kernel(const int32_t *__restrict__ offs, int32_t n_c
     emit_pieces(seg_start, N, perm, LORA_SPAN_TOKENS, s.spans, s.n_spans, s.max_spans, base, s.n_tokens, s.status);
 }
 
+// ---------------------------------------------------------------- unsorted ids, one launch
+// When the N x ceil(T / 32) chunk counts fit in shared memory, one block of
+// 1024 threads does the whole build in one launch instead of six: the counts,
+// their exclusive scan in the same adapter-major order, the stable scatter,
+// seg_start, and the tiles and spans -- the same perm, bit for bit.  The ids
+// are first copied into shared memory, all at once, so that the two passes
+// over them pay no memory round trip per chunk;
+// the scan walks the counts in 1024-wide rows (one count per thread, no bank
+// conflicts), and the pieces are cut with seg_start and the piece bases in
+// shared memory.
+constexpr int64_t kSmallHistWords = 40 * 1024;         // 160 KB of counts at most
+constexpr int64_t kSmallSmemWords = (200 * 1024) / 4;  // counts, ids, seg_start and piece bases
+
+// Cut every adapter's group into pieces of at most `len` tokens (see
+// emit_pieces); seg and base are shared memory, perm global (this block's).
+__device__ void emit_pieces_local(const int32_t *seg, int32_t N, const int32_t *__restrict__ perm, int32_t len,
+                                  int32_t *__restrict__ out, int32_t *__restrict__ n_out, int32_t max_out,
+                                  int32_t *base, int32_t T, int32_t *__restrict__ status)
+{
+    int32_t carry = 0;
+    for (int32_t i0 = 0; i0 < N; i0 += blockDim.x) {
+        const int32_t i = i0 + threadIdx.x;
+        const int32_t n = i < N ? seg[i + 1] - seg[i] : 0;
+        const int32_t cnt = n > 0 ? (n + len - 1) / len : 0;
+        int32_t tot;
+        const int32_t e = block_exclusive_scan(cnt, &tot);
+        if (i < N) base[i] = carry + e;
+        carry += tot;
+    }
+    if (threadIdx.x == 0) base[N] = carry;
+    __syncthreads();
+    const int32_t total = min(carry, max_out);
+    for (int32_t q = threadIdx.x; q < total; q += blockDim.x) {
+        int32_t lo = 0, hi = N;
+        while (hi - lo > 1) {
+            const int32_t mid = (lo + hi) >> 1;
+            if (base[mid] <= q) lo = mid;
+            else hi = mid;
+        }
+        const int32_t j = q - base[lo];
+        const int32_t n = seg[lo + 1] - seg[lo];
+        const int32_t b = seg[lo] + j * len;
+        const int32_t rows = min(len, n - j * len);
+        const int32_t contiguous =
+            (perm[LORA_DBG_INDEX((int64_t)b + rows - 1, T, status)] - perm[LORA_DBG_INDEX(b, T, status)] == rows - 1)
+                ? 1
+                : 0;
+        reinterpret_cast<int4 *>(out)[q] = make_int4(lo, b, rows, contiguous);
+    }
+    if (threadIdx.x == 0) *n_out = total;
+    __syncthreads();  // base is reused by the next call
+}
+
+__global__ void __launch_bounds__(1024) route_small_kernel(const int32_t *__restrict__ ids_g, int32_t T, int32_t N,
+                                                           int32_t n_chunks, lora_segments s)
+{
+    extern __shared__ int32_t sm[];  // counts [N][n_chunks] (then their exclusive prefix), seg [N+1], base [N+1], ids [T]
+    const int64_t M = (int64_t)N * n_chunks;
+    int32_t *cnt = sm;
+    int32_t *seg = sm + M;
+    int32_t *base = seg + N + 1;
+    int32_t *ids = base + N + 1;
+#pragma unroll 8
+    for (int32_t i = threadIdx.x; i < T; i += blockDim.x) ids[i] = ids_g[i];
+    for (int64_t i = threadIdx.x; i < M; i += blockDim.x) cnt[i] = 0;
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int32_t c = warp; c < n_chunks; c += 32) {  // warp-uniform: every lane of a warp takes the same chunks
+        const int64_t t = (int64_t)c * 32 + lane;
+        int32_t id = -1;
+        if (t < T) {
+            id = ids[t];
+            if (id < 0 || id >= N) {
+                set_status(s.status, LORA_ERR_BAD_ADAPTER_ID);
+                id = -1;
+            }
+        }
+        const uint32_t same = __match_any_sync(0xffffffffu, id);
+        if (id >= 0 && lane == __ffs(same) - 1) cnt[(int64_t)id * n_chunks + c] = __popc(same);
+    }
+    __syncthreads();
+    // exclusive scan in place, a 1024-wide row at a time
+    int32_t carry = 0;
+    for (int64_t r0 = 0; r0 < M; r0 += blockDim.x) {
+        const int64_t i = r0 + threadIdx.x;
+        const int32_t v = i < M ? cnt[i] : 0;
+        int32_t tot;
+        const int32_t e = block_exclusive_scan(v, &tot);
+        if (i < M) cnt[i] = carry + e;
+        carry += tot;
+    }
+    __syncthreads();
+    for (int32_t c = warp; c < n_chunks; c += 32) {
+        const int64_t t = (int64_t)c * 32 + lane;
+        int32_t id = -1;
+        if (t < T) {
+            id = ids[t];
+            if (id < 0 || id >= N) id = -1;
+        }
+        const uint32_t same = __match_any_sync(0xffffffffu, id);
+        if (id >= 0) {
+            const int32_t rank = __popc(same & ((1u << lane) - 1u));
+            s.perm[LORA_DBG_INDEX((int64_t)cnt[(int64_t)id * n_chunks + c] + rank, T, s.status)] = (int32_t)t;
+        }
+    }
+    for (int32_t i = threadIdx.x; i <= N; i += blockDim.x) {
+        const int32_t v = i < N ? cnt[(int64_t)i * n_chunks] : carry;
+        seg[i] = v;
+        s.seg_start[i] = v;
+    }
+    __syncthreads();  // perm and seg are this block's writes
+    emit_pieces_local(seg, N, s.perm, LORA_TILE_M, s.tiles, s.n_tiles, s.max_tiles, base, T, s.status);
+    emit_pieces_local(seg, N, s.perm, LORA_SPAN_TOKENS, s.spans, s.n_spans, s.max_spans, base, T, s.status);
+}
+
 // ---------------------------------------------------------------- sorted input, one launch
 // For tokens already grouped by adapter the permutation is the identity and
 // every piece is a run of consecutive tokens, so the whole builder is one
@@ -386,7 +501,17 @@ lora_status_t build_segments(const int32_t *ids, const int32_t *seg_offsets, int
         int32_t *hist = s.scratch;
         int32_t *bsum = hist + ((L.hist_words + 63) & ~int64_t(63));
         int32_t *total = bsum + ((L.block_sums + 63) & ~int64_t(63));
-        if (L.hist_words > 0) {
+        // one launch when the counts, the ids and the two small tables fit in
+        // shared memory (read from global memory the ids cost a round trip per
+        // chunk, which made a single block slower than the six launches)
+        const int64_t small_words = L.hist_words + 2 * ((int64_t)N + 1) + T;
+        if (L.hist_words > 0 && L.hist_words <= kSmallHistWords && small_words <= kSmallSmemWords) {
+            const int smem = (int)(small_words * 4);
+            if (cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+                cudaSuccess)
+                return LORA_ERR_CUDA;
+            route_small_kernel<<<1, 1024, smem, stream>>>(ids, T, N, L.n_chunks, s);
+        } else if (L.hist_words > 0) {
             if (cudaMemsetAsync(hist, 0, (size_t)L.hist_words * 4, stream) != cudaSuccess) return LORA_ERR_CUDA;
             const int threads = 256;
             const int blocks = (int)(((int64_t)L.n_chunks * 32 + threads - 1) / threads);
