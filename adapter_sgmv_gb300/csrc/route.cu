@@ -232,21 +232,19 @@ __global__ void route_tiles_kernel(const int32_t *__restrict__ offs, int32_t n_c
 }
 
 // ---------------------------------------------------------------- unsorted ids, one launch
-// When the N x ceil(T / 32) chunk counts fit in shared memory, one block of
-// 1024 threads does the whole build in one launch instead of six: the counts,
-// their exclusive scan in the same adapter-major order, the stable scatter,
-// seg_start, and the tiles and spans -- the same perm, bit for bit.  The ids
-// are first copied into shared memory, all at once, so that the two passes
-// over them pay no memory round trip per chunk;
-// the scan walks the counts in 1024-wide rows (one count per thread, no bank
-// conflicts), and the pieces are cut with seg_start and the piece bases in
-// shared memory.
-constexpr int64_t kSmallHistWords = 40 * 1024;         // 160 KB of counts at most
-constexpr int64_t kSmallSmemWords = (200 * 1024) / 4;  // counts, ids, seg_start and piece bases
+// When the ids, their permutation and a table of N x 32 counts fit in shared
+// memory, one block of 1024 threads does the whole build in one launch
+// instead of six.  Warp w takes a contiguous run of warp-sized chunks (so the
+// warps cover the batch in token order); pass 1 counts each adapter's tokens
+// per warp, one exclusive scan of the counts (adapter-major, then warp) gives
+// every (adapter, warp) its first slot, and pass 2 walks the same chunks again
+// placing each token at its slot plus its rank among the chunk's lanes of the
+// same adapter.  That is the same stable order as the six-launch build, so
+// the same perm bit for bit.  The permutation is built in shared memory, cut
+// into tiles and spans there, then copied out.
+constexpr int64_t kSmallSmemWords = (200 * 1024) / 4;
 
-// Cut every adapter's group into pieces of at most `len` tokens (see
-// emit_pieces); seg and base are shared memory, perm global (this block's).
-__device__ void emit_pieces_local(const int32_t *seg, int32_t N, const int32_t *__restrict__ perm, int32_t len,
+__device__ void emit_pieces_local(const int32_t *seg, int32_t N, const int32_t *perm, int32_t len,
                                   int32_t *__restrict__ out, int32_t *__restrict__ n_out, int32_t max_out,
                                   int32_t *base, int32_t T, int32_t *__restrict__ status)
 {
@@ -284,22 +282,27 @@ __device__ void emit_pieces_local(const int32_t *seg, int32_t N, const int32_t *
     __syncthreads();  // base is reused by the next call
 }
 
+int64_t small_build_words(int32_t T, int32_t N) { return 2 * (int64_t)T + 32 * (int64_t)N + 2 * ((int64_t)N + 1); }
+
 __global__ void __launch_bounds__(1024) route_small_kernel(const int32_t *__restrict__ ids_g, int32_t T, int32_t N,
                                                            int32_t n_chunks, lora_segments s)
 {
-    extern __shared__ int32_t sm[];  // counts [N][n_chunks] (then their exclusive prefix), seg [N+1], base [N+1], ids [T]
-    const int64_t M = (int64_t)N * n_chunks;
-    int32_t *cnt = sm;
-    int32_t *seg = sm + M;
+    // ids [T], perm [T], counts [N][32] (then each (adapter, warp)'s next slot), seg [N+1], base [N+1]
+    extern __shared__ int32_t sm[];
+    int32_t *ids = sm;
+    int32_t *perm = ids + T;
+    int32_t *cnt = perm + T;
+    int32_t *seg = cnt + 32 * (int64_t)N;
     int32_t *base = seg + N + 1;
-    int32_t *ids = base + N + 1;
 #pragma unroll 8
     for (int32_t i = threadIdx.x; i < T; i += blockDim.x) ids[i] = ids_g[i];
-    for (int64_t i = threadIdx.x; i < M; i += blockDim.x) cnt[i] = 0;
+    for (int32_t i = threadIdx.x; i < 32 * N; i += blockDim.x) cnt[i] = 0;
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int32_t c = warp; c < n_chunks; c += 32) {  // warp-uniform: every lane of a warp takes the same chunks
-        const int64_t t = (int64_t)c * 32 + lane;
+    const int32_t per = (n_chunks + 31) / 32;
+    const int32_t c_lo = warp * per, c_hi = min(n_chunks, c_lo + per);
+    for (int32_t c = c_lo; c < c_hi; ++c) {  // warp-uniform
+        const int32_t t = c * 32 + lane;
         int32_t id = -1;
         if (t < T) {
             id = ids[t];
@@ -309,41 +312,43 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const int32_t *__rest
             }
         }
         const uint32_t same = __match_any_sync(0xffffffffu, id);
-        if (id >= 0 && lane == __ffs(same) - 1) cnt[(int64_t)id * n_chunks + c] = __popc(same);
+        if (id >= 0 && lane == __ffs(same) - 1) cnt[id * 32 + warp] += __popc(same);  // only this warp's column
+        __syncwarp();
     }
     __syncthreads();
-    // exclusive scan in place, a 1024-wide row at a time
-    int32_t carry = 0;
-    for (int64_t r0 = 0; r0 < M; r0 += blockDim.x) {
-        const int64_t i = r0 + threadIdx.x;
-        const int32_t v = i < M ? cnt[i] : 0;
+    int32_t carry = 0;  // exclusive scan in place, a 1024-wide row at a time
+    for (int32_t r0 = 0; r0 < 32 * N; r0 += blockDim.x) {
+        const int32_t i = r0 + threadIdx.x;
+        const int32_t v = i < 32 * N ? cnt[i] : 0;
         int32_t tot;
         const int32_t e = block_exclusive_scan(v, &tot);
-        if (i < M) cnt[i] = carry + e;
+        if (i < 32 * N) cnt[i] = carry + e;
         carry += tot;
     }
+    for (int32_t i = threadIdx.x; i <= N; i += blockDim.x) seg[i] = i < N ? cnt[i * 32] : carry;
     __syncthreads();
-    for (int32_t c = warp; c < n_chunks; c += 32) {
-        const int64_t t = (int64_t)c * 32 + lane;
+    for (int32_t c = c_lo; c < c_hi; ++c) {
+        const int32_t t = c * 32 + lane;
         int32_t id = -1;
         if (t < T) {
             id = ids[t];
             if (id < 0 || id >= N) id = -1;
         }
         const uint32_t same = __match_any_sync(0xffffffffu, id);
+        const int32_t slot = id >= 0 ? cnt[id * 32 + warp] : 0;
+        __syncwarp();  // every lane has read its adapter's slot before the group's leader moves it on
         if (id >= 0) {
-            const int32_t rank = __popc(same & ((1u << lane) - 1u));
-            s.perm[LORA_DBG_INDEX((int64_t)cnt[(int64_t)id * n_chunks + c] + rank, T, s.status)] = (int32_t)t;
+            perm[LORA_DBG_INDEX((int64_t)slot + __popc(same & ((1u << lane) - 1u)), T, s.status)] = t;
+            if (lane == __ffs(same) - 1) cnt[id * 32 + warp] = slot + __popc(same);
         }
+        __syncwarp();
     }
-    for (int32_t i = threadIdx.x; i <= N; i += blockDim.x) {
-        const int32_t v = i < N ? cnt[(int64_t)i * n_chunks] : carry;
-        seg[i] = v;
-        s.seg_start[i] = v;
-    }
-    __syncthreads();  // perm and seg are this block's writes
-    emit_pieces_local(seg, N, s.perm, LORA_TILE_M, s.tiles, s.n_tiles, s.max_tiles, base, T, s.status);
-    emit_pieces_local(seg, N, s.perm, LORA_SPAN_TOKENS, s.spans, s.n_spans, s.max_spans, base, T, s.status);
+    __syncthreads();
+    const int32_t n_valid = seg[N];
+    for (int32_t i = threadIdx.x; i < n_valid; i += blockDim.x) s.perm[i] = perm[i];
+    for (int32_t i = threadIdx.x; i <= N; i += blockDim.x) s.seg_start[i] = seg[i];
+    emit_pieces_local(seg, N, perm, LORA_TILE_M, s.tiles, s.n_tiles, s.max_tiles, base, T, s.status);
+    emit_pieces_local(seg, N, perm, LORA_SPAN_TOKENS, s.spans, s.n_spans, s.max_spans, base, T, s.status);
 }
 
 // ---------------------------------------------------------------- sorted input, one launch
@@ -501,11 +506,10 @@ lora_status_t build_segments(const int32_t *ids, const int32_t *seg_offsets, int
         int32_t *hist = s.scratch;
         int32_t *bsum = hist + ((L.hist_words + 63) & ~int64_t(63));
         int32_t *total = bsum + ((L.block_sums + 63) & ~int64_t(63));
-        // one launch when the counts, the ids and the two small tables fit in
-        // shared memory (read from global memory the ids cost a round trip per
-        // chunk, which made a single block slower than the six launches)
-        const int64_t small_words = L.hist_words + 2 * ((int64_t)N + 1) + T;
-        if (L.hist_words > 0 && L.hist_words <= kSmallHistWords && small_words <= kSmallSmemWords) {
+        // one launch when the ids, their permutation and N x 32 counts fit in
+        // shared memory
+        const int64_t small_words = small_build_words(T, N);
+        if (L.hist_words > 0 && small_words <= kSmallSmemWords) {
             const int smem = (int)(small_words * 4);
             if (cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
                 cudaSuccess)

@@ -55,11 +55,11 @@ ID_CASES = {
     "runs_and_singletons": lambda: (np.concatenate([np.full(129, 1), [0], np.full(257, 1), [2, 0, 2]]).astype(np.int32), 3),
     "odd_length_random": lambda: (np.random.default_rng(2).integers(0, 7, 4099).astype(np.int32), 7),
     "ten_thousand_adapters": lambda: (np.random.default_rng(3).integers(0, 10000, 5000).astype(np.int32), 10000),
-    # the one-launch build holds the N x ceil(T / 32) chunk counts, the ids and
-    # two tables of N + 1 in 200 KB of shared memory: just inside that, and
-    # just past it (the six-launch build)
-    "one_launch_near_limit": lambda: (np.random.default_rng(4).integers(0, 66, 16384).astype(np.int32), 66),
-    "past_one_launch_limit": lambda: (np.random.default_rng(5).integers(0, 68, 16384).astype(np.int32), 68),
+    # the one-launch build holds the ids, their permutation, N x 32 counts and
+    # two tables of N + 1 in 200 KB of shared memory: at the limit, and just
+    # past it (the six-launch build)
+    "one_launch_limit": lambda: (np.random.default_rng(4).integers(0, 542, 16384).astype(np.int32), 542),
+    "past_one_launch_limit": lambda: (np.random.default_rng(5).integers(0, 543, 16384).astype(np.int32), 543),
 }
 
 
