@@ -89,7 +89,7 @@ size_t packed_workspace_bytes(const lora_adapter_table &tab, int32_t T)
 lora_status_t run_shrink(float *H, const void *x, const lora_adapter_table &tab, const lora_segments &segs,
                          cudaStream_t stream)
 {
-    return tc_shrink(x, tab, segs, H, nullptr, nullptr, 0, nullptr, nullptr, 0, stream);  // no workspace: not split
+    return tc_shrink(x, tab, segs, H, nullptr, nullptr, 0, nullptr, nullptr, 0, nullptr, 0, stream);  // not split
 }
 
 lora_status_t run_expand(void *y, const float *H, const lora_adapter_table &tab, const lora_segments &segs,
@@ -129,7 +129,8 @@ lora_status_t run_fwd(void *y, float *H_save, const void *x, void *ws, size_t ws
     int32_t *claims = claim_region(ws, ws_bytes, segs.n_tokens, tab.r_max);
     int32_t *c_expand = claims != nullptr ? claims + kClaimExpand : nullptr;
     lora_status_t st = marked(
-        marks, stream, [&] { return tc_shrink(x, tab, segs, H_save, hi, lo, rw, part, c_expand, 1, stream); });
+        marks, stream,
+        [&] { return tc_shrink(x, tab, segs, H_save, hi, lo, rw, part, c_expand, 1, nullptr, 0, stream); });
     if (st != LORA_OK) return st;
     int32_t *use = segs.sorted != 0 ? nullptr : c_expand;
     return marked(marks, stream, [&] { return tc_expand_bf16(y, hi, lo, rw, use, tab, segs, stream); });
@@ -187,10 +188,21 @@ lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void
         if (cudaMemsetAsync(tk_B, 0, ticket_region_bytes(tab, segs.n_tokens), stream) != cudaSuccess)
             return LORA_ERR_CUDA;
     }
-    // dA and dB are sums over token spans added into zeroed outputs
-    if (dB != nullptr && cudaMemsetAsync(dB, 0, (size_t)tab.sum_r * tab.d_out * sizeof(float), stream) != cudaSuccess)
+    // dA and dB are sums over token spans added into zeroed outputs.  dA is
+    // cleared by dh, the kernel before it (its full grid zeroes it in a few
+    // us, where a separate memset launch would sit on the critical path).  dB
+    // is cleared the same way by the kernel before it on its stream (the
+    // small bf16 copy of H, or the recomputing shrink) when it is small; a
+    // large dB goes to a memset at the start, faster than that small grid.
+    // With no tokens no kernel runs: memsets.
+    const int64_t nB = (int64_t)tab.sum_r * tab.d_out, nA = (int64_t)tab.sum_r * tab.d_in;
+    const bool empty = segs.n_tokens == 0 || segs.max_tiles == 0;
+    constexpr int64_t kFoldMaxFloats = (int64_t)4 << 20;  // 16 MB
+    float *zero_B = dB != nullptr && !empty && nB <= kFoldMaxFloats ? dB : nullptr;
+    if (dB != nullptr && zero_B == nullptr &&
+        cudaMemsetAsync(dB, 0, (size_t)nB * sizeof(float), stream) != cudaSuccess)
         return LORA_ERR_CUDA;
-    if (dA != nullptr && cudaMemsetAsync(dA, 0, (size_t)tab.sum_r * tab.d_in * sizeof(float), stream) != cudaSuccess)
+    if (dA != nullptr && empty && cudaMemsetAsync(dA, 0, (size_t)nA * sizeof(float), stream) != cudaSuccess)
         return LORA_ERR_CUDA;
     lora_status_t st = LORA_OK;
     // dB needs only dY and the bf16 rows of H, so with side streams it runs
@@ -208,7 +220,7 @@ lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void
     bool forked_B = false, forked_A = false;
     if (H_saved == nullptr)
         st = marked(marks, stream, [&] {
-            return tc_shrink(X, tab, segs, nullptr, hb, nullptr, rw, part, claim(kClaimDB), 1, stream);
+            return tc_shrink(X, tab, segs, nullptr, hb, nullptr, rw, part, claim(kClaimDB), 1, zero_B, nB, stream);
         });
     if (st == LORA_OK && par && dB != nullptr) {  // fork B once the outputs are zeroed (and H recomputed)
         forked_B = fork(side->ev[0], sB);
@@ -216,12 +228,14 @@ lora_status_t run_bwd(void *dX, float *dA, float *dB, const void *dY, const void
     }
     if (st == LORA_OK && dB != nullptr) {
         if (H_saved != nullptr)
-            st = marked(marks, sB, [&] { return tc_h_to_bf16(H_saved, hb, rw, claim(kClaimDB), 1, tab, segs, sB); });
+            st = marked(marks, sB,
+                        [&] { return tc_h_to_bf16(H_saved, hb, rw, claim(kClaimDB), 1, zero_B, nB, tab, segs, sB); });
         if (st == LORA_OK)
             st = marked(marks, sB, [&] { return tc_db(dB, dY, hb, rw, tk_B, use(kClaimDB, dyn || ordered), tab, segs, sB); });
     }
     if (st == LORA_OK)
-        st = marked(marks, stream, [&] { return tc_dh(dY, tab, segs, dhb, rw, part, claim(kClaimDA), 2, stream); });
+        st = marked(marks, stream,
+                    [&] { return tc_dh(dY, tab, segs, dhb, rw, part, claim(kClaimDA), 2, dA, nA, stream); });
     if (st == LORA_OK && par && dA != nullptr) {  // fork A after dh
         forked_A = fork(side->ev[3], sA);
         if (!forked_A) st = LORA_ERR_CUDA;

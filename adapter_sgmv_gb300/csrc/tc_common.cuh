@@ -239,6 +239,18 @@ LORA_DEV void claim_release_warp(const ClaimRing &R, uint32_t q)
     if ((threadIdx.x & 31) == 0) mbar_arrive(&R.empty[q % kClaimSlots]);
 }
 
+// n floats at p (16-byte aligned, n a multiple of 4) set to zero by every
+// thread of the grid: a kernel that runs before the one accumulating into
+// them, on the same stream, clears them (no separate memset launch).
+LORA_DEV void zero_grid(float *p, int64_t n)
+{
+    if (p == nullptr) return;
+    float4 *q = reinterpret_cast<float4 *>(p);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n / 4; i += stride)
+        q[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 // A kernel that runs before the claiming kernels of the same call, on the
 // same stream, zeroes their counters (block 0, before anything else).
 LORA_DEV void zero_claims(int32_t *claims, int32_t n)

@@ -47,19 +47,23 @@ inline int32_t handoff_cols(int32_t r_max) { return r_max <= 64 ? 64 : 128; }
 // parts whose partials a second small kernel adds.
 // zero_claims: null, or n_zero work-claim counters of kernels that follow on
 // the same stream in the same call, set to zero before anything else.
+// zero_out: null, or zero_out_n floats (16-byte aligned, a multiple of 4)
+// that a later kernel of the call adds into, set to zero by the whole grid.
 lora_status_t tc_shrink(const void *x, const lora_adapter_table &tab, const lora_segments &segs, float *H,
                         uint16_t *hi, uint16_t *lo, int32_t rw, float *part, int32_t *zero_claims, int32_t n_zero,
-                        cudaStream_t stream);
+                        float *zero_out, int64_t zero_out_n, cudaStream_t stream);
 // case i.  dh = s_i B_i^T dy as bf16 by perm position.
 lora_status_t tc_dh(const void *dY, const lora_adapter_table &tab, const lora_segments &segs, uint16_t *dh_bf16,
-                    int32_t rw, float *part, int32_t *zero_claims, int32_t n_zero, cudaStream_t stream);
+                    int32_t rw, float *part, int32_t *zero_claims, int32_t n_zero, float *zero_out,
+                    int64_t zero_out_n, cudaStream_t stream);
 int32_t rowproj_splits(int32_t max_tiles, int32_t d);
 int32_t rowproj_part_ld(int32_t r_max);
 
 // A saved fp32 H (by token) converted to the bf16 hand-off rows (by perm
 // position) that cases iii reads; the same values case i writes as its hi.
 lora_status_t tc_h_to_bf16(const float *H, uint16_t *hb, int32_t rw, int32_t *zero_claims, int32_t n_zero,
-                           const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream);
+                           float *zero_out, int64_t zero_out_n, const lora_adapter_table &tab,
+                           const lora_segments &segs, cudaStream_t stream);
 // case ii.  y += s_i B_i h from the bf16 hand-off buffers (lo may be null).
 // claim: null (CTA b takes items b, b + grid, ...) or a counter that is zero
 // when the kernel starts, from which items are claimed at run time.

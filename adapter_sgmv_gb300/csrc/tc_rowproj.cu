@@ -88,6 +88,10 @@ struct RowOut {
     // here before anything else (null: none)
     int32_t *zero_claims;
     int32_t n_zero;
+    // an output of a later kernel of the call that accumulates into zeros
+    // (dA, dB), cleared here by the whole grid (null: none)
+    float *zero_out;
+    int64_t zero_out_n;
 };
 
 // the k-blocks [lo, hi) of part q of a d of nk blocks cut into `splits` parts
@@ -102,6 +106,7 @@ tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_cons
     const Smem S = carve(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     zero_claims(o.zero_claims, o.n_zero);
+    zero_grid(o.zero_out, o.zero_out_n);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -417,9 +422,11 @@ namespace {
 // are kept small (1024-thread CTAs converted faster alone but crowded out dh's).
 __global__ void __launch_bounds__(256) h_to_bf16_kernel(const float *__restrict__ H, uint16_t *__restrict__ hb,
                                                         int32_t rw, int32_t *zero, int32_t n_zero,
+                                                        float *zero_out, int64_t zero_out_n,
                                                         lora_adapter_table tab, lora_segments segs)
 {
     zero_claims(zero, n_zero);  // the counters of the kernels after this one in the call
+    zero_grid(zero_out, zero_out_n);  // and the output they add into
     const int32_t n_tiles = N_TILES(segs);
     const int32_t r_max = tab.r_max;
     const bool vec = (r_max & 3) == 0 && (reinterpret_cast<uintptr_t>(H) & 15u) == 0;
@@ -451,12 +458,13 @@ __global__ void __launch_bounds__(256) h_to_bf16_kernel(const float *__restrict_
 }  // namespace
 
 lora_status_t tc_h_to_bf16(const float *H, uint16_t *hb, int32_t rw, int32_t *zero_claims, int32_t n_zero,
-                           const lora_adapter_table &tab, const lora_segments &segs, cudaStream_t stream)
+                           float *zero_out, int64_t zero_out_n, const lora_adapter_table &tab,
+                           const lora_segments &segs, cudaStream_t stream)
 {
     if (segs.n_tokens == 0 || segs.max_tiles == 0) return LORA_OK;
     const int sms = sm_count();
     const int grid = segs.max_tiles < 4 * sms ? segs.max_tiles : 4 * sms;
-    h_to_bf16_kernel<<<grid, 256, 0, stream>>>(H, hb, rw, zero_claims, n_zero, tab, segs);
+    h_to_bf16_kernel<<<grid, 256, 0, stream>>>(H, hb, rw, zero_claims, n_zero, zero_out, zero_out_n, tab, segs);
     return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
@@ -473,16 +481,17 @@ int32_t rowproj_part_ld(int32_t r_max) { return (r_max + 15) & ~15; }
 
 lora_status_t tc_shrink(const void *x, const lora_adapter_table &tab, const lora_segments &segs, float *H,
                         uint16_t *hi, uint16_t *lo, int32_t rw, float *part, int32_t *zero_claims, int32_t n_zero,
-                        cudaStream_t stream)
+                        float *zero_out, int64_t zero_out_n, cudaStream_t stream)
 {
-    RowOut o{H, hi, lo, rw, 0.f, 1, 0, nullptr, zero_claims, n_zero};
+    RowOut o{H, hi, lo, rw, 0.f, 1, 0, nullptr, zero_claims, n_zero, zero_out, zero_out_n};
     return launch_rowproj(x, tab.A, tab.d_in, o, tab, segs, part, stream);
 }
 
 lora_status_t tc_dh(const void *dY, const lora_adapter_table &tab, const lora_segments &segs, uint16_t *dh_bf16,
-                    int32_t rw, float *part, int32_t *zero_claims, int32_t n_zero, cudaStream_t stream)
+                    int32_t rw, float *part, int32_t *zero_claims, int32_t n_zero, float *zero_out,
+                    int64_t zero_out_n, cudaStream_t stream)
 {
-    RowOut o{nullptr, dh_bf16, nullptr, rw, 1.f, 1, 0, nullptr, zero_claims, n_zero};
+    RowOut o{nullptr, dh_bf16, nullptr, rw, 1.f, 1, 0, nullptr, zero_claims, n_zero, zero_out, zero_out_n};
     return launch_rowproj(dY, tab.B, tab.d_out, o, tab, segs, part, stream);
 }
 
