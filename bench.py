@@ -237,7 +237,9 @@ class Workload:
 
 def kernels_per_step(spec: wl.Spec) -> int:
     """Kernels the library launches per step (builder + forward + backward)."""
-    build = 1 if spec.sorted and spec.n_adapters <= 4095 else 6  # sorted offsets: one launch
+    T, N = spec.n_tokens, spec.n_adapters
+    one_block = 2 * T + 32 * N + 2 * (N + 1) <= 200 * 1024 // 4  # ids, perm and counts in shared memory
+    build = 1 if (spec.sorted and N <= 4095) or (not spec.sorted and one_block) else 6
     return build + 2 + 5  # forward: shrink, expand; backward: H to bf16, dB, dh, dA, dX
 
 
