@@ -417,8 +417,10 @@ namespace {
 
 // A saved fp32 H (by token, stride r_max) to the bf16 hand-off rows (by perm
 // position, stride rw, zero from each adapter's rank up to the rank rounded to
-// 16, unwritten past that): one CTA per tile,
-// one thread per (row, 8 columns).  It runs beside case i (dh), so its CTAs
+// 16, unwritten past that): one CTA per tile, each thread four (row, 8
+// columns) pieces at a time with all their loads issued before any store (one
+// round trip for the four instead of two each), the tokens of a run of
+// consecutive ones from its first.  It runs beside case i (dh), so its CTAs
 // are kept small (1024-thread CTAs converted faster alone but crowded out dh's).
 __global__ void __launch_bounds__(256) h_to_bf16_kernel(const float *__restrict__ H, uint16_t *__restrict__ hb,
                                                         int32_t rw, int32_t *zero, int32_t n_zero,
@@ -430,27 +432,47 @@ __global__ void __launch_bounds__(256) h_to_bf16_kernel(const float *__restrict_
     const int32_t n_tiles = N_TILES(segs);
     const int32_t r_max = tab.r_max;
     const bool vec = (r_max & 3) == 0 && (reinterpret_cast<uintptr_t>(H) & 15u) == 0;
+    constexpr int kBatch = 4;  // pieces a thread loads before it stores any (their round trips overlap)
     for (int32_t ti = blockIdx.x; ti < n_tiles; ti += gridDim.x) {
         const Tile T = LOAD_TILE(segs, ti);
         const AdapterInfo ad = load_adapter(tab, T.adapter, nullptr);
         const int32_t r = ad.ok ? ad.rank : 0;
         const int32_t rp8 = (r + 15) / 16 * 2;  // 8-column pieces up to the rank rounded to 16; past it no product reads
-        for (int32_t i = threadIdx.x; i < T.rows * rp8; i += blockDim.x) {
-            const int32_t m = i / rp8, k = 8 * (i % rp8);
-            const int64_t p = (int64_t)T.begin + m;
-            const float *src = H + (int64_t)PERM_AT(segs, p) * r_max;
-            float f[8];
-            if (vec && k + 8 <= r) {  // two 16-byte loads
-                const float4 a = __ldcs(reinterpret_cast<const float4 *>(src + k));
-                const float4 b = __ldcs(reinterpret_cast<const float4 *>(src + k + 4));
-                f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-                f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-            } else {
+        const int32_t n = T.rows * rp8;
+        // a run of consecutive tokens needs only its first token
+        const bool contiguous = (T.flags & 1) != 0;
+        const int32_t t0 = contiguous ? PERM_AT(segs, T.begin) : 0;
+        for (int32_t i0 = threadIdx.x; i0 < n; i0 += kBatch * blockDim.x) {
+            int32_t tok[kBatch];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = k + e < r ? src[k + e] : 0.f;
+            for (int j = 0; j < kBatch; ++j) {
+                const int32_t i = i0 + j * (int32_t)blockDim.x, m = i / rp8;
+                tok[j] = i < n ? (contiguous ? t0 + m : PERM_AT(segs, (int64_t)T.begin + m)) : -1;
             }
-            *reinterpret_cast<uint4 *>(hb + p * rw + k) = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]),
-                                                                     pack_bf16(f[4], f[5]), pack_bf16(f[6], f[7]));
+            float f[kBatch][8];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const int32_t i = i0 + j * (int32_t)blockDim.x, k = 8 * (i % rp8);
+                const float *src = H + (int64_t)(tok[j] < 0 ? 0 : tok[j]) * r_max;
+                if (tok[j] >= 0 && vec && k + 8 <= r) {  // two 16-byte loads
+                    const float4 a = __ldcs(reinterpret_cast<const float4 *>(src + k));
+                    const float4 b = __ldcs(reinterpret_cast<const float4 *>(src + k + 4));
+                    f[j][0] = a.x; f[j][1] = a.y; f[j][2] = a.z; f[j][3] = a.w;
+                    f[j][4] = b.x; f[j][5] = b.y; f[j][6] = b.z; f[j][7] = b.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[j][e] = tok[j] >= 0 && k + e < r ? src[k + e] : 0.f;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const int32_t i = i0 + j * (int32_t)blockDim.x;
+                if (tok[j] < 0) continue;
+                const int32_t m = i / rp8, k = 8 * (i % rp8);
+                *reinterpret_cast<uint4 *>(hb + ((int64_t)T.begin + m) * rw + k) =
+                    make_uint4(pack_bf16(f[j][0], f[j][1]), pack_bf16(f[j][2], f[j][3]), pack_bf16(f[j][4], f[j][5]),
+                               pack_bf16(f[j][6], f[j][7]));
+            }
         }
     }
 }
