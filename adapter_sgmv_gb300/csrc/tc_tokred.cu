@@ -14,14 +14,16 @@
 // copied with cp.async and zero-filled so that rows past the span add
 // nothing).  A work item is (span of <= LORA_SPAN_TOKENS tokens of one
 // adapter, 512 columns of d): four TMEM accumulators of up to 128 columns
-// accumulate over the span in 32-token stages; the epilogue stages each
-// warp's 32 x r_pad block in shared memory and adds it into the
-// zero-initialised output with TMA bulk reductions (spans of an adapter sum).
+// accumulate over the span in 32-token stages; the epilogue moves each
+// warp's 32 x r_pad block 16 rows at a time through two small shared-memory
+// buffers and adds it into the zero-initialised output with TMA bulk
+// reductions (spans of an adapter sum).  With the staging that small the
+// ring holds five stages, 160 KB of activations in flight per SM.
 //
-// Warp roles (288 threads): 0..3 load, warp w filling every stage of ring slot
+// Warp roles (320 threads): 0..4 load, warp w filling every stage of ring slot
 // w (a gathered stage's copies are waited for by the warp that issued them,
 // which makes them visible to the tensor cores and releases the stage at once,
-// so all four stages can be in flight); 4 MMA + TMEM owner; 5..8 epilogue.
+// so all five stages can be in flight); 5 MMA + TMEM owner; 6..9 epilogue.
 #define LORA_DBG_FILE 4
 #include "internal.h"
 #include "tc_common.cuh"
@@ -32,7 +34,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kProd = kStages;  // producer warps, one per ring slot
 constexpr int kMmaWarp = kProd;
 constexpr int kEpi0 = kProd + 1;  // first epilogue warp
@@ -43,7 +45,8 @@ constexpr uint32_t kActBytes = kTok * kRange * 2;         // 8 boxes of [64 cols
 constexpr uint32_t kBox = kTok * 64 * 2;                  // one [64 x 32] box
 constexpr uint32_t kHBytes = 2 * kBox;                    // h: up to 128 columns
 constexpr uint32_t kStageBytes = kActBytes + kHBytes;
-constexpr uint32_t kRedBytes = LORA_MAX_RANK * 32 * 4;  // per epilogue warp: [r_pad rows x 32 columns] fp32
+constexpr uint32_t kRedBlock = 16 * 32 * 4;  // one reduction box: [16 rows x 32 columns] fp32
+constexpr uint32_t kRedBytes = 2 * kRedBlock;  // per epilogue warp: two boxes in turn
 constexpr uint32_t kTmemCols = 512;
 constexpr size_t kSmemBytes = 1024 + kStages * (size_t)kStageBytes + 4 * (size_t)kRedBytes + 256;
 
@@ -137,7 +140,8 @@ LORA_DEV void release_ticket(int32_t *tk, int32_t v)
 {
     asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(tk), "r"(v) : "memory");
 }
-LORA_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// all but the newest bulk group of this thread have read their source
+LORA_DEV void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 
 // kClaim: items claimed at run time from `claim` (id-routed batches and the
 // ordered mode), else CTA b takes items b, b + gridDim.x, ...
@@ -349,14 +353,16 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        // Each warp owns 32 columns n (its TMEM lanes) of every chunk: it writes
-        // c * acc as [r_pad rows k x 32 columns] fp32 into its staging block and
-        // adds the block into G (rows row_off + k, columns n) with TMA bulk
-        // reductions of [16 x 32].  Rows k in [r_i, r_pad) add exact zeros (h is
-        // zero there); rows and columns past G's edge are clipped by the TMA.
+        // Each warp owns 32 columns n (its TMEM lanes) of every chunk: 16 rows k
+        // at a time it writes c * acc as [16 x 32] fp32 into one of its two
+        // staging boxes and adds the box into G (rows row_off + k, columns n)
+        // with a TMA bulk reduction.  Rows k in [r_i, r_pad) add exact zeros (h
+        // is zero there); rows and columns past G's edge are clipped by the
+        // TMA.  The accumulators go back to the MMA issuer once the last of
+        // them is read.
         const uint32_t lane_base = 32u * (warp & 3);
         float *red = reinterpret_cast<float *>(S.red + (warp - kEpi0) * kRedBytes);
-        uint32_t nitem = 0, n_ord = 0;
+        uint32_t nitem = 0, n_ord = 0, nbox = 0;
         uint32_t q = 0;
         for (int32_t it = blockIdx.x; kClaim || it < n_items; it += gridDim.x, ++q) {
             if (kClaim) {
@@ -395,28 +401,37 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
             }
             for (int q = 0; q < 4; ++q) {
                 if (q >= I.n_chunks) break;
-                if (lane == 0) bulk_wait_read0();  // the previous chunk's reductions have read the block
-                __syncwarp();
+                const int32_t n0 = I.n_base + 128 * q + (int32_t)lane_base;
+                const bool live = n0 < d;  // a box wholly past column d - 1 is not added
                 for (int c0 = 0; c0 < rp; c0 += 16) {
+                    float *buf = red + (nbox & 1u) * (kRedBlock / 4);
+                    if (live) {
+                        if (lane == 0) bulk_wait_read1();  // the reduction of this buffer's last box has read it
+                        __syncwarp();
+                    }
                     uint32_t v[16];
                     tmem_ld16(tmem_base + (lane_base << 16) + 128u * q + (uint32_t)c0, v);
                     tmem_ld_wait();
+                    if (live) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) red[(c0 + e) * 32 + lane] = c * __uint_as_float(v[e]);
+                        for (int e = 0; e < 16; ++e) buf[e * 32 + lane] = c * __uint_as_float(v[e]);
+                    }
+                    if (q == I.n_chunks - 1 && c0 + 16 >= rp) {  // every accumulator is read: free them
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(S.tempty);
+                    }
+                    if (live) {
+                        fence_proxy_async();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_reduce_add_2d(&map_g, buf, n0, I.ad.row_off + c0);
+                            bulk_commit();
+                        }
+                        ++nbox;
+                    }
                 }
-                fence_proxy_async();
-                __syncwarp();
-                const int32_t n0 = I.n_base + 128 * q + (int32_t)lane_base;
-                if (lane == 0 && n0 < d) {  // a box wholly past column d - 1 is not issued
-                    for (int q16 = 0; q16 < rp / 16; ++q16)
-                        tma_reduce_add_2d(&map_g, red + q16 * 16 * 32, n0, I.ad.row_off + 16 * q16);
-                    bulk_commit();
-                }
-                __syncwarp();
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(S.tempty);
             ++nitem;
             if (tk != nullptr) {  // the span's adds are complete in every warp: pass the ticket on
                 if (lane == 0) {
