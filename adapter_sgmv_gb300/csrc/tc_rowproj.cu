@@ -22,11 +22,15 @@
 // TMA; their products stop at r_pad.  A small kernel beside them converts a
 // saved fp32 H into the same hand-off rows for the backward.
 //
-// Warp roles (352 threads): 0..5 load, warp w filling every stage of ring
-// slot w (a gathered stage's copies are waited for by the warp that issued
-// them, which makes them visible to the tensor cores and releases the stage at
-// once, so all six stages can be in flight); 6 issues MMAs and owns TMEM;
-// 7..10 epilogue.  Every wait is bounded (tc::mbar_wait).
+// Warp roles (32 (S + 5) threads for a ring of S stages): 0..S-1 load, warp w
+// filling every stage of ring slot w (a gathered stage's copies are waited for
+// by the warp that issued them, which makes them visible to the tensor cores
+// and releases the stage at once, so all S stages can be in flight); S issues
+// MMAs and owns TMEM; S+1..S+4 epilogue.  Every wait is bounded
+// (tc::mbar_wait).  Two ring depths: six stages with one CTA per SM, or three
+// stages with two CTAs per SM, taken when there are enough tiles to give most
+// SMs two; the two CTAs of an SM then stream two tiles side by side and each
+// one's tile changes and epilogues are covered by the other's loads.
 #define LORA_DBG_FILE 2
 #include "internal.h"
 #include "tc_common.cuh"
@@ -37,15 +41,14 @@ namespace {
 
 using namespace tc;
 
-constexpr int kStages = 6;
-constexpr int kProd = kStages;     // producer warps, one per ring slot
-constexpr int kMmaWarp = kProd;
-constexpr int kThreads = 32 * (kProd + 1 + 4);
 constexpr uint32_t kActBytes = 128 * 64 * 2;
 constexpr uint32_t kWBytes = LORA_MAX_RANK * 64 * 2;
 constexpr uint32_t kStageBytes = kActBytes + kWBytes;
-constexpr uint32_t kTmemCols = 256;  // two accumulators of up to 128 columns
-constexpr size_t kSmemBytes = 1024 + kStages * (size_t)kStageBytes + 256;
+constexpr uint32_t kTmemCols = 256;  // two accumulators of up to 128 columns (two CTAs fill an SM's 512)
+template <int kStages>
+constexpr int threads_of() { return 32 * (kStages + 1 + 4); }
+template <int kStages>
+constexpr size_t smem_of() { return 1024 + kStages * (size_t)kStageBytes + 256; }
 
 struct Smem {
     uint8_t *act, *w;
@@ -54,6 +57,7 @@ struct Smem {
     volatile int32_t *abort;
 };
 
+template <int kStages>
 LORA_DEV Smem carve(uint8_t *raw)
 {
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
@@ -97,13 +101,16 @@ struct RowOut {
 // the k-blocks [lo, hi) of part q of a d of nk blocks cut into `splits` parts
 LORA_DEV int32_t part_lo(int32_t q, int32_t nk, int32_t splits) { return (int32_t)((int64_t)q * nk / splits); }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <int kStages>
+__global__ void __launch_bounds__(threads_of<kStages>(), kStages <= 3 ? 2 : 1)
 tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_constant__ WMaps map_w,
                   const uint16_t *__restrict__ act, int32_t d, RowOut o, lora_adapter_table tab,
                   lora_segments segs)
 {
+    constexpr int kProd = kStages;  // producer warps, one per ring slot
+    constexpr int kMmaWarp = kProd;
     extern __shared__ uint8_t smem_raw[];
-    const Smem S = carve(smem_raw);
+    const Smem S = carve<kStages>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     zero_claims(o.zero_claims, o.n_zero);
     zero_grid(o.zero_out, o.zero_out_n);
@@ -394,14 +401,21 @@ lora_status_t launch_rowproj(const void *act, const void *w, int32_t d, RowOut o
     if (!make_tmap_bf16_2d(&map_act, act, (uint64_t)d, (uint64_t)segs.n_tokens, 64, 128, true) ||
         !make_wmaps(&map_w, w, (uint64_t)d, (uint64_t)tab.sum_r))
         return LORA_ERR_CUDA;
-    if (cudaFuncSetAttribute(tc_rowproj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-        cudaSuccess)
-        return LORA_ERR_CUDA;
     const int sms = sm_count();
     const int64_t units = (int64_t)segs.max_tiles * o.splits;
-    const int grid = units < sms ? (int)units : sms;
-    tc_rowproj_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_act, map_w, static_cast<const uint16_t *>(act), d,
-                                                              o, tab, segs);
+    // two CTAs per SM once there are at least 1.5 tiles per SM (packed
+    // 4096-token adapters, 256 tiles: dh 61.9 -> 54.8 us); with about one
+    // per SM most SMs would hold a single three-stage CTA (skewed batch, 160
+    // gathered tiles: dh 114 -> 142 us)
+    const bool two = 2 * units >= 3 * (int64_t)sms;
+    auto *kernel = two ? tc_rowproj_kernel<3> : tc_rowproj_kernel<6>;
+    const size_t smem = two ? smem_of<3>() : smem_of<6>();
+    const int per_sm = two ? 2 : 1;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return LORA_ERR_CUDA;
+    const int grid = units < per_sm * sms ? (int)units : per_sm * sms;
+    kernel<<<grid, two ? threads_of<3>() : threads_of<6>(), smem, stream>>>(
+        map_act, map_w, static_cast<const uint16_t *>(act), d, o, tab, segs);
     if (cudaGetLastError() != cudaSuccess) return LORA_ERR_CUDA;
     if (o.splits > 1) {
         const int cgrid = segs.max_tiles < 4 * sms ? segs.max_tiles : 4 * sms;
