@@ -18,12 +18,16 @@
 // warp's 32 x r_pad block 16 rows at a time through two small shared-memory
 // buffers and adds it into the zero-initialised output with TMA bulk
 // reductions (spans of an adapter sum).  With the staging that small the
-// ring holds five stages, 160 KB of activations in flight per SM.
+// ring holds five stages, 160 KB of activations in flight per SM.  Segment-
+// sorted batches in the default order run a second shape (struct Shape): two
+// CTAs per SM, each with three stages of 256-column items and two
+// accumulators.
 //
-// Warp roles (320 threads): 0..4 load, warp w filling every stage of ring slot
-// w (a gathered stage's copies are waited for by the warp that issued them,
-// which makes them visible to the tensor cores and releases the stage at once,
-// so all five stages can be in flight); 5 MMA + TMEM owner; 6..9 epilogue.
+// Warp roles (32 (S + 5) threads for S stages): 0..S-1 load, warp w filling
+// every stage of ring slot w (a gathered stage's copies are waited for by the
+// warp that issued them, which makes them visible to the tensor cores and
+// releases the stage at once, so all S stages can be in flight); S MMA + TMEM
+// owner; S+1..S+4 epilogue.
 #define LORA_DBG_FILE 4
 #include "internal.h"
 #include "tc_common.cuh"
@@ -34,21 +38,30 @@ namespace {
 
 using namespace tc;
 
-constexpr int kStages = 5;
-constexpr int kProd = kStages;  // producer warps, one per ring slot
-constexpr int kMmaWarp = kProd;
-constexpr int kEpi0 = kProd + 1;  // first epilogue warp
-constexpr int kThreads = 32 * (kProd + 1 + 4);
 constexpr int kTok = 32;                                  // tokens per stage
-constexpr int kRange = 512;                               // most columns of d per work item
-constexpr uint32_t kActBytes = kTok * kRange * 2;         // 8 boxes of [64 cols x 32 tokens]
 constexpr uint32_t kBox = kTok * 64 * 2;                  // one [64 x 32] box
 constexpr uint32_t kHBytes = 2 * kBox;                    // h: up to 128 columns
-constexpr uint32_t kStageBytes = kActBytes + kHBytes;
 constexpr uint32_t kRedBlock = 16 * 32 * 4;  // one reduction box: [16 rows x 32 columns] fp32
 constexpr uint32_t kRedBytes = 2 * kRedBlock;  // per epilogue warp: two boxes in turn
-constexpr uint32_t kTmemCols = 512;
-constexpr size_t kSmemBytes = 1024 + kStages * (size_t)kStageBytes + 4 * (size_t)kRedBytes + 256;
+
+// Two shapes.  One CTA per SM: five stages of 32 tokens x 512 columns, four
+// TMEM accumulators (512 columns).  Two CTAs per SM (segment-sorted batches in
+// the default order): three stages of 32 tokens x 256 columns and two
+// accumulators each, so that one CTA's item changes and epilogue are covered
+// by the other's loads.
+template <bool kTwo>
+struct Shape {
+    static constexpr int kStages = kTwo ? 3 : 5;
+    static constexpr int kProd = kStages;  // producer warps, one per ring slot
+    static constexpr int kMmaWarp = kProd;
+    static constexpr int kEpi0 = kProd + 1;  // first epilogue warp
+    static constexpr int kThreads = 32 * (kProd + 1 + 4);
+    static constexpr int kRange = kTwo ? 256 : 512;  // most columns of d per work item
+    static constexpr uint32_t kActBytes = kTok * kRange * 2;  // kRange / 64 boxes of [64 cols x 32 tokens]
+    static constexpr uint32_t kStageBytes = kActBytes + kHBytes;
+    static constexpr uint32_t kTmemCols = kRange;  // one accumulator of up to 128 columns per 128 of d
+    static constexpr size_t kSmemBytes = 1024 + kStages * (size_t)kStageBytes + 4 * (size_t)kRedBytes + 256;
+};
 
 struct Smem {
     uint8_t *act, *h, *red;
@@ -58,8 +71,11 @@ struct Smem {
     ClaimRing claims;  // items claimed at run time
 };
 
+template <bool kTwo>
 LORA_DEV Smem carve(uint8_t *raw)
 {
+    constexpr int kStages = Shape<kTwo>::kStages;
+    constexpr uint32_t kActBytes = Shape<kTwo>::kActBytes;
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     Smem s;
     s.act = base;
@@ -145,8 +161,8 @@ LORA_DEV void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;
 
 // kClaim: items claimed at run time from `claim` (id-routed batches and the
 // ordered mode), else CTA b takes items b, b + gridDim.x, ...
-template <bool kClaim>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kClaim, bool kTwo>
+__global__ void __launch_bounds__(Shape<kTwo>::kThreads, kTwo ? 2 : 1)
 tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_constant__ CUtensorMap map_act3,
                  const __grid_constant__ CUtensorMap map_h,
                  const __grid_constant__ CUtensorMap map_g, const uint16_t *__restrict__ act, int32_t d,
@@ -154,7 +170,10 @@ tc_tokred_kernel(const __grid_constant__ CUtensorMap map_act, const __grid_const
                  int32_t *__restrict__ tickets, int32_t *claim, lora_adapter_table tab, lora_segments segs)
 {
     extern __shared__ uint8_t smem_raw[];
-    const Smem S = carve(smem_raw);
+    using Sh = Shape<kTwo>;
+    constexpr int kStages = Sh::kStages, kProd = Sh::kProd, kMmaWarp = Sh::kMmaWarp, kEpi0 = Sh::kEpi0;
+    constexpr uint32_t kActBytes = Sh::kActBytes, kTmemCols = Sh::kTmemCols;
+    const Smem S = carve<kTwo>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // the claimer's first item, claimed before the set-up so that its round trip overlaps it
     const int32_t first = kClaim && warp == 0 && lane == 0 ? claim_first(claim) : 0;
@@ -465,12 +484,27 @@ lora_status_t launch_tokred(float *G, const void *act, int32_t d, const uint16_t
     if (tickets != nullptr && claim == nullptr) return LORA_ERR_INVALID_ARG;  // the ordered adds need claimed items
     if (segs.n_tokens == 0 || segs.max_spans == 0) return LORA_OK;
     CUtensorMap map_act, map_act3, map_h, map_g;
-    // d a multiple of 64: a stage's eight column blocks come in one 3-D copy
-    // 512-column items, or 128-column ones when 512-column items would leave
-    // half the SMs idle (few spans: a narrow batch of large adapters); in
-    // between, the wider items' fewer reads of h win
+    // 512-column items (256 in the two-CTA shape), or 128-column ones when the
+    // wide items would leave half the SMs idle (few spans: a narrow batch of
+    // large adapters); in between, the wider items' fewer reads of h win
     const int sms = sm_count();
-    const int32_t rng = 2 * (int64_t)segs.max_spans * ((d + kRange - 1) / kRange) < sms ? 128 : kRange;
+    auto range_for = [&](int32_t wide) {
+        return 2 * (int64_t)segs.max_spans * ((d + wide - 1) / wide) < sms ? 128 : wide;
+    };
+    // Two CTAs per SM for segment-sorted batches in the default order (no
+    // claim counter given) with 1.5 to 3 items of the one-CTA shape per SM:
+    // packed4096 (1.7) dB 70.0 -> 64.2 us, dA 60.6 -> 54.9 us.  Id-routed
+    // batches gather their stages and lost with it (skewed dB 125 -> 139 us);
+    // with about one item per SM most SMs would hold a single three-stage CTA
+    // (sweep N = 2, dA 18.3 -> 21.4 us); with many items per SM the kernel
+    // still gained but the step, where dB runs beside dh, lost (sweep N = 32,
+    // 1.83 -> 1.86 ms).  The ordered mode claims its spans.
+    const int64_t items1 = (int64_t)segs.max_spans * ((d + range_for(Shape<false>::kRange) - 1) /
+                                                      range_for(Shape<false>::kRange));
+    const bool two = claim == nullptr && tickets == nullptr && 2 * items1 >= 3 * (int64_t)sms &&
+                     items1 < 3 * (int64_t)sms;
+    const int32_t rng = range_for(two ? Shape<true>::kRange : Shape<false>::kRange);
+    // d a multiple of 64: a stage's column blocks come in one 3-D copy
     const int32_t blocks3 = (d % 64 == 0 && make_tmap_bf16_blocks(&map_act3, act, (uint64_t)d,
                                                                    (uint64_t)segs.n_tokens, kTok, rng / 64))
                                 ? 1
@@ -479,23 +513,25 @@ lora_status_t launch_tokred(float *G, const void *act, int32_t d, const uint16_t
         !make_tmap_bf16_2d(&map_h, hbuf, (uint64_t)rw, (uint64_t)segs.n_tokens, 64, kTok, true) ||
         !make_tmap_f32_2d(&map_g, G, (uint64_t)d, (uint64_t)tab.sum_r, 32, 16))
         return LORA_ERR_CUDA;
-    if (cudaFuncSetAttribute(tc_tokred_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(tc_tokred_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-            cudaSuccess)
-        return LORA_ERR_CUDA;
     const int n_ranges = (d + rng - 1) / rng;
     const int64_t items = (int64_t)segs.max_spans * n_ranges;
-    const int grid = items < sms ? (int)items : sms;
     // run-time claims balance uneven items once every CTA has several to
     // take; with fewer than three per CTA (at most) the split by CTA index did
     // better (skewed batch, dA: 50 against 55 us).  The ordered mode always
     // claims: its waits rely on it.
     if (tickets == nullptr && items < 3 * (int64_t)sms) claim = nullptr;
     if (!blocks3) map_act3 = map_act;
-    auto *kernel = claim != nullptr ? tc_tokred_kernel<true> : tc_tokred_kernel<false>;
-    kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_act, map_act3, map_h, map_g, static_cast<const uint16_t *>(act),
-                                                   d, hbuf, rw, use_scale, blocks3, rng, tickets, claim, tab, segs);
+    auto *kernel = claim != nullptr ? tc_tokred_kernel<true, false>
+                   : two            ? tc_tokred_kernel<false, true>
+                                    : tc_tokred_kernel<false, false>;
+    const size_t smem = two ? Shape<true>::kSmemBytes : Shape<false>::kSmemBytes;
+    const int threads = two ? Shape<true>::kThreads : Shape<false>::kThreads;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return LORA_ERR_CUDA;
+    const int per_sm = two ? 2 : 1;
+    const int grid = items < per_sm * sms ? (int)items : per_sm * sms;
+    kernel<<<grid, threads, smem, stream>>>(map_act, map_act3, map_h, map_g, static_cast<const uint16_t *>(act), d,
+                                            hbuf, rw, use_scale, blocks3, rng, tickets, claim, tab, segs);
     return cudaGetLastError() == cudaSuccess ? LORA_OK : LORA_ERR_CUDA;
 }
 
