@@ -88,6 +88,25 @@ def test_wide_projection_sorted_three_thousand_tokens(route):
     full_check(spec, route=route)
 
 
+def test_two_ctas_per_sm_shapes_ragged():
+    # A sorted batch sized so that, on 152 SMs, case i has 1.5+ tiles per SM
+    # (three-stage ring, two CTAs per SM) and cases iii/iv 1.5 to 3 items per
+    # SM (two CTAs per SM, 256-column items): 45 adapters, T = 30720, d_in and
+    # d_out ending 8 columns into their last 256-column range (and into a
+    # 64-column block, so the activations come by 2-D boxes); an empty
+    # adapter, one of a single token, one of three spans, ranks 8..128 with
+    # 24 and 40 among them
+    rng = np.random.default_rng(31)
+    n = 45
+    ranks = [[8, 16, 24, 32, 40, 64, 128, 16, 8][i % 9] for i in range(n)]
+    lengths = rng.integers(300, 1000, n)
+    lengths[3], lengths[7], lengths[11], lengths[20] = 0, 1, 2500, 129
+    lengths[-1] += 30720 - lengths.sum()
+    ids = np.concatenate([np.full(m, i, np.int32) for i, m in enumerate(lengths)])
+    spec = wl.custom("two_cta", 1032, 1288, ranks, [2.0 * r for r in ranks], ids)
+    full_check(spec)
+
+
 def test_zipf_runs_unsorted_small():
     rng = np.random.default_rng(8)
     runs = []
