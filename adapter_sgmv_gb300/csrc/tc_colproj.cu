@@ -17,7 +17,10 @@
 // rows being updated are staged through a ring of 128 x 64 shared-memory
 // blocks (TMA for consecutive tokens, cp.async gather otherwise); the epilogue
 // adds c * acc in fp32, rounds once, and writes back with a TMA store (full
-// tiles of consecutive tokens) or plain stores of the valid rows.
+// tiles of consecutive tokens) or, from the same staged block, plain stores
+// of the valid rows in which eight lanes cover one row's 128 bytes (a lane
+// per row stored 16 bytes to each of 32 rows per instruction: skewed batch
+// expand 207 -> 178 us, dX 70 -> 60 us).
 //
 // Warp roles: 0 loads (TMA / cp.async), 1 MMA + TMEM owner, then the
 // epilogue: warps 2..9 for sorted batches (both column halves of a chunk at
@@ -407,14 +410,20 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
             const float c = in.use_scale != 0.f ? I.ad.scale : 1.0f;
             const int32_t t = m < I.tile.rows ? PERM_AT(segs, I.tile.begin + m) : -1;
             const int32_t t0 = PERM_AT(segs, I.tile.begin);
-            uint16_t *row = out + (int64_t)(t < 0 ? 0 : t) * d;
             // a gathered tile: this warp copies its own 32 rows of each chunk's
             // halves into the chunk's stages, kLook chunks ahead; lane l copies
             // 16 bytes (piece l & 7) of rows (l >> 3) + 4 q, q < 8, of the warp
             const bool gathered = kGather && (I.tile.flags & 1) == 0;
             const uint32_t a0 = a;
             const int32_t n_chunks = (I.n_hi - I.n_lo + kNC - 1) / kNC;
+            // tokens of rows (l >> 3) + 4 q, q < 8, of the warp (-1 past the tile):
+            // a gathered tile's copies and any tile that is not full move rows in
+            // that pattern, four rows of 128 bytes per warp instruction
             int32_t tg[8];
+            if (gathered || !I.full) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) tg[q] = __shfl_sync(0xffffffffu, t, (lane >> 3) + 4 * q);
+            }
             auto copy_rows = [&](int32_t j) -> bool {
                 for (int h = hg; h < 2; h += kHStep) {
                     const uint32_t gy = 2u * (a0 + (uint32_t)j) + (uint32_t)h;
@@ -435,8 +444,6 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
                 return true;
             };
             if (gathered) {
-#pragma unroll
-                for (int q = 0; q < 8; ++q) tg[q] = __shfl_sync(0xffffffffu, t, (lane >> 3) + 4 * q);
                 for (int32_t j = 0; j < kLook && j < n_chunks && ok; ++j) ok = copy_rows(j);
                 if (!ok) break;
             }
@@ -496,14 +503,23 @@ tc_colproj_kernel(const __grid_constant__ WMaps map_w, const __grid_constant__ C
                             const float hi = bf16hi(w[e]) + c * __uint_as_float(acc8[2 * e + 1]);
                             w[e] = pack_bf16(lo, hi);
                         }
-                        const uint4 nv = make_uint4(w[0], w[1], w[2], w[3]);
-                        if (I.full)
-                            *reinterpret_cast<uint4 *>(y_s + sw128_offset((uint32_t)m, (uint32_t)q)) = nv;
-                        else if (t >= 0 && c0 + 8 * q < d)
-                            *reinterpret_cast<uint4 *>(row + c0 + 8 * q) = nv;
+                        *reinterpret_cast<uint4 *>(y_s + sw128_offset((uint32_t)m, (uint32_t)q)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
                     }
                     if (I.full) fence_proxy_async();
                     __syncwarp();
+                    if (!I.full) {  // the warp's rows back to their tokens, 128 contiguous bytes per row and lane octet
+                        const int cc = lane & 7;
+                        if (c0 + 8 * cc < d) {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                if (tg[q] >= 0)
+                                    *reinterpret_cast<uint4 *>(out + (int64_t)tg[q] * d + c0 + 8 * cc) =
+                                        *reinterpret_cast<const uint4 *>(
+                                            y_s + sw128_offset(lane_base + (uint32_t)((lane >> 3) + 4 * q), (uint32_t)cc));
+                        }
+                        __syncwarp();
+                    }
                     if (lane == 0) mbar_arrive(&S.ysync[s]);
                     if (lead_warp) {  // the group's four warps have their rows in place: store, free stages
                         if (!mbar_wait_warp(&S.ysync[s], ph, S.abort, segs.status)) {
