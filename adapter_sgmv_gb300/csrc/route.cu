@@ -294,25 +294,42 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const int32_t *__rest
     int32_t *cnt = perm + T;
     int32_t *seg = cnt + 32 * (int64_t)N;
     int32_t *base = seg + N + 1;
+    if ((reinterpret_cast<uintptr_t>(ids_g) & 15u) == 0) {  // 16-byte loads, the ragged end one by one
+        const int32_t T4 = T / 4;
+#pragma unroll 4
+        for (int32_t i = threadIdx.x; i < T4; i += blockDim.x)
+            reinterpret_cast<int4 *>(ids)[i] = __ldg(reinterpret_cast<const int4 *>(ids_g) + i);
+        for (int32_t i = 4 * T4 + threadIdx.x; i < T; i += blockDim.x) ids[i] = ids_g[i];
+    } else {
 #pragma unroll 8
-    for (int32_t i = threadIdx.x; i < T; i += blockDim.x) ids[i] = ids_g[i];
+        for (int32_t i = threadIdx.x; i < T; i += blockDim.x) ids[i] = ids_g[i];
+    }
     for (int32_t i = threadIdx.x; i < 32 * N; i += blockDim.x) cnt[i] = 0;
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int32_t per = (n_chunks + 31) / 32;
     const int32_t c_lo = warp * per, c_hi = min(n_chunks, c_lo + per);
-    for (int32_t c = c_lo; c < c_hi; ++c) {  // warp-uniform
+    // the id of lane `lane` in chunk c (-1 past T or for an id out of range, which is reported)
+    auto chunk_id = [&](int32_t c, bool report) {
         const int32_t t = c * 32 + lane;
         int32_t id = -1;
-        if (t < T) {
+        if (c < c_hi && t < T) {
             id = ids[t];
             if (id < 0 || id >= N) {
-                set_status(s.status, LORA_ERR_BAD_ADAPTER_ID);
+                if (report) set_status(s.status, LORA_ERR_BAD_ADAPTER_ID);
                 id = -1;
             }
         }
-        const uint32_t same = __match_any_sync(0xffffffffu, id);
-        if (id >= 0 && lane == __ffs(same) - 1) cnt[id * 32 + warp] += __popc(same);  // only this warp's column
+        return id;
+    };
+    // two chunks per step: both match operations are in flight before either
+    // chunk's leaders add their counts (in chunk order, one after the other)
+    for (int32_t c = c_lo; c < c_hi; c += 2) {  // warp-uniform
+        const int32_t id0 = chunk_id(c, true), id1 = chunk_id(c + 1, true);
+        const uint32_t same0 = __match_any_sync(0xffffffffu, id0), same1 = __match_any_sync(0xffffffffu, id1);
+        if (id0 >= 0 && lane == __ffs(same0) - 1) cnt[id0 * 32 + warp] += __popc(same0);  // only this warp's column
+        __syncwarp();
+        if (id1 >= 0 && lane == __ffs(same1) - 1) cnt[id1 * 32 + warp] += __popc(same1);
         __syncwarp();
     }
     __syncthreads();
@@ -327,25 +344,33 @@ __global__ void __launch_bounds__(1024) route_small_kernel(const int32_t *__rest
     }
     for (int32_t i = threadIdx.x; i <= N; i += blockDim.x) seg[i] = i < N ? cnt[i * 32] : carry;
     __syncthreads();
-    for (int32_t c = c_lo; c < c_hi; ++c) {
-        const int32_t t = c * 32 + lane;
-        int32_t id = -1;
-        if (t < T) {
-            id = ids[t];
-            if (id < 0 || id >= N) id = -1;
+    for (int32_t c = c_lo; c < c_hi; c += 2) {
+        const int32_t id0 = chunk_id(c, false), id1 = chunk_id(c + 1, false);
+        const uint32_t same0 = __match_any_sync(0xffffffffu, id0), same1 = __match_any_sync(0xffffffffu, id1);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {  // chunk c, then c + 1
+            const int32_t id = k ? id1 : id0;
+            const uint32_t same = k ? same1 : same0;
+            const int32_t slot = id >= 0 ? cnt[id * 32 + warp] : 0;
+            __syncwarp();  // every lane has read its adapter's slot before the group's leader moves it on
+            if (id >= 0) {
+                perm[LORA_DBG_INDEX((int64_t)slot + __popc(same & ((1u << lane) - 1u)), T, s.status)] =
+                    (c + k) * 32 + lane;
+                if (lane == __ffs(same) - 1) cnt[id * 32 + warp] = slot + __popc(same);
+            }
+            __syncwarp();
         }
-        const uint32_t same = __match_any_sync(0xffffffffu, id);
-        const int32_t slot = id >= 0 ? cnt[id * 32 + warp] : 0;
-        __syncwarp();  // every lane has read its adapter's slot before the group's leader moves it on
-        if (id >= 0) {
-            perm[LORA_DBG_INDEX((int64_t)slot + __popc(same & ((1u << lane) - 1u)), T, s.status)] = t;
-            if (lane == __ffs(same) - 1) cnt[id * 32 + warp] = slot + __popc(same);
-        }
-        __syncwarp();
     }
     __syncthreads();
     const int32_t n_valid = seg[N];
-    for (int32_t i = threadIdx.x; i < n_valid; i += blockDim.x) s.perm[i] = perm[i];
+    if ((T & 3) == 0 && (reinterpret_cast<uintptr_t>(s.perm) & 15u) == 0) {  // the shared perm is 16-byte aligned too
+        const int32_t n4 = n_valid / 4;
+        for (int32_t i = threadIdx.x; i < n4; i += blockDim.x)
+            reinterpret_cast<int4 *>(s.perm)[i] = reinterpret_cast<const int4 *>(perm)[i];
+        for (int32_t i = 4 * n4 + threadIdx.x; i < n_valid; i += blockDim.x) s.perm[i] = perm[i];
+    } else {
+        for (int32_t i = threadIdx.x; i < n_valid; i += blockDim.x) s.perm[i] = perm[i];
+    }
     for (int32_t i = threadIdx.x; i <= N; i += blockDim.x) s.seg_start[i] = seg[i];
     emit_pieces_local(seg, N, perm, LORA_TILE_M, s.tiles, s.n_tiles, s.max_tiles, base, T, s.status);
     emit_pieces_local(seg, N, perm, LORA_SPAN_TOKENS, s.spans, s.n_spans, s.max_spans, base, T, s.status);
